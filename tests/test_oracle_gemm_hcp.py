@@ -1,0 +1,139 @@
+"""Pins for the oracle's block-scaled GEMM and hot-channel compensation (CPU)."""
+import numpy as np
+import pytest
+
+import oracle as o
+
+
+def _decode_nibble_by_hand(byte, hi):
+    c = (byte >> 4) if hi else (byte & 0xF)
+    sign = -1.0 if c & 8 else 1.0
+    e, m = (c >> 1) & 3, c & 1
+    mag = m * 0.5 if e == 0 else (1.0 + m * 0.5) * 2.0 ** (e - 1)   # E2M1, bias 1
+    return sign * mag
+
+
+@pytest.mark.parametrize("fmt", [o.MXFP4, o.NVFP4])
+def test_gemm_matches_triple_loop(fmt):
+    rng = np.random.default_rng(21)
+    M, N, K = 3, 5, 64
+    a = (rng.standard_normal((M, K)) * 2).astype(np.float32)
+    b = (rng.standard_normal((N, K)) * 0.1).astype(np.float32)
+    ac, asc, ga = o.quantize(a, fmt)
+    bc, bsc, gb = o.quantize(b, fmt)
+    y, bound = o.gemm(ac, asc, bc, bsc, fmt, ga, gb)
+    bsz = o.BLOCK[fmt]
+
+    def scale(sb):
+        if fmt == o.MXFP4:
+            return 2.0 ** (int(sb) - 127)
+        e, m = int(sb) >> 3, int(sb) & 7      # E4M3 by hand
+        return (m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+
+    alpha = 1.0 if fmt == o.MXFP4 else float(ga) * float(gb)
+    for m in range(M):
+        for n in range(N):
+            acc = 0.0
+            for k in range(K):
+                va = _decode_nibble_by_hand(int(ac[m, k // 2]), k % 2) * scale(asc[m, k // bsz])
+                vb = _decode_nibble_by_hand(int(bc[n, k // 2]), k % 2) * scale(bsc[n, k // bsz])
+                acc += va * vb
+            assert abs(alpha * acc - y[m, n]) <= 1e-12 * max(1.0, bound[m, n])
+
+
+def test_gemm_closed_form_ones():
+    # x = 1 everywhere: MXFP4 scale 2^-2, code 4.0 -> value exactly 1; Y = K
+    K = 96
+    a = np.ones((4, K), np.float32)
+    ac, asc, _ = o.quantize(a, o.MXFP4)
+    assert np.all(asc == 125) and np.all(ac == 0x66)
+    y, _ = o.gemm(ac, asc, ac, asc, o.MXFP4)
+    assert np.all(y == K)
+
+
+def test_page_error_decomposition_identity():
+    # quantized product = exact + first-order + second-order terms (outlier page §3.1)
+    rng = np.random.default_rng(22)
+    X = rng.standard_normal((8, 64)).astype(np.float32)
+    W = (rng.standard_normal((12, 64)) * 0.02).astype(np.float32)
+    xc, xs, gx = o.quantize(X, o.NVFP4)
+    wc, ws, gw = o.quantize(W, o.NVFP4)
+    Xh = o.dequantize(xc, xs, o.NVFP4, gx).astype(np.float64)
+    Wh = o.dequantize(wc, ws, o.NVFP4, gw).astype(np.float64)
+    dX, dW = Xh - X, Wh - W
+    lhs = Xh @ Wh.T
+    rhs = X.astype(np.float64) @ W.T + (dX @ W.T + X @ dW.T) + dX @ dW.T
+    assert np.allclose(lhs, rhs, atol=1e-12)
+    y, bound = o.gemm(xc, xs, wc, ws, o.NVFP4, gx, gw)
+    # dequantize rounds each value to fp32 once (2^-24 relative)
+    assert np.all(np.abs(y - lhs) <= 2.0 ** -23 * bound)
+
+
+def _hcp_fixture(fmt, seed=23, M=64, K=128, N=48):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    hot_true = rng.permutation(K)[:6]
+    X[:, hot_true] *= 100
+    X = o.bf16_round(X)
+    W = o.bf16_round((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    xq = o.quantize(X, fmt)
+    wq = o.quantize(W, fmt)
+    return X, W, xq, wq, np.sort(hot_true)
+
+
+@pytest.mark.parametrize("fmt", [o.MXFP4, o.NVFP4])
+def test_hcp_order2_equals_plain_definition(fmt):
+    X, W, (xc, xs, gx), (wc, ws, gw), _ = _hcp_fixture(fmt)
+    h = 12
+    hot = o.hcp_select(X, xc, xs, fmt, gx, h)
+    y, bound = o.hcp_gemm(X, xc, xs, W, wc, ws, fmt, gx, gw, hot, order=2)
+    # plain definition: quantized product on cold channels, exact product on hot ones
+    Xh = o.dequantize(xc, xs, fmt, gx).astype(np.float64)
+    Wh = o.dequantize(wc, ws, fmt, gw).astype(np.float64)
+    mask = np.zeros(X.shape[1], bool)
+    mask[hot] = True
+    ydef = Xh[:, ~mask] @ Wh[:, ~mask].T + X[:, mask].astype(np.float64) @ W[:, mask].astype(np.float64).T
+    # the residual columns are bf16: allow their rounding (2^-8 relative per term)
+    tol = 2.0 ** -7 * (np.abs(X[:, mask]) @ np.abs(W[:, mask]).T) + 1e-6 * bound
+    assert np.all(np.abs(y - ydef) <= tol)
+    # and compensation helps: closer to the unquantized product than plain FP4
+    exact = X.astype(np.float64) @ W.astype(np.float64).T
+    y0, _ = o.gemm(xc, xs, wc, ws, fmt, gx, gw)
+    assert np.abs(y - exact).sum() < np.abs(y0 - exact).sum()
+
+
+def test_hcp_order1_is_the_literal_concatenation():
+    X, W, (xc, xs, gx), (wc, ws, gw), _ = _hcp_fixture(o.NVFP4)
+    hot = o.hcp_select(X, xc, xs, o.NVFP4, gx, 8)
+    y, bound = o.hcp_gemm(X, xc, xs, W, wc, ws, o.NVFP4, gx, gw, hot, order=1)
+    Xh = o.dequantize(xc, xs, o.NVFP4, gx).astype(np.float64)
+    Wh = o.dequantize(wc, ws, o.NVFP4, gw).astype(np.float64)
+    dW = W[:, hot].astype(np.float64) - Wh[:, hot]
+    XH = X[:, hot].astype(np.float64)
+    want = Xh @ Wh.T + XH @ dW.T
+    tol = 2.0 ** -7 * (np.abs(XH) @ np.abs(dW).T) + 1e-6 * bound
+    assert np.all(np.abs(y - want) <= tol)
+
+
+def test_hcp_with_no_hot_channels_is_the_plain_gemm():
+    X, W, (xc, xs, gx), (wc, ws, gw), _ = _hcp_fixture(o.NVFP4)
+    y, _ = o.hcp_gemm(X, xc, xs, W, wc, ws, o.NVFP4, gx, gw, np.array([], np.int32))
+    y0, _ = o.gemm(xc, xs, wc, ws, o.NVFP4, gx, gw)
+    assert np.allclose(y, y0, rtol=1e-12, atol=0)
+
+
+def test_hcp_select_finds_planted_channels_and_breaks_ties_low():
+    X, W, (xc, xs, gx), _, hot_true = _hcp_fixture(o.MXFP4, seed=24)
+    hot = o.hcp_select(X, xc, xs, o.MXFP4, None, len(hot_true))
+    assert np.array_equal(hot, hot_true)
+    assert np.all(np.diff(hot) > 0)
+    # all-equal errors: the lowest indices win
+    Z = np.zeros((16, 64), np.float32)
+    zc, zs, _ = o.quantize(Z, o.MXFP4)
+    assert o.hcp_select(Z, zc, zs, o.MXFP4, None, 5).tolist() == [0, 1, 2, 3, 4]
+
+
+def test_hcp_num_hot_is_ceil_of_nine_percent():
+    assert o.hcp_num_hot(4096) == 369
+    assert o.hcp_num_hot(100) == 9
+    assert o.hcp_num_hot(128) == 12
