@@ -1,0 +1,346 @@
+"""Block-scaled FP4 (MXFP4 / NVFP4) quantization and GEMMs for GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI declared in ``include/fp4.h``; every step
+of the computation runs in the library's CUDA kernels.  PyTorch supplies
+device memory and the current stream.  The functions carry the C names;
+outputs that are not passed in are allocated with ``torch.empty``.
+
+There is no CPU fallback: if the shared library has not been built, or no GPU
+is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from .build import lib_path
+
+# ---- constants (mirror include/fp4.h) ---------------------------------------
+FP4_OK, FP4_ERR_INVALID_ARG, FP4_ERR_UNSUPPORTED, FP4_ERR_MISALIGNED, FP4_ERR_CUDA, FP4_ERR_TIMEOUT = range(6)
+FP4_FMT_MXFP4, FP4_FMT_NVFP4 = 0, 1
+FP4_ROUND_RTN, FP4_ROUND_SR = 0, 1
+FP4_SCALING_1D, FP4_SCALING_2D = 0, 1
+FP4_SF_ROWMAJOR, FP4_SF_MMA = 0, 1
+FP4_DTYPE_BF16, FP4_DTYPE_F32 = 0, 1
+FP4_HCP_SINGLE, FP4_HCP_TWO = 0, 1
+BLOCK = {FP4_FMT_MXFP4: 32, FP4_FMT_NVFP4: 16}
+
+
+class FP4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fp4_status_string(status)} (status {status})")
+
+
+class fp4_quant_params(ctypes.Structure):
+    _fields_ = [("format", ctypes.c_int32), ("block", ctypes.c_int32), ("rounding", ctypes.c_int32),
+                ("scaling", ctypes.c_int32), ("transpose", ctypes.c_int32), ("rht", ctypes.c_int32),
+                ("sf_layout", ctypes.c_int32), ("sr_stream", ctypes.c_uint32), ("sr_seed", ctypes.c_uint64),
+                ("sr_offset", ctypes.c_uint64), ("rht_seed", ctypes.c_uint64)]
+
+
+class fp4_operand(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p),
+                ("format", ctypes.c_int32), ("sf_layout", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("k", ctypes.c_int64)]
+
+
+_P = ctypes.c_void_p
+_I32, _I64, _U64, _F32, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t
+_SIGNATURES = {
+    "fp4_create": (ctypes.c_int, [ctypes.POINTER(_P)]),
+    "fp4_destroy": (None, [_P]),
+    "fp4_sync_status": (ctypes.c_int, [_P, _P]),
+    "fp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fp4_scales_bytes": (_SZ, [_I64, _I64, _I32, _I32]),
+    "fp4_amax": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, _I32, _U64, _P, _P]),
+    "fp4_quantize": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, ctypes.POINTER(fp4_quant_params), _P, _P, _P,
+                                    _P, _P]),
+    "fp4_quantize_dual": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, ctypes.POINTER(fp4_quant_params),
+                                         ctypes.POINTER(fp4_quant_params), _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "fp4_dequantize": (ctypes.c_int, [_P, ctypes.POINTER(fp4_operand), _I32, _P, _I64, _P]),
+    "fp4_rht16": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, _I32, _U64, _P, _P]),
+    "fp4_dge_backward": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _I32, _I64, _P, _I64,
+                                        _F32, _F32, _F32, _P]),
+    "fp4_gemm": (ctypes.c_int, [_P, ctypes.POINTER(fp4_operand), ctypes.POINTER(fp4_operand), _I32, _P, _I64, _I32,
+                                _P]),
+    "fp4_hcp_select_workspace_bytes": (_SZ, [_I64]),
+    "fp4_hcp_select": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(fp4_operand), _I32, _P, _P, _SZ, _P]),
+    "fp4_hcp_workspace_bytes": (_SZ, [_I64, _I64, _I32, _I32]),
+    "fp4_hcp_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _I64, ctypes.POINTER(fp4_operand),
+                                    ctypes.POINTER(fp4_operand), _P, _I32, _I32, _I32, _P, _SZ, _I32, _P, _I64, _P]),
+    "fp4_encode_e2m1": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P]),
+    "fp4_encode_e4m3": (ctypes.c_int, [_P, _P, _P, _I64, _P]),
+}
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with fp4_block_scaled_e8m0_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path == lib_path():
+        _lib = lib
+    return lib
+
+
+def declared_symbols(header: Optional[str] = None) -> list[str]:
+    """Names of the functions include/fp4.h declares."""
+    header = header or os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fp4.h")
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp4_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status: int, where: str) -> None:
+    if status != FP4_OK:
+        raise FP4Error(status, where)
+
+
+def fp4_status_string(status: int) -> str:
+    try:
+        return load_library().fp4_status_string(status).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def fp4_scales_bytes(rows: int, k: int, fmt: int, sf_layout: int) -> int:
+    return int(load_library().fp4_scales_bytes(rows, k, fmt, sf_layout))
+
+
+# ---- context ----------------------------------------------------------------
+class Context:
+    """Owns an fp4_ctx (device scratch for one stream at a time)."""
+
+    def __init__(self):
+        self._lib = load_library()
+        h = _P()
+        _check(self._lib.fp4_create(ctypes.byref(h)), "fp4_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self._lib.fp4_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_contexts: dict[int, Context] = {}
+
+
+def fp4_create() -> Context:
+    return Context()
+
+
+def fp4_destroy(ctx: Context) -> None:
+    ctx.close()
+
+
+def default_context() -> Context:
+    dev = torch.cuda.current_device()
+    if dev not in _contexts:
+        _contexts[dev] = Context()
+    return _contexts[dev]
+
+
+def _ctx(ctx):
+    return (ctx or default_context()).handle
+
+
+def _stream(stream) -> _P:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _P(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def fp4_sync_status(ctx: Optional[Context] = None, stream=None) -> int:
+    """Synchronize the stream and return the context's device status (0 = ok)."""
+    return load_library().fp4_sync_status(_ctx(ctx), _stream(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else _P(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FP4_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return FP4_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ld(t: torch.Tensor) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+# ---- quantized tensor ---------------------------------------------------------
+@dataclass
+class QTensor:
+    """A quantized operand: rows x k values, blocks along k."""
+    codes: torch.Tensor                # uint8 [rows, k/2]
+    scales: torch.Tensor               # uint8, layout sf_layout
+    tensor_scale: Optional[torch.Tensor]  # float32 [1] (NVFP4)
+    fmt: int
+    sf_layout: int
+    rows: int
+    k: int
+
+    def operand(self) -> fp4_operand:
+        return fp4_operand(self.codes.data_ptr(), self.scales.data_ptr(),
+                           self.tensor_scale.data_ptr() if self.tensor_scale is not None else None,
+                           self.fmt, self.sf_layout, self.rows, self.k)
+
+
+def quant_params(fmt=FP4_FMT_NVFP4, rounding=FP4_ROUND_RTN, scaling=FP4_SCALING_1D, transpose=False, rht=False,
+                 sf_layout=FP4_SF_MMA, sr_seed=0, sr_offset=0, sr_stream=0, rht_seed=0) -> fp4_quant_params:
+    return fp4_quant_params(fmt, BLOCK[fmt], rounding, scaling, int(transpose), int(rht), sf_layout, sr_stream,
+                            sr_seed, sr_offset, rht_seed)
+
+
+def alloc_qtensor(rows: int, k: int, fmt: int, sf_layout: int, device) -> QTensor:
+    sb = fp4_scales_bytes(rows, k, fmt, sf_layout)
+    return QTensor(torch.empty((rows, k // 2), dtype=torch.uint8, device=device),
+                   torch.empty((max(sb, 1),), dtype=torch.uint8, device=device),
+                   torch.empty((1,), dtype=torch.float32, device=device) if fmt == FP4_FMT_NVFP4 else None,
+                   fmt, sf_layout, rows, k)
+
+
+def fp4_amax(x: torch.Tensor, rht_axis: int = -1, rht_seed: int = 0, out: Optional[torch.Tensor] = None,
+             ctx=None, stream=None) -> torch.Tensor:
+    out = out if out is not None else torch.empty((1,), dtype=torch.float32, device=x.device)
+    _check(load_library().fp4_amax(_ctx(ctx), _ptr(x), _dtype_code(x), x.shape[0], x.shape[1], _ld(x), rht_axis,
+                                   rht_seed, _ptr(out), _stream(stream)), "fp4_amax")
+    return out
+
+
+def fp4_quantize(x: torch.Tensor, params: fp4_quant_params, given_amax: Optional[torch.Tensor] = None,
+                 out: Optional[QTensor] = None, ctx=None, stream=None) -> QTensor:
+    rows, cols = x.shape
+    o_rows, blocked = (cols, rows) if params.transpose else (rows, cols)
+    out = out or alloc_qtensor(o_rows, blocked, params.format, params.sf_layout, x.device)
+    _check(load_library().fp4_quantize(_ctx(ctx), _ptr(x), _dtype_code(x), rows, cols, _ld(x), ctypes.byref(params),
+                                       _ptr(given_amax), _ptr(out.codes), _ptr(out.scales), _ptr(out.tensor_scale),
+                                       _stream(stream)), "fp4_quantize")
+    return out
+
+
+def fp4_quantize_dual(x: torch.Tensor, p_rows: fp4_quant_params, p_cols: fp4_quant_params,
+                      given_amax_rows=None, given_amax_cols=None, out_rows: Optional[QTensor] = None,
+                      out_cols: Optional[QTensor] = None, ctx=None, stream=None):
+    rows, cols = x.shape
+    out_rows = out_rows or alloc_qtensor(rows, cols, p_rows.format, p_rows.sf_layout, x.device)
+    out_cols = out_cols or alloc_qtensor(cols, rows, p_cols.format, p_cols.sf_layout, x.device)
+    _check(load_library().fp4_quantize_dual(
+        _ctx(ctx), _ptr(x), _dtype_code(x), rows, cols, _ld(x), ctypes.byref(p_rows), ctypes.byref(p_cols),
+        _ptr(given_amax_rows), _ptr(given_amax_cols), _ptr(out_rows.codes), _ptr(out_rows.scales),
+        _ptr(out_rows.tensor_scale), _ptr(out_cols.codes), _ptr(out_cols.scales), _ptr(out_cols.tensor_scale),
+        _stream(stream)), "fp4_quantize_dual")
+    return out_rows, out_cols
+
+
+def fp4_dequantize(q: QTensor, out_dtype=torch.float32, out: Optional[torch.Tensor] = None, ctx=None,
+                   stream=None) -> torch.Tensor:
+    out = out if out is not None else torch.empty((q.rows, q.k), dtype=out_dtype, device=q.codes.device)
+    op = q.operand()
+    _check(load_library().fp4_dequantize(_ctx(ctx), ctypes.byref(op), _dtype_code(out), _ptr(out), _ld(out),
+                                         _stream(stream)), "fp4_dequantize")
+    return out
+
+
+def fp4_rht16(x: torch.Tensor, axis: int, seed: int, out: Optional[torch.Tensor] = None, ctx=None,
+              stream=None) -> torch.Tensor:
+    out = out if out is not None else torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    _check(load_library().fp4_rht16(_ctx(ctx), _ptr(x), _dtype_code(x), x.shape[0], x.shape[1], _ld(x), axis, seed,
+                                     _ptr(out), _stream(stream)), "fp4_rht16")
+    return out
+
+
+def fp4_dge_backward(x: torch.Tensor, q: QTensor, dy: torch.Tensor, k: float = 5.0, clamp: float = 3.0,
+                     outside: float = 1.0, out: Optional[torch.Tensor] = None, ctx=None, stream=None) -> torch.Tensor:
+    out = out if out is not None else torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    op = q.operand()
+    _check(load_library().fp4_dge_backward(_ctx(ctx), _ptr(x), _dtype_code(x), _ld(x), ctypes.byref(op), _ptr(dy),
+                                           _dtype_code(dy), _ld(dy), _ptr(out), _ld(out), k, clamp, outside,
+                                           _stream(stream)), "fp4_dge_backward")
+    return out
+
+
+def fp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None,
+             accumulate: bool = False, ctx=None, stream=None) -> torch.Tensor:
+    out = out if out is not None else torch.empty((a.rows, b.rows), dtype=out_dtype, device=a.codes.device)
+    oa, ob = a.operand(), b.operand()
+    _check(load_library().fp4_gemm(_ctx(ctx), ctypes.byref(oa), ctypes.byref(ob), _dtype_code(out), _ptr(out),
+                                   _ld(out), int(accumulate), _stream(stream)), "fp4_gemm")
+    return out
+
+
+def hcp_num_hot(k: int, ratio: float = 0.09) -> int:
+    """h = ceil(ratio * K): the "top 9% of channels" count."""
+    return int(math.ceil(ratio * k))
+
+
+def fp4_hcp_select(x: torch.Tensor, xq: QTensor, k_hot: int, out: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, ctx=None, stream=None) -> torch.Tensor:
+    lib = load_library()
+    out = out if out is not None else torch.empty((max(k_hot, 1),), dtype=torch.int32, device=x.device)
+    ws_bytes = int(lib.fp4_hcp_select_workspace_bytes(xq.k))
+    workspace = workspace if workspace is not None else torch.empty((max(ws_bytes, 1),), dtype=torch.uint8,
+                                                                   device=x.device)
+    op = xq.operand()
+    _check(lib.fp4_hcp_select(_ctx(ctx), _ptr(x), _ld(x), ctypes.byref(op), k_hot, _ptr(out), _ptr(workspace),
+                              workspace.numel(), _stream(stream)), "fp4_hcp_select")
+    return out[:k_hot]
+
+
+def fp4_hcp_gemm(x: torch.Tensor, w: torch.Tensor, xq: QTensor, wq: QTensor, hot_idx: torch.Tensor, k_hot: int,
+                 mode: int = FP4_HCP_SINGLE, order: int = 2, out_dtype=torch.bfloat16,
+                 out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, ctx=None,
+                 stream=None) -> torch.Tensor:
+    lib = load_library()
+    out = out if out is not None else torch.empty((xq.rows, wq.rows), dtype=out_dtype, device=x.device)
+    ws_bytes = int(lib.fp4_hcp_workspace_bytes(xq.rows, wq.rows, k_hot, order))
+    workspace = workspace if workspace is not None else torch.empty((max(ws_bytes, 1),), dtype=torch.uint8,
+                                                                   device=x.device)
+    ox, ow = xq.operand(), wq.operand()
+    _check(lib.fp4_hcp_gemm(_ctx(ctx), _ptr(x), _ld(x), _ptr(w), _ld(w), ctypes.byref(ox), ctypes.byref(ow),
+                            _ptr(hot_idx), k_hot, mode, order, _ptr(workspace), workspace.numel(), _dtype_code(out),
+                            _ptr(out), _ld(out), _stream(stream)), "fp4_hcp_gemm")
+    return out
+
+
+def fp4_encode_e2m1(xs: torch.Tensor, method: int = 0, ctx=None, stream=None) -> torch.Tensor:
+    out = torch.empty(xs.shape, dtype=torch.uint8, device=xs.device)
+    _check(load_library().fp4_encode_e2m1(_ctx(ctx), _ptr(xs), _ptr(out), xs.numel(), method, _stream(stream)),
+           "fp4_encode_e2m1")
+    return out
+
+
+def fp4_encode_e4m3(t: torch.Tensor, ctx=None, stream=None) -> torch.Tensor:
+    out = torch.empty(t.shape, dtype=torch.uint8, device=t.device)
+    _check(load_library().fp4_encode_e4m3(_ctx(ctx), _ptr(t), _ptr(out), t.numel(), _stream(stream)),
+           "fp4_encode_e4m3")
+    return out

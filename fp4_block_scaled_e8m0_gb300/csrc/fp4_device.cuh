@@ -1,0 +1,259 @@
+// Device helpers for the block-scaled FP4 kernels (sm_103a).
+//
+// Number formats ([outlier] §1.1, [msr] §一: E2M1 with 2 exponent bits and 1
+// mantissa bit covering [-6, 6]; [lowprec] §1.1: E8M0 and E4M3 scales) and the
+// per-element steps of Q(x) = s * round(x / s) ([grad] §2.1).
+//
+// Every floating-point step that decides a code uses explicitly rounded fp32
+// intrinsics (__fmul_rn, __fdiv_rn, __frcp_rn, __fadd_rn) so the compiler can
+// neither contract nor reorder it: the results are bit-reproducible.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "fp4_internal.h"
+
+namespace fp4dev {
+
+// ----------------------------------------------------------------------------
+// loads
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// 8 consecutive input elements (16 bytes of bf16 or 32 bytes of fp32) -> fp32
+template <int DT>
+__device__ __forceinline__ void load8(const void* base, int64_t elem, float* v) {
+  if constexpr (DT == FP4_DTYPE_BF16) {
+    uint4 q = ld_nc_v4(static_cast<const uint16_t*>(base) + elem);
+    uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float* p = static_cast<const float*>(base) + elem;
+    uint4 a = ld_nc_v4(p), b = ld_nc_v4(p + 4);
+    v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+    v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+    v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+    v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ float load1(const void* base, int64_t elem) {
+  if constexpr (DT == FP4_DTYPE_BF16)
+    return bf16_bits_to_float(__ldg(static_cast<const uint16_t*>(base) + elem));
+  else
+    return __ldg(static_cast<const float*>(base) + elem);
+}
+
+// ----------------------------------------------------------------------------
+// E2M1 element encoding
+// ----------------------------------------------------------------------------
+// Hardware conversion of two fp32 values to packed E2M1 (round to nearest even,
+// saturating).  `lo` lands in bits 0-3, `hi` in bits 4-7.
+__device__ __forceinline__ uint32_t e2m1x2_hw(float lo, float hi) {
+  uint32_t r;
+  asm("{\n.reg .b8 q;\ncvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\ncvt.u32.u8 %0, q;\n}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r & 0xFFu;
+}
+
+// Compare chain against the midpoints of the grid {0,.5,1,1.5,2,3,4,6}; at a
+// midpoint the even code wins (0.25->0, 0.75->2, 1.25->2, 1.75->4, 2.5->4,
+// 3.5->6, 5->6); the sign bit is kept.
+__device__ __forceinline__ uint32_t e2m1_sw(float xs) {
+  float a = fabsf(xs);
+  uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+               (a >= 3.5f) + (a > 5.0f);
+  return ((__float_as_uint(xs) >> 28) & 8u) | m;
+}
+
+// Stochastic rounding onto the grid: lo = largest grid point <= |xs| (saturated
+// at 6), frac = (|xs| - lo) / step, round up iff u16 < frac * 65536 ([lowprec]
+// §3.2's floor(x) + (rand < frac) on the non-uniform grid).
+__device__ __forceinline__ uint32_t e2m1_sr(float xs, uint32_t u16) {
+  float a = fminf(fabsf(xs), 6.0f);
+  uint32_t lo_code;
+  float lo, inv_step;
+  if (a < 2.0f) {
+    lo_code = (uint32_t)__fmul_rn(a, 2.0f);           // exact, truncation = floor
+    lo = __fmul_rn((float)lo_code, 0.5f);
+    inv_step = 2.0f;
+  } else if (a < 4.0f) {
+    float f = floorf(a);
+    lo_code = 2u + (uint32_t)f;                       // 2 -> 4, 3 -> 5
+    lo = f;
+    inv_step = 1.0f;
+  } else {
+    lo_code = (a < 6.0f) ? 6u : 7u;
+    lo = 4.0f;
+    inv_step = 0.5f;
+  }
+  float frac = __fmul_rn(__fsub_rn(a, lo), inv_step);  // exact
+  bool up = (lo_code < 7u) && ((float)u16 < __fmul_rn(frac, 65536.0f));
+  return ((__float_as_uint(xs) >> 28) & 8u) | (lo_code + (up ? 1u : 0u));
+}
+
+// ----------------------------------------------------------------------------
+// E4M3 (NVFP4 block scale) and E8M0 (MXFP4 block scale)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3_rn_satfinite(float t) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(t));
+  return r & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_decode(uint32_t b) {
+  uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  return e == 0 ? __fmul_rn((float)m, 0.001953125f)            // m * 2^-9
+                : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// E8M0 byte of a non-negative block amax: floor(log2 amax) - 2 + 127, clamped to
+// [0, 254]; amax = 0 and subnormal amax give byte 0.
+__device__ __forceinline__ uint32_t e8m0_byte(float amax) {
+  int E = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  return E >= 2 ? (uint32_t)(E - 2) : 0u;
+}
+// 2^(127 - byte): the exact power of two applied to each element
+__device__ __forceinline__ float e8m0_inv_scale(uint32_t byte) {
+  return __uint_as_float((254u - byte) << 23);
+}
+__device__ __forceinline__ float e8m0_scale(uint32_t byte) {
+  return byte == 0 ? 5.877471754111438e-39f /* 2^-127 */ : __uint_as_float(byte << 23);
+}
+
+// Block scale of one block: writes the scale byte and the multiplier r with
+// xs = x * r (zero_block = codes forced to 0 when the NVFP4 scale is 0).
+template <int FMT>
+__device__ __forceinline__ void block_scale(float amax_b, float g, uint32_t& byte, float& r,
+                                            bool& zero_block) {
+  if constexpr (FMT == FP4_FMT_MXFP4) {
+    byte = e8m0_byte(amax_b);
+    r = e8m0_inv_scale(byte);
+    zero_block = false;
+  } else {
+    if (g == 0.0f) {
+      byte = 0;
+      r = 0.0f;
+      zero_block = true;
+      return;
+    }
+    float d = __fmul_rn(6.0f, g);
+    float t = __fdiv_rn(amax_b, d);
+    byte = e4m3_rn_satfinite(t);
+    float s = __fmul_rn(e4m3_decode(byte), g);
+    zero_block = (s == 0.0f);
+    r = zero_block ? 0.0f : __frcp_rn(s);
+  }
+}
+
+__device__ __forceinline__ float nvfp4_tensor_scale(float amax_t) { return __fdiv_rn(amax_t, 2688.0f); }
+
+// ----------------------------------------------------------------------------
+// Philox4x32-10 (Salmon et al., SC'11)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int rnd = 0; rnd < 10; ++rnd) {
+    if (rnd) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Eight 16-bit uniforms for output elements 8n .. 8n+7 (n = offset + i/8).
+__device__ __forceinline__ uint4 sr_bits8(uint64_t seed, uint64_t offset, uint32_t stream,
+                                          uint64_t first_elem) {
+  uint64_t n = offset + (first_elem >> 3);
+  return philox4x32_10(make_uint4((uint32_t)n, (uint32_t)(n >> 32), 0u, stream),
+                       (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+__device__ __forceinline__ uint32_t u16_lane(const uint4& w, int j) {
+  uint32_t word = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
+  return (j & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
+// ----------------------------------------------------------------------------
+// 16-point random Hadamard transform: y = 1/4 H16 diag(sigma) x, butterfly with
+// strides 1, 2, 4, 8 (fixed fp32 order)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void rht16(float* v, uint32_t sign_bits) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((sign_bits >> j) & 1u) << 31));
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & h) continue;
+      float a = v[i], b = v[i + h];
+      v[i] = __fadd_rn(a, b);
+      v[i + h] = __fsub_rn(a, b);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+}
+
+__device__ __forceinline__ uint32_t rht_sign_bits(uint64_t seed) {
+  return philox4x32_10(make_uint4(0u, 0u, 0u, 0u), (uint32_t)seed, (uint32_t)(seed >> 32)).x & 0xFFFFu;
+}
+
+// ----------------------------------------------------------------------------
+// scale-factor addressing
+// ----------------------------------------------------------------------------
+// MMA layout: rows padded to 128, blocks along k padded to 256 elements; 512-byte
+// atoms of 128 rows x 4 scales.
+__device__ __forceinline__ int64_t sf_offset(int sf_layout, int64_t r, int64_t j, int64_t nsf_row,
+                                             int64_t nsf_pad) {
+  if (sf_layout == FP4_SF_ROWMAJOR) return r * nsf_row + j;
+  return ((r >> 7) * (nsf_pad >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
+// ----------------------------------------------------------------------------
+// reductions and status
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// block-wide max (blockDim.x multiple of 32, <= 1024), then one atomicMax on
+// the fp32 bit pattern (valid for non-negative floats)
+__device__ __forceinline__ void block_amax_atomic(float v, float* out) {
+  __shared__ float red[32];
+  v = warp_max(v);
+  int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    v = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.0f;
+    v = warp_max(v);
+    if (l == 0 && v > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(out), __float_as_uint(v));
+  }
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+}  // namespace fp4dev

@@ -1,0 +1,98 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/fp4.h"
+
+// Bits of the context's device status word.
+#define FP4_DEVICE_TIMEOUT 1u
+
+// Device scratch owned by a context: status word + amax slots.
+struct fp4_ctx_scratch {
+  unsigned int status;
+  unsigned int pad[3];
+  float amax[4];
+};
+
+struct fp4_ctx {
+  int device;
+  int num_sms;
+  fp4_ctx_scratch* scratch;  // device memory
+};
+
+namespace fp4 {
+
+struct QuantOut {
+  uint8_t* codes;
+  uint8_t* scales;
+  float* tensor_scale;   // NVFP4 only (may be null)
+  const float* amax;     // device amax the NVFP4 scale is derived from
+  int64_t out_rows;      // rows of the output layout
+  int64_t out_cols;      // elements per output row (the blocked extent)
+  int64_t nsf_row;       // scales per output row
+  int64_t nsf_pad;       // MMA layout: scales per row padded to 256 elements
+  int sf_layout;
+  int rounding;
+  int rht;
+  uint32_t sr_stream;
+  uint64_t sr_seed, sr_offset;
+  uint32_t rht_signs;    // 16 sign bits
+};
+
+// Launchers (quant.cu).  All return cudaError_t of the launch.
+cudaError_t launch_amax(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int rht_axis,
+                        uint32_t rht_signs, float* amax_out, int num_sms, cudaStream_t st);
+cudaError_t launch_amax_dual(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx,
+                             uint32_t signs_rows, uint32_t signs_cols, bool rht_rows, bool rht_cols,
+                             float* amax_rows, float* amax_cols, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_rows(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                              const QuantOut& o, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_tile(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                              bool two_d, bool transpose, const QuantOut& o, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_dual(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                              const QuantOut& orow, const QuantOut& ocol, int num_sms, cudaStream_t st);
+cudaError_t launch_dequant(const fp4_operand& q, int out_dt, void* out, int64_t ldo, int num_sms,
+                           cudaStream_t st);
+cudaError_t launch_rht16(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int axis,
+                         uint32_t signs, float* y, int num_sms, cudaStream_t st);
+cudaError_t launch_dge(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
+                       int64_t lddy, float* dx, int64_t lddx, float k, float clamp, float outside,
+                       int num_sms, cudaStream_t st);
+cudaError_t launch_encode_e2m1(const float* xs, uint8_t* codes, int64_t n, int method, cudaStream_t st);
+cudaError_t launch_encode_e4m3(const float* t, uint8_t* out, int64_t n, cudaStream_t st);
+
+// GEMM (gemm.cu).  Extra bf16 K columns (the hot-channel tail) are optional.
+struct GemmArgs {
+  const fp4_operand* A;
+  const fp4_operand* B;
+  const uint16_t* a_ext;   // [M][kx] bf16 or null
+  const uint16_t* b_ext;   // [N][kx] bf16 or null
+  int64_t kx;              // extra K (multiple of 64), 0 if none
+  bool fp4_part;           // false: only the bf16 columns (two-kernel residual GEMM)
+  int out_dtype;
+  void* C;
+  int64_t ldc;
+  int accumulate;
+  unsigned int* status;
+  int num_sms;
+};
+int launch_gemm(const GemmArgs& g, cudaStream_t st);  // returns fp4 status
+
+// Hot-channel compensation (hcp.cu)
+cudaError_t launch_hcp_channel_errors(const uint16_t* x, int64_t ldx, const fp4_operand& q, float* err,
+                                      int num_sms, cudaStream_t st);
+cudaError_t launch_hcp_topk(const float* err, int64_t k, int k_hot, int32_t* hot_idx, cudaStream_t st);
+cudaError_t launch_hcp_gather(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
+                              const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot,
+                              int k_hot, int order, int64_t kx, uint16_t* a_ext, uint16_t* b_ext,
+                              int num_sms, cudaStream_t st);
+
+__host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// scales per row in the MMA layout: k padded to 256 elements
+__host__ __device__ inline int64_t nsf_padded(int64_t k, int fmt) {
+  return cdiv(k, 256) * (256 / (fmt == FP4_FMT_MXFP4 ? 32 : 16));
+}
+
+}  // namespace fp4

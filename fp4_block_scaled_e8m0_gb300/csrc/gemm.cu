@@ -1,0 +1,537 @@
+// Block-scaled FP4 GEMM on the sm_103a tensor cores (tcgen05).
+//
+//   C[M,N] = alpha * ( sum_k A[m,k] B[n,k]  +  sum_j Aext[m,j] Bext[n,j] )
+//
+// The FP4 part is the quantized matmul that carries ">95% of the compute"
+// ([msr] §四): E2M1 operands with per-block scales (E8M0 / block 32 = MXFP4,
+// E4M3 / block 16 = NVFP4, [lowprec] §1.1) multiplied by
+// tcgen05.mma.kind::mxf4nvf4.block_scale, FP32 accumulation in tensor memory.
+// The optional bf16 part is the hot-channel compensation tail of [outlier]
+// §3.1 ("S" mode: extra K columns in the same GEMM), multiplied by
+// tcgen05.mma.kind::f16 into the same accumulator.
+//
+// Kernel structure (one CTA per SM, persistent over 128 x BN output tiles):
+//   warp 0      TMA producer: A/B code tiles (128-byte K slabs, 128B swizzle)
+//               and the scale-factor atoms (bulk copies) into a 4-stage ring
+//   warp 1      TMEM allocator + MMA issuer (one elected lane): copies the
+//               stage's scale factors shared->tensor memory (tcgen05.cp) and
+//               issues 4 MMAs per stage; tcgen05.commit frees the stage
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, * alpha, store
+// Every wait is bounded (globaltimer); a wait that gives up sets the context's
+// status word and the CTA drains and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "fp4_device.cuh"
+
+namespace fp4 {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int STAGES = 4;
+constexpr int KSLAB = 128;                 // bytes of K per stage per row
+constexpr int A_TILE = BM * KSLAB;         // 16 KB
+constexpr int B_TILE = BN * KSLAB;         // 32 KB
+constexpr int SF_A_MAX = 4 * 512;          // NVFP4: 4 atoms of 128 rows x 4 scales
+constexpr int SF_B_MAX = (BN / 128) * 4 * 512;
+constexpr int STAGE_BYTES = A_TILE + B_TILE + SF_A_MAX + SF_B_MAX;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_SF_BASE = BN;      // scale-factor slots after the accumulator
+constexpr uint32_t SF_SLOT_COLS = 48;      // 16 (A) + 32 (B) columns per stage
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+struct Params {
+  int M, N;
+  int k_tiles;        // FP4 K stages (256 elements each)
+  int ext_tiles;      // bf16 K stages (64 elements each)
+  int nvfp4;
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int64_t sf_group_bytes;   // bytes of scales per 128-row group
+  int sf_atoms_per_stage;   // 4 (NVFP4) or 2 (MXFP4)
+  const float* ts_a;
+  const float* ts_b;
+  void* C;
+  int64_t ldc;
+  int out_bf16;
+  int accumulate;
+  unsigned int* status;
+  int tiles_m, tiles_n;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: returns false (and raises the abort flag + status word) when the
+// barrier phase does not complete within WAIT_LIMIT_NS or another thread of
+// the CTA has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = fp4dev::globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (fp4dev::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      *abort_flag = 1;
+      atomicOr(status, FP4_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// shared-memory matrix descriptor (K-major, 128-byte swizzle; SBO = 1024 B
+// between 8-row groups)
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)(1) << 16;                  // leading byte offset (unused with swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
+  d |= (uint64_t)1 << 46;                    // descriptor version (sm_100 family)
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+// descriptor of a 32-row x 16-byte scale-factor block (no swizzle, 8-row core
+// matrices 128 B apart) for tcgen05.cp.32x128b
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)(0) << 16;
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// instruction descriptors
+__device__ __forceinline__ uint32_t idesc_fp4(bool ue8m0, uint32_t sf_id) {
+  uint32_t d = 0;
+  d |= sf_id << 4;              // B scale-factor byte
+  d |= 1u << 7;                 // A: E2M1
+  d |= 1u << 10;                // B: E2M1
+  d |= (uint32_t)(BN >> 3) << 17;
+  d |= (ue8m0 ? 1u : 0u) << 23; // scale type: 1 = UE8M0, 0 = UE4M3
+  d |= (uint32_t)(BM >> 4) << 24;
+  d |= sf_id << 29;             // A scale-factor byte
+  return d;
+}
+__device__ __forceinline__ uint32_t idesc_bf16() {
+  uint32_t d = 0;
+  d |= 1u << 4;                 // accumulate in F32
+  d |= 1u << 7;                 // A: BF16
+  d |= 1u << 10;                // B: BF16
+  d |= (uint32_t)(BN >> 3) << 17;
+  d |= (uint32_t)(BM >> 4) << 24;
+  return d;
+}
+
+__device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t acc, bool nvfp4) {
+  if (nvfp4) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa_tmem), "r"(sfb_tmem));
+  } else {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa_tmem), "r"(sfb_tmem));
+  }
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void sf_copy(uint32_t tmem, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem), "l"(sdesc));
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_ax, const __grid_constant__ CUtensorMap tm_bx,
+                    const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto stage_a = [&](int s) { return smem + s * STAGE_BYTES; };
+  auto stage_b = [&](int s) { return smem + s * STAGE_BYTES + A_TILE; };
+  auto stage_sfa = [&](int s) { return smem + s * STAGE_BYTES + A_TILE + B_TILE; };
+  auto stage_sfb = [&](int s) { return smem + s * STAGE_BYTES + A_TILE + B_TILE + SF_A_MAX; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int total_k = p.k_tiles + p.ext_tiles;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int s = 0;
+      uint32_t phase = 0;
+      uint32_t armed_mask = 0, armed_phase = 0;  // per stage: ever armed, parity of the last arm
+      bool ok = true;
+      const int sf_groups_b = (p.N + 127) / 128;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+        const int groups_b = min(BN / 128, sf_groups_b - tn * (BN / 128));
+        for (int kt = 0; kt < total_k; ++kt) {
+          if (!mbar_wait(&empty[s], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (kt < p.k_tiles) {
+            const uint32_t sf_bytes = p.sf_atoms_per_stage * 512;
+            mbar_expect_tx(&full[s], A_TILE + B_TILE + sf_bytes * (1 + groups_b));
+            tma_load_2d(stage_a(s), &tm_a, &full[s], kt * KSLAB, tm * BM);
+            tma_load_2d(stage_b(s), &tm_b, &full[s], kt * KSLAB, tn * BN);
+            bulk_load(stage_sfa(s), p.sfa + tm * p.sf_group_bytes + (int64_t)kt * sf_bytes, sf_bytes, &full[s]);
+            // scale groups past the operand's last 128 rows are not loaded: they
+            // only feed accumulator columns the epilogue never stores
+            for (int g = 0; g < groups_b; ++g)
+              bulk_load(stage_sfb(s) + g * sf_bytes,
+                        p.sfb + (int64_t)(tn * (BN / 128) + g) * p.sf_group_bytes + (int64_t)kt * sf_bytes, sf_bytes,
+                        &full[s]);
+          } else {
+            const int kx = kt - p.k_tiles;
+            mbar_expect_tx(&full[s], A_TILE + B_TILE);
+            tma_load_2d(stage_a(s), &tm_ax, &full[s], kx * 64, tm * BM);
+            tma_load_2d(stage_b(s), &tm_bx, &full[s], kx * 64, tn * BN);
+          }
+          armed_mask |= 1u << s;
+          armed_phase = (armed_phase & ~(1u << s)) | (phase << s);
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+      }
+      // Before exit every load issued into the ring must have landed (on the
+      // normal path this holds already: the MMA warp consumed each stage).
+      for (int si = 0; si < STAGES; ++si) {
+        if (!(armed_mask >> si & 1u)) continue;
+        const uint32_t ph = (armed_phase >> si) & 1u;
+        const uint64_t t0 = fp4dev::globaltimer_ns();
+        while (!mbar_try_wait(&full[si], ph)) {
+          if (fp4dev::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+            atomicOr(p.status, FP4_DEVICE_TIMEOUT);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int s = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      const bool nvfp4 = p.nvfp4 != 0;
+      const uint32_t sfb_off = nvfp4 ? 16u : 8u;  // B columns start after A's per slot
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+        acc_phase ^= 1;
+        tc_fence_after();
+        for (int kt = 0; kt < total_k; ++kt) {
+          if (!mbar_wait(&full[s], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stage_a(s)), b_addr = smem_u32(stage_b(s));
+          if (kt < p.k_tiles) {
+            const uint32_t slot = tmem + TMEM_SF_BASE + (uint32_t)s * SF_SLOT_COLS;
+            const int atoms = p.sf_atoms_per_stage;
+            for (int a = 0; a < atoms; ++a) {
+              sf_copy(slot + 4 * a, desc_sf(smem_u32(stage_sfa(s)) + a * 512));
+              for (int g = 0; g < BN / 128; ++g)
+                sf_copy(slot + sfb_off + (uint32_t)(a * (BN / 128) + g) * 4,
+                        desc_sf(smem_u32(stage_sfb(s)) + g * atoms * 512 + a * 512));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int atom = nvfp4 ? j : (j >> 1);
+              const uint32_t sf_id = nvfp4 ? 0u : (uint32_t)(j & 1) * 2u;
+              mma_fp4(tmem, desc_sw128(a_addr + 32 * j), desc_sw128(b_addr + 32 * j), idesc_fp4(!nvfp4, sf_id),
+                      slot + 4 * atom, slot + sfb_off + (uint32_t)atom * (BN / 128) * 4,
+                      (kt > 0 || j > 0) ? 1u : 0u, nvfp4);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_bf16(tmem, desc_sw128(a_addr + 32 * j), desc_sw128(b_addr + 32 * j), idesc_bf16(),
+                       (kt > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+      }
+      // make sure no MMA is in flight before the allocation is released
+      tc_commit(drain);
+      uint64_t t0 = fp4dev::globaltimer_ns();
+      while (!mbar_try_wait(drain, 0)) {
+        if (fp4dev::globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    uint32_t acc_phase = 0;
+    float alpha = 1.0f;
+    if (p.nvfp4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(acc_full, acc_phase, abort_flag, p.status);
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      acc_phase ^= 1;
+      tc_fence_after();
+      const int row = tm * BM + quad * 32 + lane;
+      const bool row_ok = row < p.M;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, r);
+        const int col0 = tn * BN + c0;
+        if (!row_ok || col0 >= p.N) continue;
+        const int ncol = min(32, p.N - col0);
+        if (p.out_bf16) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col0;
+          if (ncol == 32 && !p.accumulate) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * q + 2 * i]), alpha),
+                                                         __fmul_rn(__uint_as_float(r[8 * q + 2 * i + 1]), alpha));
+                w[i] = *reinterpret_cast<uint32_t*>(&h);
+              }
+              reinterpret_cast<uint4*>(out)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            for (int i = 0; i < ncol; ++i) {
+              float v = __fmul_rn(__uint_as_float(r[i]), alpha);
+              if (p.accumulate) v = __fadd_rn(__bfloat162float(out[i]), v);
+              out[i] = __float2bfloat16_rn(v);
+            }
+          }
+        } else {
+          float* out = static_cast<float*>(p.C) + (int64_t)row * p.ldc + col0;
+          if (ncol == 32) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float4 v = make_float4(__fmul_rn(__uint_as_float(r[4 * q]), alpha), __fmul_rn(__uint_as_float(r[4 * q + 1]), alpha),
+                                     __fmul_rn(__uint_as_float(r[4 * q + 2]), alpha), __fmul_rn(__uint_as_float(r[4 * q + 3]), alpha));
+              if (p.accumulate) {
+                float4 o = reinterpret_cast<float4*>(out)[q];
+                v.x = __fadd_rn(o.x, v.x); v.y = __fadd_rn(o.y, v.y); v.z = __fadd_rn(o.z, v.z); v.w = __fadd_rn(o.w, v.w);
+              }
+              reinterpret_cast<float4*>(out)[q] = v;
+            }
+          } else {
+            for (int i = 0; i < ncol; ++i) {
+              float v = __fmul_rn(__uint_as_float(r[i]), alpha);
+              out[i] = p.accumulate ? __fadd_rn(out[i], v) : v;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side: tensor maps
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major [rows][inner] matrix with a box of box_rows x 128 bytes
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t inner, int64_t rows,
+              int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(inner * elem_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_gemm(const GemmArgs& g, cudaStream_t st) {
+  const fp4_operand& A = *g.A;
+  const fp4_operand& B = *g.B;
+  const int64_t M = A.rows, N = B.rows;
+  if (M == 0 || N == 0) return FP4_OK;
+  Params p{};
+  p.M = (int)M;
+  p.N = (int)N;
+  p.nvfp4 = A.format == FP4_FMT_NVFP4;
+  p.k_tiles = g.fp4_part ? (int)cdiv(A.k, 256) : 0;
+  p.ext_tiles = (int)(g.kx / 64);
+  p.sfa = A.scales;
+  p.sfb = B.scales;
+  p.sf_atoms_per_stage = p.nvfp4 ? 4 : 2;
+  p.sf_group_bytes = (int64_t)128 * nsf_padded(A.k, A.format);
+  p.ts_a = A.tensor_scale;
+  p.ts_b = B.tensor_scale;
+  p.C = g.C;
+  p.ldc = g.ldc;
+  p.out_bf16 = g.out_dtype == FP4_DTYPE_BF16;
+  p.accumulate = g.accumulate;
+  p.status = g.status;
+  p.tiles_m = (int)cdiv(M, BM);
+  p.tiles_n = (int)cdiv(N, BN);
+  if (p.k_tiles + p.ext_tiles == 0) return FP4_ERR_INVALID_ARG;
+  if (!p.nvfp4) {
+    p.ts_a = p.ts_b = nullptr;
+  }
+
+  CUtensorMap ta{}, tb{}, tax{}, tbx{};
+  bool ok = true;
+  if (g.fp4_part) {
+    ok &= make_map(&ta, A.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.k / 2, M, BM);
+    ok &= make_map(&tb, B.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B.k / 2, N, BN);
+  }
+  if (g.kx > 0) {
+    ok &= make_map(&tax, g.a_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, M, BM);
+    ok &= make_map(&tbx, g.b_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, N, BN);
+  }
+  if (!g.fp4_part) {  // residual-only GEMM: alpha still applies (B_ext is divided by it)
+    ta = tax;
+    tb = tbx;
+  }
+  if (g.kx == 0) {
+    tax = ta;
+    tbx = tb;
+  }
+  if (!ok) return FP4_ERR_CUDA;
+
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+      return FP4_ERR_CUDA;
+    attr_set = true;
+  }
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int grid = std::min(tiles, g.num_sms);
+  fp4_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, tax, tbx, p);
+  return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
+
+}  // namespace fp4

@@ -1,0 +1,221 @@
+// Hot-channel compensation ([outlier] §3.1-3.2, §4.1).
+//
+// The quantized product splits into the exact product, first-order and
+// second-order error terms ([outlier] §3.1, error-decomposition equation).
+// On the k_hot channels with the largest quantization error ("top 9% of
+// channels", [outlier] §4.1) the GEMM gets bf16 extra K columns that restore
+// those terms: with dX = X - X_hat and dW = W - W_hat,
+//   order 2:  A_ext = [dX_H | X_H],  B_ext = [W_hat_H | dW_H] / alpha
+//   order 1:  A_ext = [X_H],         B_ext = [dW_H] / alpha  (the page's concat)
+// B_ext is divided by alpha = gX * gW so that the GEMM epilogue multiplies the
+// whole accumulator (FP4 part and bf16 part) by alpha.
+//
+// Kernels: per-channel squared error (selection metric), rank-based top-k
+// selection (ties to the lower index), and the gather of the extra columns.
+#include <cuda_bf16.h>
+
+#include "fp4_device.cuh"
+
+using namespace fp4dev;
+
+namespace fp4 {
+namespace {
+
+template <int FMT>
+__device__ __forceinline__ float dequant_elem(const fp4_operand& q, int64_t r, int64_t c, float g, int64_t nsf_row,
+                                              int64_t nsf_pad) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  uint32_t byte = q.codes[r * (q.k >> 1) + (c >> 1)];
+  uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
+  uint32_t sb = q.scales[sf_offset(q.sf_layout, r, c / B, nsf_row, nsf_pad)];
+  uint32_t m = code & 7u;
+  float mag = m < 4 ? 0.5f * (float)m : (m == 4 ? 2.0f : m == 5 ? 3.0f : m == 6 ? 4.0f : 6.0f);
+  float v;
+  if (FMT == FP4_FMT_MXFP4) {
+    v = __fmul_rn(mag, e8m0_scale(sb));
+  } else {
+    v = __fmul_rn(__fmul_rn(mag, e4m3_decode(sb)), g);
+  }
+  return (code & 8u) ? -v : v;
+}
+
+// err[c] += sum over this thread's rows of (x - x_hat)^2; one thread per block of
+// B consecutive channels, rows strided over gridDim.y
+template <int FMT>
+__global__ void __launch_bounds__(256) channel_err_kernel(const uint16_t* __restrict__ x, int64_t ldx, fp4_operand q,
+                                                          float* err) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nblk = q.k / B;
+  const int64_t cb = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (cb >= nblk) return;
+  const int64_t nsf_row = nblk, nsf_pad = nsf_padded(q.k, FMT);
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
+  float acc[B];
+#pragma unroll
+  for (int j = 0; j < B; ++j) acc[j] = 0.0f;
+  for (int64_t r = blockIdx.y; r < q.rows; r += gridDim.y) {
+    uint32_t sb = q.scales[sf_offset(q.sf_layout, r, cb, nsf_row, nsf_pad)];
+    float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
+    float v[B];
+#pragma unroll
+    for (int h = 0; h < B / 8; ++h) load8<FP4_DTYPE_BF16>(x, r * ldx + cb * B + 8 * h, v + 8 * h);
+    const uint8_t* cp = q.codes + r * (q.k >> 1) + cb * (B / 2);
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      uint32_t code = (cp[j >> 1] >> (4 * (j & 1))) & 15u;
+      uint32_t m = code & 7u;
+      float mag = m < 4 ? 0.5f * (float)m : (m == 4 ? 2.0f : m == 5 ? 3.0f : m == 6 ? 4.0f : 6.0f);
+      float xh = __fmul_rn(mag, s);
+      if (FMT == FP4_FMT_NVFP4) xh = __fmul_rn(xh, g);
+      if (code & 8u) xh = -xh;
+      float d = __fsub_rn(v[j], xh);
+      acc[j] = __fmaf_rn(d, d, acc[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < B; ++j) atomicAdd(&err[cb * B + j], acc[j]);
+}
+
+// flag[c] = 1 iff fewer than k_hot channels beat c (larger error, or equal
+// error and lower index)
+__global__ void __launch_bounds__(256) rank_kernel(const float* __restrict__ err, int64_t k, int k_hot, int* flag) {
+  __shared__ float chunk[1024];
+  const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const float e = c < k ? err[c] : 0.0f;
+  int64_t rank = 0;
+  for (int64_t base = 0; base < k; base += 1024) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x) chunk[i] = base + i < k ? err[base + i] : -1.0f;
+    __syncthreads();
+    const int64_t n = min((int64_t)1024, k - base);
+    for (int i = 0; i < n; ++i) {
+      float o = chunk[i];
+      rank += (o > e) || (o == e && base + i < c);
+    }
+  }
+  if (c < k) flag[c] = rank < k_hot ? 1 : 0;
+}
+
+// hot_idx = ascending list of flagged channels (one CTA, block-wide scan)
+__global__ void __launch_bounds__(1024) compact_kernel(const int* __restrict__ flag, int64_t k, int32_t* hot_idx) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int64_t base = 0; base < k; base += blockDim.x) {
+    const int64_t c = base + threadIdx.x;
+    int f = c < k ? flag[c] : 0;
+    int x = f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int s = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+        if (lane >= o) s += y;
+      }
+      warp_sums[lane] = s;
+    }
+    __syncthreads();
+    int excl = carry + (w ? warp_sums[w - 1] : 0) + x - f;
+    if (f) hot_idx[excl] = (int32_t)c;
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry = excl + f;
+    __syncthreads();
+  }
+}
+
+// Extra K columns.  One thread per output element (row, j), j in [0, kx).
+template <int FMT>
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ src, int64_t ld, fp4_operand q,
+                                                     const int32_t* __restrict__ hot, int k_hot, int order, int64_t kx,
+                                                     bool is_a, const float* ts_other, uint16_t* __restrict__ out) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
+  // B columns are divided by alpha = fp32(gX * gW): inv_alpha = fp32(1 / alpha)
+  const float inv_alpha = (FMT == FP4_FMT_NVFP4 && !is_a) ? __frcp_rn(__fmul_rn(*ts_other, g)) : 1.0f;
+  const int64_t total = q.rows * kx;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / kx, j = i - r * kx;
+    float v = 0.0f;
+    const int nterm = order == 2 ? 2 : 1;
+    if (j < (int64_t)nterm * k_hot) {
+      const int part = (int)(j / k_hot);            // 0: first half, 1: second half
+      const int64_t c = hot[j - (int64_t)part * k_hot];
+      const float x = bf16_bits_to_float(src[r * ld + c]);
+      // which term this column holds
+      //   A, order 2: part 0 -> x - x_hat, part 1 -> x ;  A, order 1: x
+      //   B, order 2: part 0 -> x_hat/alpha, part 1 -> (x - x_hat)/alpha ;  B, order 1: (x - x_hat)/alpha
+      bool want_delta, want_hat;
+      if (is_a) {
+        want_delta = order == 2 && part == 0;
+        want_hat = false;
+      } else {
+        want_hat = order == 2 && part == 0;
+        want_delta = !want_hat;
+      }
+      if (want_delta || want_hat) {
+        const float xh = dequant_elem<FMT>(q, r, c, g, nsf_row, nsf_pad);
+        v = want_hat ? xh : __fsub_rn(x, xh);
+      } else {
+        v = x;
+      }
+      if (!is_a) v = __fmul_rn(v, inv_alpha);
+    }
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    out[i] = *reinterpret_cast<uint16_t*>(&h);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_hcp_channel_errors(const uint16_t* x, int64_t ldx, const fp4_operand& q, float* err, int num_sms,
+                                      cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(float) * q.k, st);
+  if (e != cudaSuccess || q.rows == 0 || q.k == 0) return e;
+  const int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nblk = q.k / B;
+  dim3 grid((unsigned)cdiv(nblk, 256), 1);
+  int64_t want_y = cdiv((int64_t)num_sms * 8, grid.x);
+  grid.y = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want_y, q.rows));
+  if (q.format == FP4_FMT_MXFP4)
+    channel_err_kernel<FP4_FMT_MXFP4><<<grid, 256, 0, st>>>(x, ldx, q, err);
+  else
+    channel_err_kernel<FP4_FMT_NVFP4><<<grid, 256, 0, st>>>(x, ldx, q, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hcp_topk(const float* err, int64_t k, int k_hot, int32_t* hot_idx, cudaStream_t st) {
+  if (k == 0 || k_hot == 0) return cudaSuccess;
+  int* flag = reinterpret_cast<int*>(const_cast<float*>(err) + k);
+  rank_kernel<<<(unsigned)cdiv(k, 256), 256, 0, st>>>(err, k, k_hot, flag);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  compact_kernel<<<1, 1024, 0, st>>>(flag, k, hot_idx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hcp_gather(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw, const fp4_operand& xq,
+                              const fp4_operand& wq, const int32_t* hot, int k_hot, int order, int64_t kx,
+                              uint16_t* a_ext, uint16_t* b_ext, int num_sms, cudaStream_t st) {
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(xq.rows * kx, 256), (int64_t)num_sms * 8));
+  const int gridb = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(wq.rows * kx, 256), (int64_t)num_sms * 8));
+  if (xq.format == FP4_FMT_MXFP4) {
+    gather_kernel<FP4_FMT_MXFP4><<<grid, 256, 0, st>>>(x, ldx, xq, hot, k_hot, order, kx, true, nullptr, a_ext);
+    gather_kernel<FP4_FMT_MXFP4><<<gridb, 256, 0, st>>>(w, ldw, wq, hot, k_hot, order, kx, false, nullptr, b_ext);
+  } else {
+    gather_kernel<FP4_FMT_NVFP4><<<grid, 256, 0, st>>>(x, ldx, xq, hot, k_hot, order, kx, true, nullptr, a_ext);
+    gather_kernel<FP4_FMT_NVFP4><<<gridb, 256, 0, st>>>(w, ldw, wq, hot, k_hot, order, kx, false, xq.tensor_scale, b_ext);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fp4

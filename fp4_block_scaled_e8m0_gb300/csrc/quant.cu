@@ -1,0 +1,569 @@
+// Quantization-side kernels: per-tensor amax, block-scaled FP4 quantize in the
+// row and transposed layouts (1D and 16x16 2D scaling, optional RHT16, RTN or
+// Philox SR), dequantize, the standalone RHT16, the DGE backward and the
+// element encoders.  All are HBM-bound streaming kernels.
+//
+// Q(x) = s * round(x / s)  ([grad] §2.1); E2M1 elements ([outlier] §1.1, [msr] §一);
+// E8M0 / E4M3 block scales, NVFP4 per-tensor scale ([lowprec] §1.1);
+// RTN forward, SR + 16x16 2D + RHT backward ([outlier] §4.1-4.2);
+// SR as floor + (rand < frac) ([lowprec] §3.2); DGE derivative clamped at 3.0
+// ([msr] §二).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "fp4_device.cuh"
+
+using namespace fp4dev;
+
+namespace fp4 {
+namespace {
+
+constexpr int kThreads = 256;
+
+inline int grid_for(int64_t work_items, int per_block, int num_sms, int blocks_per_sm = 8) {
+  int64_t need = cdiv(work_items, per_block);
+  int64_t cap = (int64_t)num_sms * blocks_per_sm;
+  return (int)(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+// ----------------------------------------------------------------------------
+// Encode the B values of one block (already RHT'ed if requested) and store
+// codes + scale.  `first_elem` is the linear output index of v[0] (SR counter).
+// ----------------------------------------------------------------------------
+template <int FMT, int B>
+__device__ __forceinline__ void encode_store_block(const float* v, float g, const QuantOut& o,
+                                                   int64_t out_row, int64_t out_col0, float amax_b,
+                                                   bool sr) {
+  uint32_t byte;
+  float r;
+  bool zero;
+  block_scale<FMT>(amax_b, g, byte, r, zero);
+  uint32_t packed[B / 8];
+  if (!sr) {
+#pragma unroll
+    for (int q = 0; q < B / 8; ++q) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        float a = __fmul_rn(v[8 * q + 2 * p], r), b = __fmul_rn(v[8 * q + 2 * p + 1], r);
+        w |= e2m1x2_hw(a, b) << (8 * p);
+      }
+      packed[q] = zero ? 0u : w;
+    }
+  } else {
+    int64_t first_elem = out_row * o.out_cols + out_col0;
+#pragma unroll
+    for (int q = 0; q < B / 8; ++q) {
+      uint4 bits = sr_bits8(o.sr_seed, o.sr_offset, o.sr_stream, (uint64_t)(first_elem + 8 * q));
+      uint32_t w = 0;
+#pragma unroll
+      for (int p = 0; p < 8; ++p)
+        w |= e2m1_sr(__fmul_rn(v[8 * q + p], r), u16_lane(bits, p)) << (4 * p);
+      packed[q] = zero ? 0u : w;
+    }
+  }
+  uint8_t* dst = o.codes + out_row * (o.out_cols >> 1) + (out_col0 >> 1);
+  if constexpr (B == 16) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+  } else {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+  o.scales[sf_offset(o.sf_layout, out_row, out_col0 / B, o.nsf_row, o.nsf_pad)] = (uint8_t)byte;
+}
+
+__device__ __forceinline__ float load_g(const QuantOut& o, int fmt) {
+  if (fmt != FP4_FMT_NVFP4) return 0.0f;
+  float g = nvfp4_tensor_scale(*o.amax);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && o.tensor_scale) *o.tensor_scale = g;
+  return g;
+}
+
+// ----------------------------------------------------------------------------
+// amax over a row-blocked tensor (plain or RHT16 along cols); cols % 16 == 0,
+// rows 16-byte aligned.  One thread per 16-element chunk.
+// ----------------------------------------------------------------------------
+template <int DT, bool RHT>
+__global__ void __launch_bounds__(kThreads) amax_rows_kernel(const void* __restrict__ x, int64_t rows,
+                                                             int64_t cols, int64_t ldx, uint32_t signs,
+                                                             float* amax_out) {
+  int64_t nchunk_row = cols >> 4;
+  int64_t total = rows * nchunk_row;
+  float m = 0.0f;
+  for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < total;
+       c += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r = c / nchunk_row, k0 = (c - r * nchunk_row) << 4;
+    float v[16];
+    load8<DT>(x, r * ldx + k0, v);
+    load8<DT>(x, r * ldx + k0 + 8, v + 8);
+    if (RHT) rht16(v, signs);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
+  }
+  block_amax_atomic(m, amax_out);
+}
+
+// ----------------------------------------------------------------------------
+// Row quantizer: blocks along cols, output [rows][cols/2].  One thread per block.
+// ----------------------------------------------------------------------------
+template <int FMT, int DT>
+__global__ void __launch_bounds__(kThreads) quant_rows_kernel(const void* __restrict__ x, int64_t rows,
+                                                              int64_t cols, int64_t ldx, QuantOut o) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const float g = load_g(o, FMT);
+  const bool sr = o.rounding == FP4_ROUND_SR;
+  const bool rht = o.rht != 0;
+  int64_t nblk_row = cols / B;
+  int64_t total = rows * nblk_row;
+  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
+       blk += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r = blk / nblk_row, k0 = (blk - r * nblk_row) * B;
+    float v[B];
+#pragma unroll
+    for (int q = 0; q < B / 8; ++q) load8<DT>(x, r * ldx + k0 + 8 * q, v + 8 * q);
+    if (rht) {
+#pragma unroll
+      for (int h = 0; h < B / 16; ++h) rht16(v + 16 * h, o.rht_signs);
+    }
+    float amax_b = 0.0f;
+#pragma unroll
+    for (int j = 0; j < B; ++j) amax_b = fmaxf(amax_b, fabsf(v[j]));
+    encode_store_block<FMT, B>(v, g, o, r, k0, amax_b, sr);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Tiled kernels: a TR x 64 tile of the input is staged in shared memory (fp32)
+// so that both the row-blocked and the column-blocked (transposed) outputs are
+// read and written coalesced.  TR = 4 blocks (64 rows for NVFP4, 128 for MXFP4).
+// ----------------------------------------------------------------------------
+enum TileMode { T_AMAX_COLS = 0, T_AMAX_DUAL = 1, T_Q_COLS = 2, T_Q_DUAL = 3, T_Q_ROWS2D = 4 };
+
+constexpr int TC = 64;
+constexpr int TSTRIDE = TC + 1;
+
+template <int DT, int TR>
+__device__ __forceinline__ void load_tile(const void* __restrict__ x, int64_t rows, int64_t cols,
+                                          int64_t ldx, int64_t r0, int64_t c0, float* tile) {
+  const bool full = (r0 + TR <= rows) && (c0 + TC <= cols);
+  constexpr int CH = TR * TC / 8;  // 8-element chunks
+  for (int q = threadIdx.x; q < CH; q += blockDim.x) {
+    int rr = q / (TC / 8), cc = (q % (TC / 8)) * 8;
+    float v[8];
+    if (full) {
+      load8<DT>(x, (r0 + rr) * ldx + c0 + cc, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        int64_t R = r0 + rr, C = c0 + cc + i;
+        v[i] = (R < rows && C < cols) ? load1<DT>(x, R * ldx + C) : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tile[rr * TSTRIDE + cc + i] = v[i];
+  }
+}
+
+template <int FMT, int DT, int MODE>
+__global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__ x, int64_t rows,
+                                                        int64_t cols, int64_t ldx, QuantOut oc,
+                                                        QuantOut orr, int two_d, uint32_t signs_c,
+                                                        uint32_t signs_r, int rht_c, int rht_r,
+                                                        float* amax_c, float* amax_r) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  constexpr int TR = 4 * B;
+  __shared__ float tile[TR * TSTRIDE];
+  constexpr bool QUANT = MODE >= T_Q_COLS;
+  constexpr bool DO_COLS = MODE == T_AMAX_COLS || MODE == T_AMAX_DUAL || MODE == T_Q_COLS || MODE == T_Q_DUAL;
+  constexpr bool DO_ROWS = MODE == T_AMAX_DUAL || MODE == T_Q_DUAL || MODE == T_Q_ROWS2D;
+  float g_c = 0.0f, g_r = 0.0f;
+  if constexpr (QUANT) {
+    if (DO_COLS) g_c = load_g(oc, FMT);
+    if (DO_ROWS) g_r = load_g(orr, FMT);
+  }
+  float m_c = 0.0f, m_r = 0.0f;
+  const int64_t ntr = cdiv(rows, TR), ntc = cdiv(cols, TC);
+  const int t = threadIdx.x;
+  for (int64_t tid = blockIdx.x; tid < ntr * ntc; tid += gridDim.x) {
+    int64_t r0 = (tid / ntc) * TR, c0 = (tid % ntc) * TC;
+    load_tile<DT, TR>(x, rows, cols, ldx, r0, c0, tile);
+    __syncthreads();
+    if constexpr (DO_COLS) {
+      // column item: column c of the tile, row-block rb (B rows); lanes = columns
+      int c = t % TC, rb = t / TC;
+      float v[B];
+#pragma unroll
+      for (int j = 0; j < B; ++j) v[j] = tile[(rb * B + j) * TSTRIDE + c];
+      if (rht_c) {
+#pragma unroll
+        for (int h = 0; h < B / 16; ++h) rht16(v + 16 * h, signs_c);
+      }
+      float a = 0.0f;
+#pragma unroll
+      for (int j = 0; j < B; ++j) a = fmaxf(a, fabsf(v[j]));
+      bool valid = (c0 + c < cols) && (r0 + rb * B < rows);
+      if constexpr (!QUANT) {
+        if (valid) m_c = fmaxf(m_c, a);
+      } else {
+        if (two_d) {  // 16x16 tile: the 16 lanes of consecutive columns share one scale
+#pragma unroll
+          for (int o = 8; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+        }
+        if (valid) encode_store_block<FMT, B>(v, g_c, oc, c0 + c, r0 + rb * B, a, oc.rounding == FP4_ROUND_SR);
+      }
+    }
+    if constexpr (DO_ROWS) {
+      // row item: row r of the tile, col-block cb; lanes = consecutive rows
+      int r = t % TR, cb = t / TR;
+      if (cb < TC / B) {
+        float v[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) v[j] = tile[r * TSTRIDE + cb * B + j];
+        if (rht_r) {
+#pragma unroll
+          for (int h = 0; h < B / 16; ++h) rht16(v + 16 * h, signs_r);
+        }
+        float a = 0.0f;
+#pragma unroll
+        for (int j = 0; j < B; ++j) a = fmaxf(a, fabsf(v[j]));
+        bool valid = (r0 + r < rows) && (c0 + cb * B < cols);
+        if constexpr (!QUANT) {
+          if (valid) m_r = fmaxf(m_r, a);
+        } else {
+          if (MODE == T_Q_ROWS2D) {
+#pragma unroll
+            for (int o = 8; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+          }
+          if (valid) encode_store_block<FMT, B>(v, g_r, orr, r0 + r, c0 + cb * B, a, orr.rounding == FP4_ROUND_SR);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if constexpr (!QUANT) {
+    if (DO_COLS) block_amax_atomic(m_c, amax_c);
+    if (DO_ROWS) {
+      __syncthreads();
+      block_amax_atomic(m_r, amax_r);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// dequantize: one thread per block
+// ----------------------------------------------------------------------------
+template <int FMT, int ODT>
+__global__ void __launch_bounds__(kThreads) dequant_kernel(fp4_operand q, void* out, int64_t ldo) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 1.0f;
+  const int64_t total = q.rows * nsf_row;
+  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
+       blk += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r = blk / nsf_row, j = blk - r * nsf_row;
+    uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
+    float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
+    const uint8_t* cp = q.codes + r * (q.k >> 1) + j * (B / 2);
+    uint32_t w[B / 8];
+    if constexpr (B == 16) {
+      uint2 u = *reinterpret_cast<const uint2*>(cp);
+      w[0] = u.x; w[1] = u.y;
+    } else {
+      uint4 u = *reinterpret_cast<const uint4*>(cp);
+      w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+    }
+    float v[B];
+#pragma unroll
+    for (int e = 0; e < B; ++e) {
+      uint32_t c = (w[e >> 3] >> (4 * (e & 7))) & 15u;
+      uint32_t m = c & 7u;
+      float mag = m < 4 ? 0.5f * (float)m : (m == 4 ? 2.0f : m == 5 ? 3.0f : m == 6 ? 4.0f : 6.0f);
+      float val = __fmul_rn(mag, s);  // exact (short significands; MXFP4 power of two)
+      if (FMT == FP4_FMT_NVFP4) val = __fmul_rn(val, g);
+      v[e] = (c & 8u) ? -val : val;
+    }
+    int64_t base = r * ldo + j * B;
+    if constexpr (ODT == FP4_DTYPE_F32) {
+      float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + base);
+#pragma unroll
+      for (int e = 0; e < B / 4; ++e) o4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+    } else {
+      uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + base);
+#pragma unroll
+      for (int e = 0; e < B / 8; ++e) {
+        uint32_t p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * e + 2 * i], v[8 * e + 2 * i + 1]);
+          p[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        o4[e] = make_uint4(p[0], p[1], p[2], p[3]);
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// standalone RHT16 (fp32 out, pitch cols)
+// ----------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kThreads) rht_rows_kernel(const void* __restrict__ x, int64_t rows,
+                                                            int64_t cols, int64_t ldx, uint32_t signs,
+                                                            float* y) {
+  int64_t nch = cols >> 4, total = rows * nch;
+  for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < total;
+       c += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r = c / nch, k0 = (c - r * nch) << 4;
+    float v[16];
+    load8<DT>(x, r * ldx + k0, v);
+    load8<DT>(x, r * ldx + k0 + 8, v + 8);
+    rht16(v, signs);
+    float4* o = reinterpret_cast<float4*>(y + r * cols + k0);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) rht_cols_kernel(const void* __restrict__ x, int64_t rows,
+                                                            int64_t cols, int64_t ldx, uint32_t signs,
+                                                            float* y) {
+  int64_t nrb = rows >> 4, total = nrb * cols;
+  for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    int64_t rb = it / cols, c = it - rb * cols;  // lanes = consecutive columns
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = load1<DT>(x, (rb * 16 + j) * ldx + c);
+    rht16(v, signs);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) y[(rb * 16 + j) * cols + c] = v[j];
+  }
+}
+
+// ----------------------------------------------------------------------------
+// DGE backward ([msr] §二): dx = dy * min(clamp, (1/k)|u|^(1/k-1)), one thread
+// per block of x (blocks along cols)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float dge_fprime(float xs, float inv_k, float expo, float clamp, float outside) {
+  float a = fabsf(xs);
+  if (a >= 6.0f) return outside;
+  float lo, two_over_d;
+  if (a < 2.0f) {
+    lo = __fmul_rn(floorf(__fmul_rn(a, 2.0f)), 0.5f);
+    two_over_d = 4.0f;
+  } else if (a < 4.0f) {
+    lo = floorf(a);
+    two_over_d = 2.0f;
+  } else {
+    lo = 4.0f;
+    two_over_d = 1.0f;
+  }
+  float u = __fsub_rn(__fmul_rn(__fsub_rn(a, lo), two_over_d), 1.0f);
+  float au = fabsf(u);
+  if (au == 0.0f) return clamp;
+  float f = __fmul_rn(inv_k, powf(au, expo));
+  return fminf(clamp, f);
+}
+
+template <int FMT, int XDT, int DYDT>
+__global__ void __launch_bounds__(kThreads) dge_kernel(const void* __restrict__ x, int64_t ldx, fp4_operand q,
+                                                       const void* __restrict__ dy, int64_t lddy, float* dx,
+                                                       int64_t lddx, float inv_k, float expo, float clamp,
+                                                       float outside) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
+  const int64_t total = q.rows * nsf_row;
+  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
+       blk += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r = blk / nsf_row, j = blk - r * nsf_row;
+    uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
+    float mult;
+    if (FMT == FP4_FMT_MXFP4) {
+      mult = e8m0_inv_scale(sb);
+    } else {
+      float s = __fmul_rn(e4m3_decode(sb), g);
+      mult = s == 0.0f ? 0.0f : __frcp_rn(s);
+    }
+#pragma unroll
+    for (int q8 = 0; q8 < B / 8; ++q8) {
+      float v[8], d[8];
+      load8<XDT>(x, r * ldx + j * B + 8 * q8, v);
+      load8<DYDT>(dy, r * lddy + j * B + 8 * q8, d);
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(d[e], dge_fprime(__fmul_rn(v[e], mult), inv_k, expo, clamp, outside));
+      float4* dst = reinterpret_cast<float4*>(dx + r * lddx + j * B + 8 * q8);
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// element encoders
+// ----------------------------------------------------------------------------
+__global__ void encode_e2m1_kernel(const float* xs, uint8_t* codes, int64_t n, int method) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    float v = xs[i];
+    codes[i] = (uint8_t)(method == 0 ? e2m1x2_hw(v, 0.0f) & 15u : e2m1_sw(v));
+  }
+}
+__global__ void encode_e4m3_kernel(const float* t, uint8_t* out, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = (uint8_t)e4m3_rn_satfinite(t[i]);
+}
+
+}  // namespace
+
+// ============================================================================
+// launchers
+// ============================================================================
+#define FP4_DISPATCH_DT(dt, DT, ...)          \
+  if ((dt) == FP4_DTYPE_BF16) {               \
+    constexpr int DT = FP4_DTYPE_BF16;        \
+    __VA_ARGS__;                              \
+  } else {                                    \
+    constexpr int DT = FP4_DTYPE_F32;         \
+    __VA_ARGS__;                              \
+  }
+#define FP4_DISPATCH_FMT(fmt, FMT, ...)       \
+  if ((fmt) == FP4_FMT_MXFP4) {               \
+    constexpr int FMT = FP4_FMT_MXFP4;        \
+    __VA_ARGS__;                              \
+  } else {                                    \
+    constexpr int FMT = FP4_FMT_NVFP4;        \
+    __VA_ARGS__;                              \
+  }
+
+cudaError_t launch_amax(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int rht_axis,
+                        uint32_t rht_signs, float* amax_out, int num_sms, cudaStream_t st) {
+  // rht_axis: -1 none, 1 along cols (needs cols % 16 == 0), 0 along rows (rows % 16 == 0)
+  cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (rht_axis != 0 && cols % 16 == 0) {
+    int grid = grid_for(rows * (cols / 16), kThreads, num_sms);
+    FP4_DISPATCH_DT(dt, DT,
+      if (rht_axis == 1) amax_rows_kernel<DT, true><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, rht_signs, amax_out);
+      else amax_rows_kernel<DT, false><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, rht_signs, amax_out));
+    return cudaGetLastError();
+  }
+  // transform along rows, or a plain amax of a tensor whose cols are not a
+  // multiple of 16: column items of the tiled kernel (64 x 64 tiles)
+  QuantOut none{};
+  int64_t ntiles = cdiv(rows, 64) * cdiv(cols, TC);
+  int grid = grid_for(ntiles, 1, num_sms);
+  FP4_DISPATCH_DT(dt, DT, tile_kernel<FP4_FMT_NVFP4, DT, T_AMAX_COLS><<<grid, kThreads, 0, st>>>(
+      x, rows, cols, ldx, none, none, 0, rht_signs, 0u, rht_axis == 0 ? 1 : 0, 0, amax_out, nullptr));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_dual(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx,
+                             uint32_t signs_rows, uint32_t signs_cols, bool rht_rows, bool rht_cols,
+                             float* amax_rows, float* amax_cols, int num_sms, cudaStream_t st) {
+  // amax_rows: the tensor that is blocked along cols (RHT along cols, "row items")
+  cudaError_t e = cudaMemsetAsync(amax_rows, 0, sizeof(float), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(amax_cols, 0, sizeof(float), st);
+  if (e != cudaSuccess || rows == 0 || cols == 0) return e;
+  QuantOut none{};
+  int64_t ntiles = cdiv(rows, 64) * cdiv(cols, TC);
+  int grid = grid_for(ntiles, 1, num_sms);
+  FP4_DISPATCH_DT(dt, DT, tile_kernel<FP4_FMT_NVFP4, DT, T_AMAX_DUAL><<<grid, kThreads, 0, st>>>(
+      x, rows, cols, ldx, none, none, 0, signs_cols, signs_rows, rht_cols, rht_rows, amax_cols, amax_rows));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                              const QuantOut& o, int num_sms, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  int B = fmt == FP4_FMT_MXFP4 ? 32 : 16;
+  int grid = grid_for(rows * (cols / B), kThreads, num_sms);
+  FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT,
+      quant_rows_kernel<FMT, DT><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, o)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_tile(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                              bool two_d, bool transpose, const QuantOut& o, int num_sms, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  int TRv = fmt == FP4_FMT_MXFP4 ? 128 : 64;
+  int64_t ntiles = cdiv(rows, TRv) * cdiv(cols, TC);
+  int grid = grid_for(ntiles, 1, num_sms);
+  if (transpose) {
+    FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT, tile_kernel<FMT, DT, T_Q_COLS><<<grid, kThreads, 0, st>>>(
+        x, rows, cols, ldx, o, o, two_d ? 1 : 0, o.rht_signs, 0u, o.rht, 0, nullptr, nullptr)));
+  } else {  // 2D, blocks along cols
+    FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT, tile_kernel<FMT, DT, T_Q_ROWS2D><<<grid, kThreads, 0, st>>>(
+        x, rows, cols, ldx, o, o, 1, 0u, o.rht_signs, 0, o.rht, nullptr, nullptr)));
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_dual(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                              const QuantOut& orow, const QuantOut& ocol, int num_sms, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  int TRv = fmt == FP4_FMT_MXFP4 ? 128 : 64;
+  int64_t ntiles = cdiv(rows, TRv) * cdiv(cols, TC);
+  int grid = grid_for(ntiles, 1, num_sms);
+  FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT, tile_kernel<FMT, DT, T_Q_DUAL><<<grid, kThreads, 0, st>>>(
+      x, rows, cols, ldx, ocol, orow, 0, ocol.rht_signs, orow.rht_signs, ocol.rht, orow.rht, nullptr, nullptr)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const fp4_operand& q, int out_dt, void* out, int64_t ldo, int num_sms,
+                           cudaStream_t st) {
+  int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
+  int64_t total = q.rows * (q.k / B);
+  if (total == 0) return cudaSuccess;
+  int grid = grid_for(total, kThreads, num_sms);
+  FP4_DISPATCH_FMT(q.format, FMT,
+    if (out_dt == FP4_DTYPE_F32) dequant_kernel<FMT, FP4_DTYPE_F32><<<grid, kThreads, 0, st>>>(q, out, ldo);
+    else dequant_kernel<FMT, FP4_DTYPE_BF16><<<grid, kThreads, 0, st>>>(q, out, ldo));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rht16(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int axis,
+                         uint32_t signs, float* y, int num_sms, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  if (axis == 1) {
+    int grid = grid_for(rows * (cols / 16), kThreads, num_sms);
+    FP4_DISPATCH_DT(dt, DT, rht_rows_kernel<DT><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, signs, y));
+  } else {
+    int grid = grid_for((rows / 16) * cols, kThreads, num_sms);
+    FP4_DISPATCH_DT(dt, DT, rht_cols_kernel<DT><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, signs, y));
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dge(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
+                       int64_t lddy, float* dx, int64_t lddx, float k, float clamp, float outside,
+                       int num_sms, cudaStream_t st) {
+  int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
+  int64_t total = q.rows * (q.k / B);
+  if (total == 0) return cudaSuccess;
+  int grid = grid_for(total, kThreads, num_sms);
+  float inv_k = 1.0f / k, expo = 1.0f / k - 1.0f;
+  FP4_DISPATCH_FMT(q.format, FMT, FP4_DISPATCH_DT(xdt, XDT,
+    if (dydt == FP4_DTYPE_BF16)
+      dge_kernel<FMT, XDT, FP4_DTYPE_BF16><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo, clamp, outside);
+    else
+      dge_kernel<FMT, XDT, FP4_DTYPE_F32><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo, clamp, outside)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_e2m1(const float* xs, uint8_t* codes, int64_t n, int method, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  int grid = (int)std::min<int64_t>(cdiv(n, kThreads), 4096);
+  encode_e2m1_kernel<<<grid, kThreads, 0, st>>>(xs, codes, n, method);
+  return cudaGetLastError();
+}
+cudaError_t launch_encode_e4m3(const float* t, uint8_t* out, int64_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  int grid = (int)std::min<int64_t>(cdiv(n, kThreads), 4096);
+  encode_e4m3_kernel<<<grid, kThreads, 0, st>>>(t, out, n);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4

@@ -1,0 +1,232 @@
+/*
+ * fp4.h -- C ABI of the GB300 (sm_103a) block-scaled FP4 library.
+ *
+ * The library quantizes bf16/fp32 tensors to E2M1 FP4 with a shared per-block
+ * scale and runs the block-scaled GEMMs that consume them, following these
+ * pages on FP4 LLM training (cited by short name):
+ *
+ *   [grad]    aicoding.csdn.net "深度学习中的梯度计算基础": Q(x) = s*round(x/s)
+ *             (§2.1), the straight-through estimator (§3.1), block size (§4.2)
+ *   [lowprec] framerc.cn "低精度训练技术概述": E4M3 / E8M0 / MXFP4 / NVFP4
+ *             (§1.1), stochastic rounding (§1.2, §3.2), the unsupported-format
+ *             error of the quantize_to_fp4 snippet (§3.2)
+ *   [outlier] devpress.csdn.net "大模型4位训练中的异常值动态分析与优化实践":
+ *             E2M1 range (§1.1), hot-channel compensation (§3.1-3.2), forward
+ *             RTN + 1D scaling / backward SR + 16x16 2D scaling + RHT (§4.1-4.2)
+ *   [msr]     lsdiaocha.cn write-up of the MSR FP4 training paper: E2M1 (§一),
+ *             the differentiable gradient estimator and its 3.0 clamp (§二),
+ *             GEMMs are >95% of the compute (§四), the FP4 LUT kernel (§六)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All pointers named x, codes, scales, out, ... are DEVICE pointers owned by
+ *    the caller.  The library allocates only the context (fp4_create).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  The return value reports argument validation and
+ *    launch errors synchronously; FP4_OK means the work was enqueued.
+ *  - A device-side wait that gives up (see FP4_ERR_TIMEOUT) sets a status word
+ *    in the context; fp4_sync_status() reports and clears it.
+ *  - A context serves one stream at a time (it holds scratch used by NVFP4
+ *    quantization).  Use one context per concurrently used stream.
+ *  - Tensors are row-major.  `ld*` arguments are row pitches in elements.
+ *  - Codes: uint8 [rows][k/2]; element 2j in the low nibble, 2j+1 in the high
+ *    nibble; 4-bit E2M1 code = sign<<3 | exponent<<1 | mantissa.
+ *  - Scales: one byte per block of `block` consecutive elements along k:
+ *    MXFP4 = E8M0 exponent byte (scale 2^(byte-127)), block 32;
+ *    NVFP4 = E4M3 byte, block 16, times the fp32 per-tensor scale g.
+ *    Layout FP4_SF_ROWMAJOR: [rows][k/block].
+ *    Layout FP4_SF_MMA (what fp4_gemm reads): rows padded to 128 and k padded
+ *    to 256 elements; 512-byte atoms of 128 rows x 4 scales, atom (rt, kt) at
+ *    byte ((rt * (kpad/block/4)) + kt) * 512, element (r, j) inside the atom
+ *    at (r % 32) * 16 + ((r / 32) % 4) * 4 + (j % 4).  Padding bytes are 0.
+ */
+#ifndef FP4_GB300_H
+#define FP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+enum {
+  FP4_OK = 0,
+  FP4_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad enum value        */
+  FP4_ERR_UNSUPPORTED = 2,  /* format/block/mode combination not supported
+                               (the "Unsupported format" error of [lowprec]
+                               §3.2's quantize_to_fp4)                         */
+  FP4_ERR_MISALIGNED = 3,   /* pointer or pitch not 16-byte aligned           */
+  FP4_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed              */
+  FP4_ERR_TIMEOUT = 5       /* a device-side wait gave up (bounded wait)       */
+};
+
+/* ---- enums --------------------------------------------------------------- */
+enum { FP4_FMT_MXFP4 = 0, FP4_FMT_NVFP4 = 1 };           /* [lowprec] §1.1 */
+enum { FP4_ROUND_RTN = 0, FP4_ROUND_SR = 1 };            /* [outlier] §4.1 */
+enum { FP4_SCALING_1D = 0, FP4_SCALING_2D = 1 };         /* [outlier] §4.1 */
+enum { FP4_SF_ROWMAJOR = 0, FP4_SF_MMA = 1 };
+enum { FP4_DTYPE_BF16 = 0, FP4_DTYPE_F32 = 1 };
+enum { FP4_HCP_SINGLE = 0, FP4_HCP_TWO = 1 };            /* [outlier] §3.1 */
+
+typedef struct fp4_ctx fp4_ctx;
+
+/* Quantization parameters: Q(x) = s * round(x / s)  ([grad] §2.1).
+ *  format    FP4_FMT_MXFP4 (block must be 32) or FP4_FMT_NVFP4 (block 16);
+ *            any other pairing -> FP4_ERR_UNSUPPORTED.
+ *  rounding  RTN (ties to even) or SR (Philox4x32-10, 16 random bits per
+ *            element: round up iff u16 < frac * 65536).
+ *  scaling   1D (one scale per `block` elements along the blocked axis) or
+ *            2D (one scale per 16x16 tile; NVFP4 only; the scale is repeated
+ *            for each of the tile's 16 output rows).
+ *  transpose 0: blocks along cols, output [rows][cols/2];
+ *            1: blocks along rows, output [cols][rows/2] (the operand layout
+ *            of dgrad/wgrad).
+ *  rht       1: apply the 16-point random Hadamard transform along the
+ *            blocked axis before quantizing ([outlier] §4.1).
+ *  SR random bits: element at linear output index i uses Philox call
+ *  n = sr_offset + i/8 with counter (n lo, n hi, 0, sr_stream) and key
+ *  (sr_seed lo, sr_seed hi), 16-bit lane i % 8.
+ *  RHT signs: bit j of word 0 of Philox(counter 0, key rht_seed) set -> -1. */
+typedef struct {
+  int32_t format;
+  int32_t block;
+  int32_t rounding;
+  int32_t scaling;
+  int32_t transpose;
+  int32_t rht;
+  int32_t sf_layout;
+  uint32_t sr_stream;
+  uint64_t sr_seed;
+  uint64_t sr_offset;
+  uint64_t rht_seed;
+} fp4_quant_params;
+
+/* A quantized GEMM operand: `rows` x `k` FP4 values, blocks along k. */
+typedef struct {
+  const uint8_t* codes;        /* [rows][k/2]                                  */
+  const uint8_t* scales;       /* layout `sf_layout`                           */
+  const float* tensor_scale;   /* NVFP4: device fp32 g; MXFP4: NULL            */
+  int32_t format;
+  int32_t sf_layout;
+  int64_t rows;
+  int64_t k;
+} fp4_operand;
+
+/* ---- context --------------------------------------------------------------
+ * fp4_create allocates a small device scratch (status word, amax slots) on the
+ * current device.  Returns FP4_ERR_CUDA if no device is usable.               */
+int fp4_create(fp4_ctx** out);
+void fp4_destroy(fp4_ctx* ctx);
+/* Synchronize `stream`, then read and clear the context's device status word.
+ * Returns FP4_ERR_TIMEOUT if any kernel of this context gave up a wait.      */
+int fp4_sync_status(fp4_ctx* ctx, void* stream);
+const char* fp4_status_string(int status);
+
+/* Bytes of the scale buffer for a rows x k operand in the given layout. */
+size_t fp4_scales_bytes(int64_t rows, int64_t k, int32_t format, int32_t sf_layout);
+
+/* ---- per-tensor amax ([lowprec] §1.1 "tensor scaling"; NVFP4's fp32 level)
+ * *amax_out = max |x| over a rows x cols tensor, after an optional RHT16
+ * along `rht_axis` (-1 none, 1 along cols, 0 along rows).  Overwrites
+ * *amax_out (device fp32).  Exposed so that a caller can reduce the amax over
+ * shards and pass it back as `given_amax`.                                   */
+int fp4_amax(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+             int64_t ldx, int32_t rht_axis, uint64_t rht_seed, float* amax_out, void* stream);
+
+/* ---- quantize ([grad] §2.1; [lowprec] §1.1-1.2, §3.2; [outlier] §4.1-4.2;
+ *      [msr] §六 "maps any float to the nearest of the 16 FP4 values")
+ * x: rows x cols, dtype bf16 or fp32, pitch ldx, 16-byte aligned rows.
+ * NVFP4: g = amax/2688 (6 * 448) with amax = *given_amax if non-NULL else the
+ * tensor's own amax (after the RHT, if any); g is written to *tensor_scale.
+ * Block scale sb = E4M3_rn_satfinite(amax_b / (6 g)); s = dec(sb) * g;
+ * codes = E2M1(x * (1/s)), all zero when s == 0.
+ * MXFP4: scale 2^e, e = floor(log2 amax_b) - 2 clamped to [-127, 127];
+ * tensor_scale may be NULL.
+ * Requirements: blocked extent % block == 0 (and % 16 with rht or 2D).    */
+int fp4_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+                 int64_t ldx, const fp4_quant_params* params, const float* given_amax,
+                 uint8_t* codes, uint8_t* scales, float* tensor_scale, void* stream);
+
+/* Both operand layouts of one tensor from a single read (the dY of a linear
+ * layer feeds dgrad with blocks along cols and wgrad with blocks along rows).
+ * p_rows must have transpose 0, p_cols transpose 1; both 1D scaling.       */
+int fp4_quantize_dual(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+                      int64_t ldx, const fp4_quant_params* p_rows, const fp4_quant_params* p_cols,
+                      const float* given_amax_rows, const float* given_amax_cols,
+                      uint8_t* codes_rows, uint8_t* scales_rows, float* tensor_scale_rows,
+                      uint8_t* codes_cols, uint8_t* scales_cols, float* tensor_scale_cols,
+                      void* stream);
+
+/* ---- dequantize ([grad] §2.1 x_hat = s * code value)
+ * out[r][j] = cv * 2^e (MXFP4) or fp32(fp32(cv * dec(sb)) * g) (NVFP4), stored
+ * as fp32 or bf16 (round to nearest even), pitch ldo.                        */
+int fp4_dequantize(fp4_ctx* ctx, const fp4_operand* q, int32_t out_dtype, void* out,
+                   int64_t ldo, void* stream);
+
+/* ---- 16-point random Hadamard transform ([outlier] §4.1)
+ * y = 1/4 H16 diag(sigma) x on consecutive 16-element chunks along `axis`
+ * (1: along cols, 0: along rows); fp32 butterfly, strides 1,2,4,8.  y is fp32
+ * with pitch cols.                                                            */
+int fp4_rht16(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
+              int64_t ldx, int32_t axis, uint64_t seed, float* y, void* stream);
+
+/* ---- differentiable gradient estimator backward ([msr] §二)
+ * dx = dy * f'(x/s), f'(xs) = min(clamp, (1/k)|u|^(1/k-1)) with u the local
+ * coordinate of |xs| inside its E2M1 interval (u = 0 -> clamp); |xs| >= 6 ->
+ * `outside` (1 = straight-through, [grad] §3.1).  x/s is formed exactly as the
+ * quantizer formed it from the stored scales `q` (q->codes unused, may be
+ * NULL; blocks along cols, no RHT).  dy bf16 or fp32; dx fp32.             */
+int fp4_dge_backward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx,
+                     const fp4_operand* q, const void* dy, int32_t dy_dtype, int64_t lddy,
+                     float* dx, int64_t lddx, float k, float clamp, float outside, void* stream);
+
+/* ---- block-scaled FP4 GEMM ([msr] §四: the GEMMs are >95% of the compute)
+ * C[M,N] = alpha * sum_k A[m,k] * B[n,k]  (TN: both operands K-major), FP32
+ * accumulation on tcgen05 tensor cores, alpha = gA * gB (NVFP4) or 1 (MXFP4).
+ * accumulate = 1: C += result.  out_dtype bf16 or fp32, pitch ldc.
+ * Requirements: A and B same format, sf_layout FP4_SF_MMA, k % 32 == 0,
+ * code and output pointers 16-byte aligned, ldc*size % 16 == 0.             */
+int fp4_gemm(fp4_ctx* ctx, const fp4_operand* A, const fp4_operand* B, int32_t out_dtype,
+             void* C, int64_t ldc, int32_t accumulate, void* stream);
+
+/* ---- hot-channel compensation ([outlier] §3.1-3.2, §4.1)
+ * fp4_hcp_select: e_c = sum_m (X[m,c] - X_hat[m,c])^2 over the M rows of the
+ * bf16 activation X (pitch ldx) and its quantization xq (blocks along K);
+ * writes the k_hot channels with the largest e_c, ascending, to hot_idx
+ * (device int32[k_hot]); ties go to the lower index.  Caller workspace of
+ * fp4_hcp_select_workspace_bytes(K) bytes.                                  */
+size_t fp4_hcp_select_workspace_bytes(int64_t k);
+int fp4_hcp_select(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const fp4_operand* xq,
+                   int32_t k_hot, int32_t* hot_idx, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/* fp4_hcp_gemm: Y = alpha * (X_hat W_hat^T + A_ext B_ext^T) with bf16 extra K
+ * columns on the hot channels H (order 2, "S-O2-B"):
+ *   A_ext = [X - X_hat | X]_H,  B_ext = [W_hat | W - W_hat]_H / alpha
+ * (order 1 = the page's literal concat: A_ext = X_H, B_ext = (W - W_hat)_H / alpha).
+ * mode FP4_HCP_SINGLE: one kernel, FP4 K-steps then bf16 K-steps into one
+ * TMEM accumulator; FP4_HCP_TWO: the FP4 GEMM, then a bf16 GEMM with C +=.
+ * X (M x K) and W (N x K) bf16 with pitches ldx, ldw; xq, wq their
+ * quantizations (FP4_SF_MMA).  Workspace: fp4_hcp_workspace_bytes().       */
+size_t fp4_hcp_workspace_bytes(int64_t m, int64_t n, int32_t k_hot, int32_t order);
+int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf16, int64_t ldw,
+                 const fp4_operand* xq, const fp4_operand* wq, const int32_t* hot_idx,
+                 int32_t k_hot, int32_t mode, int32_t order, void* workspace, size_t ws_bytes,
+                 int32_t out_dtype, void* y, int64_t ldy, void* stream);
+
+/* ---- element encoders (the "nearest of the 16 FP4 values" step, [msr] §六)
+ * fp4_encode_e2m1: codes[i] = RTN E2M1 code of xs[i] (one code per byte).
+ *   method 0: the hardware cvt.rn.satfinite.e2m1x2 conversion;
+ *   method 1: a compare chain against the grid midpoints.
+ * fp4_encode_e4m3: out[i] = E4M3 byte of t[i], round to nearest even,
+ *   saturating at 448 (the NVFP4 block-scale encoding).                      */
+int fp4_encode_e2m1(fp4_ctx* ctx, const float* xs, uint8_t* codes, int64_t n, int32_t method,
+                    void* stream);
+int fp4_encode_e4m3(fp4_ctx* ctx, const float* t, uint8_t* out, int64_t n, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP4_GB300_H */

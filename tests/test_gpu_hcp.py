@@ -1,0 +1,92 @@
+"""GPU <-> oracle parity for hot-channel compensation, through the C ABI.
+
+Selection: the set of k_hot channels must equal the oracle's, except for
+channels whose error lies within 1e-5 (relative) of the k-th largest error
+(the GPU sums the per-channel errors in fp32 in a different order).  The
+planted x100 channels must be selected.
+GEMM (single- and two-kernel modes, orders 1 and 2): the GEMM bound with the
+oracle's bf16 residual columns.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp4_block_scaled_e8m0_gb300 as fp4
+import oracle as o
+
+pytestmark = pytest.mark.gpu
+
+FMT = {fp4.FP4_FMT_MXFP4: o.MXFP4, fp4.FP4_FMT_NVFP4: o.NVFP4}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import os
+    from fp4_block_scaled_e8m0_gb300 import build
+    if not os.path.exists(build.lib_path()):
+        build.build()
+    fp4.load_library()
+
+
+def _data(fmt, M=320, K=512, N=264, seed=1):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_t(3, (M, K)).astype(np.float32)
+    hot = np.sort(rng.permutation(K)[: max(1, K // 100)])
+    x[:, hot] *= 100
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    wt = torch.from_numpy(w).to(torch.bfloat16)
+    return xt, wt, xt.float().numpy(), wt.float().numpy(), hot
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+def test_hcp_select_matches_oracle(fmt):
+    xt, _, xn, _, planted = _data(fmt)
+    K = xn.shape[1]
+    h = fp4.hcp_num_hot(K)
+    xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
+    got = fp4.fp4_hcp_select(xt.cuda(), xq, h).cpu().numpy()
+    assert np.all(np.diff(got) > 0), "indices must be ascending and distinct"
+    c, s, g = o.quantize(xn, FMT[fmt])
+    e = o.hcp_channel_errors(xn, c, s, FMT[fmt], g)
+    want = o.hcp_select(xn, c, s, FMT[fmt], g, h)
+    kth = np.sort(e)[::-1][h - 1]
+    band = np.abs(e - kth) <= 1e-5 * kth
+    diff = set(got.tolist()) ^ set(want.tolist())
+    assert all(band[i] for i in diff), f"selection differs outside the tie band: {sorted(diff)[:10]}"
+    assert set(planted.tolist()) <= set(got.tolist())
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+@pytest.mark.parametrize("mode", [fp4.FP4_HCP_SINGLE, fp4.FP4_HCP_TWO])
+@pytest.mark.parametrize("order", [1, 2])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_hcp_gemm_matches_oracle(fmt, mode, order, out_dtype):
+    xt, wt, xn, wn, _ = _data(fmt, seed=2)
+    K = xn.shape[1]
+    h = fp4.hcp_num_hot(K)
+    xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
+    wq = fp4.fp4_quantize(wt.cuda(), fp4.quant_params(fmt))
+    cx, sx, gx = o.quantize(xn, FMT[fmt])
+    cw, sw, gw = o.quantize(wn, FMT[fmt])
+    hot = o.hcp_select(xn, cx, sx, FMT[fmt], gx, h)
+    y = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, torch.from_numpy(hot).cuda(), h, mode, order, out_dtype)
+    got = y.float().cpu().numpy().astype(np.float64)
+    yref, bound = o.hcp_gemm(xn, cx, sx, wn, cw, sw, FMT[fmt], gx, gw, hot, order)
+    tol = o.gemm_tolerance(bound, yref, out_dtype == torch.bfloat16)
+    if mode == fp4.FP4_HCP_TWO and out_dtype == torch.bfloat16:
+        tol = tol + 2.0 ** -9 * np.abs(yref)          # the base result is rounded to bf16 once more
+    err = np.abs(got - yref)
+    assert np.all(err <= tol), f"{(err > tol).sum()} outside; worst {np.max(err - tol)}"
+
+
+def test_hcp_zero_hot_is_plain_gemm():
+    xt, wt, xn, wn, _ = _data(fp4.FP4_FMT_NVFP4, seed=3)
+    xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fp4.FP4_FMT_NVFP4))
+    wq = fp4.fp4_quantize(wt.cuda(), fp4.quant_params(fp4.FP4_FMT_NVFP4))
+    y0 = fp4.fp4_gemm(xq, wq, torch.float32)
+    y1 = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, torch.zeros(1, dtype=torch.int32, device="cuda"), 0,
+                          out_dtype=torch.float32)
+    assert torch.equal(y0, y1)
