@@ -1,7 +1,7 @@
 """GPU <-> oracle parity for the tcgen05 block-scaled GEMM, through the C ABI.
 
-Bound (per element): |Y - Y_ref| <= 1e-3 * sum_k |a||b|  (+ 2^-9 |Y_ref| for a
-bf16 output), Y_ref the fp64 sum of the dequantized operands.
+Bound (per element): |Y - Y_ref| <= 1e-3 * sum_k |a||b|  (+ 2^-8 |Y_ref| for a
+bf16 output: an 8-bit significand), Y_ref the fp64 sum of the dequantized operands.
 The structured cases isolate the data path (all block scales 1), the A-side
 scales, the B-side scales and the scale index along K.
 """

@@ -77,7 +77,7 @@ def test_hcp_gemm_matches_oracle(fmt, mode, order, out_dtype):
     yref, bound = o.hcp_gemm(xn, cx, sx, wn, cw, sw, FMT[fmt], gx, gw, hot, order)
     tol = o.gemm_tolerance(bound, yref, out_dtype == torch.bfloat16)
     if mode == fp4.FP4_HCP_TWO and out_dtype == torch.bfloat16:
-        tol = tol + 2.0 ** -9 * np.abs(yref)          # the base result is rounded to bf16 once more
+        tol = tol + 2.0 ** -8 * np.abs(yref)          # the base result is rounded to bf16 once more
     err = np.abs(got - yref)
     assert np.all(err <= tol), f"{(err > tol).sum()} outside; worst {np.max(err - tol)}"
 
