@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of the block-scaled FP4 hot path on one LLaMA-1B-shaped linear layer.
+
+One step = the forward and backward pass of the MLP up-projection
+Y[M,N] = X[M,K] W[N,K]^T with M = 8192 tokens, K = 2048, N = 5632 in NVFP4:
+
+  forward   quantize X and W (RTN, 1D blocks of 16 along K, E4M3 scale x
+            per-tensor fp32 scale), fprop GEMM  Y = Xq Wq^T          (bf16 out)
+  backward  quantize dY in both layouts from one read (SR + RHT16 along N for
+            dgrad, along M for wgrad), W (SR + RHT16 + 16x16 2D blocks,
+            transposed) and X (SR + RHT16 along M, transposed);
+            dgrad GEMM dX = dYq Wq_t^T (bf16), wgrad GEMM dW = dYq_m Xq_t^T
+            (fp32); DGE backward dW' = dW * f'(W / s_W) (k = 5, clamp 3.0)
+
+Every step runs in the library's CUDA kernels through the C ABI.  Inputs are
+seeded synthetic tensors (X ~ N(0,1), W ~ N(0,0.02), dY ~ N(0,1e-3)) resident
+in HBM before the timed region; L2 is flushed (512 MiB write) before each
+timed step.  Prints one JSON line (see the keys below).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP4 quantize GB/s and block-scaled FP4 GEMM TFLOP/s, % of GB300 roofline"
+M, K, N = 8192, 2048, 5632
+GEMM_FLOPS = 2 * M * N * K          # per GEMM; three per step
+STEP_FLOPS = 3 * GEMM_FLOPS
+FP4_OVER_BF16 = 13.5 / 2.25         # nominal dense FP4 : BF16 tensor rate
+WORKLOAD = ("llama1b_mlp_up fwd+bwd: X[8192,2048] W[5632,2048] dY[8192,5632] bf16; NVFP4; fwd RTN 1D, "
+            "bwd SR + RHT16 (+16x16 2D on W); fprop/dgrad/wgrad GEMMs; DGE (k=5, clamp 3) on W")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", default="512x704", help="MxN rows of the CPU-baseline sample (K stays 2048)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes per element of each op (one read of inputs + writes)
+# ---------------------------------------------------------------------------
+NV_Q_BYTES = 2 + 0.5 + 1 / 16        # bf16 in, packed codes, one E4M3 byte per 16
+OPS = {
+    #  name           kind     units per launch (bytes or flops)
+    "quant_x":      ("hbm", M * K * NV_Q_BYTES),
+    "quant_w":      ("hbm", N * K * NV_Q_BYTES),
+    "fprop":        ("tensor", GEMM_FLOPS),
+    "quant_dy_dual": ("hbm", M * N * (2 + 2 * (0.5 + 1 / 16))),
+    "quant_w_t2d":  ("hbm", N * K * NV_Q_BYTES),
+    "quant_x_t":    ("hbm", M * K * NV_Q_BYTES),
+    "dgrad":        ("tensor", GEMM_FLOPS),
+    "wgrad":        ("tensor", GEMM_FLOPS),
+    "dge":          ("hbm", N * K * (2 + 4 + 4) + N * K / 16),
+}
+KERNELS_PER_OP = {"quant_x": 2, "quant_w": 2, "fprop": 1, "quant_dy_dual": 2, "quant_w_t2d": 2,
+                  "quant_x_t": 2, "dgrad": 1, "wgrad": 1, "dge": 1}
+
+
+class Step:
+    """Buffers and calls of one fwd+bwd step (all device-resident)."""
+
+    def __init__(self, fp4, X, W, dY, dev):
+        self.fp4 = fp4
+        self.X, self.W, self.dY = X, W, dY
+        NV, SR, T2D = fp4.FP4_FMT_NVFP4, fp4.FP4_ROUND_SR, fp4.FP4_SCALING_2D
+        self.p_fwd = fp4.quant_params(NV)
+        self.p_dy_n = fp4.quant_params(NV, SR, rht=True, sr_seed=2, sr_stream=0, rht_seed=2)
+        self.p_w_t = fp4.quant_params(NV, SR, T2D, transpose=True, rht=True, sr_seed=2, sr_stream=1, rht_seed=2)
+        self.p_dy_m = fp4.quant_params(NV, SR, transpose=True, rht=True, sr_seed=2, sr_stream=2, rht_seed=2)
+        self.p_x_t = fp4.quant_params(NV, SR, transpose=True, rht=True, sr_seed=2, sr_stream=3, rht_seed=2)
+        a = fp4.alloc_qtensor
+        self.xq = a(M, K, NV, fp4.FP4_SF_MMA, dev)
+        self.wq = a(N, K, NV, fp4.FP4_SF_MMA, dev)
+        self.dyq_n = a(M, N, NV, fp4.FP4_SF_MMA, dev)
+        self.dyq_m = a(N, M, NV, fp4.FP4_SF_MMA, dev)
+        self.wq_t = a(K, N, NV, fp4.FP4_SF_MMA, dev)
+        self.xq_t = a(K, M, NV, fp4.FP4_SF_MMA, dev)
+        self.Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        self.dW = torch.empty((N, K), dtype=torch.float32, device=dev)
+        self.dWd = torch.empty((N, K), dtype=torch.float32, device=dev)
+
+    def ops(self, step_idx: int):
+        f = self.fp4
+        off = step_idx << 40      # a fresh SR draw every step
+        for p in (self.p_dy_n, self.p_w_t, self.p_dy_m, self.p_x_t):
+            p.sr_offset = off
+        return [
+            ("quant_x", lambda: f.fp4_quantize(self.X, self.p_fwd, out=self.xq)),
+            ("quant_w", lambda: f.fp4_quantize(self.W, self.p_fwd, out=self.wq)),
+            ("fprop", lambda: f.fp4_gemm(self.xq, self.wq, out=self.Y)),
+            ("quant_dy_dual", lambda: f.fp4_quantize_dual(self.dY, self.p_dy_n, self.p_dy_m, out_rows=self.dyq_n,
+                                                          out_cols=self.dyq_m)),
+            ("quant_w_t2d", lambda: f.fp4_quantize(self.W, self.p_w_t, out=self.wq_t)),
+            ("quant_x_t", lambda: f.fp4_quantize(self.X, self.p_x_t, out=self.xq_t)),
+            ("dgrad", lambda: f.fp4_gemm(self.dyq_n, self.wq_t, out=self.dX)),
+            ("wgrad", lambda: f.fp4_gemm(self.dyq_m, self.xq_t, out=self.dW)),
+            ("dge", lambda: f.fp4_dge_backward(self.W, self.wq, self.dW, 5.0, 3.0, 1.0, out=self.dWd)),
+        ]
+
+    def run(self, step_idx: int, events=None):
+        for name, fn in self.ops(step_idx):
+            if events is not None:
+                events[name][0].record()
+            fn()
+            if events is not None:
+                events[name][1].record()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        loaded = [r for r in rows if (num(r[4]) or 0) > 0] or rows
+        sm = [num(r[1]) for r in loaded if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in loaded:
+            for name, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(loaded)}
+
+
+# ---------------------------------------------------------------------------
+# roofline denominators
+# ---------------------------------------------------------------------------
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp4_block_scaled_e8m0_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(op: str):
+    """DRAM bytes per launch of `op` from the committed ncu summary, or None when
+    the kernels changed since those counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    if d.get("source_digest") != source_digest():
+        return None
+    v = d.get("ops", {}).get(op)
+    return None if v is None else float(v)
+
+
+# ---------------------------------------------------------------------------
+# CPU legs (the oracle)
+# ---------------------------------------------------------------------------
+def oracle_step(Ms, Ns, Kk=K, seed=0):
+    """The step's arithmetic on an Ms x Kk / Ns x Kk / Ms x Ns sample, by the oracle."""
+    import oracle as o
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((Ms, Kk)).astype(np.float32)
+    W = (rng.standard_normal((Ns, Kk)) * 0.02).astype(np.float32)
+    dY = (rng.standard_normal((Ms, Ns)) * 1e-3).astype(np.float32)
+    t0 = time.perf_counter()
+    xq = o.quantize(X, o.NVFP4)
+    wq = o.quantize(W, o.NVFP4)
+    o.gemm(*xq[:2], *wq[:2], o.NVFP4, xq[2], wq[2])
+    dyn = o.quantize(dY, o.NVFP4, "sr", rht=True, sr_seed=2, sr_stream=0, rht_seed=2)
+    dym = o.quantize(dY, o.NVFP4, "sr", transpose=True, rht=True, sr_seed=2, sr_stream=2, rht_seed=2)
+    wt = o.quantize(W, o.NVFP4, "sr", "2d", True, True, sr_seed=2, sr_stream=1, rht_seed=2)
+    xt = o.quantize(X, o.NVFP4, "sr", transpose=True, rht=True, sr_seed=2, sr_stream=3, rht_seed=2)
+    o.gemm(*dyn[:2], *wt[:2], o.NVFP4, dyn[2], wt[2])
+    dw, _ = o.gemm(*dym[:2], *xt[:2], o.NVFP4, dym[2], xt[2])
+    o.dge_backward(W, wq[1], o.NVFP4, wq[2], dw)
+    return time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(sample: str):
+    Ms, Ns = (int(v) for v in sample.split("x"))
+    t = oracle_step(Ms, Ns)
+    flops = 3 * 2 * Ms * Ns * K
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"the full step on X[{Ms},{K}] W[{Ns},{K}] dY[{Ms},{Ns}] (numpy oracle; BLAS matmul may use all "
+                      f"cores, elementwise steps one core); {t:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    # each step: the oracle on a bounded sample, sized so that the run ends in minutes
+    Ms, Ns = 16, 16
+    for _ in range(args.warmup):
+        oracle_step(Ms, Ns)
+    ts = [oracle_step(Ms, Ns, seed=i) for i in range(args.steps)]
+    t = float(np.mean(ts))
+    flops = 3 * 2 * Ms * Ns * K
+    value = flops / t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64 (numpy oracle)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": f"M={Ms} N={Ns} K={K} per step"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"the full step on X[{Ms},{K}] W[{Ns},{K}] dY[{Ms},{Ns}] per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# multi-rank aggregation (replicas: each rank runs the whole step on its own
+# data; the job's step time is the slowest rank's)
+# ---------------------------------------------------------------------------
+def reduce_step_time(t_local: float, dist, device) -> float:
+    if dist is None:
+        return t_local
+    t = torch.tensor([t_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, t_step: float) -> float:
+    """Whole-job TFLOP/s: every rank processes one step's GEMM flops per t_step."""
+    return world * STEP_FLOPS / t_step / 1e12
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import fp4_block_scaled_e8m0_gb300 as fp4
+    from fp4_block_scaled_e8m0_gb300 import build as fbuild
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    if not os.path.exists(fbuild.lib_path()):
+        if rank == 0:
+            fbuild.build()
+        if dist:
+            dist.barrier()
+    fp4.load_library()
+
+    data = inputs.llama1b_mlp_up()
+    host = {k: data[k].pin_memory() for k in ("X", "W", "dY")}
+    X, W, dY = (host[k].to(dev) for k in ("X", "W", "dY"))
+    step = Step(fp4, X, W, dY, dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        step.run(i)
+    torch.cuda.synchronize()
+
+    names = list(OPS)
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev_ops = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
+              for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)                    # L2 flush, outside the step's events
+        ev_step[i][0].record(stream)
+        step.run(args.warmup + i, ev_ops[i])
+        ev_step[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    step_s = np.array([a.elapsed_time(b) * 1e-3 for a, b in ev_step])
+    op_s = {n: float(np.mean([e[n][0].elapsed_time(e[n][1]) * 1e-3 for e in ev_ops])) for n in names}
+    t_step = reduce_step_time(float(step_s.mean()), dist, dev)
+    status = fp4.fp4_sync_status()
+
+    # ---- end to end through the C ABI with host buffers --------------------------
+    h_out = {"Y": torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
+             "dX": torch.empty((M, K), dtype=torch.bfloat16).pin_memory(),
+             "dW": torch.empty((N, K), dtype=torch.float32).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    e2e = []
+    for i in range(args.e2e_steps):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        X.copy_(host["X"], non_blocking=True)
+        W.copy_(host["W"], non_blocking=True)
+        dY.copy_(host["dY"], non_blocking=True)
+        step.run(10_000 + i)
+        h_out["Y"].copy_(step.Y, non_blocking=True)
+        h_out["dX"].copy_(step.dX, non_blocking=True)
+        h_out["dW"].copy_(step.dWd, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        e2e.append(a.elapsed_time(b) * 1e-3)
+    t_e2e = float(np.mean(e2e)) if e2e else float("nan")
+
+    # ---- roofline of the dominant kernel --------------------------------------------
+    pk = peaks()
+    dom = max(names, key=lambda n: op_s[n])
+    kind, units = OPS[dom]
+    if kind == "tensor":
+        peak = pk["bf16_tflops_sustained"] * FP4_OVER_BF16
+        achieved = units / op_s[dom] / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{pk['source']} bf16 sustained x {FP4_OVER_BF16:g} (nominal FP4:BF16)"}
+    else:
+        peak = pk["hbm_gbs"]
+        achieved = units / op_s[dom] / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{pk['source']} HBM copy"}
+    roof["kernel"] = dom
+    traffic = measured_traffic(dom)
+    roof["traffic"] = traffic
+
+    breakdown = {}
+    for n in names:
+        k_, u = OPS[n]
+        rate = u / op_s[n] / (1e12 if k_ == "tensor" else 1e9)
+        pkv = pk["bf16_tflops_sustained"] * FP4_OVER_BF16 if k_ == "tensor" else pk["hbm_gbs"]
+        breakdown[n] = {"us": op_s[n] * 1e6, "rate": rate, "unit": "TFLOP/s" if k_ == "tensor" else "GB/s",
+                        "frac": rate / pkv}
+    q_names = [n for n in names if OPS[n][0] == "hbm" and n.startswith("quant")]
+    q_bytes = sum(OPS[n][1] for n in q_names)
+    q_time = sum(op_s[n] for n in q_names)
+    g_time = sum(op_s[n] for n in names if OPS[n][0] == "tensor")
+
+    value = job_value(world, t_step)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e4m3 block scale x fp32 tensor scale), fp32 accumulate",
+        "data": "synthetic (seeded numpy: X~N(0,1), W~N(0,0.02), dY~N(0,1e-3))",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "parallelism": "replicas" if world > 1 else "1 gpu",
+                   "l2": "flushed before each timed step (512 MiB write)"},
+        "quantize_gbs": q_bytes / q_time / 1e9, "gemm_tflops": 3 * GEMM_FLOPS / g_time / 1e12,
+        "step_roofline_frac": (sum(OPS[n][1] / (pk['bf16_tflops_sustained'] * FP4_OVER_BF16 * 1e12)
+                                   if OPS[n][0] == "tensor" else OPS[n][1] / (pk['hbm_gbs'] * 1e9) for n in names)
+                               / t_step),
+        "ops": breakdown, "roofline": roof, "clocks": clk,
+        "e2e": {"value": world * STEP_FLOPS / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
+        "gpu_launches": sum(KERNELS_PER_OP.values()) * args.steps, "wall_s_timed_region": wall,
+        "device_status": status,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_sample)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -80,27 +80,18 @@ __device__ __forceinline__ uint32_t e2m1_sw(float xs) {
 
 // Stochastic rounding onto the grid: lo = largest grid point <= |xs| (saturated
 // at 6), frac = (|xs| - lo) / step, round up iff u16 < frac * 65536 ([lowprec]
-// §3.2's floor(x) + (rand < frac) on the non-uniform grid).
+// §3.2's floor(x) + (rand < frac) on the non-uniform grid).  Branch-free: the
+// grid step is 2^(e-1) with e = [|xs| >= 2] + [|xs| >= 4], so t = |xs| / step is
+// exact, lo's code is 2e + floor(t) and frac = t - floor(t) (both exact).
 __device__ __forceinline__ uint32_t e2m1_sr(float xs, uint32_t u16) {
-  float a = fminf(fabsf(xs), 6.0f);
-  uint32_t lo_code;
-  float lo, inv_step;
-  if (a < 2.0f) {
-    lo_code = (uint32_t)__fmul_rn(a, 2.0f);           // exact, truncation = floor
-    lo = __fmul_rn((float)lo_code, 0.5f);
-    inv_step = 2.0f;
-  } else if (a < 4.0f) {
-    float f = floorf(a);
-    lo_code = 2u + (uint32_t)f;                       // 2 -> 4, 3 -> 5
-    lo = f;
-    inv_step = 1.0f;
-  } else {
-    lo_code = (a < 6.0f) ? 6u : 7u;
-    lo = 4.0f;
-    inv_step = 0.5f;
-  }
-  float frac = __fmul_rn(__fsub_rn(a, lo), inv_step);  // exact
-  bool up = (lo_code < 7u) && ((float)u16 < __fmul_rn(frac, 65536.0f));
+  const float a = fminf(fabsf(xs), 6.0f);
+  const uint32_t e = (a >= 2.0f) + (a >= 4.0f);
+  const float inv_step = __uint_as_float((128u - e) << 23);  // 2, 1, 0.5
+  const float t = __fmul_rn(a, inv_step);
+  const float f = floorf(t);
+  const uint32_t lo_code = 2u * e + (uint32_t)f;
+  const float frac = __fsub_rn(t, f);
+  const bool up = (lo_code < 7u) && ((float)u16 < __fmul_rn(frac, 65536.0f));
   return ((__float_as_uint(xs) >> 28) & 8u) | (lo_code + (up ? 1u : 0u));
 }
 
@@ -170,9 +161,9 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
       k0 += 0x9E3779B9u;
       k1 += 0xBB67AE85u;
     }
-    uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;   // one wide multiply each
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
   }
   return c;
 }

@@ -345,25 +345,16 @@ __global__ void __launch_bounds__(kThreads) rht_cols_kernel(const void* __restri
 // DGE backward ([msr] §二): dx = dy * min(clamp, (1/k)|u|^(1/k-1)), one thread
 // per block of x (blocks along cols)
 // ----------------------------------------------------------------------------
+// Branch-free: with step 2^(e-1), e = [a >= 2] + [a >= 4], t = a / step is exact
+// and u = 2 (t - floor(t)) - 1 is the local coordinate.  powf(0, negative) is
+// +inf, so u = 0 lands on the clamp without a special case.
 __device__ __forceinline__ float dge_fprime(float xs, float inv_k, float expo, float clamp, float outside) {
-  float a = fabsf(xs);
-  if (a >= 6.0f) return outside;
-  float lo, two_over_d;
-  if (a < 2.0f) {
-    lo = __fmul_rn(floorf(__fmul_rn(a, 2.0f)), 0.5f);
-    two_over_d = 4.0f;
-  } else if (a < 4.0f) {
-    lo = floorf(a);
-    two_over_d = 2.0f;
-  } else {
-    lo = 4.0f;
-    two_over_d = 1.0f;
-  }
-  float u = __fsub_rn(__fmul_rn(__fsub_rn(a, lo), two_over_d), 1.0f);
-  float au = fabsf(u);
-  if (au == 0.0f) return clamp;
-  float f = __fmul_rn(inv_k, powf(au, expo));
-  return fminf(clamp, f);
+  const float a = fabsf(xs);
+  const uint32_t e = (a >= 2.0f) + (a >= 4.0f);
+  const float t = __fmul_rn(a, __uint_as_float((128u - e) << 23));
+  const float u = __fsub_rn(__fmul_rn(__fsub_rn(t, floorf(t)), 2.0f), 1.0f);
+  const float f = fminf(clamp, __fmul_rn(inv_k, powf(fabsf(u), expo)));
+  return a >= 6.0f ? outside : f;
 }
 
 template <int FMT, int XDT, int DYDT>

@@ -1,0 +1,221 @@
+"""Parity at the benchmark workloads' full sizes, in the launch configuration the
+benchmark times.  Quantized tensors are checked bit for bit on sampled row
+blocks (the oracle quantizes those rows with the tensor's full amax); GEMM
+outputs on sampled rows (all columns), computed by the oracle one row at a time.
+
+Workloads: the small linear fprop (X 256x512, W 512x512, MXFP4), the NVFP4
+4096x4096 tensor with outlier columns (RTN, SR, DGE), the LLaMA-1B MLP
+up-projection fwd+bwd (NVFP4, SR + RHT + 2D backward), the 7B FFN GEMMs in MXFP4
+and the hot-channel-compensated NVFP4 GEMM.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp4_block_scaled_e8m0_gb300 as fp4
+import oracle as o
+from _util import mismatch_report, untile_scales
+
+pytestmark = pytest.mark.gpu
+NV, MX = fp4.FP4_FMT_NVFP4, fp4.FP4_FMT_MXFP4
+OF = {MX: o.MXFP4, NV: o.NVFP4}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import os
+    from fp4_block_scaled_e8m0_gb300 import build
+    if not os.path.exists(build.lib_path()):
+        build.build()
+    fp4.load_library()
+
+
+def _sample_rows(n, count, seed):
+    rng = np.random.default_rng(seed)
+    idx = np.concatenate([[0, n - 1], rng.choice(n, size=min(count, n), replace=False)])
+    return np.unique(idx)
+
+
+def _check_quant_rows(x_np, q: fp4.QTensor, params_oracle, rows_out, label):
+    """Compare output rows `rows_out` of q with the oracle run on the matching
+    slice (the output layout's rows; for a transposed output these are input
+    columns).  NVFP4 uses the full tensor's amax (after any RHT)."""
+    fmt = OF[q.fmt]
+    transpose = params_oracle.get("transpose", False)
+    rht = params_oracle.get("rht", False)
+    w = x_np.T if transpose else x_np
+    given = None
+    if q.fmt == NV:
+        ww = o.rht16(np.ascontiguousarray(w), 1, params_oracle.get("rht_seed", 0)) if rht else w
+        given = o.tensor_amax(ww)
+    codes = q.codes.cpu().numpy()
+    nsf = q.k // fp4.BLOCK[q.fmt]
+    scales = untile_scales(q.scales.cpu().numpy(), q.rows, nsf)
+    two_d = params_oracle.get("scaling") == "2d"
+    # whole 16-row groups for 2D scaling (one scale per 16x16 tile)
+    if two_d:
+        rows_out = np.unique(np.concatenate([np.arange(r - r % 16, r - r % 16 + 16) for r in rows_out]))
+    kw = {k: v for k, v in params_oracle.items() if k not in ("transpose",)}
+    # the SR counter of output element (r, c) is r * cols + c: a one-row slice
+    # starts its indices at 0, so its offset is shifted by r * cols / 8
+    want_c, want_s, want_g = [], [], None
+    for r in rows_out:
+        if two_d:
+            continue
+        c, s, g = o.quantize(w[r:r + 1], fmt, **{**kw, "given_amax": given,
+                                                 "sr_offset": kw.get("sr_offset", 0) + (r * w.shape[1]) // 8})
+        want_c.append(c[0])
+        want_s.append(s[0])
+        want_g = g
+    if two_d:
+        for g0 in range(0, len(rows_out), 16):
+            rr = rows_out[g0:g0 + 16]
+            c, s, g = o.quantize(w[rr[0]:rr[0] + 16], fmt, **{**kw, "given_amax": given,
+                                                             "sr_offset": kw.get("sr_offset", 0) + (rr[0] * w.shape[1]) // 8})
+            want_c.extend(c)
+            want_s.extend(s)
+            want_g = g
+    want_c = np.array(want_c)
+    want_s = np.array(want_s)
+    assert np.array_equal(scales[rows_out], want_s), mismatch_report(scales[rows_out], want_s, label + " scales")
+    assert np.array_equal(codes[rows_out], want_c), mismatch_report(codes[rows_out], want_c, label + " codes")
+    if want_g is not None:
+        got_g = q.tensor_scale.cpu().numpy()[0]
+        assert np.float32(got_g).view(np.uint32) == np.float32(want_g).view(np.uint32)
+
+
+def _check_gemm_rows(qa, qb, y, rows, fmt, out_bf16, label):
+    ca = qa.codes.cpu().numpy()
+    cb = qb.codes.cpu().numpy()
+    sa = untile_scales(qa.scales.cpu().numpy(), qa.rows, qa.k // fp4.BLOCK[fmt])
+    sb = untile_scales(qb.scales.cpu().numpy(), qb.rows, qb.k // fp4.BLOCK[fmt])
+    ga = qa.tensor_scale.cpu().numpy()[0] if qa.tensor_scale is not None else None
+    gb = qb.tensor_scale.cpu().numpy()[0] if qb.tensor_scale is not None else None
+    yr, bound = o.gemm(ca[rows], sa[rows], cb, sb, OF[fmt], ga, gb)
+    got = y[rows].float().cpu().numpy().astype(np.float64)
+    tol = o.gemm_tolerance(bound, yr, out_bf16)
+    bad = np.abs(got - yr) > tol
+    assert not bad.any(), f"{label}: {bad.sum()} of {bad.size} sampled outputs outside the bound"
+
+
+def test_linear_fprop_small_full():
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    d = inputs.linear_fprop_small()
+    x, w = d["X"], d["W"]
+    qx = fp4.fp4_quantize(x.cuda(), fp4.quant_params(MX))
+    qw = fp4.fp4_quantize(w.cuda(), fp4.quant_params(MX))
+    y = fp4.fp4_gemm(qx, qw, torch.float32)
+    cx, sx, _ = o.quantize(x.float().numpy(), o.MXFP4)
+    cw, sw, _ = o.quantize(w.float().numpy(), o.MXFP4)
+    assert np.array_equal(qx.codes.cpu().numpy(), cx) and np.array_equal(qw.codes.cpu().numpy(), cw)
+    yr, bound = o.gemm(cx, sx, cw, sw, o.MXFP4)
+    assert np.all(np.abs(y.cpu().numpy() - yr) <= 1e-3 * bound)
+
+
+def test_nvfp4_square_quantize_sr_dge():
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    d = inputs.nvfp4_square()
+    t, dy = d["T"], d["dy"]
+    tn = t.float().numpy()
+    rows = _sample_rows(4096, 24, 1)
+    for rnd, name in ((fp4.FP4_ROUND_RTN, "rtn"), (fp4.FP4_ROUND_SR, "sr")):
+        q = fp4.fp4_quantize(t.cuda(), fp4.quant_params(NV, rnd, sr_seed=1))
+        _check_quant_rows(tn, q, {"rounding": name, "sr_seed": 1}, rows, f"nvfp4 4096^2 {name}")
+    # dequantize and DGE on the sampled rows
+    q = fp4.fp4_quantize(t.cuda(), fp4.quant_params(NV))
+    deq = fp4.fp4_dequantize(q, torch.float32).cpu().numpy()
+    dx = fp4.fp4_dge_backward(t.cuda(), q, dy.cuda(), 5.0, 3.0).cpu().numpy()
+    g = q.tensor_scale.cpu().numpy()[0]
+    sc = untile_scales(q.scales.cpu().numpy(), 4096, 256)
+    codes = q.codes.cpu().numpy()
+    want = o.dequantize(codes[rows], sc[rows], o.NVFP4, g)
+    assert np.array_equal(deq[rows].view(np.uint32), want.view(np.uint32))
+    wdx = o.dge_backward(tn[rows], sc[rows], o.NVFP4, g, dy.float().numpy()[rows], 5.0, 3.0)
+    assert np.all(np.abs(dx[rows] - wdx) <= 1e-6 * np.abs(wdx))
+
+
+def test_llama1b_mlp_up_step():
+    """The benchmark's step, op for op, checked on sampled rows."""
+    import bench
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    d = inputs.llama1b_mlp_up()
+    X, W, dY = (d[k].cuda() for k in ("X", "W", "dY"))
+    step = bench.Step(fp4, X, W, dY, torch.device("cuda"))
+    step.run(0)
+    torch.cuda.synchronize()
+    xn, wn, dyn = (d[k].float().numpy() for k in ("X", "W", "dY"))
+    off = 0                                      # step 0: sr_offset = 0
+    r_m = _sample_rows(bench.M, 6, 2)
+    r_n = _sample_rows(bench.N, 6, 3)
+    r_k = _sample_rows(bench.K, 6, 4)
+    _check_quant_rows(xn, step.xq, {}, r_m, "fwd X")
+    _check_quant_rows(wn, step.wq, {}, r_n, "fwd W")
+    _check_quant_rows(dyn, step.dyq_n, {"rounding": "sr", "rht": True, "sr_seed": 2, "sr_stream": 0, "rht_seed": 2,
+                                        "sr_offset": off}, r_m, "dY rows")
+    _check_quant_rows(dyn, step.dyq_m, {"rounding": "sr", "rht": True, "sr_seed": 2, "sr_stream": 2, "rht_seed": 2,
+                                        "sr_offset": off, "transpose": True}, r_n, "dY cols")
+    _check_quant_rows(wn, step.wq_t, {"rounding": "sr", "rht": True, "sr_seed": 2, "sr_stream": 1, "rht_seed": 2,
+                                      "sr_offset": off, "transpose": True, "scaling": "2d"}, r_k, "W 2d t")
+    _check_quant_rows(xn, step.xq_t, {"rounding": "sr", "rht": True, "sr_seed": 2, "sr_stream": 3, "rht_seed": 2,
+                                      "sr_offset": off, "transpose": True}, r_k, "X t")
+    _check_gemm_rows(step.xq, step.wq, step.Y, r_m, NV, True, "fprop")
+    _check_gemm_rows(step.dyq_n, step.wq_t, step.dX, r_m, NV, True, "dgrad")
+    _check_gemm_rows(step.dyq_m, step.xq_t, step.dW, r_n, NV, False, "wgrad")
+    # DGE on the sampled rows of W
+    sc = untile_scales(step.wq.scales.cpu().numpy(), bench.N, bench.K // 16)
+    g = step.wq.tensor_scale.cpu().numpy()[0]
+    dw = step.dW.cpu().numpy()
+    want = o.dge_backward(wn[r_n], sc[r_n], o.NVFP4, g, dw[r_n], 5.0, 3.0)
+    got = step.dWd.cpu().numpy()[r_n]
+    assert np.all(np.abs(got - want) <= 1e-6 * np.abs(want))
+
+
+def test_ffn7b_gemms_mxfp4():
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    d = inputs.ffn7b()
+    X, W, dY = (d[k].cuda() for k in ("X", "W", "dY"))
+    M, K = X.shape
+    N = W.shape[0]
+    qx = fp4.fp4_quantize(X, fp4.quant_params(MX))
+    qw = fp4.fp4_quantize(W, fp4.quant_params(MX))
+    y = fp4.fp4_gemm(qx, qw, torch.bfloat16)
+    r_m = _sample_rows(M, 4, 5)
+    _check_quant_rows(d["X"].float().numpy(), qx, {}, r_m, "7b X")
+    _check_gemm_rows(qx, qw, y, r_m, MX, True, "7b fprop")
+    qdy_n, qdy_m = fp4.fp4_quantize_dual(dY, fp4.quant_params(MX), fp4.quant_params(MX, transpose=True))
+    qw_t = fp4.fp4_quantize(W, fp4.quant_params(MX, transpose=True))
+    qx_t = fp4.fp4_quantize(X, fp4.quant_params(MX, transpose=True))
+    dx = fp4.fp4_gemm(qdy_n, qw_t, torch.bfloat16)
+    dw = fp4.fp4_gemm(qdy_m, qx_t, torch.bfloat16)
+    _check_gemm_rows(qdy_n, qw_t, dx, r_m, MX, True, "7b dgrad")
+    _check_gemm_rows(qdy_m, qx_t, dw, _sample_rows(N, 4, 6), MX, True, "7b wgrad")
+
+
+def test_hcp_square_full():
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    d = inputs.hcp_square()
+    X, W = d["X"].cuda(), d["W"].cuda()
+    M, K = X.shape
+    h = fp4.hcp_num_hot(K)
+    assert h == 369
+    qx = fp4.fp4_quantize(X, fp4.quant_params(NV))
+    qw = fp4.fp4_quantize(W, fp4.quant_params(NV))
+    hot = fp4.fp4_hcp_select(X, qx, h)
+    assert set(d["hot_cols"].tolist()) <= set(hot.cpu().numpy().tolist())
+    y1 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot, h, fp4.FP4_HCP_SINGLE, 2, torch.float32)
+    y2 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot, h, fp4.FP4_HCP_TWO, 2, torch.float32)
+    rows = _sample_rows(M, 3, 7)
+    xn = d["X"].float().numpy()[rows]
+    wn = d["W"].float().numpy()
+    cx = qx.codes.cpu().numpy()[rows]
+    sx = untile_scales(qx.scales.cpu().numpy(), M, K // 16)[rows]
+    cw = qw.codes.cpu().numpy()
+    sw = untile_scales(qw.scales.cpu().numpy(), W.shape[0], K // 16)
+    gx = qx.tensor_scale.cpu().numpy()[0]
+    gw = qw.tensor_scale.cpu().numpy()[0]
+    yr, bound = o.hcp_gemm(xn, cx, sx, wn, cw, sw, o.NVFP4, gx, gw, hot.cpu().numpy(), 2)
+    for y, label in ((y1, "single"), (y2, "two")):
+        got = y.cpu().numpy()[rows].astype(np.float64)
+        assert np.all(np.abs(got - yr) <= 1e-3 * bound), label
