@@ -22,7 +22,9 @@ import torch
 from .build import lib_path
 
 # ---- constants (mirror include/fp4.h) ---------------------------------------
-FP4_OK, FP4_ERR_INVALID_ARG, FP4_ERR_UNSUPPORTED, FP4_ERR_MISALIGNED, FP4_ERR_CUDA, FP4_ERR_TIMEOUT = range(6)
+(FP4_OK, FP4_ERR_INVALID_ARG, FP4_ERR_UNSUPPORTED, FP4_ERR_MISALIGNED, FP4_ERR_CUDA, FP4_ERR_TIMEOUT,
+ FP4_ERR_TOO_LARGE) = range(7)
+FP4_NOALLOC_MAX_CHANNELS = 65536
 FP4_FMT_MXFP4, FP4_FMT_NVFP4 = 0, 1
 FP4_ROUND_RTN, FP4_ROUND_SR = 0, 1
 FP4_SCALING_1D, FP4_SCALING_2D = 0, 1
@@ -72,6 +74,7 @@ _SIGNATURES = {
                                 _P]),
     "fp4_hcp_select_workspace_bytes": (_SZ, [_I64]),
     "fp4_hcp_select": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(fp4_operand), _I32, _P, _P, _SZ, _P]),
+    "fp4_hcp_select_noalloc": (ctypes.c_int, [_P, _I64, ctypes.POINTER(fp4_operand), _I32, _P, _P]),
     "fp4_hcp_workspace_bytes": (_SZ, [_I64, _I64, _I32, _I32]),
     "fp4_hcp_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _I64, ctypes.POINTER(fp4_operand),
                                     ctypes.POINTER(fp4_operand), _P, _I32, _I32, _I32, _P, _SZ, _I32, _P, _I64, _P]),
@@ -313,6 +316,24 @@ def fp4_hcp_select(x: torch.Tensor, xq: QTensor, k_hot: int, out: Optional[torch
     op = xq.operand()
     _check(lib.fp4_hcp_select(_ctx(ctx), _ptr(x), _ld(x), ctypes.byref(op), k_hot, _ptr(out), _ptr(workspace),
                               workspace.numel(), _stream(stream)), "fp4_hcp_select")
+    return out[:k_hot]
+
+
+def fp4_hcp_select_noalloc(x: torch.Tensor, xq: QTensor, k_hot: int, out: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """Hot-channel selection without a context or workspace.
+
+    For callers that may not allocate device memory (their memory belongs to
+    their own caching pool, or they cannot afford the synchronization that
+    cudaMalloc/cudaFree may cause): the library keeps a fixed scratch array for
+    up to FP4_NOALLOC_MAX_CHANNELS channels.  Calls that overlap on the GPU
+    race; the first call on a device should come before any stream capture.
+    `out` (int32[k_hot]) must be given by a caller that may not allocate.
+    """
+    out = out if out is not None else torch.empty((max(k_hot, 1),), dtype=torch.int32, device=x.device)
+    op = xq.operand()
+    _check(load_library().fp4_hcp_select_noalloc(_ptr(x), _ld(x), ctypes.byref(op), k_hot, _ptr(out),
+                                                 _stream(stream)), "fp4_hcp_select_noalloc")
     return out[:k_hot]
 
 

@@ -106,6 +106,7 @@ const char* fp4_status_string(int s) {
     case FP4_ERR_MISALIGNED: return "pointer or pitch not 16-byte aligned";
     case FP4_ERR_CUDA: return "CUDA call failed";
     case FP4_ERR_TIMEOUT: return "device wait timed out";
+    case FP4_ERR_TOO_LARGE: return "input exceeds the fixed scratch limit of this entry point";
     default: return "unknown status";
   }
 }

@@ -14,6 +14,8 @@
 // selection (ties to the lower index), and the gather of the extra columns.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "fp4_device.cuh"
 
 using namespace fp4dev;
@@ -219,3 +221,66 @@ cudaError_t launch_hcp_gather(const uint16_t* x, int64_t ldx, const uint16_t* w,
 }
 
 }  // namespace fp4
+
+// ============================================================================
+// fp4_hcp_select_noalloc: selection with a fixed scratch array in the library
+// (no context, no workspace, no allocation).  For callers that may not allocate
+// device memory: their memory belongs to their own caching pool, or they cannot
+// afford the synchronization that cudaMalloc/cudaFree may bring.
+// ============================================================================
+namespace fp4 {
+namespace {
+
+// per-channel fp32 error sums, then one int flag per channel
+static __device__ __align__(256) unsigned char g_hcp_select_scratch[FP4_NOALLOC_MAX_CHANNELS * 8];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+int g_noalloc_sms[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (host code may not
+// use the array's name as a device pointer).  Looked up once per device.
+int noalloc_setup(int dev, void** ptr, int* sms) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_hcp_select_scratch) != cudaSuccess || !p) return FP4_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 148;
+    g_noalloc_sms[dev] = n;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  *sms = g_noalloc_sms[dev];
+  return FP4_OK;
+}
+
+}  // namespace
+}  // namespace fp4
+
+extern "C" int fp4_hcp_select_noalloc(const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
+                                      int32_t* hot_idx, void* stream) {
+  using namespace fp4;
+  if (!xq || !xq->codes || !xq->scales || !x_bf16 || xq->rows < 0 || xq->k < 0) return FP4_ERR_INVALID_ARG;
+  if (xq->k > FP4_NOALLOC_MAX_CHANNELS) return FP4_ERR_TOO_LARGE;
+  if (xq->format != FP4_FMT_MXFP4 && xq->format != FP4_FMT_NVFP4) return FP4_ERR_UNSUPPORTED;
+  if (xq->sf_layout != FP4_SF_ROWMAJOR && xq->sf_layout != FP4_SF_MMA) return FP4_ERR_INVALID_ARG;
+  if (xq->k % (xq->format == FP4_FMT_MXFP4 ? 32 : 16)) return FP4_ERR_INVALID_ARG;
+  if (xq->format == FP4_FMT_NVFP4 && !xq->tensor_scale) return FP4_ERR_INVALID_ARG;
+  if (k_hot < 0 || k_hot > xq->k || (k_hot > 0 && !hot_idx) || ldx < xq->k) return FP4_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x_bf16) & 15u) || (ldx * 2) % 16 || (reinterpret_cast<uintptr_t>(xq->codes) & 15u))
+    return FP4_ERR_MISALIGNED;
+  if (k_hot == 0 || xq->k == 0 || xq->rows == 0) return FP4_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4_ERR_CUDA;
+  void* scratch = nullptr;
+  int sms = 0;
+  int s = noalloc_setup(dev, &scratch, &sms);
+  if (s) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* err = static_cast<float*>(scratch);   // cleared by the launcher before accumulating
+  cudaError_t e = launch_hcp_channel_errors(static_cast<const uint16_t*>(x_bf16), ldx, *xq, err, sms, st);
+  if (e == cudaSuccess) e = launch_hcp_topk(err, xq->k, k_hot, hot_idx, st);
+  return e == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}

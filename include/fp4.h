@@ -59,7 +59,9 @@ enum {
                                §3.2's quantize_to_fp4)                         */
   FP4_ERR_MISALIGNED = 3,   /* pointer or pitch not 16-byte aligned           */
   FP4_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed              */
-  FP4_ERR_TIMEOUT = 5       /* a device-side wait gave up (bounded wait)       */
+  FP4_ERR_TIMEOUT = 5,      /* a device-side wait gave up (bounded wait)       */
+  FP4_ERR_TOO_LARGE = 6     /* input exceeds a fixed scratch limit (see
+                               fp4_hcp_select_noalloc)                        */
 };
 
 /* ---- enums --------------------------------------------------------------- */
@@ -215,6 +217,27 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
                  const fp4_operand* xq, const fp4_operand* wq, const int32_t* hot_idx,
                  int32_t k_hot, int32_t mode, int32_t order, void* workspace, size_t ws_bytes,
                  int32_t out_dtype, void* y, int64_t ldy, void* stream);
+
+/* fp4_hcp_select_noalloc: the same selection as fp4_hcp_select, for callers
+ * that must not allocate device memory.  Some callers cannot: a framework that
+ * hands every byte of the GPU to its own caching pool, a serving loop whose
+ * latency budget cannot absorb the device-wide synchronization cudaMalloc and
+ * cudaFree may cause, or code running where the allocator is off limits.  This
+ * entry point needs neither a context nor a workspace: its scratch (per-channel
+ * errors and flags) is a fixed array inside the library, FP4_NOALLOC_MAX_CHANNELS
+ * channels (512 KiB), which every GPU that loads the library keeps until the
+ * process exits.  The pages have no counterpart; it exists for such callers.
+ *  - K > FP4_NOALLOC_MAX_CHANNELS returns FP4_ERR_TOO_LARGE (nothing launched).
+ *  - The first call on a device looks up the array's device address (once per
+ *    device); make that first call before any stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (different
+ *    streams, or different host threads, on the same device) race and give
+ *    wrong results.  Each call clears the error sums it accumulates.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ * Arguments, layout and result as fp4_hcp_select.                          */
+#define FP4_NOALLOC_MAX_CHANNELS 65536
+int fp4_hcp_select_noalloc(const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
+                           int32_t* hot_idx, void* stream);
 
 /* ---- element encoders (the "nearest of the 16 FP4 values" step, [msr] §六)
  * fp4_encode_e2m1: codes[i] = RTN E2M1 code of xs[i] (one code per byte).
