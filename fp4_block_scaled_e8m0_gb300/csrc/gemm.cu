@@ -10,19 +10,24 @@
 // §3.1 ("S" mode: extra K columns in the same GEMM), multiplied by
 // tcgen05.mma.kind::f16 into the same accumulator.
 //
-// Kernel structure (one CTA per SM, persistent over 128 x BN output tiles):
-//   warp 0      TMA producer: A/B code tiles (128-byte K slabs, 128B swizzle)
-//               and the scale-factor atoms (bulk copies) into a 4-stage ring
-//   warp 1      TMEM allocator + MMA issuer (one elected lane): copies the
-//               stage's scale factors shared->tensor memory (tcgen05.cp) and
-//               issues 4 MMAs per stage; tcgen05.commit frees the stage
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, * alpha, store
+// Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0       TMA producer: A/B code slabs (128-byte K slabs, 128B swizzle)
+//                and the stage's scale-factor atoms (3-D tensor maps) into a
+//                4-stage shared-memory ring
+//   warp 1       TMEM allocator + MMA issuer (one elected lane): 4 MMAs per
+//                stage; tcgen05.commit frees the stage
+//   warps 2-5    scale-factor stagers, one per TMEM lane quadrant: copy the
+//                stage's scale factors shared -> registers -> tensor memory
+//                (tcgen05.st), so the copies stay out of the MMA pipe
+//   warps 6-13   epilogue, two per lane quadrant (128 columns each):
+//                tcgen05.ld of the accumulator, * alpha, store
 // Every wait is bounded (globaltimer); a wait that gives up sets the context's
 // status word and the CTA drains and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "fp4_device.cuh"
@@ -40,7 +45,8 @@ constexpr int SF_A_MAX = 4 * 512;          // NVFP4: 4 atoms of 128 rows x 4 sca
 constexpr int SF_B_MAX = (BN / 128) * 4 * 512;
 constexpr int STAGE_BYTES = A_TILE + B_TILE + SF_A_MAX + SF_B_MAX;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 32 * (6 + NUM_EPI_WARPS);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = BN;      // scale-factor slots after the accumulator
 constexpr uint32_t SF_SLOT_COLS = 48;      // 16 (A) + 32 (B) columns per stage
@@ -51,10 +57,7 @@ struct Params {
   int k_tiles;        // FP4 K stages (256 elements each)
   int ext_tiles;      // bf16 K stages (64 elements each)
   int nvfp4;
-  const uint8_t* sfa;
-  const uint8_t* sfb;
-  int64_t sf_group_bytes;   // bytes of scales per 128-row group
-  int sf_atoms_per_stage;   // 4 (NVFP4) or 2 (MXFP4)
+  int sf_atoms;       // atoms (128 rows x 4 scales) per stage and 128-row group: 4 NVFP4, 2 MXFP4
   const float* ts_a;
   const float* ts_b;
   void* C;
@@ -90,17 +93,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait: returns false (and raises the abort flag + status word) when the
 // barrier phase does not complete within WAIT_LIMIT_NS or another thread of
 // the CTA has already aborted.
+// The time limit and the abort flag are checked only every 1024 polls: reading
+// %globaltimer is slow, and a check after every failed poll delays the wake-up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned int* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = fp4dev::globaltimer_ns();
-  while (true) {
+  uint64_t t0 = 0;
+  for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (fp4dev::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
-      *abort_flag = 1;
-      atomicOr(status, FP4_DEVICE_TIMEOUT);
-      return false;
+    if ((n & 1023u) == 0) {
+      if (*abort_flag) return false;
+      const uint64_t now = fp4dev::globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > WAIT_LIMIT_NS) {
+        *abort_flag = 1;
+        atomicOr(status, FP4_DEVICE_TIMEOUT);
+        return false;
+      }
     }
   }
 }
@@ -112,12 +122,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
 }
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
+
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -126,6 +131,8 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
+// arrive on the barrier at the same shared-memory offset in every CTA of `mask`
+
 
 // shared-memory matrix descriptor (K-major, 128-byte swizzle; SBO = 1024 B
 // between 8-row groups)
@@ -136,16 +143,6 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
   d |= (uint64_t)1 << 46;                    // descriptor version (sm_100 family)
   d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-  return d;
-}
-// descriptor of a 32-row x 16-byte scale-factor block (no swizzle, 8-row core
-// matrices 128 B apart) for tcgen05.cp.32x128b
-__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)(0) << 16;
-  d |= (uint64_t)(128 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
   return d;
 }
 
@@ -193,9 +190,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
 }
-__device__ __forceinline__ void sf_copy(uint32_t tmem, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem), "l"(sdesc));
-}
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile(
@@ -210,17 +204,47 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
 }
 
 // ---------------------------------------------------------------------------
+// the kernel.  CM CTAs along M form a cluster: they share the B tile, which
+// each loads one CM-th of and multicasts to all; a stage is refilled only after
+// every CTA of the cluster has released it.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// 32 lanes x 16 / 32 consecutive 32-bit columns of tensor memory, one register each
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                     const __grid_constant__ CUtensorMap tm_ax, const __grid_constant__ CUtensorMap tm_bx,
                     const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
+  uint64_t* sf_ready = empty + STAGES;
+  uint64_t* acc_full = sf_ready + STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -236,9 +260,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_ready[s], 4);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    mbar_init(acc_empty, NUM_EPI_WARPS);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -255,55 +280,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int num_tiles = p.tiles_m * p.tiles_n;
   const int total_k = p.k_tiles + p.ext_tiles;
+  const bool nvfp4 = p.nvfp4 != 0;
+  const int atoms = p.sf_atoms;
+  const uint32_t sfb_off = nvfp4 ? 16u : 8u;  // B scale columns start after A's in a slot
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       int s = 0;
       uint32_t phase = 0;
-      uint32_t armed_mask = 0, armed_phase = 0;  // per stage: ever armed, parity of the last arm
       bool ok = true;
-      const int sf_groups_b = (p.N + 127) / 128;
+      const uint32_t sf_bytes = (uint32_t)atoms * 512;             // one 128-row group, one stage
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
-        const int groups_b = min(BN / 128, sf_groups_b - tn * (BN / 128));
         for (int kt = 0; kt < total_k; ++kt) {
           if (!mbar_wait(&empty[s], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           if (kt < p.k_tiles) {
-            const uint32_t sf_bytes = p.sf_atoms_per_stage * 512;
-            mbar_expect_tx(&full[s], A_TILE + B_TILE + sf_bytes * (1 + groups_b));
+            mbar_expect_tx(&full[s], A_TILE + B_TILE + sf_bytes * (1 + BN / 128));
             tma_load_2d(stage_a(s), &tm_a, &full[s], kt * KSLAB, tm * BM);
             tma_load_2d(stage_b(s), &tm_b, &full[s], kt * KSLAB, tn * BN);
-            bulk_load(stage_sfa(s), p.sfa + tm * p.sf_group_bytes + (int64_t)kt * sf_bytes, sf_bytes, &full[s]);
-            // scale groups past the operand's last 128 rows are not loaded: they
-            // only feed accumulator columns the epilogue never stores
-            for (int g = 0; g < groups_b; ++g)
-              bulk_load(stage_sfb(s) + g * sf_bytes,
-                        p.sfb + (int64_t)(tn * (BN / 128) + g) * p.sf_group_bytes + (int64_t)kt * sf_bytes, sf_bytes,
-                        &full[s]);
+            // scale atoms of this stage: rows of 128 bytes inside a 128-row group
+            tma_load_3d(stage_sfa(s), &tm_sfa, &full[s], 0, kt * atoms * 4, tm);
+            tma_load_3d(stage_sfb(s), &tm_sfb, &full[s], 0, kt * atoms * 4, tn * (BN / 128));
           } else {
             const int kx = kt - p.k_tiles;
             mbar_expect_tx(&full[s], A_TILE + B_TILE);
             tma_load_2d(stage_a(s), &tm_ax, &full[s], kx * 64, tm * BM);
             tma_load_2d(stage_b(s), &tm_bx, &full[s], kx * 64, tn * BN);
           }
-          armed_mask |= 1u << s;
-          armed_phase = (armed_phase & ~(1u << s)) | (phase << s);
           if (++s == STAGES) { s = 0; phase ^= 1; }
         }
       }
-      // Before exit every load issued into the ring must have landed (on the
-      // normal path this holds already: the MMA warp consumed each stage).
-      for (int si = 0; si < STAGES; ++si) {
-        if (!(armed_mask >> si & 1u)) continue;
-        const uint32_t ph = (armed_phase >> si) & 1u;
+      // Drain: acquire every stage once more, i.e. wait (bounded) until the last
+      // data loaded into each stage has been consumed; then no load is in flight.
+      for (int i = 0; i < STAGES; ++i) {
         const uint64_t t0 = fp4dev::globaltimer_ns();
-        while (!mbar_try_wait(&full[si], ph)) {
-          if (fp4dev::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+        for (uint32_t n = 1; !mbar_try_wait(&empty[s], phase ^ 1); ++n) {
+          if ((n & 1023u) == 0 && fp4dev::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
             atomicOr(p.status, FP4_DEVICE_TIMEOUT);
             break;
           }
         }
+        if (++s == STAGES) { s = 0; phase ^= 1; }
       }
     }
   } else if (warp == 1) {
@@ -312,32 +330,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int s = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      const bool nvfp4 = p.nvfp4 != 0;
-      const uint32_t sfb_off = nvfp4 ? 16u : 8u;  // B columns start after A's per slot
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.status)) { ok = false; break; }
         acc_phase ^= 1;
         tc_fence_after();
         for (int kt = 0; kt < total_k; ++kt) {
-          if (!mbar_wait(&full[s], phase, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(&full[s], phase, abort_flag, p.status) || !mbar_wait(&sf_ready[s], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_a(s)), b_addr = smem_u32(stage_b(s));
           if (kt < p.k_tiles) {
             const uint32_t slot = tmem + TMEM_SF_BASE + (uint32_t)s * SF_SLOT_COLS;
-            const int atoms = p.sf_atoms_per_stage;
-            for (int a = 0; a < atoms; ++a) {
-              sf_copy(slot + 4 * a, desc_sf(smem_u32(stage_sfa(s)) + a * 512));
-              for (int g = 0; g < BN / 128; ++g)
-                sf_copy(slot + sfb_off + (uint32_t)(a * (BN / 128) + g) * 4,
-                        desc_sf(smem_u32(stage_sfb(s)) + g * atoms * 512 + a * 512));
-            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int atom = nvfp4 ? j : (j >> 1);
               const uint32_t sf_id = nvfp4 ? 0u : (uint32_t)(j & 1) * 2u;
               mma_fp4(tmem, desc_sw128(a_addr + 32 * j), desc_sw128(b_addr + 32 * j), idesc_fp4(!nvfp4, sf_id),
-                      slot + 4 * atom, slot + sfb_off + (uint32_t)atom * (BN / 128) * 4,
-                      (kt > 0 || j > 0) ? 1u : 0u, nvfp4);
+                      slot + 4 * atom, slot + sfb_off + (uint32_t)atom * (BN / 128) * 4, (kt > 0 || j > 0) ? 1u : 0u,
+                      nvfp4);
             }
           } else {
 #pragma unroll
@@ -353,14 +365,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // make sure no MMA is in flight before the allocation is released
       tc_commit(drain);
-      uint64_t t0 = fp4dev::globaltimer_ns();
-      while (!mbar_try_wait(drain, 0)) {
-        if (fp4dev::globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+      const uint64_t t0 = fp4dev::globaltimer_ns();
+      for (uint32_t n = 1; !mbar_try_wait(drain, 0); ++n) {
+        if ((n & 1023u) == 0 && fp4dev::globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------- scale-factor stagers (warps 2..5) ----------------
+    // The tensor-memory image equals a 32x128b.warpx4 copy of each 512-byte
+    // atom: lane 32q+i, columns c..c+3 of the atom's slot hold the 16 bytes of
+    // the atom's shared-memory row i, for every lane quadrant q.
+    const int quad = warp & 3;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    int s = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int kt = 0; kt < total_k; ++kt) {
+        bool got = true;
+        if (lane == 0) got = mbar_wait(&full[s], phase, abort_flag, p.status);
+        if (__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) == 0) { ok = false; break; }
+        if (kt < p.k_tiles) {
+          const uint32_t slot = tmem + lane_base + TMEM_SF_BASE + (uint32_t)s * SF_SLOT_COLS;
+          uint32_t v[32];
+          if (nvfp4) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+              const uint4 w = *reinterpret_cast<const uint4*>(stage_sfa(s) + a * 512 + lane * 16);
+              v[4 * a] = w.x; v[4 * a + 1] = w.y; v[4 * a + 2] = w.z; v[4 * a + 3] = w.w;
+            }
+            tmem_st16(slot, v);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+#pragma unroll
+              for (int g = 0; g < 2; ++g) {
+                const uint4 w = *reinterpret_cast<const uint4*>(stage_sfb(s) + g * 4 * 512 + a * 512 + lane * 16);
+                const int c = (a * 2 + g) * 4;
+                v[c] = w.x; v[c + 1] = w.y; v[c + 2] = w.z; v[c + 3] = w.w;
+              }
+            }
+            tmem_st16(slot + sfb_off, v);
+            tmem_st16(slot + sfb_off + 16, v + 16);
+          } else {
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+              const uint4 w = *reinterpret_cast<const uint4*>(stage_sfa(s) + a * 512 + lane * 16);
+              v[4 * a] = w.x; v[4 * a + 1] = w.y; v[4 * a + 2] = w.z; v[4 * a + 3] = w.w;
+            }
+            tmem_st8(slot, v);
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+#pragma unroll
+              for (int g = 0; g < 2; ++g) {
+                const uint4 w = *reinterpret_cast<const uint4*>(stage_sfb(s) + g * 2 * 512 + a * 512 + lane * 16);
+                const int c = (a * 2 + g) * 4;
+                v[c] = w.x; v[c + 1] = w.y; v[c + 2] = w.z; v[c + 3] = w.w;
+              }
+            }
+            tmem_st16(slot + sfb_off, v);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_ready[s]);
+        if (++s == STAGES) { s = 0; phase ^= 1; }
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
-    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    // ---------------- epilogue (warps 6..13) ----------------
+    const int quad = warp & 3;               // TMEM lanes 32*quad .. 32*quad+31
+    const int half = (warp - 6) >> 2;        // accumulator columns half*128 .. +127
     uint32_t acc_phase = 0;
     float alpha = 1.0f;
     if (p.nvfp4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
@@ -375,7 +450,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row = tm * BM + quad * 32 + lane;
       const bool row_ok = row < p.M;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, r);
         const int col0 = tn * BN + c0;
@@ -471,6 +546,22 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a scale buffer in the MMA layout, seen as [group][row][128 bytes]:
+// a box of `rows_box` rows x `groups_box` groups is one stage's atoms of
+// `groups_box` consecutive 128-row groups
+bool make_sf_map(CUtensorMap* m, const void* base, int64_t group_bytes, int64_t groups, int rows_box, int groups_box) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)(group_bytes / 128), (cuuint64_t)groups};
+  cuuint64_t strides[2] = {128, (cuuint64_t)group_bytes};
+  cuuint32_t box[3] = {128, (cuuint32_t)rows_box, (cuuint32_t)groups_box};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int launch_gemm(const GemmArgs& g, cudaStream_t st) {
@@ -484,12 +575,9 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   p.nvfp4 = A.format == FP4_FMT_NVFP4;
   p.k_tiles = g.fp4_part ? (int)cdiv(A.k, 256) : 0;
   p.ext_tiles = (int)(g.kx / 64);
-  p.sfa = A.scales;
-  p.sfb = B.scales;
-  p.sf_atoms_per_stage = p.nvfp4 ? 4 : 2;
-  p.sf_group_bytes = (int64_t)128 * nsf_padded(A.k, A.format);
-  p.ts_a = A.tensor_scale;
-  p.ts_b = B.tensor_scale;
+  p.sf_atoms = p.nvfp4 ? 4 : 2;
+  p.ts_a = p.nvfp4 ? A.tensor_scale : nullptr;
+  p.ts_b = p.nvfp4 ? B.tensor_scale : nullptr;
   p.C = g.C;
   p.ldc = g.ldc;
   p.out_bf16 = g.out_dtype == FP4_DTYPE_BF16;
@@ -498,23 +586,25 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   p.tiles_m = (int)cdiv(M, BM);
   p.tiles_n = (int)cdiv(N, BN);
   if (p.k_tiles + p.ext_tiles == 0) return FP4_ERR_INVALID_ARG;
-  if (!p.nvfp4) {
-    p.ts_a = p.ts_b = nullptr;
-  }
 
-  CUtensorMap ta{}, tb{}, tax{}, tbx{};
+  CUtensorMap ta{}, tb{}, tsa{}, tsb{}, tax{}, tbx{};
   bool ok = true;
   if (g.fp4_part) {
+    const int64_t group_bytes = (int64_t)128 * nsf_padded(A.k, A.format);
     ok &= make_map(&ta, A.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.k / 2, M, BM);
     ok &= make_map(&tb, B.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B.k / 2, N, BN);
+    ok &= make_sf_map(&tsa, A.scales, group_bytes, cdiv(M, 128), p.sf_atoms * 4, 1);
+    ok &= make_sf_map(&tsb, B.scales, group_bytes, cdiv(N, 128), p.sf_atoms * 4, BN / 128);
   }
   if (g.kx > 0) {
     ok &= make_map(&tax, g.a_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, M, BM);
     ok &= make_map(&tbx, g.b_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, N, BN);
   }
-  if (!g.fp4_part) {  // residual-only GEMM: alpha still applies (B_ext is divided by it)
+  if (!g.fp4_part) {  // residual-only GEMM: no FP4 stages, the maps are never read
     ta = tax;
     tb = tbx;
+    tsa = tax;
+    tsb = tbx;
   }
   if (g.kx == 0) {
     tax = ta;
@@ -530,7 +620,7 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   }
   const int tiles = p.tiles_m * p.tiles_n;
   const int grid = std::min(tiles, g.num_sms);
-  fp4_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, tax, tbx, p);
+  fp4_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, tsa, tsb, tax, tbx, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
