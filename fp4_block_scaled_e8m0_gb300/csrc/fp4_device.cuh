@@ -80,18 +80,20 @@ __device__ __forceinline__ uint32_t e2m1_sw(float xs) {
 
 // Stochastic rounding onto the grid: lo = largest grid point <= |xs| (saturated
 // at 6), frac = (|xs| - lo) / step, round up iff u16 < frac * 65536 ([lowprec]
-// §3.2's floor(x) + (rand < frac) on the non-uniform grid).  Branch-free: the
-// grid step is 2^(e-1) with e = [|xs| >= 2] + [|xs| >= 4], so t = |xs| / step is
-// exact, lo's code is 2e + floor(t) and frac = t - floor(t) (both exact).
+// §3.2's floor(x) + (rand < frac) on the non-uniform grid).  Branch-free and
+// without integer/float conversions: the grid step is 2^(e-1) with
+// e = [|xs| >= 2] + [|xs| >= 4], t = |xs| / step is exact and below 4, adding
+// 2^23 with rounding toward -inf yields 2^23 + floor(t) (its low bits are
+// floor(t)), and u16 becomes a float exactly as (2^23 | u16) - 2^23.
 __device__ __forceinline__ uint32_t e2m1_sr(float xs, uint32_t u16) {
   const float a = fminf(fabsf(xs), 6.0f);
   const uint32_t e = (a >= 2.0f) + (a >= 4.0f);
-  const float inv_step = __uint_as_float((128u - e) << 23);  // 2, 1, 0.5
-  const float t = __fmul_rn(a, inv_step);
-  const float f = floorf(t);
-  const uint32_t lo_code = 2u * e + (uint32_t)f;
-  const float frac = __fsub_rn(t, f);
-  const bool up = (lo_code < 7u) && ((float)u16 < __fmul_rn(frac, 65536.0f));
+  const float t = __fmul_rn(a, __uint_as_float((128u - e) << 23));  // a * 2^(1-e)
+  const float tf = __fadd_rd(t, 8388608.0f);                        // 2^23 + floor(t)
+  const uint32_t lo_code = 2u * e + (__float_as_uint(tf) & 7u);
+  const float frac = __fsub_rn(t, __fsub_rn(tf, 8388608.0f));       // exact
+  const float u = __fsub_rn(__uint_as_float(0x4B000000u | u16), 8388608.0f);
+  const bool up = (lo_code < 7u) && (u < __fmul_rn(frac, 65536.0f));
   return ((__float_as_uint(xs) >> 28) & 8u) | (lo_code + (up ? 1u : 0u));
 }
 
@@ -168,12 +170,44 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// Philox with the ten round keys computed once (they depend on the seed only).
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys k;
+  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = a;
+    k.k1[r] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+  return k;
+}
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& k) {
+#pragma unroll
+  for (int rnd = 0; rnd < 10; ++rnd) {
+    const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k.k0[rnd], (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k.k1[rnd],
+                   (uint32_t)p0);
+  }
+  return c;
+}
+
 // Eight 16-bit uniforms for output elements 8n .. 8n+7 (n = offset + i/8).
 __device__ __forceinline__ uint4 sr_bits8(uint64_t seed, uint64_t offset, uint32_t stream,
                                           uint64_t first_elem) {
   uint64_t n = offset + (first_elem >> 3);
   return philox4x32_10(make_uint4((uint32_t)n, (uint32_t)(n >> 32), 0u, stream),
                        (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+__device__ __forceinline__ uint4 sr_bits8(const PhiloxKeys& keys, uint64_t offset, uint32_t stream,
+                                          uint64_t first_elem) {
+  uint64_t n = offset + (first_elem >> 3);
+  return philox4x32_10(make_uint4((uint32_t)n, (uint32_t)(n >> 32), 0u, stream), keys);
 }
 __device__ __forceinline__ uint32_t u16_lane(const uint4& w, int j) {
   uint32_t word = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;

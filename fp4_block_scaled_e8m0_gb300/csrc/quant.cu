@@ -53,9 +53,10 @@ __device__ __forceinline__ void encode_store_block(const float* v, float g, cons
     }
   } else {
     int64_t first_elem = out_row * o.out_cols + out_col0;
+    const PhiloxKeys keys = philox_keys(o.sr_seed);   // loop-invariant: hoisted by the compiler
 #pragma unroll
     for (int q = 0; q < B / 8; ++q) {
-      uint4 bits = sr_bits8(o.sr_seed, o.sr_offset, o.sr_stream, (uint64_t)(first_elem + 8 * q));
+      uint4 bits = sr_bits8(keys, o.sr_offset, o.sr_stream, (uint64_t)(first_elem + 8 * q));
       uint32_t w = 0;
 #pragma unroll
       for (int p = 0; p < 8; ++p)
@@ -113,14 +114,34 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const void* __rest
   const float g = load_g(o, FMT);
   const bool sr = o.rounding == FP4_ROUND_SR;
   const bool rht = o.rht != 0;
-  int64_t nblk_row = cols / B;
-  int64_t total = rows * nblk_row;
-  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
-       blk += (int64_t)gridDim.x * blockDim.x) {
-    int64_t r = blk / nblk_row, k0 = (blk - r * nblk_row) * B;
-    float v[B];
+  const int64_t nblk_row = cols / B;
+  const int64_t total = rows * nblk_row;
+  const bool small = total < (int64_t(1) << 31);  // 32-bit index math
+  auto split = [&](int64_t blk, int64_t& r, int64_t& k0) {
+    if (small) {
+      const uint32_t b32 = (uint32_t)blk, n32 = (uint32_t)nblk_row, r32 = b32 / n32;
+      r = r32;
+      k0 = (int64_t)(b32 - r32 * n32) * B;
+    } else {
+      r = blk / nblk_row;
+      k0 = (blk - r * nblk_row) * B;
+    }
+  };
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  // two blocks per iteration: both blocks' loads are in flight together
+  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total; blk += 2 * stride) {
+    const int64_t blk2 = blk + stride;
+    const bool two = blk2 < total;
+    int64_t r, k0, r2 = 0, k2 = 0;
+    split(blk, r, k0);
+    if (two) split(blk2, r2, k2);
+    float v[B], w[B];
 #pragma unroll
     for (int q = 0; q < B / 8; ++q) load8<DT>(x, r * ldx + k0 + 8 * q, v + 8 * q);
+    if (two) {
+#pragma unroll
+      for (int q = 0; q < B / 8; ++q) load8<DT>(x, r2 * ldx + k2 + 8 * q, w + 8 * q);
+    }
     if (rht) {
 #pragma unroll
       for (int h = 0; h < B / 16; ++h) rht16(v + 16 * h, o.rht_signs);
@@ -129,6 +150,16 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const void* __rest
 #pragma unroll
     for (int j = 0; j < B; ++j) amax_b = fmaxf(amax_b, fabsf(v[j]));
     encode_store_block<FMT, B>(v, g, o, r, k0, amax_b, sr);
+    if (two) {
+      if (rht) {
+#pragma unroll
+        for (int h = 0; h < B / 16; ++h) rht16(w + 16 * h, o.rht_signs);
+      }
+      float amax2 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < B; ++j) amax2 = fmaxf(amax2, fabsf(w[j]));
+      encode_store_block<FMT, B>(w, g, o, r2, k2, amax2, sr);
+    }
   }
 }
 
@@ -164,6 +195,54 @@ __device__ __forceinline__ void load_tile(const void* __restrict__ x, int64_t ro
   }
 }
 
+// Register copy of one full tile's raw input (no bounds checks): each thread
+// holds CPT 8-element chunks, fetched while the previous tile is processed.
+template <int DT, int TR>
+struct TileRegs {
+  static constexpr int CPT = TR * TC / 8 / kThreads;   // chunks per thread
+  static constexpr int W = DT == FP4_DTYPE_BF16 ? 1 : 2;
+  uint4 r[CPT * W];
+};
+
+template <int DT, int TR>
+__device__ __forceinline__ void tile_fetch(const void* __restrict__ x, int64_t ldx, int64_t r0, int64_t c0,
+                                           TileRegs<DT, TR>& t) {
+  constexpr int ES = DT == FP4_DTYPE_BF16 ? 2 : 4;
+#pragma unroll
+  for (int i = 0; i < TileRegs<DT, TR>::CPT; ++i) {
+    const int q = threadIdx.x + i * kThreads;
+    const int rr = q / (TC / 8), cc = (q % (TC / 8)) * 8;
+    const char* src = static_cast<const char*>(x) + ((r0 + rr) * ldx + c0 + cc) * ES;
+    t.r[i * TileRegs<DT, TR>::W] = ld_nc_v4(src);
+    if (TileRegs<DT, TR>::W == 2) t.r[i * TileRegs<DT, TR>::W + 1] = ld_nc_v4(src + 16);
+  }
+}
+
+template <int DT, int TR>
+__device__ __forceinline__ void tile_store(const TileRegs<DT, TR>& t, float* tile) {
+#pragma unroll
+  for (int i = 0; i < TileRegs<DT, TR>::CPT; ++i) {
+    const int q = threadIdx.x + i * kThreads;
+    const int rr = q / (TC / 8), cc = (q % (TC / 8)) * 8;
+    float v[8];
+    if (DT == FP4_DTYPE_BF16) {
+      const uint4 w = t.r[i];
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = __uint_as_float(u[j] << 16);
+        v[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+      }
+    } else {
+      const uint4 a = t.r[i * 2], b = t.r[i * 2 + 1];
+      v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+      v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tile[rr * TSTRIDE + cc + j] = v[j];
+  }
+}
+
 template <int FMT, int DT, int MODE>
 __global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__ x, int64_t rows,
                                                         int64_t cols, int64_t ldx, QuantOut oc,
@@ -184,10 +263,25 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__
   float m_c = 0.0f, m_r = 0.0f;
   const int64_t ntr = cdiv(rows, TR), ntc = cdiv(cols, TC);
   const int t = threadIdx.x;
+  // full tiles are fetched into registers one iteration ahead; ragged edge
+  // tiles are loaded element by element when their turn comes
+  TileRegs<DT, TR> pre;
+  auto is_full = [&](int64_t id) { return (id / ntc + 1) * TR <= rows && (id % ntc + 1) * TC <= cols; };
+  bool pre_full = false;
+  if ((int64_t)blockIdx.x < ntr * ntc && is_full(blockIdx.x)) {
+    tile_fetch<DT, TR>(x, ldx, (blockIdx.x / ntc) * TR, (blockIdx.x % ntc) * TC, pre);
+    pre_full = true;
+  }
   for (int64_t tid = blockIdx.x; tid < ntr * ntc; tid += gridDim.x) {
     int64_t r0 = (tid / ntc) * TR, c0 = (tid % ntc) * TC;
-    load_tile<DT, TR>(x, rows, cols, ldx, r0, c0, tile);
+    if (pre_full)
+      tile_store<DT, TR>(pre, tile);
+    else
+      load_tile<DT, TR>(x, rows, cols, ldx, r0, c0, tile);
     __syncthreads();
+    const int64_t nxt = tid + gridDim.x;
+    pre_full = nxt < ntr * ntc && is_full(nxt);
+    if (pre_full) tile_fetch<DT, TR>(x, ldx, (nxt / ntc) * TR, (nxt % ntc) * TC, pre);
     if constexpr (DO_COLS) {
       // column item: column c of the tile, row-block rb (B rows); lanes = columns
       int c = t % TC, rb = t / TC;
