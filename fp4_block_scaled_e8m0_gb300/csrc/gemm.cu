@@ -191,7 +191,7 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -200,8 +200,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 
 // ---------------------------------------------------------------------------
 // the kernel.  CM CTAs along M form a cluster: they share the B tile, which
@@ -230,6 +231,56 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
                : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// one accumulator row's 32 consecutive columns (col0 < N) -> C, times alpha
+__device__ __forceinline__ void store_chunk(const Params& p, const uint32_t* r, int row, int col0, float alpha) {
+  const int ncol = min(32, p.N - col0);
+  if (p.out_bf16) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col0;
+    if (ncol == 32 && !p.accumulate) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * q + 2 * i]), alpha),
+                                                   __fmul_rn(__uint_as_float(r[8 * q + 2 * i + 1]), alpha));
+          w[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        reinterpret_cast<uint4*>(out)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {  // fully unrolled: r stays in registers
+        if (i >= ncol) break;
+        float v = __fmul_rn(__uint_as_float(r[i]), alpha);
+        if (p.accumulate) v = __fadd_rn(__bfloat162float(out[i]), v);
+        out[i] = __float2bfloat16_rn(v);
+      }
+    }
+  } else {
+    float* out = static_cast<float*>(p.C) + (int64_t)row * p.ldc + col0;
+    if (ncol == 32) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        float4 v = make_float4(__fmul_rn(__uint_as_float(r[4 * q]), alpha), __fmul_rn(__uint_as_float(r[4 * q + 1]), alpha),
+                               __fmul_rn(__uint_as_float(r[4 * q + 2]), alpha), __fmul_rn(__uint_as_float(r[4 * q + 3]), alpha));
+        if (p.accumulate) {
+          float4 o = reinterpret_cast<float4*>(out)[q];
+          v.x = __fadd_rn(o.x, v.x); v.y = __fadd_rn(o.y, v.y); v.z = __fadd_rn(o.z, v.z); v.w = __fadd_rn(o.w, v.w);
+        }
+        reinterpret_cast<float4*>(out)[q] = v;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (i >= ncol) break;
+        float v = __fmul_rn(__uint_as_float(r[i]), alpha);
+        out[i] = p.accumulate ? __fadd_rn(out[i], v) : v;
+      }
+    }
+  }
+}
 
 // ---------------------------------------------------------------------------
 // the kernel
@@ -330,6 +381,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int s = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
+      // Descriptors are built once: stage s and K step j only move the start
+      // address (16-byte units) by s * STAGE_BYTES / 16 + 2 j, which stays inside
+      // the 14-bit field; the instruction descriptors are constants.
+      const uint64_t da0 = desc_sw128(smem_u32(stage_a(0))), db0 = desc_sw128(smem_u32(stage_b(0)));
+      const uint32_t id_even = idesc_fp4(!nvfp4, 0u), id_odd = idesc_fp4(!nvfp4, nvfp4 ? 0u : 2u);
+      const uint32_t id_bf16 = idesc_bf16();
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.status)) { ok = false; break; }
         acc_phase ^= 1;
@@ -340,22 +397,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stage_a(s)), b_addr = smem_u32(stage_b(s));
+          const uint64_t da = da0 + (uint64_t)(s * (STAGE_BYTES >> 4)), db = db0 + (uint64_t)(s * (STAGE_BYTES >> 4));
+          const uint32_t acc0 = kt > 0 ? 1u : 0u;
           if (kt < p.k_tiles) {
             const uint32_t slot = tmem + TMEM_SF_BASE + (uint32_t)s * SF_SLOT_COLS;
+            if (nvfp4) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int atom = nvfp4 ? j : (j >> 1);
-              const uint32_t sf_id = nvfp4 ? 0u : (uint32_t)(j & 1) * 2u;
-              mma_fp4(tmem, desc_sw128(a_addr + 32 * j), desc_sw128(b_addr + 32 * j), idesc_fp4(!nvfp4, sf_id),
-                      slot + 4 * atom, slot + sfb_off + (uint32_t)atom * (BN / 128) * 4, (kt > 0 || j > 0) ? 1u : 0u,
-                      nvfp4);
+              for (int j = 0; j < 4; ++j)
+                mma_fp4(tmem, da + 2 * j, db + 2 * j, id_even, slot + 4 * j, slot + 16 + 8 * j, j > 0 ? 1u : acc0, true);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                mma_fp4(tmem, da + 2 * j, db + 2 * j, (j & 1) ? id_odd : id_even, slot + 4 * (j >> 1),
+                        slot + 8 + 8 * (j >> 1), j > 0 ? 1u : acc0, false);
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              mma_bf16(tmem, desc_sw128(a_addr + 32 * j), desc_sw128(b_addr + 32 * j), idesc_bf16(),
-                       (kt > 0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < 4; ++j) mma_bf16(tmem, da + 2 * j, db + 2 * j, id_bf16, j > 0 ? 1u : acc0);
           }
           tc_commit(&empty[s]);
           if (++s == STAGES) { s = 0; phase ^= 1; }
@@ -450,57 +508,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row = tm * BM + quad * 32 + lane;
       const bool row_ok = row < p.M;
 #pragma unroll 1
-      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, r);
-        const int col0 = tn * BN + c0;
-        if (!row_ok || col0 >= p.N) continue;
-        const int ncol = min(32, p.N - col0);
-        if (p.out_bf16) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col0;
-          if (ncol == 32 && !p.accumulate) {
+      for (int pair = 0; pair < 2; ++pair) {
+        // two 32-column loads in flight, one wait; after the second pair every
+        // column this warp owns is in registers and the accumulator is released
+        const int cbase = half * (BN / 2) + pair * 64;
+        uint32_t r2[2][32];
+        tmem_ld32_nowait(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)cbase, r2[0]);
+        tmem_ld32_nowait(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cbase + 32), r2[1]);
+        tmem_ld_wait();
+        if (pair == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty);
+        }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t w[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * q + 2 * i]), alpha),
-                                                         __fmul_rn(__uint_as_float(r[8 * q + 2 * i + 1]), alpha));
-                w[i] = *reinterpret_cast<uint32_t*>(&h);
-              }
-              reinterpret_cast<uint4*>(out)[q] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          } else {
-            for (int i = 0; i < ncol; ++i) {
-              float v = __fmul_rn(__uint_as_float(r[i]), alpha);
-              if (p.accumulate) v = __fadd_rn(__bfloat162float(out[i]), v);
-              out[i] = __float2bfloat16_rn(v);
-            }
-          }
-        } else {
-          float* out = static_cast<float*>(p.C) + (int64_t)row * p.ldc + col0;
-          if (ncol == 32) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float4 v = make_float4(__fmul_rn(__uint_as_float(r[4 * q]), alpha), __fmul_rn(__uint_as_float(r[4 * q + 1]), alpha),
-                                     __fmul_rn(__uint_as_float(r[4 * q + 2]), alpha), __fmul_rn(__uint_as_float(r[4 * q + 3]), alpha));
-              if (p.accumulate) {
-                float4 o = reinterpret_cast<float4*>(out)[q];
-                v.x = __fadd_rn(o.x, v.x); v.y = __fadd_rn(o.y, v.y); v.z = __fadd_rn(o.z, v.z); v.w = __fadd_rn(o.w, v.w);
-              }
-              reinterpret_cast<float4*>(out)[q] = v;
-            }
-          } else {
-            for (int i = 0; i < ncol; ++i) {
-              float v = __fmul_rn(__uint_as_float(r[i]), alpha);
-              out[i] = p.accumulate ? __fadd_rn(out[i], v) : v;
-            }
-          }
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t* r = r2[h];
+          const int col0 = tn * BN + cbase + 32 * h;
+          if (!row_ok || col0 >= p.N) continue;
+          store_chunk(p, r, row, col0, alpha);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
     }
   }
 
