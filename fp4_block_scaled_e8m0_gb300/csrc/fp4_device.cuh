@@ -78,23 +78,28 @@ __device__ __forceinline__ uint32_t e2m1_sw(float xs) {
   return ((__float_as_uint(xs) >> 28) & 8u) | m;
 }
 
-// Stochastic rounding onto the grid: lo = largest grid point <= |xs| (saturated
-// at 6), frac = (|xs| - lo) / step, round up iff u16 < frac * 65536 ([lowprec]
-// §3.2's floor(x) + (rand < frac) on the non-uniform grid).  Branch-free and
-// without integer/float conversions: the grid step is 2^(e-1) with
-// e = [|xs| >= 2] + [|xs| >= 4], t = |xs| / step is exact and below 4, adding
-// 2^23 with rounding toward -inf yields 2^23 + floor(t) (its low bits are
-// floor(t)), and u16 becomes a float exactly as (2^23 | u16) - 2^23.
-__device__ __forceinline__ uint32_t e2m1_sr(float xs, uint32_t u16) {
+// Stochastic rounding onto the grid ([lowprec] §3.2's floor(x) + (rand < frac)
+// on the non-uniform E2M1 grid): lo = largest grid point <= |xs| (|xs| saturated
+// at 6), frac = (|xs| - lo) / step, round up iff u16 < frac * 65536.
+// Returns the chosen grid value with the sign of xs; the hardware conversion of
+// a grid value is exact, so e2m1x2_hw packs the codes.
+//
+// Bit-level form.  From 1 up, the grid keeps one mantissa bit of each binade,
+// so with rem = the 22 mantissa bits below it, frac * 2^22 = rem and the test
+// is 64 u16 < rem: adding 0x3FFFFF - 64 u16 to the fp32 bits carries into the
+// kept bit exactly then, and masking the 22 bits leaves lo or the next grid
+// point (the carry may move into the exponent: 1.5 * 2^e -> 2^(e+1)).  Below 1
+// the step is 0.5, which is the step of [1, 2): b = 1 + |xs| rounded up puts
+// the value there with rem = ceil(frac * 2^22), and for an integer n,
+// n < R iff n < ceil(R), so the same addition decides exactly; 1 is subtracted
+// again afterwards (exact).  fminf sends NaN to the saturated 6, like the clamp.
+__device__ __forceinline__ float e2m1_sr_value(float xs, uint32_t u16_shl6) {
   const float a = fminf(fabsf(xs), 6.0f);
-  const uint32_t e = (a >= 2.0f) + (a >= 4.0f);
-  const float t = __fmul_rn(a, __uint_as_float((128u - e) << 23));  // a * 2^(1-e)
-  const float tf = __fadd_rd(t, 8388608.0f);                        // 2^23 + floor(t)
-  const uint32_t lo_code = 2u * e + (__float_as_uint(tf) & 7u);
-  const float frac = __fsub_rn(t, __fsub_rn(tf, 8388608.0f));       // exact
-  const float u = __fsub_rn(__uint_as_float(0x4B000000u | u16), 8388608.0f);
-  const bool up = (lo_code < 7u) && (u < __fmul_rn(frac, 65536.0f));
-  return ((__float_as_uint(xs) >> 28) & 8u) | (lo_code + (up ? 1u : 0u));
+  const float off = a < 1.0f ? 1.0f : 0.0f;
+  const float b = __fadd_ru(a, off);
+  const uint32_t n = (__float_as_uint(b) + 0x3FFFFFu - u16_shl6) & 0xFFC00000u;
+  const float y = __fsub_rn(__uint_as_float(n), off);
+  return __uint_as_float(__float_as_uint(y) | (__float_as_uint(xs) & 0x80000000u));
 }
 
 // ----------------------------------------------------------------------------
@@ -209,9 +214,10 @@ __device__ __forceinline__ uint4 sr_bits8(const PhiloxKeys& keys, uint64_t offse
   uint64_t n = offset + (first_elem >> 3);
   return philox4x32_10(make_uint4((uint32_t)n, (uint32_t)(n >> 32), 0u, stream), keys);
 }
-__device__ __forceinline__ uint32_t u16_lane(const uint4& w, int j) {
+// 64 * (16-bit lane j of w): the form e2m1_sr_value takes
+__device__ __forceinline__ uint32_t u16_lane_shl6(const uint4& w, int j) {
   uint32_t word = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
-  return (j & 1) ? (word >> 16) : (word & 0xFFFFu);
+  return (j & 1) ? ((word >> 10) & 0x3FFFC0u) : ((word << 6) & 0x3FFFC0u);
 }
 
 // ----------------------------------------------------------------------------

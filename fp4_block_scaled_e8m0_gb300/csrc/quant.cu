@@ -59,8 +59,11 @@ __device__ __forceinline__ void encode_store_block(const float* v, float g, cons
       uint4 bits = sr_bits8(keys, o.sr_offset, o.sr_stream, (uint64_t)(first_elem + 8 * q));
       uint32_t w = 0;
 #pragma unroll
-      for (int p = 0; p < 8; ++p)
-        w |= e2m1_sr(__fmul_rn(v[8 * q + p], r), u16_lane(bits, p)) << (4 * p);
+      for (int p = 0; p < 4; ++p) {
+        const float y0 = e2m1_sr_value(__fmul_rn(v[8 * q + 2 * p], r), u16_lane_shl6(bits, 2 * p));
+        const float y1 = e2m1_sr_value(__fmul_rn(v[8 * q + 2 * p + 1], r), u16_lane_shl6(bits, 2 * p + 1));
+        w |= e2m1x2_hw(y0, y1) << (8 * p);
+      }
       packed[q] = zero ? 0u : w;
     }
   }
@@ -261,27 +264,34 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__
     if (DO_ROWS) g_r = load_g(orr, FMT);
   }
   float m_c = 0.0f, m_r = 0.0f;
-  const int64_t ntr = cdiv(rows, TR), ntc = cdiv(cols, TC);
+  // tile ids in 32 bits (the launcher guarantees fewer than 2^31 tiles): a
+  // 64-bit division per tile costs more than the tile's element work
+  const uint32_t ntc = (uint32_t)cdiv(cols, TC), ntiles = (uint32_t)(cdiv(rows, TR) * ntc);
   const int t = threadIdx.x;
   // full tiles are fetched into registers one iteration ahead; ragged edge
   // tiles are loaded element by element when their turn comes
   TileRegs<DT, TR> pre;
-  auto is_full = [&](int64_t id) { return (id / ntc + 1) * TR <= rows && (id % ntc + 1) * TC <= cols; };
+  auto is_full = [&](uint32_t tr, uint32_t tc) {
+    return (int64_t)(tr + 1) * TR <= rows && (int64_t)(tc + 1) * TC <= cols;
+  };
+  uint32_t tr_n = blockIdx.x / ntc, tc_n = blockIdx.x - tr_n * ntc;   // next tile's coordinates
   bool pre_full = false;
-  if ((int64_t)blockIdx.x < ntr * ntc && is_full(blockIdx.x)) {
-    tile_fetch<DT, TR>(x, ldx, (blockIdx.x / ntc) * TR, (blockIdx.x % ntc) * TC, pre);
+  if (blockIdx.x < ntiles && is_full(tr_n, tc_n)) {
+    tile_fetch<DT, TR>(x, ldx, (int64_t)tr_n * TR, (int64_t)tc_n * TC, pre);
     pre_full = true;
   }
-  for (int64_t tid = blockIdx.x; tid < ntr * ntc; tid += gridDim.x) {
-    int64_t r0 = (tid / ntc) * TR, c0 = (tid % ntc) * TC;
+  for (uint32_t tid = blockIdx.x; tid < ntiles; tid += gridDim.x) {
+    const int64_t r0 = (int64_t)tr_n * TR, c0 = (int64_t)tc_n * TC;
     if (pre_full)
       tile_store<DT, TR>(pre, tile);
     else
       load_tile<DT, TR>(x, rows, cols, ldx, r0, c0, tile);
     __syncthreads();
-    const int64_t nxt = tid + gridDim.x;
-    pre_full = nxt < ntr * ntc && is_full(nxt);
-    if (pre_full) tile_fetch<DT, TR>(x, ldx, (nxt / ntc) * TR, (nxt % ntc) * TC, pre);
+    const uint32_t nxt = tid + gridDim.x;
+    tr_n = nxt / ntc;
+    tc_n = nxt - tr_n * ntc;
+    pre_full = nxt < ntiles && is_full(tr_n, tc_n);
+    if (pre_full) tile_fetch<DT, TR>(x, ldx, (int64_t)tr_n * TR, (int64_t)tc_n * TC, pre);
     if constexpr (DO_COLS) {
       // column item: column c of the tile, row-block rb (B rows); lanes = columns
       int c = t % TC, rb = t / TC;
@@ -442,16 +452,36 @@ __global__ void __launch_bounds__(kThreads) rht_cols_kernel(const void* __restri
 // Branch-free: with step 2^(e-1), e = [a >= 2] + [a >= 4], t = a / step is exact
 // and u = 2 (t - floor(t)) - 1 is the local coordinate.  powf(0, negative) is
 // +inf, so u = 0 lands on the clamp without a special case.
+//
+// K5: k = 5 (the pages' value), y = |u|^(-4/5) without powf.  y solves
+// y^5 u^4 = 1; a fast estimate y0 = __powf(|u|, -0.8) (relative error ~1e-6)
+// takes one Newton step for that equation, y1 = y0 (1 + (1 - y0^5 u^4) / 5),
+// which squares the relative error (to ~1e-12) and needs no division; what is
+// left is the fp32 rounding of the few products, a few ulp.  |u| is 0 or at
+// least 2^-24 (t has 24 significant bits), so u^4 >= 2^-96 stays normal; u = 0
+// gives y0 = inf and a NaN step, which fminf turns into the clamp, the same
+// value the general path reaches through powf(0, negative) = inf.
+template <bool K5>
 __device__ __forceinline__ float dge_fprime(float xs, float inv_k, float expo, float clamp, float outside) {
   const float a = fabsf(xs);
   const uint32_t e = (a >= 2.0f) + (a >= 4.0f);
   const float t = __fmul_rn(a, __uint_as_float((128u - e) << 23));
-  const float u = __fsub_rn(__fmul_rn(__fsub_rn(t, floorf(t)), 2.0f), 1.0f);
-  const float f = fminf(clamp, __fmul_rn(inv_k, powf(fabsf(u), expo)));
+  const float au = fabsf(__fsub_rn(__fmul_rn(__fsub_rn(t, floorf(t)), 2.0f), 1.0f));
+  float y;
+  if constexpr (K5) {
+    const float y0 = __powf(au, -0.8f);
+    const float u2 = __fmul_rn(au, au), u4 = __fmul_rn(u2, u2);
+    const float y2 = __fmul_rn(y0, y0), y5 = __fmul_rn(__fmul_rn(y2, y2), y0);
+    const float e5 = __fmul_rn(y5, u4);
+    y = __fmul_rn(y0, __fmaf_rn(-0.2f, e5, 1.2f));
+  } else {
+    y = powf(au, expo);
+  }
+  const float f = fminf(clamp, __fmul_rn(inv_k, y));
   return a >= 6.0f ? outside : f;
 }
 
-template <int FMT, int XDT, int DYDT>
+template <int FMT, int XDT, int DYDT, bool K5>
 __global__ void __launch_bounds__(kThreads) dge_kernel(const void* __restrict__ x, int64_t ldx, fp4_operand q,
                                                        const void* __restrict__ dy, int64_t lddy, float* dx,
                                                        int64_t lddx, float inv_k, float expo, float clamp,
@@ -460,9 +490,18 @@ __global__ void __launch_bounds__(kThreads) dge_kernel(const void* __restrict__ 
   const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
   const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
   const int64_t total = q.rows * nsf_row;
+  const bool small = total < (int64_t(1) << 31);  // 32-bit index math
   for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
        blk += (int64_t)gridDim.x * blockDim.x) {
-    int64_t r = blk / nsf_row, j = blk - r * nsf_row;
+    int64_t r, j;
+    if (small) {
+      const uint32_t b32 = (uint32_t)blk, n32 = (uint32_t)nsf_row, r32 = b32 / n32;
+      r = r32;
+      j = b32 - r32 * n32;
+    } else {
+      r = blk / nsf_row;
+      j = blk - r * nsf_row;
+    }
     uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
     float mult;
     if (FMT == FP4_FMT_MXFP4) {
@@ -478,7 +517,8 @@ __global__ void __launch_bounds__(kThreads) dge_kernel(const void* __restrict__ 
       load8<DYDT>(dy, r * lddy + j * B + 8 * q8, d);
       float o[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(d[e], dge_fprime(__fmul_rn(v[e], mult), inv_k, expo, clamp, outside));
+      for (int e = 0; e < 8; ++e)
+        o[e] = __fmul_rn(d[e], dge_fprime<K5>(__fmul_rn(v[e], mult), inv_k, expo, clamp, outside));
       float4* dst = reinterpret_cast<float4*>(dx + r * lddx + j * B + 8 * q8);
       dst[0] = make_float4(o[0], o[1], o[2], o[3]);
       dst[1] = make_float4(o[4], o[5], o[6], o[7]);
@@ -539,6 +579,7 @@ cudaError_t launch_amax(const void* x, int dt, int64_t rows, int64_t cols, int64
   // multiple of 16: column items of the tiled kernel (64 x 64 tiles)
   QuantOut none{};
   int64_t ntiles = cdiv(rows, 64) * cdiv(cols, TC);
+  if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
   FP4_DISPATCH_DT(dt, DT, tile_kernel<FP4_FMT_NVFP4, DT, T_AMAX_COLS><<<grid, kThreads, 0, st>>>(
       x, rows, cols, ldx, none, none, 0, rht_signs, 0u, rht_axis == 0 ? 1 : 0, 0, amax_out, nullptr));
@@ -554,6 +595,7 @@ cudaError_t launch_amax_dual(const void* x, int dt, int64_t rows, int64_t cols, 
   if (e != cudaSuccess || rows == 0 || cols == 0) return e;
   QuantOut none{};
   int64_t ntiles = cdiv(rows, 64) * cdiv(cols, TC);
+  if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
   FP4_DISPATCH_DT(dt, DT, tile_kernel<FP4_FMT_NVFP4, DT, T_AMAX_DUAL><<<grid, kThreads, 0, st>>>(
       x, rows, cols, ldx, none, none, 0, signs_cols, signs_rows, rht_cols, rht_rows, amax_cols, amax_rows));
@@ -575,6 +617,7 @@ cudaError_t launch_quant_tile(const void* x, int dt, int64_t rows, int64_t cols,
   if (rows == 0 || cols == 0) return cudaSuccess;
   int TRv = fmt == FP4_FMT_MXFP4 ? 128 : 64;
   int64_t ntiles = cdiv(rows, TRv) * cdiv(cols, TC);
+  if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
   if (transpose) {
     FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT, tile_kernel<FMT, DT, T_Q_COLS><<<grid, kThreads, 0, st>>>(
@@ -591,6 +634,7 @@ cudaError_t launch_quant_dual(const void* x, int dt, int64_t rows, int64_t cols,
   if (rows == 0 || cols == 0) return cudaSuccess;
   int TRv = fmt == FP4_FMT_MXFP4 ? 128 : 64;
   int64_t ntiles = cdiv(rows, TRv) * cdiv(cols, TC);
+  if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
   FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT, tile_kernel<FMT, DT, T_Q_DUAL><<<grid, kThreads, 0, st>>>(
       x, rows, cols, ldx, ocol, orow, 0, ocol.rht_signs, orow.rht_signs, ocol.rht, orow.rht, nullptr, nullptr)));
@@ -630,11 +674,21 @@ cudaError_t launch_dge(const void* x, int xdt, int64_t ldx, const fp4_operand& q
   if (total == 0) return cudaSuccess;
   int grid = grid_for(total, kThreads, num_sms);
   float inv_k = 1.0f / k, expo = 1.0f / k - 1.0f;
-  FP4_DISPATCH_FMT(q.format, FMT, FP4_DISPATCH_DT(xdt, XDT,
-    if (dydt == FP4_DTYPE_BF16)
-      dge_kernel<FMT, XDT, FP4_DTYPE_BF16><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo, clamp, outside);
-    else
-      dge_kernel<FMT, XDT, FP4_DTYPE_F32><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo, clamp, outside)));
+  const bool k5 = k == 5.0f;
+#define FP4_DGE_LAUNCH(K5)                                                                                      \
+  FP4_DISPATCH_FMT(q.format, FMT, FP4_DISPATCH_DT(xdt, XDT,                                                      \
+    if (dydt == FP4_DTYPE_BF16)                                                                                  \
+      dge_kernel<FMT, XDT, FP4_DTYPE_BF16, K5><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo, \
+                                                                          clamp, outside);                       \
+    else                                                                                                         \
+      dge_kernel<FMT, XDT, FP4_DTYPE_F32, K5><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo,  \
+                                                                         clamp, outside)))
+  if (k5) {
+    FP4_DGE_LAUNCH(true);
+  } else {
+    FP4_DGE_LAUNCH(false);
+  }
+#undef FP4_DGE_LAUNCH
   return cudaGetLastError();
 }
 
