@@ -19,8 +19,9 @@
 //   warps 2-5    scale-factor stagers, one per TMEM lane quadrant: copy the
 //                stage's scale factors shared -> registers -> tensor memory
 //                (tcgen05.st), so the copies stay out of the MMA pipe
-//   warps 6-13   epilogue, two per lane quadrant (128 columns each):
-//                tcgen05.ld of the accumulator, * alpha, store
+//   warps 6-21   epilogue, four per lane quadrant (64 columns each): both
+//                32-column tcgen05.ld in flight, one wait, the accumulator
+//                is released, then * alpha and store from registers
 // Every wait is bounded (globaltimer); a wait that gives up sets the context's
 // status word and the CTA drains and exits.
 #include <cuda.h>
@@ -45,7 +46,7 @@ constexpr int SF_A_MAX = 4 * 512;          // NVFP4: 4 atoms of 128 rows x 4 sca
 constexpr int SF_B_MAX = (BN / 128) * 4 * 512;
 constexpr int STAGE_BYTES = A_TILE + B_TILE + SF_A_MAX + SF_B_MAX;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_EPI_WARPS = 16;
 constexpr int NUM_THREADS = 32 * (6 + NUM_EPI_WARPS);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = BN;      // scale-factor slots after the accumulator
@@ -232,51 +233,101 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// one accumulator row's 32 consecutive columns (col0 < N) -> C, times alpha
-__device__ __forceinline__ void store_chunk(const Params& p, const uint32_t* r, int row, int col0, float alpha) {
-  const int ncol = min(32, p.N - col0);
-  if (p.out_bf16) {
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col0;
-    if (ncol == 32 && !p.accumulate) {
+// Accumulator rows -> coalesced stores.  tcgen05.ld (32x32b) gives lane t the
+// 32 words of row t; stored as is, every store instruction would touch 32
+// rows.  Exchanging lane bits 4..2 with word bits 4..2 (three butterfly
+// stages of shfl.xor; at stage m the lanes with bit m set trade their words j,
+// j without bit m, for their partner's words j + m) leaves lane 4b + a holding
+// w[4v + k] = (row 4v + a, word column 4b + k): each lane has 4 consecutive
+// words of one row for every v, and one 16-byte store per lane covers four
+// whole 128-byte row segments per warp instruction.
+__device__ __forceinline__ void warp_exchange_hi3(uint32_t* w, int lane) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[4];
+  for (int m = 16; m >= 4; m >>= 1) {
+    const bool upper = (lane & m) != 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * q + 2 * i]), alpha),
-                                                   __fmul_rn(__uint_as_float(r[8 * q + 2 * i + 1]), alpha));
-          w[i] = *reinterpret_cast<uint32_t*>(&h);
+    for (int j = 0; j < 32; ++j) {
+      if (j & m) continue;
+      const uint32_t send = upper ? w[j] : w[j + m];
+      const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
+      if (upper)
+        w[j] = recv;
+      else
+        w[j + m] = recv;
+    }
+  }
+}
+
+// After warp_exchange_hi3 on 32 columns of fp32 accumulators: lane 4b + a
+// writes columns col0 + 4b .. +3 of rows row0 + 4v + a (times alpha; C += when
+// accumulating), fp32 or bf16 out.
+__device__ __forceinline__ void store_exchanged(const Params& p, const uint32_t* w, int row0, int col0, float alpha,
+                                                int lane) {
+  const int a = lane & 3, c = col0 + 4 * (lane >> 2);
+  if (c >= p.N) return;
+  const bool full4 = c + 4 <= p.N;
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const int row = row0 + 4 * v + a;
+    if (row >= p.M) break;
+    float x[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k] = __fmul_rn(__uint_as_float(w[4 * v + k]), alpha);
+    if (p.out_bf16) {
+      __nv_bfloat16* q = static_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + c;
+      if (full4 && !p.accumulate) {
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(x[0], x[1]), h1 = __floats2bfloat162_rn(x[2], x[3]);
+        *reinterpret_cast<uint2*>(q) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (c + k >= p.N) break;
+          float y = x[k];
+          if (p.accumulate) y = __fadd_rn(__bfloat162float(q[k]), y);
+          q[k] = __float2bfloat16_rn(y);
         }
-        reinterpret_cast<uint4*>(out)[q] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     } else {
+      float* q = static_cast<float*>(p.C) + (int64_t)row * p.ldc + c;
+      if (full4) {
+        float4 y = make_float4(x[0], x[1], x[2], x[3]);
+        if (p.accumulate) {
+          const float4 o = *reinterpret_cast<const float4*>(q);
+          y.x = __fadd_rn(o.x, y.x); y.y = __fadd_rn(o.y, y.y); y.z = __fadd_rn(o.z, y.z); y.w = __fadd_rn(o.w, y.w);
+        }
+        *reinterpret_cast<float4*>(q) = y;
+      } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {  // fully unrolled: r stays in registers
-        if (i >= ncol) break;
-        float v = __fmul_rn(__uint_as_float(r[i]), alpha);
-        if (p.accumulate) v = __fadd_rn(__bfloat162float(out[i]), v);
-        out[i] = __float2bfloat16_rn(v);
+        for (int k = 0; k < 4; ++k) {
+          if (c + k >= p.N) break;
+          q[k] = p.accumulate ? __fadd_rn(q[k], x[k]) : x[k];
+        }
       }
     }
-  } else {
-    float* out = static_cast<float*>(p.C) + (int64_t)row * p.ldc + col0;
-    if (ncol == 32) {
+  }
+}
+
+// bf16 out without accumulation, 64 columns: word i of w packs columns 2i and
+// 2i + 1 (scaled and rounded).  After warp_exchange_hi3 lane 4b + a holds
+// columns col0 + 8b .. +7 of rows row0 + 4v + a: one 16-byte store each.
+__device__ __forceinline__ void store_exchanged_bf16x2(const Params& p, const uint32_t* w, int row0, int col0,
+                                                       int lane) {
+  const int a = lane & 3, c = col0 + 8 * (lane >> 2);
+  if (c >= p.N) return;
+  const bool full8 = c + 8 <= p.N;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        float4 v = make_float4(__fmul_rn(__uint_as_float(r[4 * q]), alpha), __fmul_rn(__uint_as_float(r[4 * q + 1]), alpha),
-                               __fmul_rn(__uint_as_float(r[4 * q + 2]), alpha), __fmul_rn(__uint_as_float(r[4 * q + 3]), alpha));
-        if (p.accumulate) {
-          float4 o = reinterpret_cast<float4*>(out)[q];
-          v.x = __fadd_rn(o.x, v.x); v.y = __fadd_rn(o.y, v.y); v.z = __fadd_rn(o.z, v.z); v.w = __fadd_rn(o.w, v.w);
-        }
-        reinterpret_cast<float4*>(out)[q] = v;
-      }
+  for (int v = 0; v < 8; ++v) {
+    const int row = row0 + 4 * v + a;
+    if (row >= p.M) break;
+    uint16_t* q = static_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + c;
+    if (full8) {
+      *reinterpret_cast<uint4*>(q) = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
     } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (i >= ncol) break;
-        float v = __fmul_rn(__uint_as_float(r[i]), alpha);
-        out[i] = p.accumulate ? __fadd_rn(out[i], v) : v;
+      for (int k = 0; k < 8; ++k) {
+        if (c + k >= p.N) break;
+        q[k] = (uint16_t)(w[4 * v + (k >> 1)] >> (16 * (k & 1)));
       }
     }
   }
@@ -295,7 +346,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* sf_ready = empty + STAGES;
-  uint64_t* acc_full = sf_ready + STAGES;
+  uint64_t* sf_full = sf_ready + STAGES;   // the stage's scale atoms landed (before its A/B slabs)
+  uint64_t* acc_full = sf_full + STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -312,6 +364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&sf_ready[s], 4);
+      mbar_init(&sf_full[s], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, NUM_EPI_WARPS);
@@ -347,14 +400,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kt = 0; kt < total_k; ++kt) {
           if (!mbar_wait(&empty[s], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           if (kt < p.k_tiles) {
-            mbar_expect_tx(&full[s], A_TILE + B_TILE + sf_bytes * (1 + BN / 128));
+            // scale atoms first (rows of 128 bytes inside a 128-row group): they
+            // land, and are staged into tensor memory, while the slabs stream in
+            mbar_expect_tx(&sf_full[s], sf_bytes * (1 + BN / 128));
+            tma_load_3d(stage_sfa(s), &tm_sfa, &sf_full[s], 0, kt * atoms * 4, tm);
+            tma_load_3d(stage_sfb(s), &tm_sfb, &sf_full[s], 0, kt * atoms * 4, tn * (BN / 128));
+            mbar_expect_tx(&full[s], A_TILE + B_TILE);
             tma_load_2d(stage_a(s), &tm_a, &full[s], kt * KSLAB, tm * BM);
             tma_load_2d(stage_b(s), &tm_b, &full[s], kt * KSLAB, tn * BN);
-            // scale atoms of this stage: rows of 128 bytes inside a 128-row group
-            tma_load_3d(stage_sfa(s), &tm_sfa, &full[s], 0, kt * atoms * 4, tm);
-            tma_load_3d(stage_sfb(s), &tm_sfb, &full[s], 0, kt * atoms * 4, tn * (BN / 128));
           } else {
             const int kx = kt - p.k_tiles;
+            mbar_arrive(&sf_full[s]);   // no scales in the bf16 stages
             mbar_expect_tx(&full[s], A_TILE + B_TILE);
             tma_load_2d(stage_a(s), &tm_ax, &full[s], kx * 64, tm * BM);
             tma_load_2d(stage_b(s), &tm_bx, &full[s], kx * 64, tn * BN);
@@ -441,11 +497,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       for (int kt = 0; kt < total_k; ++kt) {
         bool got = true;
-        if (lane == 0) got = mbar_wait(&full[s], phase, abort_flag, p.status);
+        if (lane == 0) got = mbar_wait(&sf_full[s], phase, abort_flag, p.status);
         if (__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) == 0) { ok = false; break; }
         if (kt < p.k_tiles) {
           const uint32_t slot = tmem + lane_base + TMEM_SF_BASE + (uint32_t)s * SF_SLOT_COLS;
-          uint32_t v[32];
+          uint32_t v[16];
           if (nvfp4) {
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
@@ -453,17 +509,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               v[4 * a] = w.x; v[4 * a + 1] = w.y; v[4 * a + 2] = w.z; v[4 * a + 3] = w.w;
             }
             tmem_st16(slot, v);
+            // B: column (2a + g) * 4 holds atom a of 128-row group g; two halves of 16 columns
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
+            for (int hb = 0; hb < 2; ++hb) {
 #pragma unroll
-              for (int g = 0; g < 2; ++g) {
-                const uint4 w = *reinterpret_cast<const uint4*>(stage_sfb(s) + g * 4 * 512 + a * 512 + lane * 16);
-                const int c = (a * 2 + g) * 4;
-                v[c] = w.x; v[c + 1] = w.y; v[c + 2] = w.z; v[c + 3] = w.w;
+              for (int a2 = 0; a2 < 2; ++a2) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                  const int a = hb * 2 + a2;
+                  const uint4 w = *reinterpret_cast<const uint4*>(stage_sfb(s) + g * 4 * 512 + a * 512 + lane * 16);
+                  const int c = (a2 * 2 + g) * 4;
+                  v[c] = w.x; v[c + 1] = w.y; v[c + 2] = w.z; v[c + 3] = w.w;
+                }
               }
+              tmem_st16(slot + sfb_off + 16 * hb, v);
             }
-            tmem_st16(slot + sfb_off, v);
-            tmem_st16(slot + sfb_off + 16, v + 16);
           } else {
 #pragma unroll
             for (int a = 0; a < 2; ++a) {
@@ -491,9 +551,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 6..13) ----------------
+    // ---------------- epilogue (warps 6..21) ----------------
+    // The accumulator is single-buffered, so the MMAs of the next tile wait
+    // until every epilogue warp has its columns in registers: each warp loads
+    // all of its 64 columns with one wait and releases before it stores.
     const int quad = warp & 3;               // TMEM lanes 32*quad .. 32*quad+31
-    const int half = (warp - 6) >> 2;        // accumulator columns half*128 .. +127
+    const int slice = (warp - 6) >> 2;       // accumulator columns 64*slice .. +63
     uint32_t acc_phase = 0;
     float alpha = 1.0f;
     if (p.nvfp4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
@@ -505,28 +568,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       acc_phase ^= 1;
       tc_fence_after();
-      const int row = tm * BM + quad * 32 + lane;
-      const bool row_ok = row < p.M;
-#pragma unroll 1
-      for (int pair = 0; pair < 2; ++pair) {
-        // two 32-column loads in flight, one wait; after the second pair every
-        // column this warp owns is in registers and the accumulator is released
-        const int cbase = half * (BN / 2) + pair * 64;
+      const int row0 = tm * BM + quad * 32;        // this warp's 32 rows
+      const int cbase = slice * 64;
+      const int colw = tn * BN + cbase;             // first output column of the slice
+      const bool any = row0 < p.M && colw < p.N;   // warp-uniform
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)cbase;
+      if (p.out_bf16 && !p.accumulate) {
         uint32_t r2[2][32];
-        tmem_ld32_nowait(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)cbase, r2[0]);
-        tmem_ld32_nowait(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cbase + 32), r2[1]);
+        tmem_ld32_nowait(taddr, r2[0]);
+        tmem_ld32_nowait(taddr + 32, r2[1]);
         tmem_ld_wait();
-        if (pair == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty);
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+        if (any) {
+          // word i packs columns 2i, 2i+1 of the slice
+          uint32_t pk[32];
 #pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const uint32_t* r = r2[i >> 4];
+            const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * (i & 15)]), alpha),
+                                                           __fmul_rn(__uint_as_float(r[2 * (i & 15) + 1]), alpha));
+            pk[i] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          warp_exchange_hi3(pk, lane);
+          store_exchanged_bf16x2(p, pk, row0, colw, lane);
+        }
+      } else {
+        // fp32 out or C += : 32 columns at a time, so the exchange and the
+        // read-modify-write fit the register budget (the release waits for
+        // the second load)
+#pragma unroll 1
         for (int h = 0; h < 2; ++h) {
-          const uint32_t* r = r2[h];
-          const int col0 = tn * BN + cbase + 32 * h;
-          if (!row_ok || col0 >= p.N) continue;
-          store_chunk(p, r, row, col0, alpha);
+          uint32_t r[32];
+          tmem_ld32_nowait(taddr + 32 * h, r);
+          tmem_ld_wait();
+          if (h == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+          }
+          if (any) {
+            warp_exchange_hi3(r, lane);
+            store_exchanged(p, r, row0, colw + 32 * h, alpha, lane);
+          }
         }
       }
     }
