@@ -4,13 +4,14 @@
 One step = the forward and backward pass of the MLP up-projection
 Y[M,N] = X[M,K] W[N,K]^T with M = 8192 tokens, K = 2048, N = 5632 in NVFP4:
 
-  forward   quantize X and W (RTN, 1D blocks of 16 along K, E4M3 scale x
-            per-tensor fp32 scale), fprop GEMM  Y = Xq Wq^T          (bf16 out)
+  forward   quantize X and W, each in both layouts from one read: the forward
+            layout (RTN, 1D blocks of 16 along K, E4M3 scale x per-tensor fp32
+            scale) and the backward one (transposed, SR + RHT16 along the
+            blocked axis; 16x16 2D blocks for W); fprop GEMM Y = Xq Wq^T (bf16)
   backward  quantize dY in both layouts from one read (SR + RHT16 along N for
-            dgrad, along M for wgrad), W (SR + RHT16 + 16x16 2D blocks,
-            transposed) and X (SR + RHT16 along M, transposed);
-            dgrad GEMM dX = dYq Wq_t^T (bf16), wgrad GEMM dW = dYq_m Xq_t^T
-            (fp32); DGE backward dW' = dW * f'(W / s_W) (k = 5, clamp 3.0)
+            dgrad, along M for wgrad); dgrad GEMM dX = dYq Wq_t^T (bf16),
+            wgrad GEMM dW = dYq_m Xq_t^T (fp32); DGE backward
+            dW' = dW * f'(W / s_W) (k = 5, clamp 3.0)
 
 Every step runs in the library's CUDA kernels through the C ABI.  Inputs are
 seeded synthetic tensors (X ~ N(0,1), W ~ N(0,0.02), dY ~ N(0,1e-3)) resident
@@ -42,7 +43,8 @@ GEMM_FLOPS = 2 * M * N * K          # per GEMM; three per step
 STEP_FLOPS = 3 * GEMM_FLOPS
 FP4_OVER_BF16 = 13.5 / 2.25         # nominal dense FP4 : BF16 tensor rate
 WORKLOAD = ("llama1b_mlp_up fwd+bwd: X[8192,2048] W[5632,2048] dY[8192,5632] bf16; NVFP4; fwd RTN 1D, "
-            "bwd SR + RHT16 (+16x16 2D on W); fprop/dgrad/wgrad GEMMs; DGE (k=5, clamp 3) on W")
+            "bwd SR + RHT16 (+16x16 2D on W); each of X, W, dY quantized in both layouts from one read; "
+            "fprop/dgrad/wgrad GEMMs; DGE (k=5, clamp 3) on W")
 
 
 def parse():
@@ -60,21 +62,20 @@ def parse():
 # ---------------------------------------------------------------------------
 # algorithmic bytes per element of each op (one read of inputs + writes)
 # ---------------------------------------------------------------------------
-NV_Q_BYTES = 2 + 0.5 + 1 / 16        # bf16 in, packed codes, one E4M3 byte per 16
+DUAL_Q_BYTES = 2 + 2 * (0.5 + 1 / 16)  # bf16 in once; codes + E4M3 bytes for both layouts
 OPS = {
     #  name           kind     units per launch (bytes or flops)
-    "quant_x":      ("hbm", M * K * NV_Q_BYTES),
-    "quant_w":      ("hbm", N * K * NV_Q_BYTES),
-    "fprop":        ("tensor", GEMM_FLOPS),
-    "quant_dy_dual": ("hbm", M * N * (2 + 2 * (0.5 + 1 / 16))),
-    "quant_w_t2d":  ("hbm", N * K * NV_Q_BYTES),
-    "quant_x_t":    ("hbm", M * K * NV_Q_BYTES),
-    "dgrad":        ("tensor", GEMM_FLOPS),
-    "wgrad":        ("tensor", GEMM_FLOPS),
-    "dge":          ("hbm", N * K * (2 + 4 + 4) + N * K / 16),
+    "quant_x_dual":  ("hbm", M * K * DUAL_Q_BYTES),
+    "quant_w_dual":  ("hbm", N * K * DUAL_Q_BYTES),
+    "fprop":         ("tensor", GEMM_FLOPS),
+    "quant_dy_dual": ("hbm", M * N * DUAL_Q_BYTES),
+    "dgrad":         ("tensor", GEMM_FLOPS),
+    "wgrad":         ("tensor", GEMM_FLOPS),
+    "dge":           ("hbm", N * K * (2 + 4 + 4) + N * K / 16),
 }
-KERNELS_PER_OP = {"quant_x": 2, "quant_w": 2, "fprop": 1, "quant_dy_dual": 2, "quant_w_t2d": 2,
-                  "quant_x_t": 2, "dgrad": 1, "wgrad": 1, "dge": 1}
+# our kernels per op: amax (both layouts) + quantize (both layouts) for each dual
+KERNELS_PER_OP = {"quant_x_dual": 2, "quant_w_dual": 2, "fprop": 1, "quant_dy_dual": 2, "dgrad": 1, "wgrad": 1,
+                  "dge": 1}
 
 
 class Step:
@@ -107,13 +108,13 @@ class Step:
         for p in (self.p_dy_n, self.p_w_t, self.p_dy_m, self.p_x_t):
             p.sr_offset = off
         return [
-            ("quant_x", lambda: f.fp4_quantize(self.X, self.p_fwd, out=self.xq)),
-            ("quant_w", lambda: f.fp4_quantize(self.W, self.p_fwd, out=self.wq)),
+            ("quant_x_dual", lambda: f.fp4_quantize_dual(self.X, self.p_fwd, self.p_x_t, out_rows=self.xq,
+                                                         out_cols=self.xq_t)),
+            ("quant_w_dual", lambda: f.fp4_quantize_dual(self.W, self.p_fwd, self.p_w_t, out_rows=self.wq,
+                                                         out_cols=self.wq_t)),
             ("fprop", lambda: f.fp4_gemm(self.xq, self.wq, out=self.Y)),
             ("quant_dy_dual", lambda: f.fp4_quantize_dual(self.dY, self.p_dy_n, self.p_dy_m, out_rows=self.dyq_n,
                                                           out_cols=self.dyq_m)),
-            ("quant_w_t2d", lambda: f.fp4_quantize(self.W, self.p_w_t, out=self.wq_t)),
-            ("quant_x_t", lambda: f.fp4_quantize(self.X, self.p_x_t, out=self.xq_t)),
             ("dgrad", lambda: f.fp4_gemm(self.dyq_n, self.wq_t, out=self.dX)),
             ("wgrad", lambda: f.fp4_gemm(self.dyq_m, self.xq_t, out=self.dW)),
             ("dge", lambda: f.fp4_dge_backward(self.W, self.wq, self.dW, 5.0, 3.0, 1.0, out=self.dWd)),

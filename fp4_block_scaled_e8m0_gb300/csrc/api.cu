@@ -215,10 +215,13 @@ int fp4_quantize_dual(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows
   s = check_params(pc);
   if (s) return s;
   if (pr->format != pc->format || pr->transpose != 0 || pc->transpose != 1) return FP4_ERR_INVALID_ARG;
-  if (pr->scaling != FP4_SCALING_1D || pc->scaling != FP4_SCALING_1D) return FP4_ERR_UNSUPPORTED;
   s = check_input(x, x_dtype, rows, cols, ldx);
   if (s) return s;
   if (cols % pr->block || rows % pc->block) return FP4_ERR_INVALID_ARG;
+  // 16x16 2D scaling: output rows in groups of 16 (rows of x for the row
+  // layout, cols of x for the transposed one)
+  if ((pr->scaling == FP4_SCALING_2D && rows % 16) || (pc->scaling == FP4_SCALING_2D && cols % 16))
+    return FP4_ERR_INVALID_ARG;
   if (!al16(codes_rows) || !al16(codes_cols)) return FP4_ERR_MISALIGNED;
   if (rows == 0 || cols == 0) return FP4_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -237,7 +240,8 @@ int fp4_quantize_dual(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows
   if (clear_sf_padding(pc, scales_cols, cols, rows, st) != cudaSuccess) return FP4_ERR_CUDA;
   QuantOut orow = make_out(pr, codes_rows, scales_rows, ts_rows, amax_r, rows, cols);
   QuantOut ocol = make_out(pc, codes_cols, scales_cols, ts_cols, amax_c, cols, rows);
-  return cuda_status(launch_quant_dual(x, x_dtype, rows, cols, ldx, pr->format, orow, ocol, ctx->num_sms, st));
+  return cuda_status(launch_quant_dual(x, x_dtype, rows, cols, ldx, pr->format, orow, ocol,
+                                      pr->scaling == FP4_SCALING_2D, pc->scaling == FP4_SCALING_2D, ctx->num_sms, st));
 }
 
 int fp4_dequantize(fp4_ctx* ctx, const fp4_operand* q, int32_t out_dtype, void* out, int64_t ldo, void* stream) {

@@ -27,11 +27,37 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
+// read-only load that allocates in L1: a thread's second 16 bytes of a 32-byte
+// sector then hit L1 instead of fetching the sector from L2 again
+__device__ __forceinline__ uint4 ld_nc_v4_l1(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// Division of 32-bit n by a divisor d fixed for the launch (1 <= d < 2^31), as
+// a multiply-high and two shifts: Granlund & Montgomery, "Division by
+// invariant integers using multiplication" (PLDI 1994), Fig. 4.1, with
+// l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1.
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+  return {d, (uint32_t)m, l < 1 ? 0u : 1u, l < 1 ? 0u : l - 1};
+}
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 // 8 consecutive input elements (16 bytes of bf16 or 32 bytes of fp32) -> fp32
-template <int DT>
+template <int DT, bool L1 = false>
 __device__ __forceinline__ void load8(const void* base, int64_t elem, float* v) {
   if constexpr (DT == FP4_DTYPE_BF16) {
-    uint4 q = ld_nc_v4(static_cast<const uint16_t*>(base) + elem);
+    uint4 q = L1 ? ld_nc_v4_l1(static_cast<const uint16_t*>(base) + elem) : ld_nc_v4(static_cast<const uint16_t*>(base) + elem);
     uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -40,7 +66,7 @@ __device__ __forceinline__ void load8(const void* base, int64_t elem, float* v) 
     }
   } else {
     const float* p = static_cast<const float*>(base) + elem;
-    uint4 a = ld_nc_v4(p), b = ld_nc_v4(p + 4);
+    uint4 a = L1 ? ld_nc_v4_l1(p) : ld_nc_v4(p), b = L1 ? ld_nc_v4_l1(p + 4) : ld_nc_v4(p + 4);
     v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
     v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
     v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);

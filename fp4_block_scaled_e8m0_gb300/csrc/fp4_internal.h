@@ -52,7 +52,8 @@ cudaError_t launch_quant_rows(const void* x, int dt, int64_t rows, int64_t cols,
 cudaError_t launch_quant_tile(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
                               bool two_d, bool transpose, const QuantOut& o, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_dual(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
-                              const QuantOut& orow, const QuantOut& ocol, int num_sms, cudaStream_t st);
+                              const QuantOut& orow, const QuantOut& ocol, bool two_d_rows, bool two_d_cols,
+                              int num_sms, cudaStream_t st);
 cudaError_t launch_dequant(const fp4_operand& q, int out_dt, void* out, int64_t ldo, int num_sms,
                            cudaStream_t st);
 cudaError_t launch_rht16(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int axis,

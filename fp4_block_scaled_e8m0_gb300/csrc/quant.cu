@@ -107,6 +107,45 @@ __global__ void __launch_bounds__(kThreads) amax_rows_kernel(const void* __restr
   block_amax_atomic(m, amax_out);
 }
 
+// Same reduction with 32-bit chunk ids (fewer than 2^31 chunks): a chunk's
+// address is 16 c when rows are contiguous, else (c / nch) ldx + 16 (c % nch)
+// with a precomputed divider; two chunks per iteration keep 64 bytes of bf16
+// in flight per thread.
+template <int DT, bool RHT>
+__global__ void __launch_bounds__(kThreads) amax_rows32_kernel(const void* __restrict__ x, int64_t ldx, FastDiv nch,
+                                                               uint32_t total, int contiguous, uint32_t signs,
+                                                               float* amax_out) {
+  float m = 0.0f;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  auto addr = [&](uint32_t c) -> int64_t {
+    if (contiguous) return (int64_t)c << 4;
+    const uint32_t r = fast_div(c, nch);
+    return (int64_t)r * ldx + ((int64_t)(c - r * nch.d) << 4);
+  };
+  for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < total; c += 2 * stride) {
+    const uint32_t c2 = c + stride;
+    const bool two = c2 < total && c2 > c;
+    float v[16], w[16];
+    const int64_t e = addr(c);
+    load8<DT, true>(x, e, v);
+    load8<DT, true>(x, e + 8, v + 8);
+    if (two) {
+      const int64_t e2 = addr(c2);
+      load8<DT, true>(x, e2, w);
+      load8<DT, true>(x, e2 + 8, w + 8);
+    }
+    if (RHT) rht16(v, signs);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
+    if (two) {
+      if (RHT) rht16(w, signs);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(w[j]));
+    }
+  }
+  block_amax_atomic(m, amax_out);
+}
+
 // ----------------------------------------------------------------------------
 // Row quantizer: blocks along cols, output [rows][cols/2].  One thread per block.
 // ----------------------------------------------------------------------------
@@ -144,6 +183,60 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const void* __rest
     if (two) {
 #pragma unroll
       for (int q = 0; q < B / 8; ++q) load8<DT>(x, r2 * ldx + k2 + 8 * q, w + 8 * q);
+    }
+    if (rht) {
+#pragma unroll
+      for (int h = 0; h < B / 16; ++h) rht16(v + 16 * h, o.rht_signs);
+    }
+    float amax_b = 0.0f;
+#pragma unroll
+    for (int j = 0; j < B; ++j) amax_b = fmaxf(amax_b, fabsf(v[j]));
+    encode_store_block<FMT, B>(v, g, o, r, k0, amax_b, sr);
+    if (two) {
+      if (rht) {
+#pragma unroll
+        for (int h = 0; h < B / 16; ++h) rht16(w + 16 * h, o.rht_signs);
+      }
+      float amax2 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < B; ++j) amax2 = fmaxf(amax2, fabsf(w[j]));
+      encode_store_block<FMT, B>(w, g, o, r2, k2, amax2, sr);
+    }
+  }
+}
+
+// Row quantizer with 32-bit block ids (fewer than 2^31 blocks): one thread per
+// block, two blocks per iteration with all four loads in flight; the block's
+// row and position come from a precomputed divider, and its input starts at
+// B * blk when rows are contiguous.  Loads allocate in L1 so that a thread's
+// second 16 bytes of each 32-byte sector do not fetch the sector again.
+// PLAIN: RTN without RHT (the forward path), compiled without the SR and RHT
+// code so that its register count, and so its occupancy, is not set by them.
+template <int FMT, int DT, bool PLAIN>
+__global__ void __launch_bounds__(kThreads) quant_rows32_kernel(const void* __restrict__ x, int64_t ldx, FastDiv nblk,
+                                                                uint32_t total, int contiguous, QuantOut o) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const float g = load_g(o, FMT);
+  const bool sr = !PLAIN && o.rounding == FP4_ROUND_SR;
+  const bool rht = !PLAIN && o.rht != 0;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t blk = blockIdx.x * blockDim.x + threadIdx.x; blk < total; blk += 2 * stride) {
+    const uint32_t blk2 = blk + stride;
+    const bool two = blk2 < total && blk2 > blk;
+    const uint32_t r = fast_div(blk, nblk), k0 = (blk - r * nblk.d) * B;
+    uint32_t r2 = 0, k2 = 0;
+    if (two) {
+      r2 = fast_div(blk2, nblk);
+      k2 = (blk2 - r2 * nblk.d) * B;
+    }
+    const int64_t e = contiguous ? (int64_t)blk * B : (int64_t)r * ldx + k0;
+    const int64_t e2 = contiguous ? (int64_t)blk2 * B : (int64_t)r2 * ldx + k2;
+    float v[B], w[B];
+#pragma unroll
+    for (int q = 0; q < B / 8; ++q) load8<DT, true>(x, e + 8 * q, v + 8 * q);
+    if (two) {
+#pragma unroll
+      for (int q = 0; q < B / 8; ++q) load8<DT, true>(x, e2 + 8 * q, w + 8 * q);
     }
     if (rht) {
 #pragma unroll
@@ -309,7 +402,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__
       if constexpr (!QUANT) {
         if (valid) m_c = fmaxf(m_c, a);
       } else {
-        if (two_d) {  // 16x16 tile: the 16 lanes of consecutive columns share one scale
+        if (two_d & 1) {  // 16x16 tile: the 16 lanes of consecutive columns share one scale
 #pragma unroll
           for (int o = 8; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
         }
@@ -334,7 +427,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__
         if constexpr (!QUANT) {
           if (valid) m_r = fmaxf(m_r, a);
         } else {
-          if (MODE == T_Q_ROWS2D) {
+          if (MODE == T_Q_ROWS2D || (two_d & 2)) {  // 16x16 tile: 16 lanes of consecutive rows
 #pragma unroll
             for (int o = 8; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
           }
@@ -569,7 +662,17 @@ cudaError_t launch_amax(const void* x, int dt, int64_t rows, int64_t cols, int64
   if (e != cudaSuccess) return e;
   if (rows == 0 || cols == 0) return cudaSuccess;
   if (rht_axis != 0 && cols % 16 == 0) {
-    int grid = grid_for(rows * (cols / 16), kThreads, num_sms);
+    const int64_t nch = cols / 16, total = rows * nch;
+    if (total < (int64_t(1) << 31)) {
+      int grid = grid_for(cdiv(total, 2), kThreads, num_sms);
+      const FastDiv fd = make_fastdiv((uint32_t)nch);
+      const int contiguous = ldx == cols;
+      FP4_DISPATCH_DT(dt, DT,
+        if (rht_axis == 1) amax_rows32_kernel<DT, true><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, rht_signs, amax_out);
+        else amax_rows32_kernel<DT, false><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, rht_signs, amax_out));
+      return cudaGetLastError();
+    }
+    int grid = grid_for(total, kThreads, num_sms);
     FP4_DISPATCH_DT(dt, DT,
       if (rht_axis == 1) amax_rows_kernel<DT, true><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, rht_signs, amax_out);
       else amax_rows_kernel<DT, false><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, rht_signs, amax_out));
@@ -606,7 +709,18 @@ cudaError_t launch_quant_rows(const void* x, int dt, int64_t rows, int64_t cols,
                               const QuantOut& o, int num_sms, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   int B = fmt == FP4_FMT_MXFP4 ? 32 : 16;
-  int grid = grid_for(rows * (cols / B), kThreads, num_sms);
+  const int64_t nblk = cols / B, total = rows * nblk;
+  if (total < (int64_t(1) << 31)) {
+    int grid = grid_for(cdiv(total, 2), kThreads, num_sms);
+    const FastDiv fd = make_fastdiv((uint32_t)nblk);
+    const int contiguous = ldx == cols;
+    const bool plain = o.rounding == FP4_ROUND_RTN && !o.rht;
+    FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT,
+      if (plain) quant_rows32_kernel<FMT, DT, true><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o);
+      else quant_rows32_kernel<FMT, DT, false><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o)));
+    return cudaGetLastError();
+  }
+  int grid = grid_for(total, kThreads, num_sms);
   FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT,
       quant_rows_kernel<FMT, DT><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, o)));
   return cudaGetLastError();
@@ -630,14 +744,16 @@ cudaError_t launch_quant_tile(const void* x, int dt, int64_t rows, int64_t cols,
 }
 
 cudaError_t launch_quant_dual(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
-                              const QuantOut& orow, const QuantOut& ocol, int num_sms, cudaStream_t st) {
+                              const QuantOut& orow, const QuantOut& ocol, bool two_d_rows, bool two_d_cols,
+                              int num_sms, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
   int TRv = fmt == FP4_FMT_MXFP4 ? 128 : 64;
   int64_t ntiles = cdiv(rows, TRv) * cdiv(cols, TC);
   if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
   FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT, tile_kernel<FMT, DT, T_Q_DUAL><<<grid, kThreads, 0, st>>>(
-      x, rows, cols, ldx, ocol, orow, 0, ocol.rht_signs, orow.rht_signs, ocol.rht, orow.rht, nullptr, nullptr)));
+      x, rows, cols, ldx, ocol, orow, (two_d_cols ? 1 : 0) | (two_d_rows ? 2 : 0), ocol.rht_signs, orow.rht_signs,
+      ocol.rht, orow.rht, nullptr, nullptr)));
   return cudaGetLastError();
 }
 

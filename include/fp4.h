@@ -152,8 +152,12 @@ int fp4_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int
                  uint8_t* codes, uint8_t* scales, float* tensor_scale, void* stream);
 
 /* Both operand layouts of one tensor from a single read (the dY of a linear
- * layer feeds dgrad with blocks along cols and wgrad with blocks along rows).
- * p_rows must have transpose 0, p_cols transpose 1; both 1D scaling.       */
+ * layer feeds dgrad with blocks along cols and wgrad with blocks along rows;
+ * X and W feed the forward GEMM in one layout and a backward GEMM in the
+ * other).  p_rows must have transpose 0, p_cols transpose 1, same format; each
+ * has its own rounding, RHT, scale layout and 1D or 16x16 2D scaling (2D needs
+ * its output rows in groups of 16).  The results equal two fp4_quantize calls
+ * with the same parameters, bit for bit.                                   */
 int fp4_quantize_dual(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols,
                       int64_t ldx, const fp4_quant_params* p_rows, const fp4_quant_params* p_cols,
                       const float* given_amax_rows, const float* given_amax_cols,

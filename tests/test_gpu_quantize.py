@@ -157,6 +157,31 @@ def test_quantize_dual(fmt, rounding, rht):
                  "dual cols")
 
 
+# Mixed parameters per layout, as a training step uses them: X and W go to the
+# forward GEMM with RTN and to a backward GEMM with SR + RHT (W also with 16x16
+# 2D blocks); each output must equal its own single-layout quantization.
+@pytest.mark.parametrize("case", ["x_fwd_bwd", "w_fwd_bwd2d", "rows2d_cols1d"])
+@pytest.mark.parametrize("sf_layout", [fp4.FP4_SF_ROWMAJOR, fp4.FP4_SF_MMA])
+def test_quantize_dual_mixed(case, sf_layout):
+    x, xn = _input((336, 208), seed=44)
+    x = x.cuda()
+    NV, RTN, SR, D1, D2 = fp4.FP4_FMT_NVFP4, fp4.FP4_ROUND_RTN, fp4.FP4_ROUND_SR, fp4.FP4_SCALING_1D, fp4.FP4_SCALING_2D
+    row_cfg, col_cfg = {
+        "x_fwd_bwd": ((RTN, D1, False), (SR, D1, True)),
+        "w_fwd_bwd2d": ((RTN, D1, False), (SR, D2, True)),
+        "rows2d_cols1d": ((RTN, D2, False), (RTN, D1, False)),
+    }[case]
+    kr = dict(sr_seed=7, sr_offset=3, sr_stream=1, rht_seed=5)
+    kc = dict(sr_seed=7, sr_offset=3, sr_stream=2, rht_seed=5)
+    pr = fp4.quant_params(NV, row_cfg[0], row_cfg[1], rht=row_cfg[2], sf_layout=sf_layout, **kr)
+    pc = fp4.quant_params(NV, col_cfg[0], col_cfg[1], transpose=True, rht=col_cfg[2], sf_layout=sf_layout, **kc)
+    qr, qc = fp4.fp4_quantize_dual(x, pr, pc)
+    mode = {RTN: "rtn", SR: "sr"}
+    sc = {D1: "1d", D2: "2d"}
+    _check_quant(qr, o.quantize(xn, o.NVFP4, mode[row_cfg[0]], sc[row_cfg[1]], False, row_cfg[2], **kr), case + " rows")
+    _check_quant(qc, o.quantize(xn, o.NVFP4, mode[col_cfg[0]], sc[col_cfg[1]], True, col_cfg[2], **kc), case + " cols")
+
+
 @pytest.mark.parametrize("axis", [-1, 0, 1])
 @pytest.mark.parametrize("shape", [(320, 208), (48, 40)])
 def test_amax(axis, shape):
