@@ -83,6 +83,7 @@ QuantOut make_out(const fp4_quant_params* p, uint8_t* codes, uint8_t* scales, fl
   o.sr_seed = p->sr_seed;
   o.sr_offset = p->sr_offset;
   o.rht_signs = p->rht ? rht_signs_host(p->rht_seed) : 0u;
+  o.keys = philox_round_keys(p->sr_seed);
   return o;
 }
 

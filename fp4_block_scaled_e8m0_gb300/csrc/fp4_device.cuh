@@ -119,6 +119,9 @@ __device__ __forceinline__ uint32_t e2m1_sw(float xs) {
 // the value there with rem = ceil(frac * 2^22), and for an integer n,
 // n < R iff n < ceil(R), so the same addition decides exactly; 1 is subtracted
 // again afterwards (exact).  fminf sends NaN to the saturated 6, like the clamp.
+// (e2m1_sr_value_finite below drops the clamp for the block quantizers, where
+// |xs| is finite and below 9 by construction of the block scale: from 6 up the
+// result is a value >= 6 that the saturating conversion maps to code 7.)
 __device__ __forceinline__ float e2m1_sr_value(float xs, uint32_t u16_shl6) {
   const float a = fminf(fabsf(xs), 6.0f);
   const float off = a < 1.0f ? 1.0f : 0.0f;
@@ -201,23 +204,8 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Philox with the ten round keys computed once (they depend on the seed only).
-struct PhiloxKeys {
-  uint32_t k0[10], k1[10];
-};
-__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
-  PhiloxKeys k;
-  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    k.k0[r] = a;
-    k.k1[r] = b;
-    a += 0x9E3779B9u;
-    b += 0xBB67AE85u;
-  }
-  return k;
-}
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKeys& k) {
+// Philox with precomputed round keys (fp4::philox_round_keys)
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const fp4::PhiloxRoundKeys& k) {
 #pragma unroll
   for (int rnd = 0; rnd < 10; ++rnd) {
     const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
@@ -235,22 +223,38 @@ __device__ __forceinline__ uint4 sr_bits8(uint64_t seed, uint64_t offset, uint32
   return philox4x32_10(make_uint4((uint32_t)n, (uint32_t)(n >> 32), 0u, stream),
                        (uint32_t)seed, (uint32_t)(seed >> 32));
 }
-__device__ __forceinline__ uint4 sr_bits8(const PhiloxKeys& keys, uint64_t offset, uint32_t stream,
+__device__ __forceinline__ uint4 sr_bits8(const fp4::PhiloxRoundKeys& keys, uint64_t offset, uint32_t stream,
                                           uint64_t first_elem) {
   uint64_t n = offset + (first_elem >> 3);
   return philox4x32_10(make_uint4((uint32_t)n, (uint32_t)(n >> 32), 0u, stream), keys);
 }
+__device__ __forceinline__ float e2m1_sr_value_finite(float xs, uint32_t u16_shl6) {
+  const float a = fabsf(xs);
+  const float off = a < 1.0f ? 1.0f : 0.0f;
+  const float b = __fadd_ru(a, off);
+  const uint32_t n = (__float_as_uint(b) + 0x3FFFFFu - u16_shl6) & 0xFFC00000u;
+  const float y = __fsub_rn(__uint_as_float(n), off);
+  return __uint_as_float(__float_as_uint(y) | (__float_as_uint(xs) & 0x80000000u));
+}
+
 // 64 * (16-bit lane j of w): the form e2m1_sr_value takes
 __device__ __forceinline__ uint32_t u16_lane_shl6(const uint4& w, int j) {
   uint32_t word = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
   return (j & 1) ? ((word >> 10) & 0x3FFFC0u) : ((word << 6) & 0x3FFFC0u);
+}
+// the same as multiplications, which the FP32/IMAD pipe can take instead of the
+// integer pipe: w * 64 and the high word of w * 2^22 (= w >> 10)
+__device__ __forceinline__ uint32_t u16_lane_shl6_mul(const uint4& w, int j) {
+  uint32_t word = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
+  return ((j & 1) ? __umulhi(word, 0x400000u) : word * 64u) & 0x3FFFC0u;
 }
 
 // ----------------------------------------------------------------------------
 // 16-point random Hadamard transform: y = 1/4 H16 diag(sigma) x, butterfly with
 // strides 1, 2, 4, 8 (fixed fp32 order)
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ void rht16(float* v, uint32_t sign_bits) {
+// signs and butterflies only: v becomes H16 diag(sigma) x (4x the transform)
+__device__ __forceinline__ void rht16_raw(float* v, uint32_t sign_bits) {
 #pragma unroll
   for (int j = 0; j < 16; ++j)
     v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((sign_bits >> j) & 1u) << 31));
@@ -264,6 +268,31 @@ __device__ __forceinline__ void rht16(float* v, uint32_t sign_bits) {
       v[i + h] = __fsub_rn(a, b);
     }
   }
+}
+// rht16_raw with the signs as multipliers sig[j] = +-1.0f (exact products):
+// the first butterfly stage becomes fma(x_i, s_i, +-(x_{i+1} s_{i+1})), the
+// same single rounding of the same sum as sign flip + add, on the FP32 pipe
+__device__ __forceinline__ void rht16_raw_mul(float* v, const float* sig) {
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const float t = __fmul_rn(v[i + 1], sig[i + 1]);
+    const float a = __fmaf_rn(v[i], sig[i], t);
+    v[i + 1] = __fmaf_rn(v[i], sig[i], -t);
+    v[i] = a;
+  }
+#pragma unroll
+  for (int h = 2; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & h) continue;
+      float a = v[i], b = v[i + h];
+      v[i] = __fadd_rn(a, b);
+      v[i + h] = __fsub_rn(a, b);
+    }
+  }
+}
+__device__ __forceinline__ void rht16(float* v, uint32_t sign_bits) {
+  rht16_raw(v, sign_bits);
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
 }

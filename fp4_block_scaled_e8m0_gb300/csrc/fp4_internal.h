@@ -24,6 +24,25 @@ struct fp4_ctx {
 
 namespace fp4 {
 
+// Philox4x32-10 round keys (Salmon et al., SC'11): round r uses
+// (seed_lo + r * 0x9E3779B9, seed_hi + r * 0xBB67AE85).  They depend on the
+// seed only, so the host computes them once and the kernels read them from
+// their parameters instead of holding twenty registers.
+struct PhiloxRoundKeys {
+  uint32_t k0[10], k1[10];
+};
+__host__ __device__ inline PhiloxRoundKeys philox_round_keys(uint64_t seed) {
+  PhiloxRoundKeys k;
+  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = a;
+    k.k1[r] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+  return k;
+}
+
 struct QuantOut {
   uint8_t* codes;
   uint8_t* scales;
@@ -39,6 +58,7 @@ struct QuantOut {
   uint32_t sr_stream;
   uint64_t sr_seed, sr_offset;
   uint32_t rht_signs;    // 16 sign bits
+  PhiloxRoundKeys keys;  // of sr_seed
 };
 
 // Launchers (quant.cu).  All return cudaError_t of the launch.

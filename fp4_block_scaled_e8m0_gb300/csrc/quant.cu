@@ -53,10 +53,9 @@ __device__ __forceinline__ void encode_store_block(const float* v, float g, cons
     }
   } else {
     int64_t first_elem = out_row * o.out_cols + out_col0;
-    const PhiloxKeys keys = philox_keys(o.sr_seed);   // loop-invariant: hoisted by the compiler
 #pragma unroll
     for (int q = 0; q < B / 8; ++q) {
-      uint4 bits = sr_bits8(keys, o.sr_offset, o.sr_stream, (uint64_t)(first_elem + 8 * q));
+      uint4 bits = sr_bits8(o.keys, o.sr_offset, o.sr_stream, (uint64_t)(first_elem + 8 * q));
       uint32_t w = 0;
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
@@ -447,6 +446,229 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__
 }
 
 // ----------------------------------------------------------------------------
+// NVFP4 with bf16 input (the training path): 64 x 128 tiles.
+//   row layout   each thread's four 16-byte loads are 32 consecutive elements
+//                of one row, i.e. two blocks: quantized straight from registers
+//   transposed   the raw bf16 tile is staged in shared memory; each thread
+//                reads one 32-bit word (two adjacent columns) from 16 rows and
+//                quantizes both columns' blocks
+// Shared memory: 68 words per tile row, word w stored at w ^ ((w & 32) >> 2):
+// the 16-byte staging stores of a quarter warp (two rows x four threads) and
+// the column reads of a warp (32 consecutive words of one row) each hit all
+// 32 banks once.
+// RHT without the per-element 1/4: the butterfly outputs w of bf16 inputs are
+// multiples of 2^-133, so w/4 is exact in fp32 and max|w/4| = max|w|/4; the
+// quantizer multiplies by r/4 instead of forming w/4 and then w/4 * r, which
+// is the same product as long as r/4 is exact (r >= 2^-124, else the two
+// multiplications are done as written).
+// ----------------------------------------------------------------------------
+constexpr int NV_TR = 64, NV_TC = 128, NV_SW = 68;
+
+// the 16 RHT signs as +-1.0f multipliers (kernel parameters)
+struct RhtSigns {
+  float s[16];
+};
+inline RhtSigns rht_sign_floats(uint32_t bits) {
+  RhtSigns r;
+  for (int j = 0; j < 16; ++j) r.s[j] = (bits >> j) & 1u ? -1.0f : 1.0f;
+  return r;
+}
+
+__device__ __forceinline__ int nv_swz(int w) { return w ^ ((w & 32) >> 2); }
+
+// one NVFP4 block: w = the values (quarter: w = 4x the true values), amax_b =
+// the true block amax; codes and scale stored like encode_store_block
+__device__ __forceinline__ void encode_nv_block(const float* w, bool quarter, float g, const QuantOut& o,
+                                                int64_t out_row, int64_t out_col0, float amax_b, bool sr) {
+  uint32_t byte;
+  float r;
+  bool zero;
+  block_scale<FP4_FMT_NVFP4>(amax_b, g, byte, r, zero);
+  float xs[16];
+  if (quarter && !(r >= 0x1p-124f) && !zero) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) xs[j] = __fmul_rn(__fmul_rn(w[j], 0.25f), r);
+  } else {
+    const float m = quarter ? __fmul_rn(r, 0.25f) : r;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) xs[j] = __fmul_rn(w[j], m);
+  }
+  uint32_t packed[2];
+  if (!sr) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) v |= e2m1x2_hw(xs[8 * q + 2 * p], xs[8 * q + 2 * p + 1]) << (8 * p);
+      packed[q] = zero ? 0u : v;
+    }
+  } else {
+    const int64_t first_elem = out_row * o.out_cols + out_col0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 bits = sr_bits8(o.keys, o.sr_offset, o.sr_stream, (uint64_t)(first_elem + 8 * q));
+      uint32_t v = 0;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float y0 = e2m1_sr_value_finite(xs[8 * q + 2 * p], u16_lane_shl6_mul(bits, 2 * p));
+        const float y1 = e2m1_sr_value_finite(xs[8 * q + 2 * p + 1], u16_lane_shl6_mul(bits, 2 * p + 1));
+        v |= e2m1x2_hw(y0, y1) << (8 * p);
+      }
+      packed[q] = zero ? 0u : v;
+    }
+  }
+  *reinterpret_cast<uint2*>(o.codes + out_row * (o.out_cols >> 1) + (out_col0 >> 1)) = make_uint2(packed[0], packed[1]);
+  o.scales[sf_offset(o.sf_layout, out_row, out_col0 / 16, o.nsf_row, o.nsf_pad)] = (uint8_t)byte;
+}
+
+// 16-byte global -> shared copy (cp.async, L2 only); bytes past `src_bytes`
+// (0..16) are zero-filled and not read
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// TWO_D: 16x16 blocks in the transposed layout (a template parameter so that
+// the 1D kernels are not compiled with its register demand)
+template <int MODE, bool TWO_D>
+__global__ void __launch_bounds__(kThreads, 4) tile_nv_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                                                           int64_t ldx, FastDiv ntc, uint32_t ntiles, QuantOut oc,
+                                                           QuantOut orr, RhtSigns sig_c, RhtSigns sig_r, int rht_c,
+                                                           int rht_r, float* amax_c, float* amax_r) {
+  constexpr bool QUANT = MODE >= T_Q_COLS;
+  constexpr bool DO_ROWS = MODE == T_AMAX_DUAL || MODE == T_Q_DUAL;
+  __shared__ __align__(16) uint32_t tile[2][NV_TR * NV_SW];   // double-buffered: the next tile streams in
+  float g_c = 0.0f, g_r = 0.0f;
+  if constexpr (QUANT) {
+    g_c = load_g(oc, FP4_FMT_NVFP4);
+    if (DO_ROWS) g_r = load_g(orr, FP4_FMT_NVFP4);
+  }
+  const bool sr_c = QUANT && oc.rounding == FP4_ROUND_SR;
+  const bool sr_r = QUANT && DO_ROWS && orr.rounding == FP4_ROUND_SR;
+  float m_c = 0.0f, m_r = 0.0f;  // amax of the values as computed (4x the true values with RHT)
+  const int t = threadIdx.x;
+  const int rr = t >> 2, q = t & 3;      // row role: row rr, columns 32q .. 32q+31
+  const int pw = t & 63, rb = t >> 6;    // column role: columns 2pw, 2pw+1 of rows 16rb .. 16rb+15
+
+  // this thread's 4 x 16 bytes of tile `id`: row r0 + rr, columns c0 + 32q .. +31
+  auto fetch = [&](uint32_t id, uint32_t* buf) {
+    const uint32_t tr = fast_div(id, ntc), tc = id - tr * ntc.d;
+    const int64_t r = (int64_t)tr * NV_TR + rr, c = (int64_t)tc * NV_TC + 32 * q;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t cc = c + 8 * i;
+      const int64_t avail = r < rows ? cols - cc : 0;
+      const uint32_t nb = avail <= 0 ? 0u : avail >= 8 ? 16u : (uint32_t)(2 * avail);
+      cp_async16(&buf[rr * NV_SW + nv_swz(16 * q + 4 * i)], nb ? x + r * ldx + cc : x, nb);
+    }
+    cp_async_commit();
+  };
+
+  if (blockIdx.x < ntiles) fetch(blockIdx.x, tile[0]);
+  int b = 0;
+  for (uint32_t id = blockIdx.x; id < ntiles; id += gridDim.x, b ^= 1) {
+    const uint32_t tr = fast_div(id, ntc), tc = id - tr * ntc.d;
+    const int64_t r0 = (int64_t)tr * NV_TR, c0 = (int64_t)tc * NV_TC;
+    const uint32_t nid = id + gridDim.x;
+    if (nid < ntiles) {
+      fetch(nid, tile[b ^ 1]);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t* cur = tile[b];
+
+    if constexpr (DO_ROWS) {
+      const bool row_ok = r0 + rr < rows;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 w0 = *reinterpret_cast<const uint4*>(&cur[rr * NV_SW + nv_swz(16 * q + 8 * h)]);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(&cur[rr * NV_SW + nv_swz(16 * q + 8 * h + 4)]);
+        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[2 * i] = __uint_as_float(wv[i] << 16);
+          v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+        }
+        if (rht_r) rht16_raw_mul(v, sig_r.s);
+        float a = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
+        const int64_t col0 = c0 + 32 * q + 16 * h;
+        if constexpr (!QUANT) {
+          m_r = fmaxf(m_r, a);   // zeros past the edges do not raise it
+        } else {
+          if (row_ok && col0 < cols)
+            encode_nv_block(v, rht_r != 0, g_r, orr, r0 + rr, col0, rht_r ? __fmul_rn(a, 0.25f) : a, sr_r);
+        }
+      }
+    }
+    const int64_t orow = c0 + 2 * pw, ocol0 = r0 + 16 * rb;   // transposed output row / first column
+    if constexpr (!QUANT || !TWO_D) {
+      // the two columns one after the other (the second re-reads the staged
+      // words), so that only one column's values are live at a time
+#pragma unroll 1
+      for (int e = 0; e < 2; ++e) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t wd = cur[(16 * rb + j) * NV_SW + nv_swz(pw)];
+          v[j] = __uint_as_float(e ? (wd & 0xFFFF0000u) : (wd << 16));
+        }
+        if (rht_c) rht16_raw_mul(v, sig_c.s);
+        float a = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
+        if constexpr (!QUANT) {
+          m_c = fmaxf(m_c, a);
+        } else {
+          if (ocol0 < rows && orow + e < cols)
+            encode_nv_block(v, rht_c != 0, g_c, oc, orow + e, ocol0, rht_c ? __fmul_rn(a, 0.25f) : a, sr_c);
+        }
+      }
+    } else {
+      // 16 x 16 blocks: 8 lanes of adjacent column pairs x 16 rows share one
+      // scale, so both columns' maxima come first
+      float va[16], vb[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t wd = cur[(16 * rb + j) * NV_SW + nv_swz(pw)];
+        va[j] = __uint_as_float(wd << 16);
+        vb[j] = __uint_as_float(wd & 0xFFFF0000u);
+      }
+      if (rht_c) {
+        rht16_raw_mul(va, sig_c.s);
+        rht16_raw_mul(vb, sig_c.s);
+      }
+      float a2 = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) a2 = fmaxf(a2, fmaxf(fabsf(va[j]), fabsf(vb[j])));
+#pragma unroll
+      for (int o = 4; o; o >>= 1) a2 = fmaxf(a2, __shfl_xor_sync(0xFFFFFFFFu, a2, o));
+      if (rht_c) a2 = __fmul_rn(a2, 0.25f);
+      if (ocol0 < rows) {
+        if (orow < cols) encode_nv_block(va, rht_c != 0, g_c, oc, orow, ocol0, a2, sr_c);
+        if (orow + 1 < cols) encode_nv_block(vb, rht_c != 0, g_c, oc, orow + 1, ocol0, a2, sr_c);
+      }
+    }
+    __syncthreads();   // every thread is done with tile[b] before it is refilled
+  }
+  if constexpr (!QUANT) {
+    if (amax_c) block_amax_atomic(rht_c ? __fmul_rn(m_c, 0.25f) : m_c, amax_c);
+    if (DO_ROWS) {
+      __syncthreads();
+      block_amax_atomic(rht_r ? __fmul_rn(m_r, 0.25f) : m_r, amax_r);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
 // dequantize: one thread per block
 // ----------------------------------------------------------------------------
 template <int FMT, int ODT>
@@ -679,8 +901,16 @@ cudaError_t launch_amax(const void* x, int dt, int64_t rows, int64_t cols, int64
     return cudaGetLastError();
   }
   // transform along rows, or a plain amax of a tensor whose cols are not a
-  // multiple of 16: column items of the tiled kernel (64 x 64 tiles)
+  // multiple of 16: column items of a tiled kernel
   QuantOut none{};
+  if (dt == FP4_DTYPE_BF16) {
+    const int64_t ntc = cdiv(cols, NV_TC), nt = cdiv(rows, NV_TR) * ntc;
+    if (nt >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    tile_nv_kernel<T_AMAX_COLS, false><<<grid_for(nt, 1, num_sms), kThreads, 0, st>>>(
+        static_cast<const uint16_t*>(x), rows, cols, ldx, make_fastdiv((uint32_t)ntc), (uint32_t)nt, none, none,
+        rht_sign_floats(rht_signs), rht_sign_floats(0u), rht_axis == 0 ? 1 : 0, 0, amax_out, nullptr);
+    return cudaGetLastError();
+  }
   int64_t ntiles = cdiv(rows, 64) * cdiv(cols, TC);
   if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
@@ -697,6 +927,15 @@ cudaError_t launch_amax_dual(const void* x, int dt, int64_t rows, int64_t cols, 
   if (e == cudaSuccess) e = cudaMemsetAsync(amax_cols, 0, sizeof(float), st);
   if (e != cudaSuccess || rows == 0 || cols == 0) return e;
   QuantOut none{};
+  if (dt == FP4_DTYPE_BF16) {
+    const int64_t ntc = cdiv(cols, NV_TC), nt = cdiv(rows, NV_TR) * ntc;
+    if (nt >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    tile_nv_kernel<T_AMAX_DUAL, false><<<grid_for(nt, 1, num_sms), kThreads, 0, st>>>(
+        static_cast<const uint16_t*>(x), rows, cols, ldx, make_fastdiv((uint32_t)ntc), (uint32_t)nt, none, none,
+        rht_sign_floats(signs_cols), rht_sign_floats(signs_rows), rht_cols ? 1 : 0, rht_rows ? 1 : 0, amax_cols,
+        amax_rows);
+    return cudaGetLastError();
+  }
   int64_t ntiles = cdiv(rows, 64) * cdiv(cols, TC);
   if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
@@ -733,6 +972,22 @@ cudaError_t launch_quant_tile(const void* x, int dt, int64_t rows, int64_t cols,
   int64_t ntiles = cdiv(rows, TRv) * cdiv(cols, TC);
   if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
+  if (transpose && fmt == FP4_FMT_NVFP4 && dt == FP4_DTYPE_BF16) {
+    const int64_t ntc = cdiv(cols, NV_TC), nt = cdiv(rows, NV_TR) * ntc;
+    if (nt >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    const FastDiv fd = make_fastdiv((uint32_t)ntc);
+    const int grid = grid_for(nt, 1, num_sms);
+    const auto* xs = static_cast<const uint16_t*>(x);
+    if (two_d)
+      tile_nv_kernel<T_Q_COLS, true><<<grid, kThreads, 0, st>>>(xs, rows, cols, ldx, fd, (uint32_t)nt, o, o,
+                                                                rht_sign_floats(o.rht_signs), rht_sign_floats(0u),
+                                                                o.rht, 0, nullptr, nullptr);
+    else
+      tile_nv_kernel<T_Q_COLS, false><<<grid, kThreads, 0, st>>>(xs, rows, cols, ldx, fd, (uint32_t)nt, o, o,
+                                                                 rht_sign_floats(o.rht_signs), rht_sign_floats(0u),
+                                                                 o.rht, 0, nullptr, nullptr);
+    return cudaGetLastError();
+  }
   if (transpose) {
     FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT, tile_kernel<FMT, DT, T_Q_COLS><<<grid, kThreads, 0, st>>>(
         x, rows, cols, ldx, o, o, two_d ? 1 : 0, o.rht_signs, 0u, o.rht, 0, nullptr, nullptr)));
@@ -747,6 +1002,24 @@ cudaError_t launch_quant_dual(const void* x, int dt, int64_t rows, int64_t cols,
                               const QuantOut& orow, const QuantOut& ocol, bool two_d_rows, bool two_d_cols,
                               int num_sms, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
+  if (fmt == FP4_FMT_NVFP4 && dt == FP4_DTYPE_BF16 && !two_d_rows) {
+    const int64_t ntc = cdiv(cols, NV_TC), nt = cdiv(rows, NV_TR) * ntc;
+    if (nt >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    const FastDiv fd = make_fastdiv((uint32_t)ntc);
+    const int grid = grid_for(nt, 1, num_sms);
+    const auto* xs = static_cast<const uint16_t*>(x);
+    if (two_d_cols)
+      tile_nv_kernel<T_Q_DUAL, true><<<grid, kThreads, 0, st>>>(xs, rows, cols, ldx, fd, (uint32_t)nt, ocol, orow,
+                                                                rht_sign_floats(ocol.rht_signs),
+                                                                rht_sign_floats(orow.rht_signs), ocol.rht, orow.rht,
+                                                                nullptr, nullptr);
+    else
+      tile_nv_kernel<T_Q_DUAL, false><<<grid, kThreads, 0, st>>>(xs, rows, cols, ldx, fd, (uint32_t)nt, ocol, orow,
+                                                                 rht_sign_floats(ocol.rht_signs),
+                                                                 rht_sign_floats(orow.rht_signs), ocol.rht, orow.rht,
+                                                                 nullptr, nullptr);
+    return cudaGetLastError();
+  }
   int TRv = fmt == FP4_FMT_MXFP4 ? 128 : 64;
   int64_t ntiles = cdiv(rows, TRv) * cdiv(cols, TC);
   if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
