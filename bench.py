@@ -338,8 +338,9 @@ def main():
 
     names = list(OPS)
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    n_breakdown = min(args.steps, 20)
     ev_ops = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
-              for _ in range(args.steps)]
+              for _ in range(n_breakdown)]
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     if dist:
@@ -349,13 +350,19 @@ def main():
     for i in range(args.steps):
         flush.fill_(i & 0xFF)                    # L2 flush, outside the step's events
         ev_step[i][0].record(stream)
-        step.run(args.warmup + i, ev_ops[i])
+        step.run(args.warmup + i)
         ev_step[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
     clk = clocks.stop()
+    # per-op breakdown: further steps with events around every op (outside the
+    # timed region, so the extra event records do not enter the step time)
+    for i in range(n_breakdown):
+        flush.fill_(i & 0xFF)
+        step.run(args.warmup + args.steps + i, ev_ops[i])
+    torch.cuda.synchronize()
     step_s = np.array([a.elapsed_time(b) * 1e-3 for a, b in ev_step])
     op_s = {n: float(np.mean([e[n][0].elapsed_time(e[n][1]) * 1e-3 for e in ev_ops])) for n in names}
     t_step = reduce_step_time(float(step_s.mean()), dist, dev)

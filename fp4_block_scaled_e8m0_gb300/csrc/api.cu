@@ -65,6 +65,17 @@ int check_operand(const fp4_operand* q, bool need_codes) {
   return FP4_OK;
 }
 
+// a new amax generation for the context's tagged slots (never 0); when the
+// 32-bit count wraps, the slots are zeroed once on the stream, so that values
+// left by the high generations before the wrap cannot win
+uint32_t next_gen(fp4_ctx* ctx, cudaStream_t st) {
+  if (++ctx->amax_gen == 0) {
+    ctx->amax_gen = 1;
+    (void)cudaMemsetAsync(ctx->scratch->amax, 0, sizeof(ctx->scratch->amax), st);
+  }
+  return ctx->amax_gen;
+}
+
 QuantOut make_out(const fp4_quant_params* p, uint8_t* codes, uint8_t* scales, float* ts, const float* amax,
                   int64_t out_rows, int64_t blocked) {
   QuantOut o{};
@@ -169,7 +180,7 @@ int fp4_amax(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t
   if (rht_axis < -1 || rht_axis > 1) return FP4_ERR_INVALID_ARG;
   if ((rht_axis == 1 && cols % 16) || (rht_axis == 0 && rows % 16)) return FP4_ERR_INVALID_ARG;
   uint32_t signs = rht_axis >= 0 ? rht_signs_host(rht_seed) : 0u;
-  return cuda_status(launch_amax(x, x_dtype, rows, cols, ldx, rht_axis, signs, amax_out, ctx->num_sms,
+  return cuda_status(launch_amax(x, x_dtype, rows, cols, ldx, rht_axis, signs, amax_out, 0u, ctx->num_sms,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -189,9 +200,10 @@ int fp4_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const float* amax = given_amax;
   if (p->format == FP4_FMT_NVFP4 && !amax) {
-    float* slot = &ctx->scratch->amax[0];
+    float* slot = reinterpret_cast<float*>(&ctx->scratch->amax[0]);
     int axis = p->rht ? (p->transpose ? 0 : 1) : -1;
-    cudaError_t e = launch_amax(x, x_dtype, rows, cols, ldx, axis, rht_signs_host(p->rht_seed), slot, ctx->num_sms, st);
+    cudaError_t e = launch_amax(x, x_dtype, rows, cols, ldx, axis, rht_signs_host(p->rht_seed), slot, next_gen(ctx, st),
+                                ctx->num_sms, st);
     if (e != cudaSuccess) return FP4_ERR_CUDA;
     amax = slot;
   }
@@ -229,10 +241,11 @@ int fp4_quantize_dual(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows
   const float* amax_r = given_amax_rows;
   const float* amax_c = given_amax_cols;
   if (pr->format == FP4_FMT_NVFP4 && (!amax_r || !amax_c)) {
-    float* sr = &ctx->scratch->amax[0];
-    float* sc = &ctx->scratch->amax[1];
+    float* sr = reinterpret_cast<float*>(&ctx->scratch->amax[0]);
+    float* sc = reinterpret_cast<float*>(&ctx->scratch->amax[1]);
     cudaError_t e = launch_amax_dual(x, x_dtype, rows, cols, ldx, rht_signs_host(pr->rht_seed),
-                                     rht_signs_host(pc->rht_seed), pr->rht != 0, pc->rht != 0, sr, sc, ctx->num_sms, st);
+                                     rht_signs_host(pc->rht_seed), pr->rht != 0, pc->rht != 0, sr, sc, next_gen(ctx, st),
+                                     ctx->num_sms, st);
     if (e != cudaSuccess) return FP4_ERR_CUDA;
     if (!amax_r) amax_r = sr;
     if (!amax_c) amax_c = sc;

@@ -322,8 +322,13 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // block-wide max (blockDim.x multiple of 32, <= 1024), then one atomicMax on
-// the fp32 bit pattern (valid for non-negative floats)
-__device__ __forceinline__ void block_amax_atomic(float v, float* out) {
+// the fp32 bit pattern (valid for non-negative floats).
+// gen == 0: *out is a float the caller zeroed.  gen != 0: out is the low word
+// of a 64-bit slot holding (generation << 32) | bits; every block writes
+// (gen << 32) | bits with a 64-bit atomicMax, so the first arrival of a new
+// generation replaces whatever an older one left and the slot needs no
+// zeroing; the low word read as a float is the amax.
+__device__ __forceinline__ void block_amax_atomic(float v, float* out, uint32_t gen = 0) {
   __shared__ float red[32];
   v = warp_max(v);
   int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -332,7 +337,13 @@ __device__ __forceinline__ void block_amax_atomic(float v, float* out) {
   if (w == 0) {
     v = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.0f;
     v = warp_max(v);
-    if (l == 0 && v > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(out), __float_as_uint(v));
+    if (l == 0) {
+      if (gen)
+        atomicMax(reinterpret_cast<unsigned long long*>(out),
+                  ((unsigned long long)gen << 32) | (unsigned long long)__float_as_uint(v));
+      else if (v > 0.0f)
+        atomicMax(reinterpret_cast<unsigned int*>(out), __float_as_uint(v));
+    }
   }
 }
 

@@ -9,17 +9,21 @@
 // Bits of the context's device status word.
 #define FP4_DEVICE_TIMEOUT 1u
 
-// Device scratch owned by a context: status word + amax slots.
+// Device scratch owned by a context: status word + amax slots.  The slots
+// hold (generation << 32) | fp32 bits: each amax launch of the context takes
+// a new generation, so a slot needs no zeroing before it is reused (the low
+// word read as a float is the amax).
 struct fp4_ctx_scratch {
   unsigned int status;
   unsigned int pad[3];
-  float amax[4];
+  unsigned long long amax[4];
 };
 
 struct fp4_ctx {
   int device;
   int num_sms;
   fp4_ctx_scratch* scratch;  // device memory
+  uint32_t amax_gen;         // last generation handed out (0 is never used)
 };
 
 namespace fp4 {
@@ -62,11 +66,13 @@ struct QuantOut {
 };
 
 // Launchers (quant.cu).  All return cudaError_t of the launch.
+// gen: 0 = amax_out is a float that is zeroed first; else the generation for a
+// tagged 64-bit context slot (see fp4_ctx_scratch)
 cudaError_t launch_amax(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int rht_axis,
-                        uint32_t rht_signs, float* amax_out, int num_sms, cudaStream_t st);
+                        uint32_t rht_signs, float* amax_out, uint32_t gen, int num_sms, cudaStream_t st);
 cudaError_t launch_amax_dual(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx,
                              uint32_t signs_rows, uint32_t signs_cols, bool rht_rows, bool rht_cols,
-                             float* amax_rows, float* amax_cols, int num_sms, cudaStream_t st);
+                             float* amax_rows, float* amax_cols, uint32_t gen, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_rows(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
                               const QuantOut& o, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_tile(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,

@@ -89,7 +89,7 @@ __device__ __forceinline__ float load_g(const QuantOut& o, int fmt) {
 template <int DT, bool RHT>
 __global__ void __launch_bounds__(kThreads) amax_rows_kernel(const void* __restrict__ x, int64_t rows,
                                                              int64_t cols, int64_t ldx, uint32_t signs,
-                                                             float* amax_out) {
+                                                             float* amax_out, uint32_t gen) {
   int64_t nchunk_row = cols >> 4;
   int64_t total = rows * nchunk_row;
   float m = 0.0f;
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) amax_rows_kernel(const void* __restr
 #pragma unroll
     for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
   }
-  block_amax_atomic(m, amax_out);
+  block_amax_atomic(m, amax_out, gen);
 }
 
 // Same reduction with 32-bit chunk ids (fewer than 2^31 chunks): a chunk's
@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads) amax_rows_kernel(const void* __restr
 template <int DT, bool RHT>
 __global__ void __launch_bounds__(kThreads) amax_rows32_kernel(const void* __restrict__ x, int64_t ldx, FastDiv nch,
                                                                uint32_t total, int contiguous, uint32_t signs,
-                                                               float* amax_out) {
+                                                               float* amax_out, uint32_t gen) {
   float m = 0.0f;
   const uint32_t stride = gridDim.x * blockDim.x;
   auto addr = [&](uint32_t c) -> int64_t {
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads) amax_rows32_kernel(const void* __res
       for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(w[j]));
     }
   }
-  block_amax_atomic(m, amax_out);
+  block_amax_atomic(m, amax_out, gen);
 }
 
 // ----------------------------------------------------------------------------
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__
                                                         int64_t cols, int64_t ldx, QuantOut oc,
                                                         QuantOut orr, int two_d, uint32_t signs_c,
                                                         uint32_t signs_r, int rht_c, int rht_r,
-                                                        float* amax_c, float* amax_r) {
+                                                        float* amax_c, float* amax_r, uint32_t gen = 0) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
   constexpr int TR = 4 * B;
   __shared__ float tile[TR * TSTRIDE];
@@ -437,10 +437,10 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__
     __syncthreads();
   }
   if constexpr (!QUANT) {
-    if (DO_COLS) block_amax_atomic(m_c, amax_c);
+    if (DO_COLS) block_amax_atomic(m_c, amax_c, gen);
     if (DO_ROWS) {
       __syncthreads();
-      block_amax_atomic(m_r, amax_r);
+      block_amax_atomic(m_r, amax_r, gen);
     }
   }
 }
@@ -538,7 +538,8 @@ template <int MODE, bool TWO_D>
 __global__ void __launch_bounds__(kThreads, 4) tile_nv_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                                                            int64_t ldx, FastDiv ntc, uint32_t ntiles, QuantOut oc,
                                                            QuantOut orr, RhtSigns sig_c, RhtSigns sig_r, int rht_c,
-                                                           int rht_r, float* amax_c, float* amax_r) {
+                                                           int rht_r, float* amax_c, float* amax_r,
+                                                           uint32_t gen = 0) {
   constexpr bool QUANT = MODE >= T_Q_COLS;
   constexpr bool DO_ROWS = MODE == T_AMAX_DUAL || MODE == T_Q_DUAL;
   __shared__ __align__(16) uint32_t tile[2][NV_TR * NV_SW];   // double-buffered: the next tile streams in
@@ -660,10 +661,10 @@ __global__ void __launch_bounds__(kThreads, 4) tile_nv_kernel(const uint16_t* __
     __syncthreads();   // every thread is done with tile[b] before it is refilled
   }
   if constexpr (!QUANT) {
-    if (amax_c) block_amax_atomic(rht_c ? __fmul_rn(m_c, 0.25f) : m_c, amax_c);
+    if (amax_c) block_amax_atomic(rht_c ? __fmul_rn(m_c, 0.25f) : m_c, amax_c, gen);
     if (DO_ROWS) {
       __syncthreads();
-      block_amax_atomic(rht_r ? __fmul_rn(m_r, 0.25f) : m_r, amax_r);
+      block_amax_atomic(rht_r ? __fmul_rn(m_r, 0.25f) : m_r, amax_r, gen);
     }
   }
 }
@@ -878,10 +879,12 @@ __global__ void encode_e4m3_kernel(const float* t, uint8_t* out, int64_t n) {
   }
 
 cudaError_t launch_amax(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int rht_axis,
-                        uint32_t rht_signs, float* amax_out, int num_sms, cudaStream_t st) {
+                        uint32_t rht_signs, float* amax_out, uint32_t gen, int num_sms, cudaStream_t st) {
   // rht_axis: -1 none, 1 along cols (needs cols % 16 == 0), 0 along rows (rows % 16 == 0)
-  cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
-  if (e != cudaSuccess) return e;
+  if (!gen) {  // a plain float output is zeroed first; a tagged slot needs no zeroing
+    cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+  }
   if (rows == 0 || cols == 0) return cudaSuccess;
   if (rht_axis != 0 && cols % 16 == 0) {
     const int64_t nch = cols / 16, total = rows * nch;
@@ -890,14 +893,14 @@ cudaError_t launch_amax(const void* x, int dt, int64_t rows, int64_t cols, int64
       const FastDiv fd = make_fastdiv((uint32_t)nch);
       const int contiguous = ldx == cols;
       FP4_DISPATCH_DT(dt, DT,
-        if (rht_axis == 1) amax_rows32_kernel<DT, true><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, rht_signs, amax_out);
-        else amax_rows32_kernel<DT, false><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, rht_signs, amax_out));
+        if (rht_axis == 1) amax_rows32_kernel<DT, true><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, rht_signs, amax_out, gen);
+        else amax_rows32_kernel<DT, false><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, rht_signs, amax_out, gen));
       return cudaGetLastError();
     }
     int grid = grid_for(total, kThreads, num_sms);
     FP4_DISPATCH_DT(dt, DT,
-      if (rht_axis == 1) amax_rows_kernel<DT, true><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, rht_signs, amax_out);
-      else amax_rows_kernel<DT, false><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, rht_signs, amax_out));
+      if (rht_axis == 1) amax_rows_kernel<DT, true><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, rht_signs, amax_out, gen);
+      else amax_rows_kernel<DT, false><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, rht_signs, amax_out, gen));
     return cudaGetLastError();
   }
   // transform along rows, or a plain amax of a tensor whose cols are not a
@@ -908,23 +911,26 @@ cudaError_t launch_amax(const void* x, int dt, int64_t rows, int64_t cols, int64
     if (nt >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
     tile_nv_kernel<T_AMAX_COLS, false><<<grid_for(nt, 1, num_sms), kThreads, 0, st>>>(
         static_cast<const uint16_t*>(x), rows, cols, ldx, make_fastdiv((uint32_t)ntc), (uint32_t)nt, none, none,
-        rht_sign_floats(rht_signs), rht_sign_floats(0u), rht_axis == 0 ? 1 : 0, 0, amax_out, nullptr);
+        rht_sign_floats(rht_signs), rht_sign_floats(0u), rht_axis == 0 ? 1 : 0, 0, amax_out, nullptr, gen);
     return cudaGetLastError();
   }
   int64_t ntiles = cdiv(rows, 64) * cdiv(cols, TC);
   if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
   FP4_DISPATCH_DT(dt, DT, tile_kernel<FP4_FMT_NVFP4, DT, T_AMAX_COLS><<<grid, kThreads, 0, st>>>(
-      x, rows, cols, ldx, none, none, 0, rht_signs, 0u, rht_axis == 0 ? 1 : 0, 0, amax_out, nullptr));
+      x, rows, cols, ldx, none, none, 0, rht_signs, 0u, rht_axis == 0 ? 1 : 0, 0, amax_out, nullptr, gen));
   return cudaGetLastError();
 }
 
 cudaError_t launch_amax_dual(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx,
                              uint32_t signs_rows, uint32_t signs_cols, bool rht_rows, bool rht_cols,
-                             float* amax_rows, float* amax_cols, int num_sms, cudaStream_t st) {
+                             float* amax_rows, float* amax_cols, uint32_t gen, int num_sms, cudaStream_t st) {
   // amax_rows: the tensor that is blocked along cols (RHT along cols, "row items")
-  cudaError_t e = cudaMemsetAsync(amax_rows, 0, sizeof(float), st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(amax_cols, 0, sizeof(float), st);
+  cudaError_t e = cudaSuccess;
+  if (!gen) {
+    e = cudaMemsetAsync(amax_rows, 0, sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(amax_cols, 0, sizeof(float), st);
+  }
   if (e != cudaSuccess || rows == 0 || cols == 0) return e;
   QuantOut none{};
   if (dt == FP4_DTYPE_BF16) {
@@ -933,14 +939,14 @@ cudaError_t launch_amax_dual(const void* x, int dt, int64_t rows, int64_t cols, 
     tile_nv_kernel<T_AMAX_DUAL, false><<<grid_for(nt, 1, num_sms), kThreads, 0, st>>>(
         static_cast<const uint16_t*>(x), rows, cols, ldx, make_fastdiv((uint32_t)ntc), (uint32_t)nt, none, none,
         rht_sign_floats(signs_cols), rht_sign_floats(signs_rows), rht_cols ? 1 : 0, rht_rows ? 1 : 0, amax_cols,
-        amax_rows);
+        amax_rows, gen);
     return cudaGetLastError();
   }
   int64_t ntiles = cdiv(rows, 64) * cdiv(cols, TC);
   if (ntiles >= (int64_t(1) << 31)) return cudaErrorInvalidValue;  // tile ids are 32-bit
   int grid = grid_for(ntiles, 1, num_sms);
   FP4_DISPATCH_DT(dt, DT, tile_kernel<FP4_FMT_NVFP4, DT, T_AMAX_DUAL><<<grid, kThreads, 0, st>>>(
-      x, rows, cols, ldx, none, none, 0, signs_cols, signs_rows, rht_cols, rht_rows, amax_cols, amax_rows));
+      x, rows, cols, ldx, none, none, 0, signs_cols, signs_rows, rht_cols, rht_rows, amax_cols, amax_rows, gen));
   return cudaGetLastError();
 }
 
