@@ -120,13 +120,20 @@ class Step:
             ("dge", lambda: f.fp4_dge_backward(self.W, self.wq, self.dW, 5.0, 3.0, 1.0, out=self.dWd)),
         ]
 
-    def run(self, step_idx: int, events=None):
+    def run(self, step_idx: int, events=None, before=None, after=None):
+        """Run the step's ops in order on the current stream.  `before`/`after`
+        map an op name to a callable run just before / after it is enqueued
+        (the end-to-end loop uses them to wait for inputs and to start copies)."""
         for name, fn in self.ops(step_idx):
+            if before and name in before:
+                before[name]()
             if events is not None:
                 events[name][0].record()
             fn()
             if events is not None:
                 events[name][1].record()
+            if after and name in after:
+                after[name]()
 
 
 # ---------------------------------------------------------------------------
@@ -374,18 +381,37 @@ def main():
              "dW": torch.empty((N, K), dtype=torch.float32).pin_memory()}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    # Copies run on their own streams and overlap with the computation: each
+    # input is waited for just before the first op that reads it, and each
+    # result is copied back as soon as the op that produces it has finished.
+    s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     e2e = []
     for i in range(args.e2e_steps):
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        X.copy_(host["X"], non_blocking=True)
-        W.copy_(host["W"], non_blocking=True)
-        dY.copy_(host["dY"], non_blocking=True)
-        step.run(10_000 + i)
-        h_out["Y"].copy_(step.Y, non_blocking=True)
-        h_out["dX"].copy_(step.dX, non_blocking=True)
-        h_out["dW"].copy_(step.dWd, non_blocking=True)
+        arrived = {k: torch.cuda.Event() for k in ("X", "W", "dY")}
+        s_h2d.wait_stream(stream)
+        with torch.cuda.stream(s_h2d):
+            for k, t in (("X", X), ("W", W), ("dY", dY)):   # in the order the step needs them
+                t.copy_(host[k], non_blocking=True)
+                arrived[k].record(s_h2d)
+
+        def copy_back(name, src):
+            done = torch.cuda.Event()
+            done.record(stream)
+            s_d2h.wait_event(done)
+            with torch.cuda.stream(s_d2h):
+                h_out[name].copy_(src, non_blocking=True)
+
+        step.run(10_000 + i,
+                 before={"quant_x_dual": lambda: stream.wait_event(arrived["X"]),
+                         "quant_w_dual": lambda: stream.wait_event(arrived["W"]),
+                         "quant_dy_dual": lambda: stream.wait_event(arrived["dY"])},
+                 after={"fprop": lambda: copy_back("Y", step.Y),
+                        "dgrad": lambda: copy_back("dX", step.dX),
+                        "dge": lambda: copy_back("dW", step.dWd)})
+        stream.wait_stream(s_d2h)
         b.record(stream)
         b.synchronize()
         e2e.append(a.elapsed_time(b) * 1e-3)

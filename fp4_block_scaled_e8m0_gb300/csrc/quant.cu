@@ -782,7 +782,9 @@ __device__ __forceinline__ float dge_fprime(float xs, float inv_k, float expo, f
   const float a = fabsf(xs);
   const uint32_t e = (a >= 2.0f) + (a >= 4.0f);
   const float t = __fmul_rn(a, __uint_as_float((128u - e) << 23));
-  const float au = fabsf(__fsub_rn(__fmul_rn(__fsub_rn(t, floorf(t)), 2.0f), 1.0f));
+  // 2 (t - floor t) - 1 as one fma: 2 (t - floor t) is exact, so the single
+  // rounding is the rounding of the subtraction
+  const float au = fabsf(__fmaf_rn(__fsub_rn(t, floorf(t)), 2.0f, -1.0f));
   float y;
   if constexpr (K5) {
     const float y0 = __powf(au, -0.8f);
@@ -801,44 +803,63 @@ template <int FMT, int XDT, int DYDT, bool K5>
 __global__ void __launch_bounds__(kThreads) dge_kernel(const void* __restrict__ x, int64_t ldx, fp4_operand q,
                                                        const void* __restrict__ dy, int64_t lddy, float* dx,
                                                        int64_t lddx, float inv_k, float expo, float clamp,
-                                                       float outside) {
+                                                       float outside, FastDiv nsf_div) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
   const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
   const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
   const int64_t total = q.rows * nsf_row;
-  const bool small = total < (int64_t(1) << 31);  // 32-bit index math
-  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
-       blk += (int64_t)gridDim.x * blockDim.x) {
-    int64_t r, j;
+  const bool small = total < (int64_t(1) << 31);  // 32-bit block ids, multiply-shift division
+  auto split = [&](int64_t blk, int64_t& r, int64_t& j) {
     if (small) {
-      const uint32_t b32 = (uint32_t)blk, n32 = (uint32_t)nsf_row, r32 = b32 / n32;
+      const uint32_t r32 = fast_div((uint32_t)blk, nsf_div);
       r = r32;
-      j = b32 - r32 * n32;
+      j = (uint32_t)blk - r32 * nsf_div.d;
     } else {
       r = blk / nsf_row;
       j = blk - r * nsf_row;
     }
-    uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
-    float mult;
-    if (FMT == FP4_FMT_MXFP4) {
-      mult = e8m0_inv_scale(sb);
-    } else {
-      float s = __fmul_rn(e4m3_decode(sb), g);
-      mult = s == 0.0f ? 0.0f : __frcp_rn(s);
-    }
+  };
+  auto multiplier = [&](int64_t r, int64_t j) {
+    const uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
+    if (FMT == FP4_FMT_MXFP4) return e8m0_inv_scale(sb);
+    const float s = __fmul_rn(e4m3_decode(sb), g);
+    return s == 0.0f ? 0.0f : __frcp_rn(s);
+  };
+  auto finish = [&](const float* v, const float* d, float mult, int64_t r, int64_t j) {
 #pragma unroll
     for (int q8 = 0; q8 < B / 8; ++q8) {
-      float v[8], d[8];
-      load8<XDT>(x, r * ldx + j * B + 8 * q8, v);
-      load8<DYDT>(dy, r * lddy + j * B + 8 * q8, d);
       float o[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        o[e] = __fmul_rn(d[e], dge_fprime<K5>(__fmul_rn(v[e], mult), inv_k, expo, clamp, outside));
+        o[e] = __fmul_rn(d[8 * q8 + e], dge_fprime<K5>(__fmul_rn(v[8 * q8 + e], mult), inv_k, expo, clamp, outside));
       float4* dst = reinterpret_cast<float4*>(dx + r * lddx + j * B + 8 * q8);
       dst[0] = make_float4(o[0], o[1], o[2], o[3]);
       dst[1] = make_float4(o[4], o[5], o[6], o[7]);
     }
+  };
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  // two blocks per iteration: both blocks' x and dy loads are in flight together
+  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total; blk += 2 * stride) {
+    const int64_t blk2 = blk + stride;
+    const bool two = blk2 < total;
+    int64_t r, j, r2 = 0, j2 = 0;
+    split(blk, r, j);
+    if (two) split(blk2, r2, j2);
+    float v[B], d[B], v2[B], d2[B];
+#pragma unroll
+    for (int q8 = 0; q8 < B / 8; ++q8) {
+      load8<XDT>(x, r * ldx + j * B + 8 * q8, v + 8 * q8);
+      load8<DYDT>(dy, r * lddy + j * B + 8 * q8, d + 8 * q8);
+    }
+    if (two) {
+#pragma unroll
+      for (int q8 = 0; q8 < B / 8; ++q8) {
+        load8<XDT>(x, r2 * ldx + j2 * B + 8 * q8, v2 + 8 * q8);
+        load8<DYDT>(dy, r2 * lddy + j2 * B + 8 * q8, d2 + 8 * q8);
+      }
+    }
+    finish(v, d, multiplier(r, j), r, j);
+    if (two) finish(v2, d2, multiplier(r2, j2), r2, j2);
   }
 }
 
@@ -1067,17 +1088,18 @@ cudaError_t launch_dge(const void* x, int xdt, int64_t ldx, const fp4_operand& q
   int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
   int64_t total = q.rows * (q.k / B);
   if (total == 0) return cudaSuccess;
-  int grid = grid_for(total, kThreads, num_sms);
   float inv_k = 1.0f / k, expo = 1.0f / k - 1.0f;
   const bool k5 = k == 5.0f;
+  const int grid = grid_for(cdiv(total, 2), kThreads, num_sms);
+  const FastDiv fd = make_fastdiv((uint32_t)std::min<int64_t>(q.k / B, 0x7FFFFFFF));
 #define FP4_DGE_LAUNCH(K5)                                                                                      \
   FP4_DISPATCH_FMT(q.format, FMT, FP4_DISPATCH_DT(xdt, XDT,                                                      \
     if (dydt == FP4_DTYPE_BF16)                                                                                  \
       dge_kernel<FMT, XDT, FP4_DTYPE_BF16, K5><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo, \
-                                                                          clamp, outside);                       \
+                                                                          clamp, outside, fd);                       \
     else                                                                                                         \
       dge_kernel<FMT, XDT, FP4_DTYPE_F32, K5><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo,  \
-                                                                         clamp, outside)))
+                                                                         clamp, outside, fd)))
   if (k5) {
     FP4_DGE_LAUNCH(true);
   } else {
