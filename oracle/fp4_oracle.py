@@ -439,6 +439,77 @@ def dge_backward(x, scales, fmt, g, dy, k=5.0, clamp=3.0, outside=1.0) -> np.nda
 
 
 # ----------------------------------------------------------------------------
+# Sigmoid-smoothed quantizer ([grad §3.2]):
+#   Q_soft(x) = sum_i v_i sigma(beta (x - c_i)),
+#   dQ_soft/dx = beta sum_i v_i sigma(beta (x - c_i)) (1 - sigma(beta (x - c_i)))
+# READING: the page calls v_i "the quantization levels" and c_i "the interval
+# midpoints" and says Q_soft tends to the standard quantizer as beta grows.
+# The reading under which that limit holds: over the 15 signed E2M1 levels
+# q_0 < ... < q_14 (-6 .. 6), c_i = (q_i + q_{i+1}) / 2 are the 14 decision
+# thresholds, v_i = q_{i+1} - q_i the level steps, and the sum starts from the
+# lowest level q_0: Q_soft(x) = q_0 + sum_i v_i sigma(beta (x - c_i)).  Each
+# sigmoid then switches one step on as x crosses c_i, so beta -> inf gives
+# round-to-nearest onto the grid, saturating at +-6.  The derivative is the
+# page's expression with these v_i, c_i (the constant q_0 drops out).  Like
+# the DGE, the smoothing acts on the scaled value x / s and the block scale s
+# is held constant: y = s Q_soft(x / s), dx = dy Q_soft'(x / s).
+# ----------------------------------------------------------------------------
+
+def soft_grid():
+    """(levels q_0..q_14, thresholds c_0..c_13, steps v_0..v_13), fp64."""
+    q = np.concatenate([-E2M1_GRID[:0:-1], E2M1_GRID])      # -6 .. -0.5, 0, 0.5 .. 6
+    c = 0.5 * (q[:-1] + q[1:])
+    v = q[1:] - q[:-1]
+    return q, c, v
+
+
+def _sigmoid(z: np.ndarray) -> np.ndarray:
+    """1 / (1 + e^-z) in fp64; e^-z overflowing to inf gives the limit 0."""
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
+def soft_quantize_scaled(xs: np.ndarray, beta: float) -> np.ndarray:
+    """Q_soft(xs) = q_0 + sum_i v_i sigma(beta (xs - c_i)), fp64.  Pinned by
+    test_soft_* (RTN limit, finite differences, odd symmetry, beta -> 0)."""
+    q, c, v = soft_grid()
+    z = float(beta) * (np.asarray(xs, dtype=np.float64)[..., None] - c)
+    return q[0] + (v * _sigmoid(z)).sum(axis=-1)
+
+
+def soft_derivative(xs: np.ndarray, beta: float) -> np.ndarray:
+    """beta sum_i v_i sigma(z_i) (1 - sigma(z_i)), z_i = beta (xs - c_i), fp64.
+    1 - sigma(z) is evaluated as sigma(-z) (the same number) so that the tails
+    keep their relative precision."""
+    _, c, v = soft_grid()
+    z = float(beta) * (np.asarray(xs, dtype=np.float64)[..., None] - c)
+    return float(beta) * (v * _sigmoid(z) * _sigmoid(-z)).sum(axis=-1)
+
+
+def block_scales_expanded(scales, fmt, g=None) -> np.ndarray:
+    """The block scale s of every element (fp32 values as the quantizer formed
+    them: 2^(e-127) for E8M0, e4m3(b) * g for NVFP4), expanded along the row."""
+    bsz = BLOCK[fmt]
+    sb = np.repeat(np.asarray(scales, dtype=np.uint8), bsz, axis=1)
+    if fmt == MXFP4:
+        return np.ldexp(1.0, sb.astype(np.int64) - 127).astype(np.float32)
+    return (e4m3_decode(sb).astype(np.float32) * np.float32(g)).astype(np.float32)
+
+
+def soft_forward(x, scales, fmt, g, beta) -> np.ndarray:
+    """y = s Q_soft(x / s) for x quantized along its rows; fp64 result."""
+    xs = scaled_inputs(x, scales, fmt, g)
+    s = block_scales_expanded(scales, fmt, g).astype(np.float64)
+    return s * soft_quantize_scaled(xs, beta)
+
+
+def soft_backward(x, scales, fmt, g, dy, beta) -> np.ndarray:
+    """dx = dy Q_soft'(x / s) for x quantized along its rows; fp64 result."""
+    xs = scaled_inputs(x, scales, fmt, g)
+    return np.asarray(dy, dtype=np.float64) * soft_derivative(xs, beta)
+
+
+# ----------------------------------------------------------------------------
 # Block-scaled GEMM  Y[M, N] = sum_k A[m, k] B[n, k]   (fp64 accumulation)
 # ----------------------------------------------------------------------------
 
