@@ -607,3 +607,74 @@ def gemm_tolerance(bound, y_ref, out_bf16: bool):
     if out_bf16:
         tol = tol + 2.0 ** -8 * np.abs(y_ref)
     return tol
+
+
+# ----------------------------------------------------------------------------
+# Outlier clamping and compensation, OCC ([msr §三, §六])
+#   The largest 1% of activation magnitudes are outliers: the 99% quantile of
+#   |X| is the threshold tau, X is clamped to [-tau, tau] before it is
+#   quantized, and the clamped-away part dX = X - clamp(X) (a sparse matrix)
+#   goes through a high-precision product beside the FP4 GEMM:
+#       Y = Q(X_c) Q(W)^T + dX W^T.
+# READING: the quantile is taken over the magnitudes of the whole tensor, by
+# nearest rank (tau = the ceil(q n)-th smallest |x|, so that at least q n
+# magnitudes are <= tau); elements with |x| > tau are the outliers.  W in the
+# compensation is the unquantized weight (bf16 values), the high-precision
+# operand; the quality numbers (cosine, MSE, SNR) compare X with its
+# reconstruction dequant(Q(X_c)) + dX (OCC) or dequant(Q(X)) (direct).
+# ----------------------------------------------------------------------------
+
+def occ_threshold(x, q: float = 0.99) -> np.float32:
+    """tau: the ceil(q n)-th smallest |x| (1-based rank) over all n elements."""
+    a = np.sort(np.abs(np.asarray(x, dtype=np.float32)).reshape(-1), kind="stable")
+    n = a.size
+    rank = max(1, int(math.ceil(q * n)))
+    return np.float32(a[rank - 1])
+
+
+def occ_split(x, tau):
+    """(X_c, dX) with X_c = min(max(x, -tau), tau) and dX = x - X_c, both fp32
+    (dX is exact: x and tau are values of the input's own precision)."""
+    w = np.asarray(x, dtype=np.float32)
+    t = np.float32(tau)
+    xc = np.minimum(np.maximum(w, -t), t).astype(np.float32)
+    return xc, (w - xc).astype(np.float32)
+
+
+def occ_outliers(x, tau):
+    """Outlier positions (row, col), row-major order, and their dX values."""
+    _, dx = occ_split(x, tau)
+    rows, cols = np.nonzero(np.abs(np.asarray(x, dtype=np.float32)) > np.float32(tau))
+    return rows, cols, dx[rows, cols]
+
+
+def occ_gemm(x, w, fmt, tau):
+    """Y = alpha Q(X_c) Q(W)^T + dX W^T in fp64 (W: its bf16/fp32 values).
+
+    Returns (Y, bound, (xc_codes, xc_scales, g_x), (w_codes, w_scales, g_w))
+    with bound = sum_k |a||b| of the FP4 part plus sum_k |dX||W|."""
+    xc, dx = occ_split(x, tau)
+    xq = quantize(xc, fmt)
+    wq = quantize(w, fmt)
+    y, bound = gemm(xq[0], xq[1], wq[0], wq[1], fmt, xq[2], wq[2])
+    wf = np.asarray(w, dtype=np.float64)
+    dxf = dx.astype(np.float64)
+    return y + dxf @ wf.T, bound + np.abs(dxf) @ np.abs(wf).T, xq, wq
+
+
+def quant_error_stats(x, x_hat):
+    """Cosine similarity, mean squared error and SNR (dB) of x_hat against x,
+    fp64: cos = <x, x_hat> / (|x| |x_hat|), MSE = mean (x - x_hat)^2,
+    SNR = 10 log10(sum x^2 / sum (x - x_hat)^2)."""
+    a = np.asarray(x, dtype=np.float64).reshape(-1)
+    b = np.asarray(x_hat, dtype=np.float64).reshape(-1)
+    err = ((a - b) ** 2).sum()
+    cos = float(a @ b / math.sqrt((a @ a) * (b @ b)))
+    return {"cos": cos, "mse": float(err / a.size), "snr_db": float(10.0 * math.log10((a @ a) / err))}
+
+
+def occ_reconstruction(x, fmt, tau):
+    """dequant(Q(X_c)) + dX, fp64: what the OCC forward stands for."""
+    xc, dx = occ_split(x, tau)
+    codes, scales, g = quantize(xc, fmt)
+    return dequantize(codes, scales, fmt, g).astype(np.float64) + dx.astype(np.float64)
