@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", default="512x704", help="MxN rows of the CPU-baseline sample (K stays 2048)")
+    ap.add_argument("--ext-launches", type=int, default=20,
+                    help="timed launches of each op outside the step (0: skip them)")
     return ap.parse_args()
 
 
@@ -134,6 +136,100 @@ class Step:
                 events[name][1].record()
             if after and name in after:
                 after[name]()
+
+
+# ---------------------------------------------------------------------------
+# ops outside the step, on the step's tensors: the sigmoid-smoothed estimator
+# (an alternative to the DGE backward on W, "深度学习中的梯度计算基础" §3.2)
+# ---------------------------------------------------------------------------
+SOFT_BWD_BYTES = N * K * (2 + 4 + 4) + N * K / 16     # W, dW in; dW' out; scales
+SOFT_FWD_BYTES = N * K * (2 + 4) + N * K / 16         # W in; s Q_soft(W/s) out; scales
+
+
+def extension_ops(fp4, step, dev):
+    out = torch.empty((N, K), dtype=torch.float32, device=dev)
+    ops = []
+    for beta in (40.0, 10.0, 1.0):
+        ops.append((f"soft_backward_beta{beta:g}", SOFT_BWD_BYTES,
+                    lambda b=beta: fp4.fp4_soft_backward(step.W, step.wq, step.dW, b, out=out)))
+    for beta in (40.0, 1.0):
+        ops.append((f"soft_forward_beta{beta:g}", SOFT_FWD_BYTES,
+                    lambda b=beta: fp4.fp4_soft_forward(step.W, step.wq, b, out=out)))
+    return ops
+
+
+def _time_op(fn, flush, launches):
+    """Mean device time of `fn` over `launches` calls, L2 flushed before each."""
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(launches)]
+    for i in range(launches):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) * 1e-3 for a, b in ev]))
+
+
+def _rate(kind, units, t, pk):
+    if kind == "tensor":
+        peak = pk["bf16_tflops_sustained"] * FP4_OVER_BF16
+        r = units / t / 1e12
+        return {"us": t * 1e6, "rate": r, "unit": "TFLOP/s", "frac": r / peak}
+    r = units / t / 1e9
+    return {"us": t * 1e6, "rate": r, "unit": "GB/s", "frac": r / pk["hbm_gbs"]}
+
+
+def time_extensions(fp4, step, dev, flush, launches, pk):
+    """Each op timed alone: L2 flushed before every launch, CUDA events around it."""
+    res = {}
+    for name, nbytes, fn in extension_ops(fp4, step, dev):
+        res[name] = dict(_rate("hbm", nbytes, _time_op(fn, flush, launches), pk), launches=launches)
+    res["occ"] = time_occ(fp4, dev, flush, launches, pk)
+    return res
+
+
+# Outlier clamping and compensation (the MSR write-up §三) on the hot-channel
+# activations: X[16384,4096] Student-t(3) with 1% of the channels x100,
+# W[4096,4096] ~N(0,0.02), NVFP4, q = 0.99, 64 dense compensation columns.
+OCC_M, OCC_K, OCC_N, OCC_DENSE = 16384, 4096, 4096, 64
+
+
+def time_occ(fp4, dev, flush, launches, pk):
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    d = inputs.hcp_square(OCC_M, OCC_K, OCC_N)
+    X, W = d["X"].to(dev), d["W"].to(dev)
+    NV = fp4.FP4_FMT_NVFP4
+    p = fp4.quant_params(NV)
+    ws_t = torch.empty((fp4.load_library().fp4_occ_threshold_workspace_bytes(fp4.FP4_DTYPE_BF16),),
+                       dtype=torch.uint8, device=dev)
+    tau, n_out = fp4.fp4_occ_threshold(X, workspace=ws_t)
+    counts = torch.empty((OCC_K,), dtype=torch.float32, device=dev)
+    xq = fp4.alloc_qtensor(OCC_M, OCC_K, NV, fp4.FP4_SF_MMA, dev)
+    fp4.fp4_occ_quantize(X, p, tau, out=xq, col_counts=counts)
+    wq = fp4.fp4_quantize(W, p)
+    xq_direct = fp4.fp4_quantize(X, p)
+    cap = fp4.fp4_occ_max_outliers(OCC_M, OCC_K)
+    ws = torch.empty((fp4.load_library().fp4_occ_gemm_workspace_bytes(OCC_M, OCC_N, OCC_K, OCC_DENSE, cap),),
+                     dtype=torch.uint8, device=dev)
+    Y = torch.empty((OCC_M, OCC_N), dtype=torch.bfloat16, device=dev)
+    flops = 2 * OCC_M * OCC_N * OCC_K
+    res = {"workload": f"X[{OCC_M},{OCC_K}] Student-t(3), 1% channels x100; W[{OCC_N},{OCC_K}]; NVFP4; q=0.99; "
+                       f"{OCC_DENSE} dense columns; bf16 Y",
+           "outliers": int(n_out.item()), "tau": float(tau.item())}
+    res["threshold"] = _rate("hbm", OCC_M * OCC_K * 2, _time_op(
+        lambda: fp4.fp4_occ_threshold(X, workspace=ws_t), flush, launches), pk)
+    res["clamp_quantize"] = _rate("hbm", OCC_M * OCC_K * (2 + 0.5 + 1 / 16), _time_op(
+        lambda: fp4.fp4_occ_quantize(X, p, tau, out=xq, col_counts=counts), flush, launches), pk)
+    res["occ_gemm"] = _rate("tensor", flops, _time_op(
+        lambda: fp4.fp4_occ_gemm(X, W, xq, wq, tau, counts, OCC_DENSE, cap, out=Y, workspace=ws), flush, launches), pk)
+    res["plain_gemm"] = _rate("tensor", flops, _time_op(lambda: fp4.fp4_gemm(xq, wq, out=Y), flush, launches), pk)
+    n = OCC_M * OCC_K
+    res["quality_direct"] = fp4.error_stats_from_sums(fp4.fp4_quant_error_sums(X, xq_direct).cpu(), n)
+    res["quality_occ"] = fp4.error_stats_from_sums(fp4.fp4_quant_error_sums(X, xq, tau).cpu(), n)
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -417,8 +513,10 @@ def main():
         e2e.append(a.elapsed_time(b) * 1e-3)
     t_e2e = float(np.mean(e2e)) if e2e else float("nan")
 
-    # ---- roofline of the dominant kernel --------------------------------------------
     pk = peaks()
+    extensions = time_extensions(fp4, step, dev, flush, args.ext_launches, pk) if args.ext_launches > 0 else {}
+
+    # ---- roofline of the dominant kernel --------------------------------------------
     dom = max(names, key=lambda n: op_s[n])
     kind, units = OPS[dom]
     if kind == "tensor":
@@ -462,6 +560,7 @@ def main():
         "ops": breakdown, "roofline": roof, "clocks": clk,
         "e2e": {"value": world * STEP_FLOPS / t_e2e / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3},
+        "extensions": extensions,
         "gpu_launches": sum(KERNELS_PER_OP.values()) * args.steps, "wall_s_timed_region": wall,
         "device_status": status,
     }

@@ -70,6 +70,18 @@ _SIGNATURES = {
     "fp4_rht16": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, _I32, _U64, _P, _P]),
     "fp4_dge_backward": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _I32, _I64, _P, _I64,
                                         _F32, _F32, _F32, _P]),
+    "fp4_soft_forward": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _I64, _F32, _P]),
+    "fp4_soft_backward": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _I32, _I64, _P, _I64,
+                                         _F32, _P]),
+    "fp4_occ_threshold_workspace_bytes": (_SZ, [_I32]),
+    "fp4_occ_max_outliers": (_I64, [_I64, _I64, ctypes.c_double]),
+    "fp4_occ_threshold": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, ctypes.c_double, _P, _P, _P, _SZ, _P]),
+    "fp4_occ_quantize": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, ctypes.POINTER(fp4_quant_params), _P, _P, _P,
+                                        _P, _P, _P]),
+    "fp4_occ_gemm_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32, _I64]),
+    "fp4_occ_gemm": (ctypes.c_int, [_P, _P, _I32, _I64, _P, _I64, ctypes.POINTER(fp4_operand),
+                                    ctypes.POINTER(fp4_operand), _P, _P, _I32, _I64, _I32, _P, _I64, _P, _SZ, _P]),
+    "fp4_quant_error_stats": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _P, _P]),
     "fp4_gemm": (ctypes.c_int, [_P, ctypes.POINTER(fp4_operand), ctypes.POINTER(fp4_operand), _I32, _P, _I64, _I32,
                                 _P]),
     "fp4_hcp_select_workspace_bytes": (_SZ, [_I64]),
@@ -292,6 +304,27 @@ def fp4_dge_backward(x: torch.Tensor, q: QTensor, dy: torch.Tensor, k: float = 5
     return out
 
 
+def fp4_soft_forward(x: torch.Tensor, q: QTensor, beta: float, out: Optional[torch.Tensor] = None, ctx=None,
+                     stream=None) -> torch.Tensor:
+    """y = s Q_soft(x / s), fp32 (sigmoid-smoothed quantizer)."""
+    out = out if out is not None else torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    op = q.operand()
+    _check(load_library().fp4_soft_forward(_ctx(ctx), _ptr(x), _dtype_code(x), _ld(x), ctypes.byref(op), _ptr(out),
+                                           _ld(out), beta, _stream(stream)), "fp4_soft_forward")
+    return out
+
+
+def fp4_soft_backward(x: torch.Tensor, q: QTensor, dy: torch.Tensor, beta: float, out: Optional[torch.Tensor] = None,
+                      ctx=None, stream=None) -> torch.Tensor:
+    """dx = dy Q_soft'(x / s), fp32 (sigmoid-smoothed estimator)."""
+    out = out if out is not None else torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    op = q.operand()
+    _check(load_library().fp4_soft_backward(_ctx(ctx), _ptr(x), _dtype_code(x), _ld(x), ctypes.byref(op), _ptr(dy),
+                                            _dtype_code(dy), _ld(dy), _ptr(out), _ld(out), beta, _stream(stream)),
+           "fp4_soft_backward")
+    return out
+
+
 def fp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None,
              accumulate: bool = False, ctx=None, stream=None) -> torch.Tensor:
     out = out if out is not None else torch.empty((a.rows, b.rows), dtype=out_dtype, device=a.codes.device)
@@ -351,6 +384,73 @@ def fp4_hcp_gemm(x: torch.Tensor, w: torch.Tensor, xq: QTensor, wq: QTensor, hot
                             _ptr(hot_idx), k_hot, mode, order, _ptr(workspace), workspace.numel(), _dtype_code(out),
                             _ptr(out), _ld(out), _stream(stream)), "fp4_hcp_gemm")
     return out
+
+
+# ---- outlier clamping and compensation ----------------------------------------
+def fp4_occ_max_outliers(rows: int, cols: int, q: float = 0.99) -> int:
+    return int(load_library().fp4_occ_max_outliers(rows, cols, q))
+
+
+def fp4_occ_threshold(x: torch.Tensor, q: float = 0.99, workspace: Optional[torch.Tensor] = None, ctx=None,
+                      stream=None):
+    """(tau, n_outliers): device fp32[1] and int64[1]."""
+    lib = load_library()
+    tau = torch.empty((1,), dtype=torch.float32, device=x.device)
+    n_out = torch.empty((1,), dtype=torch.int64, device=x.device)
+    ws_bytes = int(lib.fp4_occ_threshold_workspace_bytes(_dtype_code(x)))
+    workspace = workspace if workspace is not None else torch.empty((ws_bytes,), dtype=torch.uint8, device=x.device)
+    _check(lib.fp4_occ_threshold(_ctx(ctx), _ptr(x), _dtype_code(x), x.shape[0], x.shape[1], _ld(x), q, _ptr(tau),
+                                 _ptr(n_out), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fp4_occ_threshold")
+    return tau, n_out
+
+
+def fp4_occ_quantize(x: torch.Tensor, params: fp4_quant_params, tau: torch.Tensor, out: Optional[QTensor] = None,
+                     col_counts: Optional[torch.Tensor] = None, ctx=None, stream=None) -> QTensor:
+    """Quantize clamp(x, -tau, tau) in the row layout; col_counts (float32[cols]) gets the outliers per column."""
+    rows, cols = x.shape
+    out = out or alloc_qtensor(rows, cols, params.format, params.sf_layout, x.device)
+    _check(load_library().fp4_occ_quantize(_ctx(ctx), _ptr(x), _dtype_code(x), rows, cols, _ld(x),
+                                           ctypes.byref(params), _ptr(tau), _ptr(out.codes), _ptr(out.scales),
+                                           _ptr(out.tensor_scale), _ptr(col_counts), _stream(stream)),
+           "fp4_occ_quantize")
+    return out
+
+
+def fp4_occ_gemm(x: torch.Tensor, w: torch.Tensor, xq: QTensor, wq: QTensor, tau: torch.Tensor,
+                 col_counts: Optional[torch.Tensor], k_dense: int, max_outliers: int, out_dtype=torch.bfloat16,
+                 out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, ctx=None,
+                 stream=None) -> torch.Tensor:
+    """Y = alpha Q(X_c) Q(W)^T + dX W^T."""
+    lib = load_library()
+    out = out if out is not None else torch.empty((xq.rows, wq.rows), dtype=out_dtype, device=x.device)
+    ws_bytes = int(lib.fp4_occ_gemm_workspace_bytes(xq.rows, wq.rows, xq.k, k_dense, max_outliers))
+    workspace = workspace if workspace is not None else torch.empty((max(ws_bytes, 1),), dtype=torch.uint8,
+                                                                   device=x.device)
+    ox, ow = xq.operand(), wq.operand()
+    _check(lib.fp4_occ_gemm(_ctx(ctx), _ptr(x), _dtype_code(x), _ld(x), _ptr(w), _ld(w), ctypes.byref(ox),
+                            ctypes.byref(ow), _ptr(tau), _ptr(col_counts), k_dense, max_outliers, _dtype_code(out),
+                            _ptr(out), _ld(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fp4_occ_gemm")
+    return out
+
+
+def fp4_quant_error_sums(x: torch.Tensor, q: QTensor, tau: Optional[torch.Tensor] = None,
+                         out: Optional[torch.Tensor] = None, ctx=None, stream=None) -> torch.Tensor:
+    """Device float64[4]: sum x^2, sum x_hat^2, sum x x_hat, sum (x - x_hat)^2."""
+    out = out if out is not None else torch.empty((4,), dtype=torch.float64, device=x.device)
+    op = q.operand()
+    _check(load_library().fp4_quant_error_stats(_ctx(ctx), _ptr(x), _dtype_code(x), _ld(x), ctypes.byref(op),
+                                                _ptr(tau), _ptr(out), _stream(stream)), "fp4_quant_error_stats")
+    return out
+
+
+def error_stats_from_sums(sums, n: int) -> dict:
+    """cosine, MSE and SNR (dB) from the four sums (host arithmetic)."""
+    sxx, shh, sxh, see = (float(v) for v in sums)
+    return {"cos": sxh / math.sqrt(sxx * shh) if sxx > 0 and shh > 0 else float("nan"),
+            "mse": see / n if n else float("nan"),
+            "snr_db": 10.0 * math.log10(sxx / see) if see > 0 and sxx > 0 else float("inf")}
 
 
 def fp4_encode_e2m1(xs: torch.Tensor, method: int = 0, ctx=None, stream=None) -> torch.Tensor:

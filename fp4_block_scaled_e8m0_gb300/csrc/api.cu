@@ -1,5 +1,6 @@
 // C ABI entry points: argument validation, context handling and dispatch to
 // the kernels.  See include/fp4.h for the contract of each call.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -49,18 +50,24 @@ int check_params(const fp4_quant_params* p) {
   return FP4_OK;
 }
 
+// a pointer may be NULL only when the buffer it names has no elements
+bool present(const void* p, bool empty) { return p != nullptr || empty; }
+
 int check_input(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx) {
-  if (!x || rows < 0 || cols < 0 || ldx < cols || !dtype_ok(dt)) return FP4_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ldx < cols || !dtype_ok(dt)) return FP4_ERR_INVALID_ARG;
+  if (!present(x, rows == 0 || cols == 0)) return FP4_ERR_INVALID_ARG;
   if (rows > 0 && cols > 0 && (!al16(x) || (ldx * esize(dt)) % 16 != 0)) return FP4_ERR_MISALIGNED;
   return FP4_OK;
 }
 
 int check_operand(const fp4_operand* q, bool need_codes) {
-  if (!q || !q->scales || (need_codes && !q->codes) || q->rows < 0 || q->k < 0) return FP4_ERR_INVALID_ARG;
+  if (!q || q->rows < 0 || q->k < 0) return FP4_ERR_INVALID_ARG;
+  const bool empty = q->rows == 0 || q->k == 0;
+  if (!present(q->scales, empty) || (need_codes && !present(q->codes, empty))) return FP4_ERR_INVALID_ARG;
   if (q->format != FP4_FMT_MXFP4 && q->format != FP4_FMT_NVFP4) return FP4_ERR_UNSUPPORTED;
   if (q->sf_layout != FP4_SF_ROWMAJOR && q->sf_layout != FP4_SF_MMA) return FP4_ERR_INVALID_ARG;
   if (q->k % block_of(q->format) != 0) return FP4_ERR_INVALID_ARG;
-  if (q->format == FP4_FMT_NVFP4 && !q->tensor_scale) return FP4_ERR_INVALID_ARG;
+  if (q->format == FP4_FMT_NVFP4 && !present(q->tensor_scale, empty)) return FP4_ERR_INVALID_ARG;
   if (need_codes && !al16(q->codes)) return FP4_ERR_MISALIGNED;
   return FP4_OK;
 }
@@ -168,6 +175,7 @@ int fp4_sync_status(fp4_ctx* ctx, void* stream) {
   if (status) {
     if (cudaMemset(&ctx->scratch->status, 0, sizeof(unsigned int)) != cudaSuccess) return FP4_ERR_CUDA;
     if (status & FP4_DEVICE_TIMEOUT) return FP4_ERR_TIMEOUT;
+    if (status & FP4_DEVICE_OVERFLOW) return FP4_ERR_TOO_LARGE;
   }
   return FP4_OK;
 }
@@ -187,7 +195,8 @@ int fp4_amax(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t
 int fp4_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols, int64_t ldx,
                  const fp4_quant_params* p, const float* given_amax, uint8_t* codes, uint8_t* scales,
                  float* tensor_scale, void* stream) {
-  if (!ctx || !codes || !scales) return FP4_ERR_INVALID_ARG;
+  if (!ctx || !present(codes, rows == 0 || cols == 0) || !present(scales, rows == 0 || cols == 0))
+    return FP4_ERR_INVALID_ARG;
   int s = check_params(p);
   if (s) return s;
   s = check_input(x, x_dtype, rows, cols, ldx);
@@ -222,7 +231,10 @@ int fp4_quantize_dual(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows
                       const fp4_quant_params* pr, const fp4_quant_params* pc, const float* given_amax_rows,
                       const float* given_amax_cols, uint8_t* codes_rows, uint8_t* scales_rows, float* ts_rows,
                       uint8_t* codes_cols, uint8_t* scales_cols, float* ts_cols, void* stream) {
-  if (!ctx || !codes_rows || !scales_rows || !codes_cols || !scales_cols) return FP4_ERR_INVALID_ARG;
+  const bool empty = rows == 0 || cols == 0;
+  if (!ctx || !present(codes_rows, empty) || !present(scales_rows, empty) || !present(codes_cols, empty) ||
+      !present(scales_cols, empty))
+    return FP4_ERR_INVALID_ARG;
   int s = check_params(pr);
   if (s) return s;
   s = check_params(pc);
@@ -259,17 +271,17 @@ int fp4_quantize_dual(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows
 }
 
 int fp4_dequantize(fp4_ctx* ctx, const fp4_operand* q, int32_t out_dtype, void* out, int64_t ldo, void* stream) {
-  if (!ctx || !out || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
+  if (!ctx || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(q, true);
   if (s) return s;
-  if (ldo < q->k) return FP4_ERR_INVALID_ARG;
+  if (ldo < q->k || !present(out, q->rows == 0 || q->k == 0)) return FP4_ERR_INVALID_ARG;
   if (!al16(out) || (ldo * esize(out_dtype)) % 16) return FP4_ERR_MISALIGNED;
   return cuda_status(launch_dequant(*q, out_dtype, out, ldo, ctx->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 int fp4_rht16(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols, int64_t ldx, int32_t axis,
               uint64_t seed, float* y, void* stream) {
-  if (!ctx || !y || (axis != 0 && axis != 1)) return FP4_ERR_INVALID_ARG;
+  if (!ctx || !present(y, rows == 0 || cols == 0) || (axis != 0 && axis != 1)) return FP4_ERR_INVALID_ARG;
   int s = check_input(x, x_dtype, rows, cols, ldx);
   if (s) return s;
   if ((axis == 1 && cols % 16) || (axis == 0 && rows % 16)) return FP4_ERR_INVALID_ARG;
@@ -281,9 +293,10 @@ int fp4_rht16(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_
 int fp4_dge_backward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q, const void* dy,
                      int32_t dy_dtype, int64_t lddy, float* dx, int64_t lddx, float k, float clamp, float outside,
                      void* stream) {
-  if (!ctx || !dx || !(k > 1.0f) || !(clamp > 0.0f)) return FP4_ERR_INVALID_ARG;
+  if (!ctx || !(k > 1.0f) || !(clamp > 0.0f)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(q, false);
   if (s) return s;
+  if (!present(dx, q->rows == 0 || q->k == 0)) return FP4_ERR_INVALID_ARG;
   s = check_input(x, x_dtype, q->rows, q->k, ldx);
   if (s) return s;
   s = check_input(dy, dy_dtype, q->rows, q->k, lddy);
@@ -294,13 +307,175 @@ int fp4_dge_backward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, 
                                 static_cast<cudaStream_t>(stream)));
 }
 
+static bool soft_beta_ok(float beta) { return beta > 0.0f && beta <= 1e6f; }
+
+int fp4_soft_forward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q, float* y,
+                     int64_t ldy, float beta, void* stream) {
+  if (!ctx || !soft_beta_ok(beta)) return FP4_ERR_INVALID_ARG;
+  int s = check_operand(q, false);
+  if (s) return s;
+  if (!present(y, q->rows == 0 || q->k == 0)) return FP4_ERR_INVALID_ARG;
+  s = check_input(x, x_dtype, q->rows, q->k, ldx);
+  if (s) return s;
+  if (ldy < q->k) return FP4_ERR_INVALID_ARG;
+  if (!al16(y) || (ldy * 4) % 16) return FP4_ERR_MISALIGNED;
+  return cuda_status(launch_soft(x, x_dtype, ldx, *q, nullptr, 0, 0, y, ldy, beta, ctx->num_sms,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int fp4_soft_backward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,
+                      const void* dy, int32_t dy_dtype, int64_t lddy, float* dx, int64_t lddx, float beta,
+                      void* stream) {
+  if (!ctx || !soft_beta_ok(beta)) return FP4_ERR_INVALID_ARG;
+  int s = check_operand(q, false);
+  if (s) return s;
+  if (!present(dx, q->rows == 0 || q->k == 0)) return FP4_ERR_INVALID_ARG;
+  s = check_input(x, x_dtype, q->rows, q->k, ldx);
+  if (s) return s;
+  s = check_input(dy, dy_dtype, q->rows, q->k, lddy);
+  if (s) return s;
+  if (lddx < q->k) return FP4_ERR_INVALID_ARG;
+  if (!al16(dx) || (lddx * 4) % 16) return FP4_ERR_MISALIGNED;
+  return cuda_status(launch_soft(x, x_dtype, ldx, *q, dy, dy_dtype, lddy, dx, lddx, beta, ctx->num_sms,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+// ---- OCC -------------------------------------------------------------------
+static uint64_t occ_rank(int64_t n, double q) {
+  const double r = std::ceil(q * (double)n);
+  return r < 1.0 ? 1u : (uint64_t)r;
+}
+
+size_t fp4_occ_threshold_workspace_bytes(int32_t x_dtype) {
+  return dtype_ok(x_dtype) ? occ_threshold_ws_bytes(x_dtype) : 0;
+}
+
+int64_t fp4_occ_max_outliers(int64_t rows, int64_t cols, double q) {
+  if (rows <= 0 || cols <= 0 || !(q > 0.0 && q <= 1.0)) return 0;
+  const int64_t n = rows * cols;
+  return n - (int64_t)occ_rank(n, q);
+}
+
+int fp4_occ_threshold(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols, int64_t ldx,
+                      double q, float* tau, int64_t* n_outliers, void* workspace, size_t ws_bytes, void* stream) {
+  if (!ctx || !tau || !n_outliers || !(q > 0.0 && q <= 1.0)) return FP4_ERR_INVALID_ARG;
+  int s = check_input(x, x_dtype, rows, cols, ldx);
+  if (s) return s;
+  if (cols % 8) return FP4_ERR_INVALID_ARG;
+  if (rows * cols / 8 >= (int64_t(1) << 31)) return FP4_ERR_TOO_LARGE;
+  if (!workspace || ws_bytes < occ_threshold_ws_bytes(x_dtype)) return FP4_ERR_INVALID_ARG;
+  if (!al16(workspace)) return FP4_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (rows == 0 || cols == 0) {
+    if (cudaMemsetAsync(tau, 0, sizeof(float), st) != cudaSuccess) return FP4_ERR_CUDA;
+    return cuda_status(cudaMemsetAsync(n_outliers, 0, sizeof(int64_t), st));
+  }
+  return cuda_status(launch_occ_threshold(x, x_dtype, rows, cols, ldx, occ_rank(rows * cols, q), workspace, tau,
+                                          reinterpret_cast<long long*>(n_outliers), ctx->num_sms, st));
+}
+
+int fp4_occ_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols, int64_t ldx,
+                     const fp4_quant_params* p, const float* tau, uint8_t* codes, uint8_t* scales,
+                     float* tensor_scale, float* col_counts, void* stream) {
+  const bool empty = rows == 0 || cols == 0;
+  if (!ctx || !tau || !present(codes, empty) || !present(scales, empty)) return FP4_ERR_INVALID_ARG;
+  int s = check_params(p);
+  if (s) return s;
+  if (p->transpose || p->rht || p->scaling != FP4_SCALING_1D) return FP4_ERR_UNSUPPORTED;
+  s = check_input(x, x_dtype, rows, cols, ldx);
+  if (s) return s;
+  if (cols % p->block) return FP4_ERR_INVALID_ARG;
+  if (rows * (cols / p->block) >= (int64_t(1) << 31)) return FP4_ERR_TOO_LARGE;
+  if (!al16(codes)) return FP4_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (col_counts && cols > 0 && cudaMemsetAsync(col_counts, 0, sizeof(float) * cols, st) != cudaSuccess)
+    return FP4_ERR_CUDA;
+  if (empty) return FP4_OK;
+  if (clear_sf_padding(p, scales, rows, cols, st) != cudaSuccess) return FP4_ERR_CUDA;
+  QuantOut o = make_out(p, codes, scales, tensor_scale, tau, rows, cols);
+  o.clamp = tau;
+  o.col_counts = col_counts;
+  return cuda_status(launch_quant_rows_clamped(x, x_dtype, rows, cols, ldx, p->format, o, ctx->num_sms, st));
+}
+
+size_t fp4_occ_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int32_t k_dense, int64_t max_outliers) {
+  if (m <= 0 || n <= 0 || k <= 0 || k_dense < 0 || max_outliers < 0) return 0;
+  return occ_layout(m, n, k, k_dense, max_outliers).bytes;
+}
+
+int fp4_occ_gemm(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const void* w_bf16, int64_t ldw,
+                 const fp4_operand* xq, const fp4_operand* wq, const float* tau, const float* col_counts,
+                 int32_t k_dense, int64_t max_outliers, int32_t out_dtype, void* y, int64_t ldy, void* workspace,
+                 size_t ws_bytes, void* stream) {
+  if (!ctx || !tau || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
+  int s = check_operand(xq, true);
+  if (s) return s;
+  s = check_operand(wq, true);
+  if (s) return s;
+  if (xq->format != wq->format || xq->k != wq->k) return FP4_ERR_INVALID_ARG;
+  if (xq->sf_layout != FP4_SF_MMA || wq->sf_layout != FP4_SF_MMA) return FP4_ERR_UNSUPPORTED;
+  const int64_t M = xq->rows, N = wq->rows, K = xq->k;
+  if (K % 32 || (K == 0 && M > 0 && N > 0)) return FP4_ERR_INVALID_ARG;
+  if (M > INT32_MAX || N > INT32_MAX) return FP4_ERR_INVALID_ARG;
+  if (k_dense < 0 || k_dense > K || (k_dense > 0 && !col_counts)) return FP4_ERR_INVALID_ARG;
+  if (max_outliers < 0 || max_outliers >= (int64_t(1) << 31)) return FP4_ERR_INVALID_ARG;
+  s = check_input(x, x_dtype, M, K, ldx);
+  if (s) return s;
+  s = check_input(w_bf16, FP4_DTYPE_BF16, N, K, ldw);
+  if (s) return s;
+  if (ldy < N || !present(y, M == 0 || N == 0)) return FP4_ERR_INVALID_ARG;
+  if (!al16(y) || (ldy * esize(out_dtype)) % 16) return FP4_ERR_MISALIGNED;
+  if (M == 0 || N == 0) return FP4_OK;
+  const OccLayout L = occ_layout(M, N, K, k_dense, max_outliers);
+  if (!workspace || ws_bytes < L.bytes) return FP4_ERR_INVALID_ARG;
+  if (!al16(workspace)) return FP4_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_occ_prepare(x, x_dtype, ldx, static_cast<const uint16_t*>(w_bf16), ldw, *xq, *wq, tau,
+                                     col_counts, k_dense, max_outliers, workspace, L, &ctx->scratch->status,
+                                     ctx->num_sms, st);
+  if (e != cudaSuccess) return FP4_ERR_CUDA;
+  GemmArgs g{};
+  g.A = xq;
+  g.B = wq;
+  g.fp4_part = true;
+  g.out_dtype = out_dtype;
+  g.C = y;
+  g.ldc = ldy;
+  g.status = &ctx->scratch->status;
+  g.num_sms = ctx->num_sms;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  if (k_dense > 0) {
+    g.a_ext = reinterpret_cast<const uint16_t*>(base + L.a_ext);
+    g.b_ext = reinterpret_cast<const uint16_t*>(base + L.b_ext);
+    g.kx = L.kx;
+  }
+  g.occ_start = reinterpret_cast<const uint32_t*>(base + L.row_start);
+  g.occ_len = reinterpret_cast<const uint32_t*>(base + L.row_len);
+  g.occ_entries = base + L.entries;
+  g.occ_wt = reinterpret_cast<const uint16_t*>(base + L.wt);
+  g.occ_ldt = L.ldt;
+  return launch_gemm(g, st);
+}
+
+int fp4_quant_error_stats(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,
+                          const float* tau, double* sums, void* stream) {
+  if (!ctx || !sums) return FP4_ERR_INVALID_ARG;
+  int s = check_operand(q, true);
+  if (s) return s;
+  s = check_input(x, x_dtype, q->rows, q->k, ldx);
+  if (s) return s;
+  return cuda_status(launch_error_stats(x, x_dtype, ldx, *q, tau, sums, ctx->num_sms,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 int fp4_gemm(fp4_ctx* ctx, const fp4_operand* A, const fp4_operand* B, int32_t out_dtype, void* C, int64_t ldc,
              int32_t accumulate, void* stream) {
-  if (!ctx || !C || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
+  if (!ctx || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(A, true);
   if (s) return s;
   s = check_operand(B, true);
   if (s) return s;
+  if (!present(C, A->rows == 0 || B->rows == 0)) return FP4_ERR_INVALID_ARG;
   if (A->format != B->format || A->k != B->k) return FP4_ERR_INVALID_ARG;
   if (A->sf_layout != FP4_SF_MMA || B->sf_layout != FP4_SF_MMA) return FP4_ERR_UNSUPPORTED;
   if (A->k % 32) return FP4_ERR_INVALID_ARG;
@@ -353,7 +528,7 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
                  const fp4_operand* xq, const fp4_operand* wq, const int32_t* hot_idx, int32_t k_hot, int32_t mode,
                  int32_t order, void* workspace, size_t ws_bytes, int32_t out_dtype, void* y, int64_t ldy,
                  void* stream) {
-  if (!ctx || !y || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
+  if (!ctx || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
   if (mode != FP4_HCP_SINGLE && mode != FP4_HCP_TWO) return FP4_ERR_INVALID_ARG;
   if (order != 1 && order != 2) return FP4_ERR_INVALID_ARG;
   int s = check_operand(xq, true);
@@ -368,7 +543,7 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
   if (s) return s;
   s = check_input(w_bf16, FP4_DTYPE_BF16, wq->rows, wq->k, ldw);
   if (s) return s;
-  if (ldy < wq->rows) return FP4_ERR_INVALID_ARG;
+  if (ldy < wq->rows || !present(y, xq->rows == 0 || wq->rows == 0)) return FP4_ERR_INVALID_ARG;
   if (!al16(y) || (ldy * esize(out_dtype)) % 16) return FP4_ERR_MISALIGNED;
   const int64_t M = xq->rows, N = wq->rows;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -405,12 +580,13 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
 }
 
 int fp4_encode_e2m1(fp4_ctx* ctx, const float* xs, uint8_t* codes, int64_t n, int32_t method, void* stream) {
-  if (!ctx || !xs || !codes || n < 0 || (method != 0 && method != 1)) return FP4_ERR_INVALID_ARG;
+  if (!ctx || !present(xs, n == 0) || !present(codes, n == 0) || n < 0 || (method != 0 && method != 1))
+    return FP4_ERR_INVALID_ARG;
   return cuda_status(launch_encode_e2m1(xs, codes, n, method, static_cast<cudaStream_t>(stream)));
 }
 
 int fp4_encode_e4m3(fp4_ctx* ctx, const float* t, uint8_t* out, int64_t n, void* stream) {
-  if (!ctx || !t || !out || n < 0) return FP4_ERR_INVALID_ARG;
+  if (!ctx || !present(t, n == 0) || !present(out, n == 0) || n < 0) return FP4_ERR_INVALID_ARG;
   return cuda_status(launch_encode_e4m3(t, out, n, static_cast<cudaStream_t>(stream)));
 }
 

@@ -8,6 +8,7 @@
 
 // Bits of the context's device status word.
 #define FP4_DEVICE_TIMEOUT 1u
+#define FP4_DEVICE_OVERFLOW 2u   // a device-filled list outgrew its caller-sized buffer
 
 // Device scratch owned by a context: status word + amax slots.  The slots
 // hold (generation << 32) | fp32 bits: each amax launch of the context takes
@@ -63,6 +64,8 @@ struct QuantOut {
   uint64_t sr_seed, sr_offset;
   uint32_t rht_signs;    // 16 sign bits
   PhiloxRoundKeys keys;  // of sr_seed
+  const float* clamp;    // row quantizer only: device tau, x is clamped to [-tau, tau] (null: no clamp)
+  float* col_counts;     // with clamp: per-column count of |x| > tau, added to (null: not counted)
 };
 
 // Launchers (quant.cu).  All return cudaError_t of the launch.
@@ -75,6 +78,9 @@ cudaError_t launch_amax_dual(const void* x, int dt, int64_t rows, int64_t cols, 
                              float* amax_rows, float* amax_cols, uint32_t gen, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_rows(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
                               const QuantOut& o, int num_sms, cudaStream_t st);
+// the row quantizer with o.clamp set (32-bit block ids: rows * cols / block < 2^31)
+cudaError_t launch_quant_rows_clamped(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                                      const QuantOut& o, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_tile(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
                               bool two_d, bool transpose, const QuantOut& o, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_dual(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
@@ -87,6 +93,11 @@ cudaError_t launch_rht16(const void* x, int dt, int64_t rows, int64_t cols, int6
 cudaError_t launch_dge(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
                        int64_t lddy, float* dx, int64_t lddx, float k, float clamp, float outside,
                        int num_sms, cudaStream_t st);
+// Q_soft forward (dy == NULL: out = s Q_soft(x/s)) or backward (out = dy Q_soft'(x/s))
+cudaError_t launch_soft(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
+                        int64_t lddy, float* out, int64_t ldo, float beta, int num_sms, cudaStream_t st);
+// thresholds evaluated on each side of x/s for this beta (0: all of them)
+int soft_window(float beta);
 cudaError_t launch_encode_e2m1(const float* xs, uint8_t* codes, int64_t n, int method, cudaStream_t st);
 cudaError_t launch_encode_e4m3(const float* t, uint8_t* out, int64_t n, cudaStream_t st);
 
@@ -104,6 +115,13 @@ struct GemmArgs {
   int accumulate;
   unsigned int* status;
   int num_sms;
+  // optional per-row sparse correction added in the epilogue (outlier
+  // compensation): Y[m, :] += sum over entries (k, v) of row m of v * WT[k, :]
+  const uint32_t* occ_start;   // [M] first entry of each row, or null
+  const uint32_t* occ_len;     // [M] entries of each row
+  const void* occ_entries;     // (int32 k, float v) pairs
+  const uint16_t* occ_wt;      // W^T bf16 [K][occ_ldt], occ_ldt a multiple of 8
+  int64_t occ_ldt;
 };
 int launch_gemm(const GemmArgs& g, cudaStream_t st);  // returns fp4 status
 
@@ -115,6 +133,25 @@ cudaError_t launch_hcp_gather(const uint16_t* x, int64_t ldx, const uint16_t* w,
                               const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot,
                               int k_hot, int order, int64_t kx, uint16_t* a_ext, uint16_t* b_ext,
                               int num_sms, cudaStream_t st);
+
+// Outlier clamping and compensation (occ.cu).  Workspace layout of fp4_occ_gemm
+// (byte offsets).
+struct OccLayout {
+  int64_t kx;    // extra bf16 K columns (k_dense rounded up to 64)
+  int64_t ldt;   // pitch of W^T (N rounded up to 8)
+  size_t counts, hot, flags, a_ext, b_ext, wt, row_start, row_len, cursor, entries, bytes;
+};
+size_t occ_threshold_ws_bytes(int dt);
+cudaError_t launch_occ_threshold(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, uint64_t rank,
+                                 void* ws, float* tau, long long* n_out, int num_sms, cudaStream_t st);
+OccLayout occ_layout(int64_t m, int64_t n, int64_t k, int k_dense, int64_t max_outliers);
+// top-k columns, their extra GEMM columns, W^T and the per-row scattered outliers
+cudaError_t launch_occ_prepare(const void* x, int xdt, int64_t ldx, const uint16_t* w, int64_t ldw,
+                               const fp4_operand& xq, const fp4_operand& wq, const float* tau, const float* col_counts,
+                               int k_dense, int64_t max_outliers, void* ws, const OccLayout& L, unsigned int* status,
+                               int num_sms, cudaStream_t st);
+cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const float* tau,
+                               double* sums, int num_sms, cudaStream_t st);
 
 __host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // scales per row in the MMA layout: k padded to 256 elements

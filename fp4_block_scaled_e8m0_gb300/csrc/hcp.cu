@@ -78,28 +78,38 @@ __global__ void __launch_bounds__(256) channel_err_kernel(const uint16_t* __rest
   for (int j = 0; j < B; ++j) atomicAdd(&err[cb * B + j], acc[j]);
 }
 
-// flag[c] = 1 iff fewer than k_hot channels beat c (larger error, or equal
-// error and lower index)
-__global__ void __launch_bounds__(256) rank_kernel(const float* __restrict__ err, int64_t k, int k_hot, int* flag) {
-  __shared__ float chunk[1024];
+// rank[c] += the number of channels j in this CTA's slice of 256 that beat c
+// (larger error, or equal error and lower index); rank is zeroed first.  The
+// grid covers (channels / 256)^2 tiles, so the k^2 comparisons spread over the
+// whole GPU.
+constexpr int kRankSlice = 256;
+__global__ void __launch_bounds__(256) rank_kernel(const float* __restrict__ err, int64_t k, int* rank) {
+  __shared__ float chunk[kRankSlice];
   const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  const float e = c < k ? err[c] : 0.0f;
-  int64_t rank = 0;
-  for (int64_t base = 0; base < k; base += 1024) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < 1024; i += blockDim.x) chunk[i] = base + i < k ? err[base + i] : -1.0f;
-    __syncthreads();
-    const int64_t n = min((int64_t)1024, k - base);
+  const int64_t base = blockIdx.y * (int64_t)kRankSlice;
+  for (int i = threadIdx.x; i < kRankSlice; i += blockDim.x) chunk[i] = base + i < k ? err[base + i] : -1.0f;
+  __syncthreads();
+  if (c >= k) return;
+  const float e = err[c];
+  const int n = (int)min((int64_t)kRankSlice, k - base);
+  int r = 0;
+  if (base + n <= c) {            // every j of the slice has a lower index
+    for (int i = 0; i < n; ++i) r += chunk[i] >= e;
+  } else if (base > c) {          // every j has a higher index
+    for (int i = 0; i < n; ++i) r += chunk[i] > e;
+  } else {
     for (int i = 0; i < n; ++i) {
-      float o = chunk[i];
-      rank += (o > e) || (o == e && base + i < c);
+      const float o = chunk[i];
+      r += (o > e) || (o == e && base + i < c);
     }
   }
-  if (c < k) flag[c] = rank < k_hot ? 1 : 0;
+  if (r) atomicAdd(&rank[c], r);
 }
 
-// hot_idx = ascending list of flagged channels (one CTA, block-wide scan)
-__global__ void __launch_bounds__(1024) compact_kernel(const int* __restrict__ flag, int64_t k, int32_t* hot_idx) {
+// hot_idx = ascending list of the channels with rank < k_hot (one CTA,
+// block-wide scan)
+__global__ void __launch_bounds__(1024) compact_kernel(const int* __restrict__ rank, int64_t k, int k_hot,
+                                                       int32_t* hot_idx) {
   __shared__ int warp_sums[32];
   __shared__ int carry;
   if (threadIdx.x == 0) carry = 0;
@@ -107,7 +117,7 @@ __global__ void __launch_bounds__(1024) compact_kernel(const int* __restrict__ f
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int64_t base = 0; base < k; base += blockDim.x) {
     const int64_t c = base + threadIdx.x;
-    int f = c < k ? flag[c] : 0;
+    int f = c < k ? (rank[c] < k_hot ? 1 : 0) : 0;
     int x = f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -197,11 +207,13 @@ cudaError_t launch_hcp_channel_errors(const uint16_t* x, int64_t ldx, const fp4_
 
 cudaError_t launch_hcp_topk(const float* err, int64_t k, int k_hot, int32_t* hot_idx, cudaStream_t st) {
   if (k == 0 || k_hot == 0) return cudaSuccess;
-  int* flag = reinterpret_cast<int*>(const_cast<float*>(err) + k);
-  rank_kernel<<<(unsigned)cdiv(k, 256), 256, 0, st>>>(err, k, k_hot, flag);
-  cudaError_t e = cudaGetLastError();
+  int* rank = reinterpret_cast<int*>(const_cast<float*>(err) + k);
+  cudaError_t e = cudaMemsetAsync(rank, 0, sizeof(int) * k, st);
   if (e != cudaSuccess) return e;
-  compact_kernel<<<1, 1024, 0, st>>>(flag, k, hot_idx);
+  rank_kernel<<<dim3((unsigned)cdiv(k, 256), (unsigned)cdiv(k, kRankSlice)), 256, 0, st>>>(err, k, rank);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  compact_kernel<<<1, 1024, 0, st>>>(rank, k, k_hot, hot_idx);
   return cudaGetLastError();
 }
 
@@ -262,12 +274,14 @@ int noalloc_setup(int dev, void** ptr, int* sms) {
 extern "C" int fp4_hcp_select_noalloc(const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
                                       int32_t* hot_idx, void* stream) {
   using namespace fp4;
-  if (!xq || !xq->codes || !xq->scales || !x_bf16 || xq->rows < 0 || xq->k < 0) return FP4_ERR_INVALID_ARG;
+  if (!xq || xq->rows < 0 || xq->k < 0) return FP4_ERR_INVALID_ARG;
+  const bool empty = xq->rows == 0 || xq->k == 0;   // pointers of empty buffers may be NULL
+  if (!empty && (!xq->codes || !xq->scales || !x_bf16)) return FP4_ERR_INVALID_ARG;
   if (xq->k > FP4_NOALLOC_MAX_CHANNELS) return FP4_ERR_TOO_LARGE;
   if (xq->format != FP4_FMT_MXFP4 && xq->format != FP4_FMT_NVFP4) return FP4_ERR_UNSUPPORTED;
   if (xq->sf_layout != FP4_SF_ROWMAJOR && xq->sf_layout != FP4_SF_MMA) return FP4_ERR_INVALID_ARG;
   if (xq->k % (xq->format == FP4_FMT_MXFP4 ? 32 : 16)) return FP4_ERR_INVALID_ARG;
-  if (xq->format == FP4_FMT_NVFP4 && !xq->tensor_scale) return FP4_ERR_INVALID_ARG;
+  if (xq->format == FP4_FMT_NVFP4 && !empty && !xq->tensor_scale) return FP4_ERR_INVALID_ARG;
   if (k_hot < 0 || k_hot > xq->k || (k_hot > 0 && !hot_idx) || ldx < xq->k) return FP4_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x_bf16) & 15u) || (ldx * 2) % 16 || (reinterpret_cast<uintptr_t>(xq->codes) & 15u))
     return FP4_ERR_MISALIGNED;

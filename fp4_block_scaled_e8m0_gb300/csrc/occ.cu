@@ -1,0 +1,620 @@
+// Outlier clamping and compensation, OCC ([msr] §三, §六), and the
+// quantization-quality statistics the same section reports (cosine similarity,
+// MSE, SNR).
+//
+//   tau  = the ceil(q n)-th smallest |x| over the tensor (nearest rank)
+//   X_c  = clamp(X, -tau, tau)            quantized by the row quantizer
+//   dX   = X - X_c                        sparse: nonzero where |x| > tau
+//   Y    = alpha Q(X_c) Q(W)^T + dX W^T
+//
+// The threshold is an order statistic of the magnitudes, found exactly with
+// integer work: a histogram of the magnitude bit patterns (bf16: all 15 bits,
+// 32768 bins; fp32: the top 15 bits, then the low 16 bits of the elements in
+// the selected bin) and a scan for the bin that holds the rank.
+//
+// dX W^T is split by column.  The k_dense columns with the most outliers (the
+// persistent hot channels of [outlier] §2) become extra bf16 K columns of the
+// FP4 GEMM, A_ext = dX_H / alpha and B_ext = W_H, so the tensor cores compute
+// them with the FP4 part; the other outliers are gathered per row and the GEMM
+// epilogue adds v * W^T[k, :] for each of them to its row of Y, in fp32 before
+// the output is rounded (the GEMM's sparse-correction variant).
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "fp4_device.cuh"
+
+using namespace fp4dev;
+
+namespace fp4 {
+namespace {
+
+constexpr int kHistBins = 32768;   // 15-bit magnitude keys
+constexpr int kLowBins = 65536;    // fp32: the low 16 bits
+constexpr int kHistThreads = 1024;
+
+struct OccSelect {
+  unsigned long long below;   // elements in bins below the selected one
+  unsigned long long in_bin;  // elements in the selected bin
+  unsigned int bin;
+  unsigned int pad;
+};
+
+template <int DT>
+__device__ __forceinline__ uint32_t mag_bits_hi(float v) {
+  // bf16 values are exact in fp32 with the low 16 bits zero: the top 15 bits
+  // below the sign are the whole magnitude
+  return (__float_as_uint(v) >> 16) & 0x7FFFu;
+}
+
+// Histogram of the top 15 magnitude bits: per-CTA shared-memory counters,
+// merged into the global fine histogram (32768 bins) and a coarse one (256
+// bins of 128: the exponent) once per CTA.  8 elements per vector.
+template <int DT>
+__global__ void __launch_bounds__(kHistThreads) occ_hist_kernel(const void* __restrict__ x, int64_t ldx,
+                                                                FastDiv vec_per_row, uint32_t total_vecs,
+                                                                unsigned long long* fine,
+                                                                unsigned long long* coarse) {
+  extern __shared__ uint32_t sh[];
+  for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) sh[b] = 0u;
+  __syncthreads();
+  for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < total_vecs; v += gridDim.x * blockDim.x) {
+    const uint32_t r = fast_div(v, vec_per_row), c = (v - r * vec_per_row.d) * 8u;
+    float e[8];
+    load8<DT>(x, (int64_t)r * ldx + c, e);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) atomicAdd(&sh[mag_bits_hi<DT>(e[j])], 1u);
+  }
+  __syncthreads();
+  // thread t owns fine bins 32t .. 32t+31, all inside coarse bin t / 4
+  constexpr int PER = kHistBins / kHistThreads;
+  uint32_t part = 0;
+  for (int i = 0; i < PER; ++i) {
+    const int b = threadIdx.x * PER + i;
+    const uint32_t c = sh[b];
+    if (c) atomicAdd(&fine[b], (unsigned long long)c);
+    part += c;
+  }
+  part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
+  part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
+  if ((threadIdx.x & 3) == 0 && part) atomicAdd(&coarse[threadIdx.x >> 2], (unsigned long long)part);
+}
+
+// fp32 second pass: low 16 bits of the elements whose top bits are the
+// selected bin (fine: 65536 bins, coarse: 256 bins of 256)
+__global__ void __launch_bounds__(256) occ_hist_low_kernel(const float* __restrict__ x, int64_t ldx,
+                                                           FastDiv vec_per_row, uint32_t total_vecs,
+                                                           const OccSelect* sel, unsigned long long* fine,
+                                                           unsigned long long* coarse) {
+  const uint32_t bin = sel->bin;
+  for (uint32_t v = blockIdx.x * blockDim.x + threadIdx.x; v < total_vecs; v += gridDim.x * blockDim.x) {
+    const uint32_t r = fast_div(v, vec_per_row), c = (v - r * vec_per_row.d) * 8u;
+    float e[8];
+    load8<FP4_DTYPE_F32>(x, (int64_t)r * ldx + c, e);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t u = __float_as_uint(e[j]);
+      if (((u >> 16) & 0x7FFFu) == bin) {
+        atomicAdd(&fine[u & 0xFFFFu], 1ull);
+        atomicAdd(&coarse[(u & 0xFFFFu) >> 8], 1ull);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ unsigned long long warp_incl_scan(unsigned long long v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// One warp finds the bin holding rank `target` among `nb` bins starting at
+// `h` (nb a multiple of 32, each lane owning nb / 32 consecutive bins): the
+// bin index and the count of the bins before it.
+__device__ __forceinline__ void warp_find_bin(const unsigned long long* h, int nb, unsigned long long target,
+                                              int& bin, unsigned long long& before) {
+  const int lane = threadIdx.x & 31, per = nb / 32;
+  unsigned long long local = 0;
+  for (int i = 0; i < per; ++i) local += h[lane * per + i];
+  const unsigned long long incl = warp_incl_scan(local), excl = incl - local;
+  const bool mine = excl < target && target <= incl;
+  const int owner = __ffs(__ballot_sync(0xFFFFFFFFu, mine)) - 1;
+  int b = 0;
+  unsigned long long cum = excl;
+  if (mine) {
+    for (; b < per; ++b) {
+      const unsigned long long c = h[lane * per + b];
+      if (cum + c >= target) break;
+      cum += c;
+    }
+  }
+  bin = __shfl_sync(0xFFFFFFFFu, lane * per + b, owner < 0 ? 0 : owner);
+  before = __shfl_sync(0xFFFFFFFFu, cum, owner < 0 ? 0 : owner);
+}
+
+// One warp: coarse bin, then the fine bin inside it.  PASS 0 over the 15-bit
+// keys (final for bf16), PASS 1 over the low 16 bits (fp32).
+template <int PASS, int DT>
+__global__ void __launch_bounds__(32) occ_select_kernel(const unsigned long long* __restrict__ fine,
+                                                        const unsigned long long* __restrict__ coarse,
+                                                        unsigned long long n, unsigned long long rank,
+                                                        OccSelect* sel, float* tau, long long* n_out) {
+  constexpr int FPC = PASS == 0 ? kHistBins / 256 : kLowBins / 256;   // fine bins per coarse bin
+  const unsigned long long target = PASS == 0 ? rank : rank - sel->below;
+  int cb, fb;
+  unsigned long long before_c, before_f;
+  warp_find_bin(coarse, 256, target, cb, before_c);
+  warp_find_bin(fine + (int64_t)cb * FPC, FPC, target - before_c, fb, before_f);
+  if (threadIdx.x != 0) return;
+  const unsigned int bin = (unsigned int)(cb * FPC + fb);
+  const unsigned long long cum = before_c + before_f, h = fine[bin];
+  if constexpr (PASS == 0) {
+    sel->bin = bin;
+    sel->below = cum;
+    sel->in_bin = h;
+    if (DT == FP4_DTYPE_BF16) {
+      *tau = __uint_as_float(bin << 16);
+      *n_out = (long long)(n - cum - h);
+    }
+  } else {
+    *tau = __uint_as_float((sel->bin << 16) | bin);
+    *n_out = (long long)((n - sel->below - sel->in_bin) + (sel->in_bin - cum - h));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// compensation
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ float load_elem(const void* x, int64_t i) {
+  if constexpr (DT == FP4_DTYPE_BF16) {
+    return bf16_bits_to_float(static_cast<const uint16_t*>(x)[i]);
+  } else {
+    return static_cast<const float*>(x)[i];
+  }
+}
+
+// dX = x - clamp(x, -tau, tau): exact in fp32 for the values the method meets
+__device__ __forceinline__ float clamp_residual(float v, float tau) {
+  return fabsf(v) > tau ? __fsub_rn(v, copysignf(tau, v)) : 0.0f;
+}
+
+// 1 / alpha for the bf16 extra columns, or 0 when alpha cannot carry them
+// (alpha zero, or 1 / alpha not finite): every outlier then takes the scattered
+// path.  Both the column gather and the row extraction take this decision from
+// the same device values.
+template <int FMT>
+__device__ __forceinline__ float tail_inv_alpha(const fp4_operand& xq, const fp4_operand& wq) {
+  if constexpr (FMT == FP4_FMT_MXFP4) {
+    return 1.0f;
+  } else {
+    const float alpha = __fmul_rn(*xq.tensor_scale, *wq.tensor_scale);
+    const float r = __frcp_rn(alpha);
+    return (alpha > 0.0f && isfinite(r)) ? r : 0.0f;
+  }
+}
+
+// dX / alpha as the bf16 value of an extra column.  (An outlier so large that
+// dX / alpha leaves the bf16 range gives an infinite column value: |x| / tau
+// would have to exceed ~1e28 for weights of amax 1e-3.)
+__device__ __forceinline__ uint16_t tail_bits(float dx, float inv_alpha) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(dx, inv_alpha));
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+// dense[c / 32] bit c % 32 set for the k_dense chosen columns
+__global__ void occ_flags_kernel(const int32_t* __restrict__ hot, int k_dense, uint32_t* dense) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j < k_dense) atomicOr(&dense[hot[j] >> 5], 1u << (hot[j] & 31));
+}
+
+// A_ext[m][j] = bf16(dX[m, H_j] / alpha) (0 where the outlier is scattered),
+// B_ext[n][j] = W[n, H_j]; columns j >= k_dense are zero.  One thread per
+// 8 consecutive columns of one row (16-byte stores).
+template <int FMT, int XDT>
+__global__ void __launch_bounds__(256) occ_tail_kernel(const void* __restrict__ x, int64_t ldx,
+                                                       const uint16_t* __restrict__ w, int64_t ldw, fp4_operand xq,
+                                                       fp4_operand wq, const float* __restrict__ tau_p,
+                                                       const int32_t* __restrict__ hot, int k_dense, int64_t kx,
+                                                       uint16_t* __restrict__ a_ext, uint16_t* __restrict__ b_ext) {
+  const float tau = *tau_p;
+  const float inv_alpha = tail_inv_alpha<FMT>(xq, wq);
+  const int64_t per_row = kx / 8;
+  const int64_t total = (xq.rows + wq.rows) * per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / per_row, j0 = (i - row * per_row) * 8;
+    const bool is_a = row < xq.rows;
+    uint16_t o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int64_t j = j0 + e;
+      uint16_t bits = 0;
+      if (j < k_dense && inv_alpha != 0.0f) {
+        const int64_t c = hot[j];
+        bits = is_a ? tail_bits(clamp_residual(load_elem<XDT>(x, row * ldx + c), tau), inv_alpha)
+                    : w[(row - xq.rows) * ldw + c];
+      }
+      o[e] = bits;
+    }
+    uint4 pk;
+    pk.x = o[0] | ((uint32_t)o[1] << 16);
+    pk.y = o[2] | ((uint32_t)o[3] << 16);
+    pk.z = o[4] | ((uint32_t)o[5] << 16);
+    pk.w = o[6] | ((uint32_t)o[7] << 16);
+    uint16_t* dst = is_a ? a_ext + row * kx + j0 : b_ext + (row - xq.rows) * kx + j0;
+    *reinterpret_cast<uint4*>(dst) = pk;
+  }
+}
+
+// W [N][K] (pitch ldw) -> WT [K][ldt], 64 x 64 tiles through shared memory,
+// reads and writes as bf16 pairs (32-bit accesses; rows of both are 16-byte
+// aligned and k, ldt even)
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ w, int64_t ldw, int64_t n,
+                                                             int64_t k, uint16_t* __restrict__ wt, int64_t ldt) {
+  __shared__ uint16_t tile[64][66];
+  const int64_t tiles_k = cdiv(k, 64), tiles = cdiv(n, 64) * tiles_k;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    const int64_t n0 = (t / tiles_k) * 64, k0 = (t % tiles_k) * 64;
+    for (int r = ty; r < 64; r += 8) {
+      const int64_t nn = n0 + r, kk = k0 + 2 * tx;
+      uint32_t v = 0;
+      if (nn < n) {
+        if (kk + 1 < k) v = *reinterpret_cast<const uint32_t*>(w + nn * ldw + kk);
+        else if (kk < k) v = w[nn * ldw + kk];
+      }
+      tile[r][2 * tx] = (uint16_t)v;
+      tile[r][2 * tx + 1] = (uint16_t)(v >> 16);
+    }
+    __syncthreads();
+    for (int r = ty; r < 64; r += 8) {
+      const int64_t kk = k0 + r, nn = n0 + 2 * tx;
+      if (kk < k) {
+        const uint32_t v = tile[2 * tx][r] | ((uint32_t)tile[2 * tx + 1][r] << 16);
+        if (nn + 1 < n) *reinterpret_cast<uint32_t*>(wt + kk * ldt + nn) = v;
+        else if (nn < n) wt[kk * ldt + nn] = (uint16_t)v;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+struct OccEntry {
+  int32_t k;
+  float v;
+};
+
+// 8-bit mask of the outliers |x| > tau among 8 consecutive elements.  bf16:
+// on the bit patterns, two elements per instruction (for bf16 x, |x| > tau iff
+// the magnitude bits exceed those of tau truncated to bf16; NaNs are not
+// outliers, as in the clamp).
+__device__ __forceinline__ uint32_t halves_to_bits(uint32_t m) { return (m & 1u) | ((m >> 15) & 2u); }
+
+template <int XDT>
+__device__ __forceinline__ uint32_t outlier_mask8(const void* x, int64_t off, float tau, uint32_t tau2) {
+  if constexpr (XDT == FP4_DTYPE_BF16) {
+    const uint4 u = ld_nc_v4_l1(static_cast<const uint16_t*>(x) + off);
+    const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+    uint32_t mask = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t a = q[j] & 0x7FFF7FFFu;
+      const uint32_t m = __vcmpgtu2(a, tau2) & ~__vcmpgtu2(a, 0x7F807F80u);
+      mask |= halves_to_bits(m) << (2 * j);
+    }
+    return mask;
+  } else {
+    float e[8];
+    load8<FP4_DTYPE_F32, true>(x, off, e);
+    uint32_t mask = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mask |= (fabsf(e[j]) > tau ? 1u : 0u) << j;
+    return mask;
+  }
+}
+
+// One warp per row: the scattered outliers of the row (|x| > tau, in a column
+// that the extra GEMM columns do not carry), lane-major: lane l writes the
+// outliers of its columns 8l..8l+7, 256+8l.., in order, after the lanes below
+// it.  The 8 warps of a CTA claim their segments with one atomic on the global
+// cursor.  The row is read twice (count, write); the second read hits the
+// caches and touches only the 8-column groups that hold scattered outliers.
+template <int FMT, int XDT>
+__global__ void __launch_bounds__(256) occ_extract_kernel(const void* __restrict__ x, int64_t ldx, int64_t rows,
+                                                          int64_t cols, fp4_operand xq, fp4_operand wq,
+                                                          const float* __restrict__ tau_p,
+                                                          const uint32_t* __restrict__ dense, uint32_t* cursor,
+                                                          uint32_t capacity, uint32_t* row_start, uint32_t* row_len,
+                                                          OccEntry* entries, unsigned int* status) {
+  __shared__ uint32_t warp_off[8];
+  __shared__ uint32_t cta_base;
+  const float tau = *tau_p;
+  const uint32_t taub = (__float_as_uint(tau) >> 16) & 0x7FFFu, tau2 = taub | (taub << 16);
+  const bool tail = tail_inv_alpha<FMT>(xq, wq) != 0.0f;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  auto scat_mask = [&](int64_t r, int64_t c0) {
+    const uint32_t m = outlier_mask8<XDT>(x, r * ldx + c0, tau, tau2);
+    if (!m || !tail) return m;
+    return m & ~((dense[c0 >> 5] >> (c0 & 31)) & 0xFFu);
+  };
+  // rows of up to 16 x 256 columns keep their 16 eight-bit masks in 4 registers
+  // between the passes; longer rows recompute them
+  const bool short_row = cols <= 16 * 256;
+  for (int64_t r0 = blockIdx.x * (int64_t)8; r0 < rows; r0 += (int64_t)gridDim.x * 8) {   // uniform over the CTA
+    const int64_t r = r0 + w;
+    const bool active = r < rows;
+    uint32_t mine = 0;
+    uint32_t mk[4] = {0u, 0u, 0u, 0u};
+    if (active) {
+      if (short_row) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int64_t c0 = 256 * i + 8 * lane;
+          if (c0 < cols) mk[i >> 2] |= scat_mask(r, c0) << (8 * (i & 3));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mine += __popc(mk[i]);
+      } else {
+#pragma unroll 4
+        for (int64_t c0 = 8 * lane; c0 < cols; c0 += 256) mine += __popc(scat_mask(r, c0));
+      }
+    }
+    uint32_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const uint32_t cnt = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (lane == 0) warp_off[w] = cnt;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t sum = 0;
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t c = warp_off[i];
+        warp_off[i] = sum;
+        sum += c;
+      }
+      cta_base = sum ? atomicAdd(cursor, sum) : 0u;
+    }
+    __syncthreads();
+    const uint32_t base = cta_base + warp_off[w];
+    __syncthreads();                       // warp_off / cta_base are rewritten next iteration
+    if (!active) continue;
+    const bool fits = (uint64_t)base + cnt <= capacity;
+    if (lane == 0) {
+      row_start[r] = base;
+      row_len[r] = fits ? cnt : 0u;
+      if (!fits) atomicOr(status, FP4_DEVICE_OVERFLOW);
+    }
+    if (!mine || !fits) continue;
+    uint32_t pos = base + incl - mine;
+    auto emit = [&](int64_t c0, uint32_t m) {
+      while (m) {
+        const int j = __ffs(m) - 1;
+        m &= m - 1;
+        entries[pos++] = OccEntry{(int32_t)(c0 + j), clamp_residual(load_elem<XDT>(x, r * ldx + c0 + j), tau)};
+      }
+    };
+    if (short_row) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t m = (mk[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+        if (m) emit(256 * i + 8 * lane, m);
+      }
+    } else {
+      for (int64_t c0 = 8 * lane; c0 < cols; c0 += 256) emit(c0, scat_mask(r, c0));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// quality statistics: sums of x^2, x_hat^2, x x_hat, (x - x_hat)^2 in fp64,
+// x_hat = dequant(code) [+ dX when tau is given].  One thread per block.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+template <int FMT, int XDT>
+__global__ void __launch_bounds__(256) error_stats_kernel(const void* __restrict__ x, int64_t ldx, fp4_operand q,
+                                                          const float* __restrict__ tau_p, double* sums) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
+  const bool occ = tau_p != nullptr;
+  const float tau = occ ? *tau_p : 0.0f;
+  const int64_t total = q.rows * nsf_row;
+  double sxx = 0.0, shh = 0.0, sxh = 0.0, see = 0.0;
+  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
+       blk += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = blk / nsf_row, j = blk - r * nsf_row;
+    const uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
+    const float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
+    float v[B];
+#pragma unroll
+    for (int q8 = 0; q8 < B / 8; ++q8) load8<XDT>(x, r * ldx + j * B + 8 * q8, v + 8 * q8);
+    const uint8_t* cp = q.codes + r * (q.k >> 1) + j * (B / 2);
+#pragma unroll
+    for (int e = 0; e < B; ++e) {
+      const uint32_t code = (cp[e >> 1] >> (4 * (e & 1))) & 15u;
+      const uint32_t mc = code & 7u;
+      const float mag = mc < 4 ? 0.5f * (float)mc : (mc == 4 ? 2.0f : mc == 5 ? 3.0f : mc == 6 ? 4.0f : 6.0f);
+      float d = __fmul_rn(mag, s);
+      if (FMT == FP4_FMT_NVFP4) d = __fmul_rn(d, g);
+      if (code & 8u) d = -d;
+      double h = (double)d;
+      if (occ) h += (double)clamp_residual(v[e], tau);
+      const double xv = (double)v[e], ev = xv - h;
+      sxx = fma(xv, xv, sxx);
+      shh = fma(h, h, shh);
+      sxh = fma(xv, h, sxh);
+      see = fma(ev, ev, see);
+    }
+  }
+  __shared__ double part[4][8];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  sxx = warp_sum_d(sxx);
+  shh = warp_sum_d(shh);
+  sxh = warp_sum_d(sxh);
+  see = warp_sum_d(see);
+  if (lane == 0) {
+    part[0][w] = sxx;
+    part[1][w] = shh;
+    part[2][w] = sxh;
+    part[3][w] = see;
+  }
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    double s = 0.0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += part[threadIdx.x][i];
+    atomicAdd(&sums[threadIdx.x], s);
+  }
+}
+
+inline int grid_cap(int64_t items, int per_block, int num_sms, int per_sm = 8) {
+  const int64_t need = cdiv(items, per_block), cap = (int64_t)num_sms * per_sm;
+  return (int)std::max<int64_t>(1, std::min(need, cap));
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+// workspace: select state, then the fine and coarse histograms of each pass
+size_t occ_threshold_ws_bytes(int dt) {
+  return 256 + sizeof(unsigned long long) * (kHistBins + 256 + (dt == FP4_DTYPE_F32 ? kLowBins + 256 : 0));
+}
+
+cudaError_t launch_occ_threshold(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, uint64_t rank,
+                                 void* ws, float* tau, long long* n_out, int num_sms, cudaStream_t st) {
+  OccSelect* sel = static_cast<OccSelect*>(ws);
+  auto* fine = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + 256);
+  auto* coarse = fine + kHistBins;
+  cudaError_t e = cudaMemsetAsync(ws, 0, occ_threshold_ws_bytes(dt), st);
+  if (e != cudaSuccess) return e;
+  const uint64_t n = (uint64_t)rows * cols;
+  const uint32_t total_vecs = (uint32_t)(n / 8);
+  const FastDiv fd = make_fastdiv((uint32_t)(cols / 8));
+  const size_t smem = kHistBins * sizeof(uint32_t);
+  const int grid = grid_cap(total_vecs, kHistThreads, num_sms, 1);
+  if (dt == FP4_DTYPE_BF16) {
+    e = cudaFuncSetAttribute(occ_hist_kernel<FP4_DTYPE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    occ_hist_kernel<FP4_DTYPE_BF16><<<grid, kHistThreads, smem, st>>>(x, ldx, fd, total_vecs, fine, coarse);
+    occ_select_kernel<0, FP4_DTYPE_BF16><<<1, 32, 0, st>>>(fine, coarse, n, rank, sel, tau, n_out);
+  } else {
+    e = cudaFuncSetAttribute(occ_hist_kernel<FP4_DTYPE_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    occ_hist_kernel<FP4_DTYPE_F32><<<grid, kHistThreads, smem, st>>>(x, ldx, fd, total_vecs, fine, coarse);
+    occ_select_kernel<0, FP4_DTYPE_F32><<<1, 32, 0, st>>>(fine, coarse, n, rank, sel, tau, n_out);
+    unsigned long long* fine_low = coarse + 256;
+    unsigned long long* coarse_low = fine_low + kLowBins;
+    occ_hist_low_kernel<<<grid_cap(total_vecs, 256, num_sms), 256, 0, st>>>(static_cast<const float*>(x), ldx, fd,
+                                                                            total_vecs, sel, fine_low, coarse_low);
+    occ_select_kernel<1, FP4_DTYPE_F32><<<1, 32, 0, st>>>(fine_low, coarse_low, n, rank, sel, tau, n_out);
+  }
+  return cudaGetLastError();
+}
+
+OccLayout occ_layout(int64_t m, int64_t n, int64_t k, int k_dense, int64_t max_outliers) {
+  OccLayout L{};
+  auto al = [](size_t v) { return (v + 255) & ~size_t(255); };
+  L.kx = k_dense > 0 ? cdiv(k_dense, 64) * 64 : 0;
+  L.ldt = cdiv(n, 8) * 8;
+  size_t off = 0;
+  L.counts = off;    off = al(off + sizeof(float) * 2 * (size_t)k);     // top-k scratch: values + flags
+  L.hot = off;       off = al(off + sizeof(int32_t) * (size_t)std::max(k_dense, 1));
+  L.flags = off;     off = al(off + sizeof(uint32_t) * (size_t)cdiv(k, 32));
+  L.a_ext = off;     off = al(off + 2 * (size_t)m * L.kx);
+  L.b_ext = off;     off = al(off + 2 * (size_t)n * L.kx);
+  L.wt = off;        off = al(off + 2 * (size_t)k * L.ldt);
+  L.row_start = off; off = al(off + sizeof(uint32_t) * (size_t)m);
+  L.row_len = off;   off = al(off + sizeof(uint32_t) * (size_t)m);
+  L.cursor = off;    off = al(off + sizeof(uint32_t));
+  L.entries = off;   off = al(off + sizeof(OccEntry) * (size_t)std::max<int64_t>(max_outliers, 1));
+  L.bytes = off;
+  return L;
+}
+
+cudaError_t launch_occ_prepare(const void* x, int xdt, int64_t ldx, const uint16_t* w, int64_t ldw,
+                               const fp4_operand& xq, const fp4_operand& wq, const float* tau, const float* col_counts,
+                               int k_dense, int64_t max_outliers, void* ws, const OccLayout& L, unsigned int* status,
+                               int num_sms, cudaStream_t st) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const int64_t M = xq.rows, N = wq.rows, K = xq.k;
+  uint32_t* flags = reinterpret_cast<uint32_t*>(base + L.flags);
+  cudaError_t e = cudaMemsetAsync(flags, 0, sizeof(uint32_t) * (size_t)cdiv(K, 32), st);
+  if (e != cudaSuccess) return e;
+  const int32_t* hot = reinterpret_cast<int32_t*>(base + L.hot);
+  if (k_dense > 0) {
+    float* counts = reinterpret_cast<float*>(base + L.counts);
+    e = cudaMemcpyAsync(counts, col_counts, sizeof(float) * K, cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return e;
+    e = launch_hcp_topk(counts, K, k_dense, reinterpret_cast<int32_t*>(base + L.hot), st);
+    if (e != cudaSuccess) return e;
+    occ_flags_kernel<<<(unsigned)cdiv(k_dense, 256), 256, 0, st>>>(hot, k_dense, flags);
+    const int grid = grid_cap((M + N) * (L.kx / 8), 256, num_sms);
+    uint16_t* a_ext = reinterpret_cast<uint16_t*>(base + L.a_ext);
+    uint16_t* b_ext = reinterpret_cast<uint16_t*>(base + L.b_ext);
+#define FP4_OCC_TAIL(FMT, XDT) \
+  occ_tail_kernel<FMT, XDT><<<grid, 256, 0, st>>>(x, ldx, w, ldw, xq, wq, tau, hot, k_dense, L.kx, a_ext, b_ext)
+    if (xq.format == FP4_FMT_MXFP4) {
+      if (xdt == FP4_DTYPE_BF16) FP4_OCC_TAIL(FP4_FMT_MXFP4, FP4_DTYPE_BF16); else FP4_OCC_TAIL(FP4_FMT_MXFP4, FP4_DTYPE_F32);
+    } else {
+      if (xdt == FP4_DTYPE_BF16) FP4_OCC_TAIL(FP4_FMT_NVFP4, FP4_DTYPE_BF16); else FP4_OCC_TAIL(FP4_FMT_NVFP4, FP4_DTYPE_F32);
+    }
+#undef FP4_OCC_TAIL
+  }
+  // W^T for the scattered pass (padding columns zeroed when N is not a multiple of 8)
+  uint16_t* wt = reinterpret_cast<uint16_t*>(base + L.wt);
+  if (L.ldt != N) {
+    e = cudaMemsetAsync(wt, 0, 2 * (size_t)K * L.ldt, st);
+    if (e != cudaSuccess) return e;
+  }
+  transpose_bf16_kernel<<<grid_cap(cdiv(N, 64) * cdiv(K, 64), 1, num_sms, 8), 256, 0, st>>>(w, ldw, N, K, wt, L.ldt);
+  uint32_t* cursor = reinterpret_cast<uint32_t*>(base + L.cursor);
+  e = cudaMemsetAsync(cursor, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  uint32_t* rs = reinterpret_cast<uint32_t*>(base + L.row_start);
+  uint32_t* rl = reinterpret_cast<uint32_t*>(base + L.row_len);
+  OccEntry* ent = reinterpret_cast<OccEntry*>(base + L.entries);
+  const int grid = grid_cap(cdiv(M, 8), 1, num_sms, 8);
+#define FP4_OCC_EXTRACT(FMT, XDT)                                                                       \
+  occ_extract_kernel<FMT, XDT><<<grid, 256, 0, st>>>(x, ldx, M, K, xq, wq, tau, flags, cursor, (uint32_t)max_outliers, \
+                                                    rs, rl, ent, status)
+  if (xq.format == FP4_FMT_MXFP4) {
+    if (xdt == FP4_DTYPE_BF16) FP4_OCC_EXTRACT(FP4_FMT_MXFP4, FP4_DTYPE_BF16); else FP4_OCC_EXTRACT(FP4_FMT_MXFP4, FP4_DTYPE_F32);
+  } else {
+    if (xdt == FP4_DTYPE_BF16) FP4_OCC_EXTRACT(FP4_FMT_NVFP4, FP4_DTYPE_BF16); else FP4_OCC_EXTRACT(FP4_FMT_NVFP4, FP4_DTYPE_F32);
+  }
+#undef FP4_OCC_EXTRACT
+  return cudaGetLastError();
+}
+
+cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const float* tau,
+                               double* sums, int num_sms, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(sums, 0, 4 * sizeof(double), st);
+  if (e != cudaSuccess) return e;
+  const int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t total = q.rows * (q.k / B);
+  if (total == 0) return cudaSuccess;
+  const int grid = grid_cap(total, 256, num_sms);
+#define FP4_STATS(FMT, XDT) error_stats_kernel<FMT, XDT><<<grid, 256, 0, st>>>(x, ldx, q, tau, sums)
+  if (q.format == FP4_FMT_MXFP4) {
+    if (xdt == FP4_DTYPE_BF16) FP4_STATS(FP4_FMT_MXFP4, FP4_DTYPE_BF16); else FP4_STATS(FP4_FMT_MXFP4, FP4_DTYPE_F32);
+  } else {
+    if (xdt == FP4_DTYPE_BF16) FP4_STATS(FP4_FMT_NVFP4, FP4_DTYPE_BF16); else FP4_STATS(FP4_FMT_NVFP4, FP4_DTYPE_F32);
+  }
+#undef FP4_STATS
+  return cudaGetLastError();
+}
+
+}  // namespace fp4

@@ -211,11 +211,40 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const void* __rest
 // second 16 bytes of each 32-byte sector do not fetch the sector again.
 // PLAIN: RTN without RHT (the forward path), compiled without the SR and RHT
 // code so that its register count, and so its occupancy, is not set by them.
-template <int FMT, int DT, bool PLAIN>
+// CLAMP: x is first clamped to [-tau, tau], tau = *o.clamp (outlier clamping,
+// [msr] §三), and the elements with |x| > tau are counted per column: in
+// shared memory (counts_s, merged once per CTA) when the row fits, else by
+// global atomics
+constexpr int kClampSmemCols = 8192;
+template <bool CLAMP, int B>
+__device__ __forceinline__ void clamp_block(float* v, float tau, float* col_counts, uint32_t* counts_s, uint32_t k0) {
+  if constexpr (CLAMP) {
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      if (fabsf(v[j]) > tau) {
+        if (counts_s) atomicAdd(counts_s + k0 + j, 1u);
+        else if (col_counts) atomicAdd(col_counts + k0 + j, 1.0f);
+        v[j] = copysignf(tau, v[j]);
+      }
+    }
+  }
+}
+
+template <int FMT, int DT, bool PLAIN, bool CLAMP = false>
 __global__ void __launch_bounds__(kThreads) quant_rows32_kernel(const void* __restrict__ x, int64_t ldx, FastDiv nblk,
                                                                 uint32_t total, int contiguous, QuantOut o) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
   const float g = load_g(o, FMT);
+  const float tau = CLAMP ? *o.clamp : 0.0f;
+  extern __shared__ uint32_t counts_smem[];
+  uint32_t* counts_s = nullptr;
+  if constexpr (CLAMP) {
+    if (o.col_counts && o.out_cols <= kClampSmemCols) {   // uniform over the grid
+      counts_s = counts_smem;
+      for (int b = threadIdx.x; b < (int)o.out_cols; b += blockDim.x) counts_s[b] = 0u;
+      __syncthreads();
+    }
+  }
   const bool sr = !PLAIN && o.rounding == FP4_ROUND_SR;
   const bool rht = !PLAIN && o.rht != 0;
   const uint32_t stride = gridDim.x * blockDim.x;
@@ -237,6 +266,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows32_kernel(const void* __re
 #pragma unroll
       for (int q = 0; q < B / 8; ++q) load8<DT, true>(x, e2 + 8 * q, w + 8 * q);
     }
+    clamp_block<CLAMP, B>(v, tau, o.col_counts, counts_s, k0);
+    if (two) clamp_block<CLAMP, B>(w, tau, o.col_counts, counts_s, k2);
     if (rht) {
 #pragma unroll
       for (int h = 0; h < B / 16; ++h) rht16(v + 16 * h, o.rht_signs);
@@ -254,6 +285,13 @@ __global__ void __launch_bounds__(kThreads) quant_rows32_kernel(const void* __re
 #pragma unroll
       for (int j = 0; j < B; ++j) amax2 = fmaxf(amax2, fabsf(w[j]));
       encode_store_block<FMT, B>(w, g, o, r2, k2, amax2, sr);
+    }
+  }
+  if constexpr (CLAMP) {
+    if (counts_s) {
+      __syncthreads();
+      for (int b = threadIdx.x; b < (int)o.out_cols; b += blockDim.x)
+        if (counts_s[b]) atomicAdd(o.col_counts + b, (float)counts_s[b]);
     }
   }
 }
@@ -799,12 +837,148 @@ __device__ __forceinline__ float dge_fprime(float xs, float inv_k, float expo, f
   return a >= 6.0f ? outside : f;
 }
 
-template <int FMT, int XDT, int DYDT, bool K5>
-__global__ void __launch_bounds__(kThreads) dge_kernel(const void* __restrict__ x, int64_t ldx, fp4_operand q,
-                                                       const void* __restrict__ dy, int64_t lddy, float* dx,
-                                                       int64_t lddx, float inv_k, float expo, float clamp,
-                                                       float outside, FastDiv nsf_div) {
+// ----------------------------------------------------------------------------
+// Sigmoid-smoothed quantizer ([grad] §3.2) on the signed E2M1 grid
+//   q_0..q_14 = -6..6, thresholds c_i = (q_i + q_{i+1}) / 2, steps v_i = q_{i+1} - q_i,
+//   Q_soft(xs) = q_0 + sum_i v_i sigma(beta (xs - c_i)),
+//   Q_soft'(xs) = beta sum_i v_i sigma(z_i) (1 - sigma(z_i)),  z_i = beta (xs - c_i).
+// ----------------------------------------------------------------------------
+// Q_soft is odd and Q_soft' even, so both are evaluated at a = |xs|.  With
+// t = e^-|z| <= 1: sigma(z) = 1 / (1 + t) for z >= 0 and t / (1 + t) below, and
+// sigma (1 - sigma) = t / (1 + t)^2, which keeps full relative precision in the
+// tails.  The derivative's terms are summed as one fraction N / D, with
+// D = prod (1 + t_i)^2 in [1, 4^14], so the whole sum costs one division.
+//
+// Window: thresholds are >= 0.5 apart, so the k-th threshold on one side of a
+// lies >= 0.5 (k - 1) beyond the nearest one on that side.  Keeping the W
+// nearest on each side leaves out terms below 16 e^(-beta W / 2) / (1 - e^(-beta / 2))
+// of a kept one (16 = the ratio of the largest to the smallest step, times the
+// 4 between e^-|z| and sigma (1 - sigma)); with beta W >= 56 ln 2 that is
+// below 2^-24 per side.  W = 0 evaluates all 14 thresholds.
+__host__ __device__ constexpr float e2m1_level(int k) {  // k = 0..7
+  return k < 4 ? 0.5f * k : (k < 6 ? float(k - 2) : float(2 * k - 8));
+}
+__host__ __device__ constexpr float soft_level(int i) {  // q_i, i = 0..14
+  return i >= 7 ? e2m1_level(i - 7) : -e2m1_level(7 - i);
+}
+// table entry i: (c_i, v_i) and q_i, the level just below c_i; past the last
+// threshold the entries contribute nothing (c = 1e30, v = 0).  (c, v) pairs
+// are read per term (8 bytes: two shared-memory wavefronts per warp), q once.
+constexpr int kSoftTab = 18;
+struct SoftTable {
+  float2 cv[kSoftTab];
+  float q[kSoftTab];
+};
+__host__ __device__ constexpr float2 soft_cv(int i) {
+  return i < 14 ? float2{0.5f * (soft_level(i) + soft_level(i + 1)), soft_level(i + 1) - soft_level(i)}
+                : float2{1e30f, 0.0f};
+}
+__host__ __device__ constexpr float soft_q(int i) { return i < 14 ? soft_level(i) : 6.0f; }
+template <int W>
+__device__ __forceinline__ float2 soft_term(const SoftTable* tab, int i0, int m) {
+  if constexpr (W == 0) {
+    return soft_cv(m);
+  } else {
+    return tab->cv[i0 + m];
+  }
+}
+
+// 2^x, PTX ex2.approx.ftz.f32 (relative error ~2^-22; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// index of the first threshold of a's window: thresholds 0..6 are negative,
+// so 7 + (number of positive thresholds <= a) is the first one above a
+template <int W>
+__device__ __forceinline__ int soft_window_start(float a) {
+  const int above = (a >= 0.25f) + (a >= 0.75f) + (a >= 1.25f) + (a >= 1.75f) + (a >= 2.5f) + (a >= 3.5f) +
+                    (a >= 5.0f);
+  return 7 + above - W;
+}
+
+// Q_soft'(xs); nbl = -beta log2(e)
+template <int W>
+__device__ __forceinline__ float soft_grad(float xs, float beta, float nbl, const SoftTable* tab) {
+  const float a = fabsf(xs);
+  constexpr int n = W == 0 ? 14 : 2 * W;
+  const int i0 = W == 0 ? 0 : soft_window_start<W>(a);
+  float num = 0.0f, den = 1.0f;
+#pragma unroll
+  for (int m = 0; m < n; ++m) {
+    const float2 e = soft_term<W>(tab, i0, m);
+    const float t = ex2_approx(fabsf(a - e.x) * nbl);
+    const float w = fmaf(t, t + 2.0f, 1.0f);              // (1 + t)^2
+    num = fmaf(num, w, e.y * t * den);
+    den *= w;
+  }
+  return beta * __fdividef(num, den);
+}
+
+// Q_soft(xs)
+template <int W>
+__device__ __forceinline__ float soft_value(float xs, float nbl, const SoftTable* tab) {
+  const float a = fabsf(xs);
+  constexpr int n = W == 0 ? 14 : 2 * W;
+  const int i0 = W == 0 ? 0 : soft_window_start<W>(a);
+  float acc = W == 0 ? -6.0f : tab->q[i0];                // the level below the window
+#pragma unroll
+  for (int m = 0; m < n; ++m) {
+    const float2 e = soft_term<W>(tab, i0, m);
+    const float d = a - e.x;
+    const float t = ex2_approx(fabsf(d) * nbl);
+    acc = fmaf(e.y, __fdividef(d >= 0.0f ? 1.0f : t, 1.0f + t), acc);
+  }
+  return xs < 0.0f ? -acc : acc;
+}
+
+// ----------------------------------------------------------------------------
+// Maps of the scaled input xs = x / s, one thread per block of x (blocks along
+// cols): DGE backward ([msr] §二), Q_soft forward and backward.  xs is formed
+// exactly as the quantizer formed it from the stored scale.  Each op gives the
+// output element from (xs, s, dy element); ops without kDy take no dy (DYDT < 0).
+// ----------------------------------------------------------------------------
+template <bool K5>
+struct DgeOp {
+  float inv_k, expo, clamp, outside;
+  static constexpr bool kTable = false, kScale = false, kDy = true;
+  __device__ float operator()(float xs, float, float d, const SoftTable*) const {
+    return __fmul_rn(d, dge_fprime<K5>(xs, inv_k, expo, clamp, outside));
+  }
+};
+template <int W>
+struct SoftGradOp {
+  float beta, nbl;
+  static constexpr bool kTable = W != 0, kScale = false, kDy = true;
+  __device__ float operator()(float xs, float, float d, const SoftTable* tab) const {
+    return d * soft_grad<W>(xs, beta, nbl, tab);
+  }
+};
+template <int W>
+struct SoftValueOp {
+  float nbl;
+  static constexpr bool kTable = W != 0, kScale = true, kDy = false;
+  __device__ float operator()(float xs, float s, float, const SoftTable* tab) const {
+    return s * soft_value<W>(xs, nbl, tab);
+  }
+};
+
+template <int FMT, int XDT, int DYDT, class Op>
+__global__ void __launch_bounds__(kThreads) scaled_map_kernel(const void* __restrict__ x, int64_t ldx, fp4_operand q,
+                                                              const void* __restrict__ dy, int64_t lddy, float* out,
+                                                              int64_t ldo, Op op, FastDiv nsf_div) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  __shared__ SoftTable tab_s;
+  const SoftTable* tab = &tab_s;
+  if constexpr (Op::kTable) {
+    if (threadIdx.x < kSoftTab) {
+      tab_s.cv[threadIdx.x] = soft_cv(threadIdx.x);
+      tab_s.q[threadIdx.x] = soft_q(threadIdx.x);
+    }
+    __syncthreads();
+  }
   const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
   const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
   const int64_t total = q.rows * nsf_row;
@@ -819,22 +993,40 @@ __global__ void __launch_bounds__(kThreads) dge_kernel(const void* __restrict__ 
       j = blk - r * nsf_row;
     }
   };
-  auto multiplier = [&](int64_t r, int64_t j) {
+  // xs = x * mult; s the block scale (computed only for ops that use it)
+  auto scale = [&](int64_t r, int64_t j, float& mult, float& s) {
     const uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
-    if (FMT == FP4_FMT_MXFP4) return e8m0_inv_scale(sb);
-    const float s = __fmul_rn(e4m3_decode(sb), g);
-    return s == 0.0f ? 0.0f : __frcp_rn(s);
+    if (FMT == FP4_FMT_MXFP4) {
+      mult = e8m0_inv_scale(sb);
+      s = Op::kScale ? e8m0_scale(sb) : 0.0f;
+    } else {
+      s = __fmul_rn(e4m3_decode(sb), g);
+      mult = s == 0.0f ? 0.0f : __frcp_rn(s);
+    }
   };
-  auto finish = [&](const float* v, const float* d, float mult, int64_t r, int64_t j) {
+  auto finish = [&](const float* v, const float* d, int64_t r, int64_t j) {
+    float mult, s;
+    scale(r, j, mult, s);
 #pragma unroll
     for (int q8 = 0; q8 < B / 8; ++q8) {
       float o[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        o[e] = __fmul_rn(d[8 * q8 + e], dge_fprime<K5>(__fmul_rn(v[8 * q8 + e], mult), inv_k, expo, clamp, outside));
-      float4* dst = reinterpret_cast<float4*>(dx + r * lddx + j * B + 8 * q8);
+      for (int e = 0; e < 8; ++e) o[e] = op(__fmul_rn(v[8 * q8 + e], mult), s, d[8 * q8 + e], tab);
+      float4* dst = reinterpret_cast<float4*>(out + r * ldo + j * B + 8 * q8);
       dst[0] = make_float4(o[0], o[1], o[2], o[3]);
       dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
+  };
+  auto load = [&](int64_t r, int64_t j, float* v, float* d) {
+#pragma unroll
+    for (int q8 = 0; q8 < B / 8; ++q8) {
+      load8<XDT>(x, r * ldx + j * B + 8 * q8, v + 8 * q8);
+      if constexpr (DYDT >= 0) {
+        load8<DYDT>(dy, r * lddy + j * B + 8 * q8, d + 8 * q8);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d[8 * q8 + e] = 0.0f;
+      }
     }
   };
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -846,20 +1038,10 @@ __global__ void __launch_bounds__(kThreads) dge_kernel(const void* __restrict__ 
     split(blk, r, j);
     if (two) split(blk2, r2, j2);
     float v[B], d[B], v2[B], d2[B];
-#pragma unroll
-    for (int q8 = 0; q8 < B / 8; ++q8) {
-      load8<XDT>(x, r * ldx + j * B + 8 * q8, v + 8 * q8);
-      load8<DYDT>(dy, r * lddy + j * B + 8 * q8, d + 8 * q8);
-    }
-    if (two) {
-#pragma unroll
-      for (int q8 = 0; q8 < B / 8; ++q8) {
-        load8<XDT>(x, r2 * ldx + j2 * B + 8 * q8, v2 + 8 * q8);
-        load8<DYDT>(dy, r2 * lddy + j2 * B + 8 * q8, d2 + 8 * q8);
-      }
-    }
-    finish(v, d, multiplier(r, j), r, j);
-    if (two) finish(v2, d2, multiplier(r2, j2), r2, j2);
+    load(r, j, v, d);
+    if (two) load(r2, j2, v2, d2);
+    finish(v, d, r, j);
+    if (two) finish(v2, d2, r2, j2);
   }
 }
 
@@ -992,6 +1174,23 @@ cudaError_t launch_quant_rows(const void* x, int dt, int64_t rows, int64_t cols,
   return cudaGetLastError();
 }
 
+cudaError_t launch_quant_rows_clamped(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                                      const QuantOut& o, int num_sms, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  int B = fmt == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nblk = cols / B, total = rows * nblk;
+  if (total >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  int grid = grid_for(cdiv(total, 2), kThreads, num_sms);
+  const FastDiv fd = make_fastdiv((uint32_t)nblk);
+  const int contiguous = ldx == cols;
+  const bool plain = o.rounding == FP4_ROUND_RTN && !o.rht;
+  const size_t smem = (o.col_counts && cols <= kClampSmemCols) ? sizeof(uint32_t) * cols : 0;
+  FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT,
+    if (plain) quant_rows32_kernel<FMT, DT, true, true><<<grid, kThreads, smem, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o);
+    else quant_rows32_kernel<FMT, DT, false, true><<<grid, kThreads, smem, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o)));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quant_tile(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
                               bool two_d, bool transpose, const QuantOut& o, int num_sms, cudaStream_t st) {
   if (rows == 0 || cols == 0) return cudaSuccess;
@@ -1082,31 +1281,53 @@ cudaError_t launch_rht16(const void* x, int dt, int64_t rows, int64_t cols, int6
   return cudaGetLastError();
 }
 
-cudaError_t launch_dge(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
-                       int64_t lddy, float* dx, int64_t lddx, float k, float clamp, float outside,
-                       int num_sms, cudaStream_t st) {
+template <class Op>
+cudaError_t launch_scaled_map(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
+                              int64_t lddy, float* out, int64_t ldo, const Op& op, int num_sms, cudaStream_t st) {
   int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
   int64_t total = q.rows * (q.k / B);
   if (total == 0) return cudaSuccess;
-  float inv_k = 1.0f / k, expo = 1.0f / k - 1.0f;
-  const bool k5 = k == 5.0f;
   const int grid = grid_for(cdiv(total, 2), kThreads, num_sms);
   const FastDiv fd = make_fastdiv((uint32_t)std::min<int64_t>(q.k / B, 0x7FFFFFFF));
-#define FP4_DGE_LAUNCH(K5)                                                                                      \
-  FP4_DISPATCH_FMT(q.format, FMT, FP4_DISPATCH_DT(xdt, XDT,                                                      \
-    if (dydt == FP4_DTYPE_BF16)                                                                                  \
-      dge_kernel<FMT, XDT, FP4_DTYPE_BF16, K5><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo, \
-                                                                          clamp, outside, fd);                       \
-    else                                                                                                         \
-      dge_kernel<FMT, XDT, FP4_DTYPE_F32, K5><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, dx, lddx, inv_k, expo,  \
-                                                                         clamp, outside, fd)))
-  if (k5) {
-    FP4_DGE_LAUNCH(true);
-  } else {
-    FP4_DGE_LAUNCH(false);
-  }
-#undef FP4_DGE_LAUNCH
+  FP4_DISPATCH_FMT(q.format, FMT, FP4_DISPATCH_DT(xdt, XDT,
+    if constexpr (!Op::kDy)
+      scaled_map_kernel<FMT, XDT, -1, Op><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, out, ldo, op, fd);
+    else if (dydt == FP4_DTYPE_BF16)
+      scaled_map_kernel<FMT, XDT, FP4_DTYPE_BF16, Op><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, out, ldo, op, fd);
+    else
+      scaled_map_kernel<FMT, XDT, FP4_DTYPE_F32, Op><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, out, ldo, op, fd)));
   return cudaGetLastError();
+}
+
+cudaError_t launch_dge(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
+                       int64_t lddy, float* dx, int64_t lddx, float k, float clamp, float outside,
+                       int num_sms, cudaStream_t st) {
+  const float inv_k = 1.0f / k, expo = 1.0f / k - 1.0f;
+  if (k == 5.0f)
+    return launch_scaled_map(x, xdt, ldx, q, dy, dydt, lddy, dx, lddx, DgeOp<true>{inv_k, expo, clamp, outside},
+                             num_sms, st);
+  return launch_scaled_map(x, xdt, ldx, q, dy, dydt, lddy, dx, lddx, DgeOp<false>{inv_k, expo, clamp, outside},
+                           num_sms, st);
+}
+
+// Window per side from beta (beta W >= 56 ln 2 = 38.816; W = 0: all thresholds).
+int soft_window(float beta) {
+  return beta >= 38.82f ? 1 : beta >= 19.41f ? 2 : beta >= 9.71f ? 4 : 0;
+}
+
+cudaError_t launch_soft(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
+                        int64_t lddy, float* out, int64_t ldo, float beta, int num_sms, cudaStream_t st) {
+  const float nbl = -beta * 1.4426950408889634f;  // -beta log2(e)
+#define FP4_SOFT_LAUNCH(W)                                                                                   \
+  return dy ? launch_scaled_map(x, xdt, ldx, q, dy, dydt, lddy, out, ldo, SoftGradOp<W>{beta, nbl}, num_sms, st) \
+            : launch_scaled_map(x, xdt, ldx, q, nullptr, 0, 0, out, ldo, SoftValueOp<W>{nbl}, num_sms, st)
+  switch (soft_window(beta)) {
+    case 1: FP4_SOFT_LAUNCH(1);
+    case 2: FP4_SOFT_LAUNCH(2);
+    case 4: FP4_SOFT_LAUNCH(4);
+    default: FP4_SOFT_LAUNCH(0);
+  }
+#undef FP4_SOFT_LAUNCH
 }
 
 cudaError_t launch_encode_e2m1(const float* xs, uint8_t* codes, int64_t n, int method, cudaStream_t st) {

@@ -21,6 +21,8 @@
  * --------------------------------
  *  - All pointers named x, codes, scales, out, ... are DEVICE pointers owned by
  *    the caller.  The library allocates only the context (fp4_create).
+ *  - A pointer may be NULL when the buffer it names holds no elements (a zero
+ *    extent); such calls validate their arguments and enqueue nothing.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  The return value reports argument validation and
  *    launch errors synchronously; FP4_OK means the work was enqueued.
@@ -187,6 +189,85 @@ int fp4_rht16(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_
 int fp4_dge_backward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx,
                      const fp4_operand* q, const void* dy, int32_t dy_dtype, int64_t lddy,
                      float* dx, int64_t lddx, float k, float clamp, float outside, void* stream);
+
+/* ---- sigmoid-smoothed quantizer ([grad] §3.2)
+ * Over the signed E2M1 levels q_0..q_14 = -6..6, with thresholds
+ * c_i = (q_i + q_{i+1})/2 and steps v_i = q_{i+1} - q_i (i = 0..13):
+ *   Q_soft(xs)  = q_0 + sum_i v_i sigma(beta (xs - c_i))        (-> RTN as beta -> inf)
+ *   Q_soft'(xs) = beta sum_i v_i sigma(z_i) (1 - sigma(z_i)),   z_i = beta (xs - c_i).
+ * xs = x/s is formed exactly as the quantizer formed it from the stored scales
+ * `q` (q->codes unused, may be NULL; blocks along cols, no RHT); s is held
+ * constant.  fp4_soft_forward: y = s Q_soft(x/s).  fp4_soft_backward:
+ * dx = dy Q_soft'(x/s); dy bf16 or fp32.  Outputs fp32, 16-byte aligned.
+ * 0 < beta <= 1e6.  For beta >= 9.71 / 19.41 / 38.82 only the 4 / 2 / 1
+ * thresholds nearest x/s on each side are evaluated: the terms left out are
+ * below 2^-23 of Q_soft' and 2^-26 in absolute value for Q_soft.             */
+int fp4_soft_forward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,
+                     float* y, int64_t ldy, float beta, void* stream);
+int fp4_soft_backward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,
+                      const void* dy, int32_t dy_dtype, int64_t lddy, float* dx, int64_t lddx, float beta,
+                      void* stream);
+
+/* ---- outlier clamping and compensation, OCC ([msr] §三, §六)
+ * The largest 1% of activation magnitudes are outliers: X is clamped to
+ * [-tau, tau] at the 99% quantile tau before it is quantized, and the part
+ * clamped away, dX = X - clamp(X) (a sparse matrix), is multiplied in high
+ * precision beside the FP4 GEMM:  Y = alpha Q(X_c) Q(W)^T + dX W^T.
+ *
+ * fp4_occ_threshold: tau = the ceil(q n)-th smallest |x| over the n = rows*cols
+ * elements (nearest rank, 0 < q <= 1; q = 0.99 is the page's choice), written
+ * to *tau (device fp32); *n_outliers (device int64) = #{|x| > tau}.  x bf16 or
+ * fp32, cols % 8 == 0, n / 8 < 2^31.  Integer selection: exact.  Caller
+ * workspace of fp4_occ_threshold_workspace_bytes(x_dtype) bytes.
+ * fp4_occ_max_outliers: n - ceil(q n), the most elements |x| > tau can hold
+ * (the capacity fp4_occ_gemm needs; host arithmetic in double).           */
+size_t fp4_occ_threshold_workspace_bytes(int32_t x_dtype);
+int64_t fp4_occ_max_outliers(int64_t rows, int64_t cols, double q);
+int fp4_occ_threshold(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols, int64_t ldx,
+                      double q, float* tau, int64_t* n_outliers, void* workspace, size_t ws_bytes, void* stream);
+
+/* fp4_occ_quantize: quantize X_c = clamp(x, -tau, tau) (tau device fp32) like
+ * fp4_quantize with transpose = 0, rht = 0 and 1D scaling (other params ->
+ * FP4_ERR_UNSUPPORTED).  NVFP4: g = tau / 2688 (tau is the amax of X_c).
+ * col_counts (device float[cols], may be NULL): overwritten with the number of
+ * outliers |x| > tau in each column (exact integers).                      */
+int fp4_occ_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols, int64_t ldx,
+                     const fp4_quant_params* p, const float* tau, uint8_t* codes, uint8_t* scales,
+                     float* tensor_scale, float* col_counts, void* stream);
+
+/* fp4_occ_gemm: Y[M,N] = alpha Q(X_c) Q(W)^T + dX W^T with xq = fp4_occ_quantize's
+ * output (FP4_SF_MMA), wq = W quantized (FP4_SF_MMA), w_bf16 = W itself [N][K]
+ * (pitch ldw) and x = the unclamped activations [M][K] (bf16 or fp32, pitch
+ * ldx).  dX W^T is computed in two parts:
+ *  - the k_dense columns with the most outliers (col_counts from
+ *    fp4_occ_quantize; ties to the lower index) become extra bf16 K columns of
+ *    the FP4 GEMM: A_ext = bf16(dX_H / alpha), B_ext = W_H (alpha = gX gW,
+ *    1 for MXFP4), accumulated with the FP4 part on the tensor cores;
+ *  - every other outlier (|x| > tau) is listed per row and the GEMM epilogue
+ *    adds v * W^T[k, :] to its row of Y in fp32 (a bf16 Y is rounded once
+ *    before and once after: each rounding within 2^-9).
+ * k_dense = 0 sends all outliers to the second part (col_counts may be NULL).
+ * An outlier so large that dX / alpha leaves the bf16 range makes its extra
+ * column infinite (|x| / tau ~ 1e28 for weights of amax 1e-3).
+ * max_outliers bounds the outliers of the second part (fp4_occ_max_outliers
+ * is always enough); a list that would outgrow it sets the context's status
+ * (fp4_sync_status -> FP4_ERR_TOO_LARGE) and the rows that did not fit are not
+ * compensated.  out_dtype bf16 or fp32, pitch ldy (16-byte rows).  Caller
+ * workspace of fp4_occ_gemm_workspace_bytes(M, N, K, k_dense, max_outliers). */
+size_t fp4_occ_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int32_t k_dense, int64_t max_outliers);
+int fp4_occ_gemm(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const void* w_bf16, int64_t ldw,
+                 const fp4_operand* xq, const fp4_operand* wq, const float* tau, const float* col_counts,
+                 int32_t k_dense, int64_t max_outliers, int32_t out_dtype, void* y, int64_t ldy, void* workspace,
+                 size_t ws_bytes, void* stream);
+
+/* ---- quantization quality ([msr] §三 reports cosine similarity, MSE, SNR)
+ * sums (device double[4], overwritten) = sum x^2, sum x_hat^2, sum x x_hat,
+ * sum (x - x_hat)^2 over the rows x k tensor x (blocks along cols) and its
+ * quantization q, x_hat = dequant(q) (+ x - clamp(x, -tau, tau) when tau is
+ * non-NULL: the OCC reconstruction).  fp64 accumulation.  cosine =
+ * s2 / sqrt(s0 s1), MSE = s3 / n, SNR = 10 log10(s0 / s3).                 */
+int fp4_quant_error_stats(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,
+                          const float* tau, double* sums, void* stream);
 
 /* ---- block-scaled FP4 GEMM ([msr] §四: the GEMMs are >95% of the compute)
  * C[M,N] = alpha * sum_k A[m,k] * B[n,k]  (TN: both operands K-major), FP32

@@ -170,6 +170,17 @@ def test_llama1b_mlp_up_step():
     want = o.dge_backward(wn[r_n], sc[r_n], o.NVFP4, g, dw[r_n], 5.0, 3.0)
     got = step.dWd.cpu().numpy()[r_n]
     assert np.all(np.abs(got - want) <= 1e-6 * np.abs(want))
+    # the sigmoid-smoothed estimator in DGE's place, in the launch the bench times
+    from test_gpu_soft import grad_tolerance, value_tolerance
+    xs = o.scaled_inputs(wn[r_n], sc[r_n], o.NVFP4, g)
+    for beta in (40.0, 1.0):
+        got = fp4.fp4_soft_backward(step.W, step.wq, step.dW, beta).cpu().numpy()[r_n].astype(np.float64)
+        want = o.soft_backward(wn[r_n], sc[r_n], o.NVFP4, g, dw[r_n], beta)
+        assert np.all(np.abs(got - want) <= grad_tolerance(xs, beta, want, dw[r_n])), beta
+    got = fp4.fp4_soft_forward(step.W, step.wq, 40.0).cpu().numpy()[r_n].astype(np.float64)
+    want = o.soft_forward(wn[r_n], sc[r_n], o.NVFP4, g, 40.0)
+    sv = o.block_scales_expanded(sc[r_n], o.NVFP4, g).astype(np.float64)
+    assert np.all(np.abs(got - want) <= value_tolerance(sv, want))
 
 
 def test_ffn7b_gemms_mxfp4():
