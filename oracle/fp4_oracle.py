@@ -311,7 +311,7 @@ def element_scale_inputs(fmt, amax_b, g):
 
 
 def quantize(x, fmt, rounding="rtn", scaling="1d", transpose=False, rht=False,
-             sr_seed=0, sr_offset=0, sr_stream=0, rht_seed=0, given_amax=None):
+             sr_seed=0, sr_offset=0, sr_stream=0, rht_seed=0, given_amax=None, block=None):
     """Block-scaled FP4 quantization of a 2-D tensor.
 
     x: fp32 array [R, C] (bf16 inputs are widened exactly).
@@ -320,6 +320,8 @@ def quantize(x, fmt, rounding="rtn", scaling="1d", transpose=False, rht=False,
     fmt MXFP4: 32-element blocks, E8M0 scale; NVFP4: 16-element blocks, E4M3
     scale times a per-tensor fp32 scale g ([lowprec §1.1]).
     rounding 'rtn' (forward) or 'sr' (backward) ([outlier §4.1]).
+    block: elements per scale (default the format's 32 / 16; [grad §4.2]
+    studies 16-128 for either scale format: block sizes are a parameter).
     scaling '1d' or '2d' (one scale per 16x16 tile, [outlier §4.1-4.2],
     NVFP4 only).  rht: RHT16 along the blocked axis first ([outlier §4.1]).
 
@@ -327,7 +329,7 @@ def quantize(x, fmt, rounding="rtn", scaling="1d", transpose=False, rht=False,
              scales uint8 [R', C'/B] (2D scales repeated over the 16 rows),
              g float32 or None).
     """
-    bsz = BLOCK[fmt]
+    bsz = block or BLOCK[fmt]
     w = np.asarray(x, dtype=np.float32)
     if transpose:
         w = np.ascontiguousarray(w.T)
@@ -372,13 +374,13 @@ def block_scale_values(scales, fmt) -> np.ndarray:
     return e4m3_decode(scales)
 
 
-def dequantize(packed, scales, fmt, g=None) -> np.ndarray:
+def dequantize(packed, scales, fmt, g=None, block=None) -> np.ndarray:
     """x_hat = code value * s  ([grad §2.1]), returned in fp32.
 
     MXFP4: cv * 2**e (exact).  NVFP4: fp32(fp32(cv * dec(sb)) * g); the inner
     product of a 2-bit and a 4-bit significand is exact, so one rounding.
     """
-    bsz = BLOCK[fmt]
+    bsz = block or BLOCK[fmt]
     cv = e2m1_decode(unpack_codes(packed))
     sv = np.repeat(block_scale_values(scales, fmt), bsz, axis=1)
     v = (cv * sv).astype(np.float32)
@@ -419,9 +421,9 @@ def dge_derivative(xs: np.ndarray, k: float, clamp: float, outside: float = 1.0)
     return np.where(a >= 6.0, outside, fp)
 
 
-def scaled_inputs(x, scales, fmt, g=None) -> np.ndarray:
+def scaled_inputs(x, scales, fmt, g=None, block=None) -> np.ndarray:
     """xs = x / s exactly as the quantizer forms it (fp32), from stored scales."""
-    bsz = BLOCK[fmt]
+    bsz = block or BLOCK[fmt]
     w = np.asarray(x, dtype=np.float32)
     sb = np.repeat(np.asarray(scales, dtype=np.uint8), bsz, axis=1)
     if fmt == MXFP4:
@@ -486,20 +488,20 @@ def soft_derivative(xs: np.ndarray, beta: float) -> np.ndarray:
     return float(beta) * (v * _sigmoid(z) * _sigmoid(-z)).sum(axis=-1)
 
 
-def block_scales_expanded(scales, fmt, g=None) -> np.ndarray:
+def block_scales_expanded(scales, fmt, g=None, block=None) -> np.ndarray:
     """The block scale s of every element (fp32 values as the quantizer formed
     them: 2^(e-127) for E8M0, e4m3(b) * g for NVFP4), expanded along the row."""
-    bsz = BLOCK[fmt]
+    bsz = block or BLOCK[fmt]
     sb = np.repeat(np.asarray(scales, dtype=np.uint8), bsz, axis=1)
     if fmt == MXFP4:
         return np.ldexp(1.0, sb.astype(np.int64) - 127).astype(np.float32)
     return (e4m3_decode(sb).astype(np.float32) * np.float32(g)).astype(np.float32)
 
 
-def soft_forward(x, scales, fmt, g, beta) -> np.ndarray:
+def soft_forward(x, scales, fmt, g, beta, block=None) -> np.ndarray:
     """y = s Q_soft(x / s) for x quantized along its rows; fp64 result."""
-    xs = scaled_inputs(x, scales, fmt, g)
-    s = block_scales_expanded(scales, fmt, g).astype(np.float64)
+    xs = scaled_inputs(x, scales, fmt, g, block)
+    s = block_scales_expanded(scales, fmt, g, block).astype(np.float64)
     return s * soft_quantize_scaled(xs, beta)
 
 
@@ -678,3 +680,11 @@ def occ_reconstruction(x, fmt, tau):
     xc, dx = occ_split(x, tau)
     codes, scales, g = quantize(xc, fmt)
     return dequantize(codes, scales, fmt, g).astype(np.float64) + dx.astype(np.float64)
+
+
+def relative_error(x, x_hat) -> float:
+    """||x - x_hat||_2 / ||x||_2 (fp64).  READING of the "relative error %"
+    table of [grad §5.1]: the relative L2 error of the reconstruction."""
+    a = np.asarray(x, dtype=np.float64).reshape(-1)
+    b = np.asarray(x_hat, dtype=np.float64).reshape(-1)
+    return float(np.sqrt(((a - b) ** 2).sum() / (a @ a)))
