@@ -188,7 +188,28 @@ def time_extensions(fp4, step, dev, flush, launches, pk):
     for name, nbytes, fn in extension_ops(fp4, step, dev):
         res[name] = dict(_rate("hbm", nbytes, _time_op(fn, flush, launches), pk), launches=launches)
     res["occ"] = time_occ(fp4, dev, flush, launches, pk)
+    res["block_sweep"] = block_sweep(fp4, step, dev, flush, launches, pk)
     return res
+
+
+def block_sweep(fp4, step, dev, flush, launches, pk):
+    """Block sizes 16-128 with E4M3 (NVFP4-style) and E8M0 (MXFP4-style) scales on the step's X
+    ("深度学习中的梯度计算基础" §4.2, §5.1): quantize throughput and the relative L2 error of the
+    dequantized (STE forward) and the sigmoid-smoothed (beta 10, 40) reconstructions, in percent."""
+    X = step.X
+    n = X.numel()
+    out = {"tensor": f"X[{M},{K}] ~N(0,1) bf16, RTN, row-major scales", "rows": []}
+    for fmt, name in ((fp4.FP4_FMT_NVFP4, "E4M3"), (fp4.FP4_FMT_MXFP4, "E8M0")):
+        for block in (16, 32, 64, 128):
+            p = fp4.quant_params(fmt, sf_layout=fp4.FP4_SF_ROWMAJOR, block=block)
+            q = fp4.alloc_qtensor(M, K, fmt, fp4.FP4_SF_ROWMAJOR, dev, block)
+            t = _time_op(lambda: fp4.fp4_quantize(X, p, out=q), flush, launches)
+            row = {"scale": name, "block": block, **_rate("hbm", n * (2 + 0.5 + 1.0 / block), t, pk)}
+            for label, beta in (("ste", 0.0), ("soft_beta10", 10.0), ("soft_beta40", 40.0)):
+                st = fp4.error_stats_from_sums(fp4.fp4_quant_error_sums(X, q, beta=beta).cpu(), n)
+                row[f"rel_err_pct_{label}"] = 100.0 * st["rel_err"]
+            out["rows"].append(row)
+    return out
 
 
 # Outlier clamping and compensation (the MSR write-up §三) on the hot-channel

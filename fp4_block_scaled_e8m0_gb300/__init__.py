@@ -50,7 +50,7 @@ class fp4_quant_params(ctypes.Structure):
 class fp4_operand(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p),
                 ("format", ctypes.c_int32), ("sf_layout", ctypes.c_int32), ("rows", ctypes.c_int64),
-                ("k", ctypes.c_int64)]
+                ("k", ctypes.c_int64), ("block", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -60,7 +60,7 @@ _SIGNATURES = {
     "fp4_destroy": (None, [_P]),
     "fp4_sync_status": (ctypes.c_int, [_P, _P]),
     "fp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
-    "fp4_scales_bytes": (_SZ, [_I64, _I64, _I32, _I32]),
+    "fp4_scales_bytes": (_SZ, [_I64, _I64, _I32, _I32, _I32]),
     "fp4_amax": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, _I32, _U64, _P, _P]),
     "fp4_quantize": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, ctypes.POINTER(fp4_quant_params), _P, _P, _P,
                                     _P, _P]),
@@ -81,7 +81,7 @@ _SIGNATURES = {
     "fp4_occ_gemm_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32, _I64]),
     "fp4_occ_gemm": (ctypes.c_int, [_P, _P, _I32, _I64, _P, _I64, ctypes.POINTER(fp4_operand),
                                     ctypes.POINTER(fp4_operand), _P, _P, _I32, _I64, _I32, _P, _I64, _P, _SZ, _P]),
-    "fp4_quant_error_stats": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _P, _P]),
+    "fp4_quant_error_stats": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _F32, _P, _P]),
     "fp4_gemm": (ctypes.c_int, [_P, ctypes.POINTER(fp4_operand), ctypes.POINTER(fp4_operand), _I32, _P, _I64, _I32,
                                 _P]),
     "fp4_hcp_select_workspace_bytes": (_SZ, [_I64]),
@@ -135,8 +135,8 @@ def fp4_status_string(status: int) -> str:
         return f"status {status}"
 
 
-def fp4_scales_bytes(rows: int, k: int, fmt: int, sf_layout: int) -> int:
-    return int(load_library().fp4_scales_bytes(rows, k, fmt, sf_layout))
+def fp4_scales_bytes(rows: int, k: int, fmt: int, sf_layout: int, block: int = 0) -> int:
+    return int(load_library().fp4_scales_bytes(rows, k, fmt, sf_layout, block))
 
 
 # ---- context ----------------------------------------------------------------
@@ -223,25 +223,28 @@ class QTensor:
     sf_layout: int
     rows: int
     k: int
+    block: int = 0                     # elements per scale; 0 = the format's own
 
     def operand(self) -> fp4_operand:
         return fp4_operand(self.codes.data_ptr(), self.scales.data_ptr(),
                            self.tensor_scale.data_ptr() if self.tensor_scale is not None else None,
-                           self.fmt, self.sf_layout, self.rows, self.k)
+                           self.fmt, self.sf_layout, self.rows, self.k, self.block)
 
 
 def quant_params(fmt=FP4_FMT_NVFP4, rounding=FP4_ROUND_RTN, scaling=FP4_SCALING_1D, transpose=False, rht=False,
-                 sf_layout=FP4_SF_MMA, sr_seed=0, sr_offset=0, sr_stream=0, rht_seed=0) -> fp4_quant_params:
-    return fp4_quant_params(fmt, BLOCK[fmt], rounding, scaling, int(transpose), int(rht), sf_layout, sr_stream,
-                            sr_seed, sr_offset, rht_seed)
+                 sf_layout=FP4_SF_MMA, sr_seed=0, sr_offset=0, sr_stream=0, rht_seed=0,
+                 block: int = 0) -> fp4_quant_params:
+    return fp4_quant_params(fmt, block or BLOCK[fmt], rounding, scaling, int(transpose), int(rht), sf_layout,
+                            sr_stream, sr_seed, sr_offset, rht_seed)
 
 
-def alloc_qtensor(rows: int, k: int, fmt: int, sf_layout: int, device) -> QTensor:
-    sb = fp4_scales_bytes(rows, k, fmt, sf_layout)
+def alloc_qtensor(rows: int, k: int, fmt: int, sf_layout: int, device, block: int = 0) -> QTensor:
+    block = 0 if block == BLOCK[fmt] else block
+    sb = fp4_scales_bytes(rows, k, fmt, sf_layout, block)
     return QTensor(torch.empty((rows, k // 2), dtype=torch.uint8, device=device),
                    torch.empty((max(sb, 1),), dtype=torch.uint8, device=device),
                    torch.empty((1,), dtype=torch.float32, device=device) if fmt == FP4_FMT_NVFP4 else None,
-                   fmt, sf_layout, rows, k)
+                   fmt, sf_layout, rows, k, block)
 
 
 def fp4_amax(x: torch.Tensor, rht_axis: int = -1, rht_seed: int = 0, out: Optional[torch.Tensor] = None,
@@ -256,7 +259,7 @@ def fp4_quantize(x: torch.Tensor, params: fp4_quant_params, given_amax: Optional
                  out: Optional[QTensor] = None, ctx=None, stream=None) -> QTensor:
     rows, cols = x.shape
     o_rows, blocked = (cols, rows) if params.transpose else (rows, cols)
-    out = out or alloc_qtensor(o_rows, blocked, params.format, params.sf_layout, x.device)
+    out = out or alloc_qtensor(o_rows, blocked, params.format, params.sf_layout, x.device, params.block)
     _check(load_library().fp4_quantize(_ctx(ctx), _ptr(x), _dtype_code(x), rows, cols, _ld(x), ctypes.byref(params),
                                        _ptr(given_amax), _ptr(out.codes), _ptr(out.scales), _ptr(out.tensor_scale),
                                        _stream(stream)), "fp4_quantize")
@@ -435,13 +438,14 @@ def fp4_occ_gemm(x: torch.Tensor, w: torch.Tensor, xq: QTensor, wq: QTensor, tau
     return out
 
 
-def fp4_quant_error_sums(x: torch.Tensor, q: QTensor, tau: Optional[torch.Tensor] = None,
+def fp4_quant_error_sums(x: torch.Tensor, q: QTensor, tau: Optional[torch.Tensor] = None, beta: float = 0.0,
                          out: Optional[torch.Tensor] = None, ctx=None, stream=None) -> torch.Tensor:
-    """Device float64[4]: sum x^2, sum x_hat^2, sum x x_hat, sum (x - x_hat)^2."""
+    """Device float64[4]: sum x^2, sum x_hat^2, sum x x_hat, sum (x - x_hat)^2 (x_hat: the dequantized
+    value, + the clamped-away part with tau, or s Q_soft(x/s) with beta > 0)."""
     out = out if out is not None else torch.empty((4,), dtype=torch.float64, device=x.device)
     op = q.operand()
     _check(load_library().fp4_quant_error_stats(_ctx(ctx), _ptr(x), _dtype_code(x), _ld(x), ctypes.byref(op),
-                                                _ptr(tau), _ptr(out), _stream(stream)), "fp4_quant_error_stats")
+                                                _ptr(tau), beta, _ptr(out), _stream(stream)), "fp4_quant_error_stats")
     return out
 
 
@@ -450,7 +454,8 @@ def error_stats_from_sums(sums, n: int) -> dict:
     sxx, shh, sxh, see = (float(v) for v in sums)
     return {"cos": sxh / math.sqrt(sxx * shh) if sxx > 0 and shh > 0 else float("nan"),
             "mse": see / n if n else float("nan"),
-            "snr_db": 10.0 * math.log10(sxx / see) if see > 0 and sxx > 0 else float("inf")}
+            "snr_db": 10.0 * math.log10(sxx / see) if see > 0 and sxx > 0 else float("inf"),
+            "rel_err": math.sqrt(see / sxx) if sxx > 0 else float("nan")}
 
 
 def fp4_encode_e2m1(xs: torch.Tensor, method: int = 0, ctx=None, stream=None) -> torch.Tensor:

@@ -17,6 +17,10 @@ int esize(int dt) { return dt == FP4_DTYPE_BF16 ? 2 : 4; }
 bool dtype_ok(int dt) { return dt == FP4_DTYPE_BF16 || dt == FP4_DTYPE_F32; }
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int block_of(int fmt) { return fmt == FP4_FMT_MXFP4 ? 32 : 16; }
+bool block_ok(int b) { return b == 16 || b == 32 || b == 64 || b == 128; }
+// elements per scale of an operand (0 = the format's own block)
+int op_block(const fp4_operand* q) { return q->block ? q->block : block_of(q->format); }
+bool native_block(const fp4_operand* q) { return op_block(q) == block_of(q->format); }
 
 // Philox4x32-10 word 0 for counter 0 (host side, for the RHT sign bits)
 uint32_t rht_signs_host(uint64_t seed) {
@@ -41,12 +45,16 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP4_OK : FP4_ERR_CUDA
 int check_params(const fp4_quant_params* p) {
   if (!p) return FP4_ERR_INVALID_ARG;
   if (p->format != FP4_FMT_MXFP4 && p->format != FP4_FMT_NVFP4) return FP4_ERR_UNSUPPORTED;
-  if (p->block != block_of(p->format)) return FP4_ERR_UNSUPPORTED;
+  if (!block_ok(p->block)) return FP4_ERR_UNSUPPORTED;
   if (p->rounding != FP4_ROUND_RTN && p->rounding != FP4_ROUND_SR) return FP4_ERR_INVALID_ARG;
   if (p->scaling != FP4_SCALING_1D && p->scaling != FP4_SCALING_2D) return FP4_ERR_INVALID_ARG;
   if (p->scaling == FP4_SCALING_2D && p->format != FP4_FMT_NVFP4) return FP4_ERR_UNSUPPORTED;
   if ((p->transpose != 0 && p->transpose != 1) || (p->rht != 0 && p->rht != 1)) return FP4_ERR_INVALID_ARG;
   if (p->sf_layout != FP4_SF_ROWMAJOR && p->sf_layout != FP4_SF_MMA) return FP4_ERR_INVALID_ARG;
+  // blocks other than the format's own: row layout, 1D, row-major scales only
+  if (p->block != block_of(p->format) &&
+      (p->transpose || p->scaling != FP4_SCALING_1D || p->sf_layout != FP4_SF_ROWMAJOR))
+    return FP4_ERR_UNSUPPORTED;
   return FP4_OK;
 }
 
@@ -66,7 +74,9 @@ int check_operand(const fp4_operand* q, bool need_codes) {
   if (!present(q->scales, empty) || (need_codes && !present(q->codes, empty))) return FP4_ERR_INVALID_ARG;
   if (q->format != FP4_FMT_MXFP4 && q->format != FP4_FMT_NVFP4) return FP4_ERR_UNSUPPORTED;
   if (q->sf_layout != FP4_SF_ROWMAJOR && q->sf_layout != FP4_SF_MMA) return FP4_ERR_INVALID_ARG;
-  if (q->k % block_of(q->format) != 0) return FP4_ERR_INVALID_ARG;
+  if (q->block != 0 && !block_ok(q->block)) return FP4_ERR_UNSUPPORTED;
+  if (!native_block(q) && q->sf_layout != FP4_SF_ROWMAJOR) return FP4_ERR_UNSUPPORTED;
+  if (q->k % op_block(q) != 0) return FP4_ERR_INVALID_ARG;
   if (q->format == FP4_FMT_NVFP4 && !present(q->tensor_scale, empty)) return FP4_ERR_INVALID_ARG;
   if (need_codes && !al16(q->codes)) return FP4_ERR_MISALIGNED;
   return FP4_OK;
@@ -110,7 +120,7 @@ cudaError_t clear_sf_padding(const fp4_quant_params* p, uint8_t* scales, int64_t
                              cudaStream_t st) {
   if (p->sf_layout != FP4_SF_MMA) return cudaSuccess;
   if (out_rows % 128 == 0 && blocked % 256 == 0) return cudaSuccess;
-  return cudaMemsetAsync(scales, 0, fp4_scales_bytes(out_rows, blocked, p->format, FP4_SF_MMA), st);
+  return cudaMemsetAsync(scales, 0, fp4_scales_bytes(out_rows, blocked, p->format, FP4_SF_MMA, 0), st);
 }
 
 }  // namespace
@@ -130,9 +140,10 @@ const char* fp4_status_string(int s) {
   }
 }
 
-size_t fp4_scales_bytes(int64_t rows, int64_t k, int32_t format, int32_t sf_layout) {
+size_t fp4_scales_bytes(int64_t rows, int64_t k, int32_t format, int32_t sf_layout, int32_t block) {
   if (rows <= 0 || k <= 0) return 0;
-  int B = block_of(format);
+  int B = block ? block : block_of(format);
+  if (!block_ok(B) || (sf_layout == FP4_SF_MMA && B != block_of(format))) return 0;
   if (sf_layout == FP4_SF_ROWMAJOR) return (size_t)(rows * (k / B));
   return (size_t)(cdiv(rows, 128) * 128 * nsf_padded(k, format));
 }
@@ -219,7 +230,9 @@ int fp4_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int
   if (clear_sf_padding(p, scales, out_rows, blocked, st) != cudaSuccess) return FP4_ERR_CUDA;
   QuantOut o = make_out(p, codes, scales, tensor_scale, amax, out_rows, blocked);
   cudaError_t e;
-  if (!p->transpose && p->scaling == FP4_SCALING_1D)
+  if (p->block != block_of(p->format))
+    e = launch_quant_rows_blk(x, x_dtype, rows, cols, ldx, p->format, p->block, o, ctx->num_sms, st);
+  else if (!p->transpose && p->scaling == FP4_SCALING_1D)
     e = launch_quant_rows(x, x_dtype, rows, cols, ldx, p->format, o, ctx->num_sms, st);
   else
     e = launch_quant_tile(x, x_dtype, rows, cols, ldx, p->format, p->scaling == FP4_SCALING_2D, p->transpose != 0, o,
@@ -240,6 +253,7 @@ int fp4_quantize_dual(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows
   s = check_params(pc);
   if (s) return s;
   if (pr->format != pc->format || pr->transpose != 0 || pc->transpose != 1) return FP4_ERR_INVALID_ARG;
+  if (pr->block != block_of(pr->format) || pc->block != block_of(pc->format)) return FP4_ERR_UNSUPPORTED;
   s = check_input(x, x_dtype, rows, cols, ldx);
   if (s) return s;
   if (cols % pr->block || rows % pc->block) return FP4_ERR_INVALID_ARG;
@@ -296,6 +310,7 @@ int fp4_dge_backward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, 
   if (!ctx || !(k > 1.0f) || !(clamp > 0.0f)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(q, false);
   if (s) return s;
+  if (!native_block(q)) return FP4_ERR_UNSUPPORTED;
   if (!present(dx, q->rows == 0 || q->k == 0)) return FP4_ERR_INVALID_ARG;
   s = check_input(x, x_dtype, q->rows, q->k, ldx);
   if (s) return s;
@@ -314,6 +329,7 @@ int fp4_soft_forward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, 
   if (!ctx || !soft_beta_ok(beta)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(q, false);
   if (s) return s;
+  if (!native_block(q)) return FP4_ERR_UNSUPPORTED;
   if (!present(y, q->rows == 0 || q->k == 0)) return FP4_ERR_INVALID_ARG;
   s = check_input(x, x_dtype, q->rows, q->k, ldx);
   if (s) return s;
@@ -329,6 +345,7 @@ int fp4_soft_backward(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx,
   if (!ctx || !soft_beta_ok(beta)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(q, false);
   if (s) return s;
+  if (!native_block(q)) return FP4_ERR_UNSUPPORTED;
   if (!present(dx, q->rows == 0 || q->k == 0)) return FP4_ERR_INVALID_ARG;
   s = check_input(x, x_dtype, q->rows, q->k, ldx);
   if (s) return s;
@@ -381,7 +398,8 @@ int fp4_occ_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows,
   if (!ctx || !tau || !present(codes, empty) || !present(scales, empty)) return FP4_ERR_INVALID_ARG;
   int s = check_params(p);
   if (s) return s;
-  if (p->transpose || p->rht || p->scaling != FP4_SCALING_1D) return FP4_ERR_UNSUPPORTED;
+  if (p->transpose || p->rht || p->scaling != FP4_SCALING_1D || p->block != block_of(p->format))
+    return FP4_ERR_UNSUPPORTED;
   s = check_input(x, x_dtype, rows, cols, ldx);
   if (s) return s;
   if (cols % p->block) return FP4_ERR_INVALID_ARG;
@@ -410,8 +428,10 @@ int fp4_occ_gemm(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, cons
   if (!ctx || !tau || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(xq, true);
   if (s) return s;
+  if (!native_block(xq)) return FP4_ERR_UNSUPPORTED;
   s = check_operand(wq, true);
   if (s) return s;
+  if (!native_block(wq)) return FP4_ERR_UNSUPPORTED;
   if (xq->format != wq->format || xq->k != wq->k) return FP4_ERR_INVALID_ARG;
   if (xq->sf_layout != FP4_SF_MMA || wq->sf_layout != FP4_SF_MMA) return FP4_ERR_UNSUPPORTED;
   const int64_t M = xq->rows, N = wq->rows, K = xq->k;
@@ -458,13 +478,14 @@ int fp4_occ_gemm(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, cons
 }
 
 int fp4_quant_error_stats(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,
-                          const float* tau, double* sums, void* stream) {
-  if (!ctx || !sums) return FP4_ERR_INVALID_ARG;
-  int s = check_operand(q, true);
+                          const float* tau, float beta, double* sums, void* stream) {
+  if (!ctx || !sums || !(beta >= 0.0f && beta <= 1e6f) || (tau && beta > 0.0f)) return FP4_ERR_INVALID_ARG;
+  int s = check_operand(q, beta == 0.0f);
   if (s) return s;
+  if (q->k % 16) return FP4_ERR_INVALID_ARG;
   s = check_input(x, x_dtype, q->rows, q->k, ldx);
   if (s) return s;
-  return cuda_status(launch_error_stats(x, x_dtype, ldx, *q, tau, sums, ctx->num_sms,
+  return cuda_status(launch_error_stats(x, x_dtype, ldx, *q, op_block(q), tau, beta, sums, ctx->num_sms,
                                         static_cast<cudaStream_t>(stream)));
 }
 
@@ -473,8 +494,10 @@ int fp4_gemm(fp4_ctx* ctx, const fp4_operand* A, const fp4_operand* B, int32_t o
   if (!ctx || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(A, true);
   if (s) return s;
+  if (!native_block(A)) return FP4_ERR_UNSUPPORTED;
   s = check_operand(B, true);
   if (s) return s;
+  if (!native_block(B)) return FP4_ERR_UNSUPPORTED;
   if (!present(C, A->rows == 0 || B->rows == 0)) return FP4_ERR_INVALID_ARG;
   if (A->format != B->format || A->k != B->k) return FP4_ERR_INVALID_ARG;
   if (A->sf_layout != FP4_SF_MMA || B->sf_layout != FP4_SF_MMA) return FP4_ERR_UNSUPPORTED;
@@ -503,6 +526,7 @@ int fp4_hcp_select(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const fp4_oper
   if (!ctx || (k_hot > 0 && !hot_idx)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(xq, true);
   if (s) return s;
+  if (!native_block(xq)) return FP4_ERR_UNSUPPORTED;
   s = check_input(x_bf16, FP4_DTYPE_BF16, xq->rows, xq->k, ldx);
   if (s) return s;
   if (k_hot < 0 || k_hot > xq->k) return FP4_ERR_INVALID_ARG;
@@ -533,8 +557,10 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
   if (order != 1 && order != 2) return FP4_ERR_INVALID_ARG;
   int s = check_operand(xq, true);
   if (s) return s;
+  if (!native_block(xq)) return FP4_ERR_UNSUPPORTED;
   s = check_operand(wq, true);
   if (s) return s;
+  if (!native_block(wq)) return FP4_ERR_UNSUPPORTED;
   if (xq->format != wq->format || xq->k != wq->k) return FP4_ERR_INVALID_ARG;
   if (xq->sf_layout != FP4_SF_MMA || wq->sf_layout != FP4_SF_MMA) return FP4_ERR_UNSUPPORTED;
   if (xq->k % 32 || xq->k == 0) return FP4_ERR_INVALID_ARG;

@@ -150,8 +150,13 @@ cudaError_t launch_occ_prepare(const void* x, int xdt, int64_t ldx, const uint16
                                const fp4_operand& xq, const fp4_operand& wq, const float* tau, const float* col_counts,
                                int k_dense, int64_t max_outliers, void* ws, const OccLayout& L, unsigned int* status,
                                int num_sms, cudaStream_t st);
-cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const float* tau,
-                               double* sums, int num_sms, cudaStream_t st);
+// quality sums over q with any block (16-128); tau: OCC reconstruction; beta > 0:
+// the sigmoid-smoothed reconstruction instead of the codes
+cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, int block,
+                               const float* tau, float beta, double* sums, int num_sms, cudaStream_t st);
+// row quantizer for any block of 16-128 elements (row-major scales, no transpose)
+cudaError_t launch_quant_rows_blk(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt, int block,
+                                  const QuantOut& o, int num_sms, cudaStream_t st);
 
 __host__ __device__ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // scales per row in the MMA layout: k padded to 256 elements

@@ -280,6 +280,7 @@ extern "C" int fp4_hcp_select_noalloc(const void* x_bf16, int64_t ldx, const fp4
   if (xq->k > FP4_NOALLOC_MAX_CHANNELS) return FP4_ERR_TOO_LARGE;
   if (xq->format != FP4_FMT_MXFP4 && xq->format != FP4_FMT_NVFP4) return FP4_ERR_UNSUPPORTED;
   if (xq->sf_layout != FP4_SF_ROWMAJOR && xq->sf_layout != FP4_SF_MMA) return FP4_ERR_INVALID_ARG;
+  if (xq->block != 0 && xq->block != (xq->format == FP4_FMT_MXFP4 ? 32 : 16)) return FP4_ERR_UNSUPPORTED;
   if (xq->k % (xq->format == FP4_FMT_MXFP4 ? 32 : 16)) return FP4_ERR_INVALID_ARG;
   if (xq->format == FP4_FMT_NVFP4 && !empty && !xq->tensor_scale) return FP4_ERR_INVALID_ARG;
   if (k_hot < 0 || k_hot > xq->k || (k_hot > 0 && !hot_idx) || ldx < xq->k) return FP4_ERR_INVALID_ARG;

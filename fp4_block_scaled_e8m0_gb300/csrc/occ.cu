@@ -1,6 +1,4 @@
-// Outlier clamping and compensation, OCC ([msr] §三, §六), and the
-// quantization-quality statistics the same section reports (cosine similarity,
-// MSE, SNR).
+// Outlier clamping and compensation, OCC ([msr] §三, §六).
 //
 //   tau  = the ceil(q n)-th smallest |x| over the tensor (nearest rank)
 //   X_c  = clamp(X, -tau, tau)            quantized by the row quantizer
@@ -412,72 +410,6 @@ __global__ void __launch_bounds__(256) occ_extract_kernel(const void* __restrict
   }
 }
 
-// ---------------------------------------------------------------------------
-// quality statistics: sums of x^2, x_hat^2, x x_hat, (x - x_hat)^2 in fp64,
-// x_hat = dequant(code) [+ dX when tau is given].  One thread per block.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
-
-template <int FMT, int XDT>
-__global__ void __launch_bounds__(256) error_stats_kernel(const void* __restrict__ x, int64_t ldx, fp4_operand q,
-                                                          const float* __restrict__ tau_p, double* sums) {
-  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
-  const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
-  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
-  const bool occ = tau_p != nullptr;
-  const float tau = occ ? *tau_p : 0.0f;
-  const int64_t total = q.rows * nsf_row;
-  double sxx = 0.0, shh = 0.0, sxh = 0.0, see = 0.0;
-  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
-       blk += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = blk / nsf_row, j = blk - r * nsf_row;
-    const uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
-    const float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
-    float v[B];
-#pragma unroll
-    for (int q8 = 0; q8 < B / 8; ++q8) load8<XDT>(x, r * ldx + j * B + 8 * q8, v + 8 * q8);
-    const uint8_t* cp = q.codes + r * (q.k >> 1) + j * (B / 2);
-#pragma unroll
-    for (int e = 0; e < B; ++e) {
-      const uint32_t code = (cp[e >> 1] >> (4 * (e & 1))) & 15u;
-      const uint32_t mc = code & 7u;
-      const float mag = mc < 4 ? 0.5f * (float)mc : (mc == 4 ? 2.0f : mc == 5 ? 3.0f : mc == 6 ? 4.0f : 6.0f);
-      float d = __fmul_rn(mag, s);
-      if (FMT == FP4_FMT_NVFP4) d = __fmul_rn(d, g);
-      if (code & 8u) d = -d;
-      double h = (double)d;
-      if (occ) h += (double)clamp_residual(v[e], tau);
-      const double xv = (double)v[e], ev = xv - h;
-      sxx = fma(xv, xv, sxx);
-      shh = fma(h, h, shh);
-      sxh = fma(xv, h, sxh);
-      see = fma(ev, ev, see);
-    }
-  }
-  __shared__ double part[4][8];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  sxx = warp_sum_d(sxx);
-  shh = warp_sum_d(shh);
-  sxh = warp_sum_d(sxh);
-  see = warp_sum_d(see);
-  if (lane == 0) {
-    part[0][w] = sxx;
-    part[1][w] = shh;
-    part[2][w] = sxh;
-    part[3][w] = see;
-  }
-  __syncthreads();
-  if (threadIdx.x < 4) {
-    double s = 0.0;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += part[threadIdx.x][i];
-    atomicAdd(&sums[threadIdx.x], s);
-  }
-}
-
 inline int grid_cap(int64_t items, int per_block, int num_sms, int per_sm = 8) {
   const int64_t need = cdiv(items, per_block), cap = (int64_t)num_sms * per_sm;
   return (int)std::max<int64_t>(1, std::min(need, cap));
@@ -599,22 +531,5 @@ cudaError_t launch_occ_prepare(const void* x, int xdt, int64_t ldx, const uint16
   return cudaGetLastError();
 }
 
-cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const float* tau,
-                               double* sums, int num_sms, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(sums, 0, 4 * sizeof(double), st);
-  if (e != cudaSuccess) return e;
-  const int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
-  const int64_t total = q.rows * (q.k / B);
-  if (total == 0) return cudaSuccess;
-  const int grid = grid_cap(total, 256, num_sms);
-#define FP4_STATS(FMT, XDT) error_stats_kernel<FMT, XDT><<<grid, 256, 0, st>>>(x, ldx, q, tau, sums)
-  if (q.format == FP4_FMT_MXFP4) {
-    if (xdt == FP4_DTYPE_BF16) FP4_STATS(FP4_FMT_MXFP4, FP4_DTYPE_BF16); else FP4_STATS(FP4_FMT_MXFP4, FP4_DTYPE_F32);
-  } else {
-    if (xdt == FP4_DTYPE_BF16) FP4_STATS(FP4_FMT_NVFP4, FP4_DTYPE_BF16); else FP4_STATS(FP4_FMT_NVFP4, FP4_DTYPE_F32);
-  }
-#undef FP4_STATS
-  return cudaGetLastError();
-}
 
 }  // namespace fp4

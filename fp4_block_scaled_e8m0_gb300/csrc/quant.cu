@@ -32,9 +32,9 @@ inline int grid_for(int64_t work_items, int per_block, int num_sms, int blocks_p
 // codes + scale.  `first_elem` is the linear output index of v[0] (SR counter).
 // ----------------------------------------------------------------------------
 template <int FMT, int B>
-__device__ __forceinline__ void encode_store_block(const float* v, float g, const QuantOut& o,
-                                                   int64_t out_row, int64_t out_col0, float amax_b,
-                                                   bool sr) {
+__device__ __forceinline__ uint32_t encode_block_codes(const float* v, float g, const QuantOut& o,
+                                                       int64_t out_row, int64_t out_col0, float amax_b,
+                                                       bool sr) {
   uint32_t byte;
   float r;
   bool zero;
@@ -72,14 +72,62 @@ __device__ __forceinline__ void encode_store_block(const float* v, float g, cons
   } else {
     *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
   }
+  return byte;
+}
+
+template <int FMT, int B>
+__device__ __forceinline__ void encode_store_block(const float* v, float g, const QuantOut& o,
+                                                   int64_t out_row, int64_t out_col0, float amax_b,
+                                                   bool sr) {
+  const uint32_t byte = encode_block_codes<FMT, B>(v, g, o, out_row, out_col0, amax_b, sr);
   o.scales[sf_offset(o.sf_layout, out_row, out_col0 / B, o.nsf_row, o.nsf_pad)] = (uint8_t)byte;
 }
+
 
 __device__ __forceinline__ float load_g(const QuantOut& o, int fmt) {
   if (fmt != FP4_FMT_NVFP4) return 0.0f;
   float g = nvfp4_tensor_scale(*o.amax);
   if (blockIdx.x == 0 && threadIdx.x == 0 && o.tensor_scale) *o.tensor_scale = g;
   return g;
+}
+
+// ----------------------------------------------------------------------------
+// Row quantizer for any block of SB = 16 * G elements (16-128; [grad] §4.2),
+// either scale format, row-major scales: one thread per 16 elements, the G
+// threads of a block share its amax through shuffles, the first stores the
+// scale byte.  The warp-uniform loop keeps every lane in the shuffles.
+// ----------------------------------------------------------------------------
+template <int FMT, int DT, int G>
+__global__ void __launch_bounds__(kThreads) quant_rows_blk_kernel(const void* __restrict__ x, int64_t rows,
+                                                                  int64_t cols, int64_t ldx, QuantOut o) {
+  const float g = load_g(o, FMT);
+  const bool sr = o.rounding == FP4_ROUND_SR;
+  const int lane = threadIdx.x & 31;
+  const int64_t units_row = cols / 16, total = rows * units_row;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = blockIdx.x * (int64_t)blockDim.x + (threadIdx.x & ~31); base < total; base += stride) {
+    const int64_t u = base + lane;
+    const bool act = u < total;
+    const int64_t r = act ? u / units_row : 0, c0 = act ? (u - r * units_row) * 16 : 0;
+    float v[16];
+    if (act) {
+      load8<DT>(x, r * ldx + c0, v);
+      load8<DT>(x, r * ldx + c0 + 8, v + 8);
+      if (o.rht) rht16(v, o.rht_signs);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+    for (int m = 1; m < G; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+    if (act) {
+      const uint32_t byte = encode_block_codes<FMT, 16>(v, g, o, r, c0, amax, sr);
+      if ((lane & (G - 1)) == 0) o.scales[r * (cols / (16 * G)) + c0 / (16 * G)] = (uint8_t)byte;
+    }
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -710,6 +758,49 @@ __global__ void __launch_bounds__(kThreads, 4) tile_nv_kernel(const uint16_t* __
 // ----------------------------------------------------------------------------
 // dequantize: one thread per block
 // ----------------------------------------------------------------------------
+// Dequantize with any block of 16-128 elements (row-major scales): one thread
+// per 16 elements, block index = column >> sb_log2.
+template <int FMT, int ODT>
+__global__ void __launch_bounds__(kThreads) dequant_blk_kernel(fp4_operand q, int sb_log2, void* out, int64_t ldo) {
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 1.0f;
+  const int64_t units_row = q.k / 16, total = q.rows * units_row, nsf_row = q.k >> sb_log2;
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = u / units_row, c0 = (u - r * units_row) * 16;
+    const uint32_t sb = q.scales[r * nsf_row + (c0 >> sb_log2)];
+    const float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
+    const uint2 cw = *reinterpret_cast<const uint2*>(q.codes + r * (q.k >> 1) + (c0 >> 1));
+    const uint32_t w[2] = {cw.x, cw.y};
+    float v[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint32_t c = (w[e >> 3] >> (4 * (e & 7))) & 15u;
+      const uint32_t m = c & 7u;
+      const float mag = m < 4 ? 0.5f * (float)m : (m == 4 ? 2.0f : m == 5 ? 3.0f : m == 6 ? 4.0f : 6.0f);
+      float val = __fmul_rn(mag, s);
+      if (FMT == FP4_FMT_NVFP4) val = __fmul_rn(val, g);
+      v[e] = (c & 8u) ? -val : val;
+    }
+    const int64_t o0 = r * ldo + c0;
+    if constexpr (ODT == FP4_DTYPE_F32) {
+      float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + o0);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+    } else {
+      uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o0);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        uint32_t pw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * e + 2 * i], v[8 * e + 2 * i + 1]);
+          pw[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        o4[e] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      }
+    }
+  }
+}
+
 template <int FMT, int ODT>
 __global__ void __launch_bounds__(kThreads) dequant_kernel(fp4_operand q, void* out, int64_t ldo) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
@@ -1046,6 +1137,92 @@ __global__ void __launch_bounds__(kThreads) scaled_map_kernel(const void* __rest
 }
 
 // ----------------------------------------------------------------------------
+// Quantization quality ([msr] §三 cosine / MSE / SNR; [grad] §5.1 relative
+// error): sums of x^2, x_hat^2, x x_hat, (x - x_hat)^2 in fp64 over a tensor and
+// its quantization (any block of 16-128), one thread per 16 elements.
+//   x_hat = dequant(code)                    (+ x - clamp(x, tau) with OCC)
+//   x_hat = s Q_soft(x / s)                  (SOFT: the sigmoid-smoothed value)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+template <int FMT, int XDT, bool SOFT>
+__global__ void __launch_bounds__(256) error_stats_kernel(const void* __restrict__ x, int64_t ldx, fp4_operand q,
+                                                          int sb_log2, const float* __restrict__ tau_p, float nbl,
+                                                          double* sums) {
+  const int64_t nsf_row = q.k >> sb_log2, nsf_pad = nsf_padded(q.k, FMT);
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
+  const bool occ = tau_p != nullptr;
+  const float tau = occ ? *tau_p : 0.0f;
+  const int64_t units_row = q.k / 16, total = q.rows * units_row;
+  double sxx = 0.0, shh = 0.0, sxh = 0.0, see = 0.0;
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = u / units_row, c0 = (u - r * units_row) * 16;
+    const uint32_t sb = q.scales[sf_offset(q.sf_layout, r, c0 >> sb_log2, nsf_row, nsf_pad)];
+    float v[16];
+    load8<XDT>(x, r * ldx + c0, v);
+    load8<XDT>(x, r * ldx + c0 + 8, v + 8);
+    float h32[16];
+    if constexpr (SOFT) {
+      float s, mult;
+      if (FMT == FP4_FMT_MXFP4) {
+        s = e8m0_scale(sb);
+        mult = e8m0_inv_scale(sb);
+      } else {
+        s = __fmul_rn(e4m3_decode(sb), g);
+        mult = s == 0.0f ? 0.0f : __frcp_rn(s);
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) h32[e] = s * soft_value<0>(__fmul_rn(v[e], mult), nbl, nullptr);
+    } else {
+      const float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
+      const uint2 cw = *reinterpret_cast<const uint2*>(q.codes + r * (q.k >> 1) + (c0 >> 1));
+      const uint32_t w[2] = {cw.x, cw.y};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const uint32_t code = (w[e >> 3] >> (4 * (e & 7))) & 15u;
+        const uint32_t mc = code & 7u;
+        const float mag = mc < 4 ? 0.5f * (float)mc : (mc == 4 ? 2.0f : mc == 5 ? 3.0f : mc == 6 ? 4.0f : 6.0f);
+        float d = __fmul_rn(mag, s);
+        if (FMT == FP4_FMT_NVFP4) d = __fmul_rn(d, g);
+        h32[e] = (code & 8u) ? -d : d;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      double h = (double)h32[e];
+      if (!SOFT && occ && fabsf(v[e]) > tau) h += (double)__fsub_rn(v[e], copysignf(tau, v[e]));
+      const double xv = (double)v[e], ev = xv - h;
+      sxx = fma(xv, xv, sxx);
+      shh = fma(h, h, shh);
+      sxh = fma(xv, h, sxh);
+      see = fma(ev, ev, see);
+    }
+  }
+  __shared__ double part[4][8];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  sxx = warp_sum_d(sxx);
+  shh = warp_sum_d(shh);
+  sxh = warp_sum_d(sxh);
+  see = warp_sum_d(see);
+  if (lane == 0) {
+    part[0][w] = sxx;
+    part[1][w] = shh;
+    part[2][w] = sxh;
+    part[3][w] = see;
+  }
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    double t = 0.0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t += part[threadIdx.x][i];
+    atomicAdd(&sums[threadIdx.x], t);
+  }
+}
+
+// ----------------------------------------------------------------------------
 // element encoders
 // ----------------------------------------------------------------------------
 __global__ void encode_e2m1_kernel(const float* xs, uint8_t* codes, int64_t n, int method) {
@@ -1256,9 +1433,53 @@ cudaError_t launch_quant_dual(const void* x, int dt, int64_t rows, int64_t cols,
   return cudaGetLastError();
 }
 
+static int log2_block(int b) { return b == 16 ? 4 : b == 32 ? 5 : b == 64 ? 6 : 7; }
+
+cudaError_t launch_quant_rows_blk(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt, int block,
+                                  const QuantOut& o, int num_sms, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int grid = grid_for(rows * (cols / 16), kThreads, num_sms);
+#define FP4_BLK(G)                                                                                         \
+  FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT,                                                       \
+    quant_rows_blk_kernel<FMT, DT, G><<<grid, kThreads, 0, st>>>(x, rows, cols, ldx, o)))
+  switch (block) {
+    case 16: FP4_BLK(1); break;
+    case 32: FP4_BLK(2); break;
+    case 64: FP4_BLK(4); break;
+    default: FP4_BLK(8); break;
+  }
+#undef FP4_BLK
+  return cudaGetLastError();
+}
+
+cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, int block,
+                               const float* tau, float beta, double* sums, int num_sms, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(sums, 0, 4 * sizeof(double), st);
+  if (e != cudaSuccess) return e;
+  const int64_t total = q.rows * (q.k / 16);
+  if (total == 0) return cudaSuccess;
+  const int grid = grid_for(total, 256, num_sms);
+  const int sbl = log2_block(block);
+  const float nbl = -beta * 1.4426950408889634f;
+  FP4_DISPATCH_FMT(q.format, FMT, FP4_DISPATCH_DT(xdt, XDT,
+    if (beta > 0.0f) error_stats_kernel<FMT, XDT, true><<<grid, 256, 0, st>>>(x, ldx, q, sbl, nullptr, nbl, sums);
+    else error_stats_kernel<FMT, XDT, false><<<grid, 256, 0, st>>>(x, ldx, q, sbl, tau, 0.0f, sums)));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dequant(const fp4_operand& q, int out_dt, void* out, int64_t ldo, int num_sms,
                            cudaStream_t st) {
   int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
+  if (q.block && q.block != B) {
+    const int64_t units = q.rows * (q.k / 16);
+    if (units == 0) return cudaSuccess;
+    const int grid = grid_for(units, kThreads, num_sms);
+    const int sbl = log2_block(q.block);
+    FP4_DISPATCH_FMT(q.format, FMT,
+      if (out_dt == FP4_DTYPE_F32) dequant_blk_kernel<FMT, FP4_DTYPE_F32><<<grid, kThreads, 0, st>>>(q, sbl, out, ldo);
+      else dequant_blk_kernel<FMT, FP4_DTYPE_BF16><<<grid, kThreads, 0, st>>>(q, sbl, out, ldo));
+    return cudaGetLastError();
+  }
   int64_t total = q.rows * (q.k / B);
   if (total == 0) return cudaSuccess;
   int grid = grid_for(total, kThreads, num_sms);

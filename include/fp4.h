@@ -77,8 +77,13 @@ enum { FP4_HCP_SINGLE = 0, FP4_HCP_TWO = 1 };            /* [outlier] §3.1 */
 typedef struct fp4_ctx fp4_ctx;
 
 /* Quantization parameters: Q(x) = s * round(x / s)  ([grad] §2.1).
- *  format    FP4_FMT_MXFP4 (block must be 32) or FP4_FMT_NVFP4 (block 16);
- *            any other pairing -> FP4_ERR_UNSUPPORTED.
+ *  format    FP4_FMT_MXFP4 (E8M0 scales) or FP4_FMT_NVFP4 (E4M3 scales x fp32
+ *            tensor scale).
+ *  block     elements per scale: the format's own (32 MXFP4, 16 NVFP4), or
+ *            16, 32, 64, 128 for either format ([grad] §4.2 studies 16-128)
+ *            with transpose 0, 1D scaling and FP4_SF_ROWMAJOR (fp4_quantize
+ *            only; such operands are read by fp4_dequantize and
+ *            fp4_quant_error_stats, not by the GEMMs); else FP4_ERR_UNSUPPORTED.
  *  rounding  RTN (ties to even) or SR (Philox4x32-10, 16 random bits per
  *            element: round up iff u16 < frac * 65536).
  *  scaling   1D (one scale per `block` elements along the blocked axis) or
@@ -116,6 +121,10 @@ typedef struct {
   int32_t sf_layout;
   int64_t rows;
   int64_t k;
+  int32_t block;               /* elements per scale; 0 = the format's own.
+                                  Other blocks (16-128, row-major scales) only
+                                  for fp4_dequantize / fp4_quant_error_stats;
+                                  every other call -> FP4_ERR_UNSUPPORTED     */
 } fp4_operand;
 
 /* ---- context --------------------------------------------------------------
@@ -128,8 +137,9 @@ void fp4_destroy(fp4_ctx* ctx);
 int fp4_sync_status(fp4_ctx* ctx, void* stream);
 const char* fp4_status_string(int status);
 
-/* Bytes of the scale buffer for a rows x k operand in the given layout. */
-size_t fp4_scales_bytes(int64_t rows, int64_t k, int32_t format, int32_t sf_layout);
+/* Bytes of the scale buffer for a rows x k operand in the given layout and
+ * block (0 = the format's own). */
+size_t fp4_scales_bytes(int64_t rows, int64_t k, int32_t format, int32_t sf_layout, int32_t block);
 
 /* ---- per-tensor amax ([lowprec] §1.1 "tensor scaling"; NVFP4's fp32 level)
  * *amax_out = max |x| over a rows x cols tensor, after an optional RHT16
@@ -260,14 +270,19 @@ int fp4_occ_gemm(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, cons
                  int32_t k_dense, int64_t max_outliers, int32_t out_dtype, void* y, int64_t ldy, void* workspace,
                  size_t ws_bytes, void* stream);
 
-/* ---- quantization quality ([msr] §三 reports cosine similarity, MSE, SNR)
+/* ---- quantization quality ([msr] §三 reports cosine similarity, MSE, SNR;
+ *      [grad] §5.1 a relative error per block size)
  * sums (device double[4], overwritten) = sum x^2, sum x_hat^2, sum x x_hat,
- * sum (x - x_hat)^2 over the rows x k tensor x (blocks along cols) and its
- * quantization q, x_hat = dequant(q) (+ x - clamp(x, -tau, tau) when tau is
- * non-NULL: the OCC reconstruction).  fp64 accumulation.  cosine =
- * s2 / sqrt(s0 s1), MSE = s3 / n, SNR = 10 log10(s0 / s3).                 */
+ * sum (x - x_hat)^2 over the rows x k tensor x (blocks along cols, any block
+ * of 16-128, k % 16 == 0) and its quantization q, with
+ *   beta == 0: x_hat = dequant(q) (+ x - clamp(x, -tau, tau) when tau is
+ *              non-NULL: the OCC reconstruction);
+ *   beta > 0:  x_hat = s Q_soft(x / s), the sigmoid-smoothed value with q's
+ *              scales (q->codes unused; tau must be NULL).
+ * fp64 accumulation.  cosine = s2 / sqrt(s0 s1), MSE = s3 / n,
+ * SNR = 10 log10(s0 / s3), relative L2 error = sqrt(s3 / s0).              */
 int fp4_quant_error_stats(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,
-                          const float* tau, double* sums, void* stream);
+                          const float* tau, float beta, double* sums, void* stream);
 
 /* ---- block-scaled FP4 GEMM ([msr] §四: the GEMMs are >95% of the compute)
  * C[M,N] = alpha * sum_k A[m,k] * B[n,k]  (TN: both operands K-major), FP32

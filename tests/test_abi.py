@@ -32,10 +32,15 @@ def test_status_strings(lib):
 
 def test_scale_buffer_sizes(lib):
     # canonical: one byte per block; MMA layout: rows padded to 128, k to 256
-    assert lib.fp4_scales_bytes(8192, 2048, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_ROWMAJOR) == 8192 * 128
-    assert lib.fp4_scales_bytes(8192, 2048, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA) == 8192 * 128
-    assert lib.fp4_scales_bytes(200, 96, fp4.FP4_FMT_MXFP4, fp4.FP4_SF_MMA) == 256 * 8
-    assert lib.fp4_scales_bytes(200, 96, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA) == 256 * 16
+    assert lib.fp4_scales_bytes(8192, 2048, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_ROWMAJOR, 0) == 8192 * 128
+    assert lib.fp4_scales_bytes(8192, 2048, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA, 0) == 8192 * 128
+    assert lib.fp4_scales_bytes(200, 96, fp4.FP4_FMT_MXFP4, fp4.FP4_SF_MMA, 0) == 256 * 8
+    assert lib.fp4_scales_bytes(200, 96, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA, 0) == 256 * 16
+    # other blocks: row-major scales only, one byte per block
+    assert lib.fp4_scales_bytes(100, 512, fp4.FP4_FMT_MXFP4, fp4.FP4_SF_ROWMAJOR, 128) == 100 * 4
+    assert lib.fp4_scales_bytes(100, 512, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_ROWMAJOR, 64) == 100 * 8
+    assert lib.fp4_scales_bytes(100, 512, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA, 64) == 0
+    assert lib.fp4_scales_bytes(100, 512, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_ROWMAJOR, 48) == 0
     assert lib.fp4_hcp_workspace_bytes(16384, 4096, 369, 2) == 16384 * 768 * 2 + 4096 * 768 * 2
     assert lib.fp4_hcp_select_workspace_bytes(4096) == 4096 * 8
 
@@ -56,7 +61,15 @@ def test_quantize_validation(lib):
     ok = fp4.quant_params(fp4.FP4_FMT_NVFP4)
     bad_block = fp4.quant_params(fp4.FP4_FMT_MXFP4)
     bad_block.block = 16
-    assert q(bad_block) == fp4.FP4_ERR_UNSUPPORTED                     # MXFP4 needs block 32
+    assert q(bad_block) == fp4.FP4_ERR_UNSUPPORTED                     # other blocks: row-major scales only
+    for blk in (48, 256, 8):
+        odd = fp4.quant_params(fp4.FP4_FMT_NVFP4, sf_layout=fp4.FP4_SF_ROWMAJOR, block=blk)
+        assert q(odd) == fp4.FP4_ERR_UNSUPPORTED                       # 16, 32, 64 or 128
+    t64 = fp4.quant_params(fp4.FP4_FMT_NVFP4, sf_layout=fp4.FP4_SF_ROWMAJOR, transpose=True, block=64)
+    assert q(t64) == fp4.FP4_ERR_UNSUPPORTED                           # row layout only
+    r64 = fp4.quant_params(fp4.FP4_FMT_MXFP4, sf_layout=fp4.FP4_SF_ROWMAJOR, block=64)
+    assert q(r64, cols=96, ld=96) == fp4.FP4_ERR_INVALID_ARG           # cols % 64
+    assert q(r64, rows=0) == fp4.FP4_OK
     two_d_mx = fp4.quant_params(fp4.FP4_FMT_MXFP4, scaling=fp4.FP4_SCALING_2D)
     assert q(two_d_mx) == fp4.FP4_ERR_UNSUPPORTED                      # 2D scaling is NVFP4-only
     fmt7 = fp4.quant_params(fp4.FP4_FMT_NVFP4)
@@ -89,6 +102,8 @@ def test_gemm_validation(lib):
     assert g(a, nots) == fp4.FP4_ERR_INVALID_ARG                        # NVFP4 needs its tensor scale
     assert g(a, b, ldc=500) == fp4.FP4_ERR_INVALID_ARG                  # ldc < N
     assert g(a, b, ldc=516) == fp4.FP4_ERR_MISALIGNED                   # ldc * 2 % 16
+    b64 = fp4.fp4_operand(p, p, p, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_ROWMAJOR, 512, 512, 64)
+    assert g(a, b64) == fp4.FP4_ERR_UNSUPPORTED                         # the MMA consumes 16 / 32 only
 
 
 def test_create_without_gpu_reports_cuda_error(lib):
