@@ -688,3 +688,46 @@ def relative_error(x, x_hat) -> float:
     a = np.asarray(x, dtype=np.float64).reshape(-1)
     b = np.asarray(x_hat, dtype=np.float64).reshape(-1)
     return float(np.sqrt(((a - b) ** 2).sum() / (a @ a)))
+
+
+# ----------------------------------------------------------------------------
+# Hot channels zeroed before quantizing: a variant of hot-channel compensation
+# ([outlier §3.1-3.2]).  READING: the hot channels H leave the FP4 operand
+# altogether -- X_H is set to 0 before X is quantized, so the hot channels no
+# longer inflate the scales of the blocks they sit in -- and their whole
+# product goes through the bf16 extra K columns:
+#     Y = alpha Q(X_0) Q(W)^T + X_H W_H^T,   X_0 = X with the columns H zeroed.
+# As in the compensated GEMM, B_ext is pre-divided by alpha so that one fp32
+# scaling of the accumulator serves both parts: A_ext = bf16(X_H),
+# B_ext = bf16(W_H / alpha).  NVFP4's tensor scale is that of X_0.
+# ----------------------------------------------------------------------------
+
+def hcp_zero_columns(x, hot) -> np.ndarray:
+    """X_0: x with the columns in `hot` set to 0 (fp32)."""
+    x0 = np.array(x, dtype=np.float32, copy=True)
+    x0[:, np.asarray(hot, dtype=np.int64)] = 0.0
+    return x0
+
+
+def hcp_zeroed_operands(x, w, fmt, g_x, g_w, hot):
+    """(A_ext, B_ext) = (bf16(X_H), bf16(W_H / alpha)) as fp32 arrays of bf16 values."""
+    hot = np.asarray(hot, dtype=np.int64)
+    if fmt == NVFP4:
+        inv_alpha = np.float32(np.float32(1.0) / np.float32(np.float32(g_x) * np.float32(g_w)))
+    else:
+        inv_alpha = np.float32(1.0)
+    a_ext = bf16_round(np.asarray(x, dtype=np.float32)[:, hot])
+    b_ext = bf16_round((np.asarray(w, dtype=np.float32)[:, hot] * inv_alpha).astype(np.float32))
+    return a_ext.astype(np.float32), b_ext.astype(np.float32)
+
+
+def hcp_zeroed_gemm(x, w, fmt, hot):
+    """Y = alpha Q(X_0) Q(W)^T + A_ext B_ext^T alpha32 in fp64; returns
+    (Y, bound, (x0 codes, scales, g), (w codes, scales, g))."""
+    x0q = quantize(hcp_zero_columns(x, hot), fmt)
+    wq = quantize(w, fmt)
+    y, bound = gemm(x0q[0], x0q[1], wq[0], wq[1], fmt, x0q[2], wq[2])
+    a_ext, b_ext = hcp_zeroed_operands(x, w, fmt, x0q[2], wq[2], hot)
+    alpha32 = 1.0 if fmt == MXFP4 else float(np.float32(np.float32(x0q[2]) * np.float32(wq[2])))
+    ae, be = a_ext.astype(np.float64), b_ext.astype(np.float64)
+    return y + alpha32 * (ae @ be.T), bound + alpha32 * (np.abs(ae) @ np.abs(be).T), x0q, wq

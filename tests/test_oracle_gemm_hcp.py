@@ -137,3 +137,53 @@ def test_hcp_num_hot_is_ceil_of_nine_percent():
     assert o.hcp_num_hot(4096) == 369
     assert o.hcp_num_hot(100) == 9
     assert o.hcp_num_hot(128) == 12
+
+
+def _grid_rows(rng, rows, cols):
+    # E2M1 grid values with a 4 in every 32-block: MXFP4 scale 2^0, exact quantization
+    g = np.array([0, 0.5, 1, 1.5, 2, 3, 4], np.float32)
+    a = rng.choice(g, (rows, cols)) * rng.choice([-1, 1], (rows, cols))
+    a[:, ::32] = 4.0
+    return a.astype(np.float32)
+
+
+def test_hcp_zeroed_is_exact_when_the_cold_part_quantizes_exactly():
+    # X: exact grid values except on the hot channels (arbitrary, huge); W on
+    # the grid.  Zeroing H leaves an exactly representable X_0 (every block
+    # keeps a 4 at its first column, which is never hot), so the FP4 part is
+    # exact and the bf16 columns carry X_H W_H^T exactly: Y = X W^T.
+    rng = np.random.default_rng(26)
+    X = _grid_rows(rng, 48, 128)
+    hot = np.array([3, 40, 77, 100])
+    X[:, hot] = o.bf16_round((rng.standard_normal((48, 4)) * 300).astype(np.float32))
+    W = _grid_rows(rng, 40, 128)
+    y, bound, _, _ = o.hcp_zeroed_gemm(X, W, o.MXFP4, hot)
+    assert np.array_equal(y, X.astype(np.float64) @ W.astype(np.float64).T)
+    assert np.all(bound >= np.abs(y))
+    # the plain FP4 product is not exact: the hot values inflate their blocks
+    xq, wq = o.quantize(X, o.MXFP4), o.quantize(W, o.MXFP4)
+    y0, _ = o.gemm(xq[0], xq[1], wq[0], wq[1], o.MXFP4)
+    assert not np.allclose(y0, y)
+
+
+def test_hcp_zeroed_without_hot_channels_is_the_plain_gemm():
+    X, W, (xc, xs, gx), (wc, ws, gw), _ = _hcp_fixture(o.NVFP4)
+    y, _, _, _ = o.hcp_zeroed_gemm(X, W, o.NVFP4, np.array([], np.int64))
+    y0, _ = o.gemm(xc, xs, wc, ws, o.NVFP4, gx, gw)
+    assert np.array_equal(y, y0)
+
+
+@pytest.mark.parametrize("fmt", [o.MXFP4, o.NVFP4])
+def test_hcp_zeroed_shrinks_the_hot_blocks_and_the_error(fmt):
+    X, W, (xc, xs, gx), (wc, ws, gw), hot_true = _hcp_fixture(fmt, seed=27)
+    hot = o.hcp_select(X, xc, xs, fmt, gx, len(hot_true))
+    y, _, (zc, zs, zg), _ = o.hcp_zeroed_gemm(X, W, fmt, hot)
+    # block scales (values, with the tensor scale) no larger than before, and
+    # much smaller, in total, in the blocks that held a hot channel
+    s_old = o.block_scales_expanded(xs, fmt, gx)
+    s_new = o.block_scales_expanded(zs, fmt, zg)
+    assert np.all(s_new <= s_old * (1 + 2 ** -3))      # E4M3 rounding under a new tensor scale
+    assert s_new[:, hot].sum() < 0.1 * s_old[:, hot].sum()
+    exact = X.astype(np.float64) @ W.astype(np.float64).T
+    y0, _ = o.gemm(xc, xs, wc, ws, fmt, gx, gw)
+    assert np.abs(y - exact).sum() < 0.5 * np.abs(y0 - exact).sum()
