@@ -88,6 +88,8 @@ _SIGNATURES = {
     "fp4_hcp_select": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(fp4_operand), _I32, _P, _P, _SZ, _P]),
     "fp4_hcp_select_noalloc": (ctypes.c_int, [_P, _I64, ctypes.POINTER(fp4_operand), _I32, _P, _P]),
     "fp4_hcp_workspace_bytes": (_SZ, [_I64, _I64, _I32, _I32]),
+    "fp4_hcp_quantize_zeroed": (ctypes.c_int, [_P, _P, _I32, _I64, _I64, _I64, ctypes.POINTER(fp4_quant_params), _P,
+                                               _I32, _P, _P, _P, _P]),
     "fp4_hcp_gemm": (ctypes.c_int, [_P, _P, _I64, _P, _I64, ctypes.POINTER(fp4_operand),
                                     ctypes.POINTER(fp4_operand), _P, _I32, _I32, _I32, _P, _SZ, _I32, _P, _I64, _P]),
     "fp4_encode_e2m1": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _P]),
@@ -371,6 +373,18 @@ def fp4_hcp_select_noalloc(x: torch.Tensor, xq: QTensor, k_hot: int, out: Option
     _check(load_library().fp4_hcp_select_noalloc(_ptr(x), _ld(x), ctypes.byref(op), k_hot, _ptr(out),
                                                  _stream(stream)), "fp4_hcp_select_noalloc")
     return out[:k_hot]
+
+
+def fp4_hcp_quantize_zeroed(x: torch.Tensor, params: fp4_quant_params, hot_idx: torch.Tensor, k_hot: int,
+                            out: Optional[QTensor] = None, ctx=None, stream=None) -> QTensor:
+    """Quantize x with the hot channels (ascending int32 list) set to zero: the operand of the order-0 HCP GEMM."""
+    rows, cols = x.shape
+    out = out or alloc_qtensor(rows, cols, params.format, params.sf_layout, x.device)
+    _check(load_library().fp4_hcp_quantize_zeroed(_ctx(ctx), _ptr(x), _dtype_code(x), rows, cols, _ld(x),
+                                                  ctypes.byref(params), _ptr(hot_idx), k_hot, _ptr(out.codes),
+                                                  _ptr(out.scales), _ptr(out.tensor_scale), _stream(stream)),
+           "fp4_hcp_quantize_zeroed")
+    return out
 
 
 def fp4_hcp_gemm(x: torch.Tensor, w: torch.Tensor, xq: QTensor, wq: QTensor, hot_idx: torch.Tensor, k_hot: int,

@@ -519,6 +519,35 @@ int fp4_gemm(fp4_ctx* ctx, const fp4_operand* A, const fp4_operand* B, int32_t o
   return launch_gemm(g, static_cast<cudaStream_t>(stream));
 }
 
+int fp4_hcp_quantize_zeroed(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols, int64_t ldx,
+                            const fp4_quant_params* p, const int32_t* hot_idx, int32_t k_hot, uint8_t* codes,
+                            uint8_t* scales, float* tensor_scale, void* stream) {
+  const bool empty = rows == 0 || cols == 0;
+  if (!ctx || !present(codes, empty) || !present(scales, empty)) return FP4_ERR_INVALID_ARG;
+  int s = check_params(p);
+  if (s) return s;
+  if (p->transpose || p->rht || p->scaling != FP4_SCALING_1D || p->block != block_of(p->format))
+    return FP4_ERR_UNSUPPORTED;
+  s = check_input(x, x_dtype, rows, cols, ldx);
+  if (s) return s;
+  if (cols % p->block || k_hot < 0 || k_hot > cols || (k_hot > 0 && !hot_idx)) return FP4_ERR_INVALID_ARG;
+  if (rows * (cols / 16) >= (int64_t(1) << 31)) return FP4_ERR_TOO_LARGE;
+  if (!al16(codes)) return FP4_ERR_MISALIGNED;
+  if (empty) return FP4_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* slot = reinterpret_cast<float*>(&ctx->scratch->amax[0]);
+  if (p->format == FP4_FMT_NVFP4) {
+    cudaError_t e = launch_amax_zeroed(x, x_dtype, rows, cols, ldx, hot_idx, k_hot, slot, next_gen(ctx, st),
+                                       ctx->num_sms, st);
+    if (e != cudaSuccess) return FP4_ERR_CUDA;
+  }
+  if (clear_sf_padding(p, scales, rows, cols, st) != cudaSuccess) return FP4_ERR_CUDA;
+  QuantOut o = make_out(p, codes, scales, tensor_scale, slot, rows, cols);
+  o.zero_idx = hot_idx;
+  o.zero_n = k_hot;
+  return cuda_status(launch_quant_rows_zeroed(x, x_dtype, rows, cols, ldx, p->format, o, ctx->num_sms, st));
+}
+
 size_t fp4_hcp_select_workspace_bytes(int64_t k) { return k > 0 ? (size_t)k * 8 : 0; }
 
 int fp4_hcp_select(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
@@ -554,7 +583,7 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
                  void* stream) {
   if (!ctx || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
   if (mode != FP4_HCP_SINGLE && mode != FP4_HCP_TWO) return FP4_ERR_INVALID_ARG;
-  if (order != 1 && order != 2) return FP4_ERR_INVALID_ARG;
+  if (order < 0 || order > 2) return FP4_ERR_INVALID_ARG;
   int s = check_operand(xq, true);
   if (s) return s;
   if (!native_block(xq)) return FP4_ERR_UNSUPPORTED;

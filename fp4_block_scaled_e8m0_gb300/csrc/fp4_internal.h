@@ -66,6 +66,8 @@ struct QuantOut {
   PhiloxRoundKeys keys;  // of sr_seed
   const float* clamp;    // row quantizer only: device tau, x is clamped to [-tau, tau] (null: no clamp)
   float* col_counts;     // with clamp: per-column count of |x| > tau, added to (null: not counted)
+  const int32_t* zero_idx;  // row quantizer only: ascending columns set to 0 before quantizing
+  int zero_n;
 };
 
 // Launchers (quant.cu).  All return cudaError_t of the launch.
@@ -154,6 +156,12 @@ cudaError_t launch_occ_prepare(const void* x, int xdt, int64_t ldx, const uint16
 // the sigmoid-smoothed reconstruction instead of the codes
 cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, int block,
                                const float* tau, float beta, double* sums, int num_sms, cudaStream_t st);
+// the row quantizer with the columns o.zero_idx[0..o.zero_n) set to 0 (32-bit block ids)
+cudaError_t launch_quant_rows_zeroed(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                                     const QuantOut& o, int num_sms, cudaStream_t st);
+// amax of x with the ascending columns hot[0..n) left out, into a tagged slot
+cudaError_t launch_amax_zeroed(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, const int32_t* hot,
+                               int n, float* amax_out, uint32_t gen, int num_sms, cudaStream_t st);
 // row quantizer for any block of 16-128 elements (row-major scales, no transpose)
 cudaError_t launch_quant_rows_blk(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt, int block,
                                   const QuantOut& o, int num_sms, cudaStream_t st);

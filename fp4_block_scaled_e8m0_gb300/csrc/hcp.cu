@@ -7,6 +7,8 @@
 // those terms: with dX = X - X_hat and dW = W - W_hat,
 //   order 2:  A_ext = [dX_H | X_H],  B_ext = [W_hat_H | dW_H] / alpha
 //   order 1:  A_ext = [X_H],         B_ext = [dW_H] / alpha  (the page's concat)
+//   order 0:  A_ext = [X_H],         B_ext = [W_H] / alpha   (hot channels zeroed in
+//             X before it was quantized: their whole product runs in bf16)
 // B_ext is divided by alpha = gX * gW so that the GEMM epilogue multiplies the
 // whole accumulator (FP4 part and bf16 part) by alpha.
 //
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
         want_hat = false;
       } else {
         want_hat = order == 2 && part == 0;
-        want_delta = !want_hat;
+        want_delta = !want_hat && order != 0;   // order 0 (hot channels zeroed): w / alpha
       }
       if (want_delta || want_hat) {
         const float xh = dequant_elem<FMT>(q, r, c, g, nsf_row, nsf_pad);

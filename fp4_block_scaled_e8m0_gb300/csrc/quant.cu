@@ -158,6 +158,20 @@ __global__ void __launch_bounds__(kThreads) amax_rows_kernel(const void* __restr
 // address is 16 c when rows are contiguous, else (c / nch) ldx + 16 (c % nch)
 // with a precomputed divider; two chunks per iteration keep 64 bytes of bf16
 // in flight per thread.
+// Bit j set iff column k0 + j (j < 16) is in the ascending list hot[0..n):
+// binary search for the first entry >= k0, then the few entries below k0 + 16.
+__device__ __forceinline__ uint32_t hot_mask16(const int32_t* __restrict__ hot, int n, uint32_t k0) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((uint32_t)hot[mid] < k0) lo = mid + 1;
+    else hi = mid;
+  }
+  uint32_t m = 0;
+  for (int i = lo; i < n && (uint32_t)hot[i] < k0 + 16u; ++i) m |= 1u << ((uint32_t)hot[i] - k0);
+  return m;
+}
+
 template <int DT, bool RHT>
 __global__ void __launch_bounds__(kThreads) amax_rows32_kernel(const void* __restrict__ x, int64_t ldx, FastDiv nch,
                                                                uint32_t total, int contiguous, uint32_t signs,
@@ -189,6 +203,25 @@ __global__ void __launch_bounds__(kThreads) amax_rows32_kernel(const void* __res
 #pragma unroll
       for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(w[j]));
     }
+  }
+  block_amax_atomic(m, amax_out, gen);
+}
+
+// amax of x with the ascending columns hot[0..n) left out (16 elements per step)
+template <int DT>
+__global__ void __launch_bounds__(kThreads) amax_zeroed_kernel(const void* __restrict__ x, int64_t ldx, FastDiv nch,
+                                                               uint32_t total, const int32_t* __restrict__ hot, int n,
+                                                               float* amax_out, uint32_t gen) {
+  float m = 0.0f;
+  for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < total; c += gridDim.x * blockDim.x) {
+    const uint32_t r = fast_div(c, nch), k0 = (c - r * nch.d) << 4;
+    float v[16];
+    load8<DT, true>(x, (int64_t)r * ldx + k0, v);
+    load8<DT, true>(x, (int64_t)r * ldx + k0 + 8, v + 8);
+    const uint32_t hm = hot_mask16(hot, n, k0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (!((hm >> j) & 1u)) m = fmaxf(m, fabsf(v[j]));
   }
   block_amax_atomic(m, amax_out, gen);
 }
@@ -278,7 +311,24 @@ __device__ __forceinline__ void clamp_block(float* v, float tau, float* col_coun
   }
 }
 
-template <int FMT, int DT, bool PLAIN, bool CLAMP = false>
+// ZERO: the columns o.zero_idx[0..o.zero_n) are set to 0 before quantizing
+// (hot channels routed around the FP4 operand)
+template <bool ZERO, int B>
+__device__ __forceinline__ void zero_block(float* v, const QuantOut& o, uint32_t k0) {
+  if constexpr (ZERO) {
+#pragma unroll
+    for (int h = 0; h < B / 16; ++h) {
+      const uint32_t m = hot_mask16(o.zero_idx, o.zero_n, k0 + 16 * h);
+      if (m) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if ((m >> j) & 1u) v[16 * h + j] = 0.0f;
+      }
+    }
+  }
+}
+
+template <int FMT, int DT, bool PLAIN, bool CLAMP = false, bool ZERO = false>
 __global__ void __launch_bounds__(kThreads) quant_rows32_kernel(const void* __restrict__ x, int64_t ldx, FastDiv nblk,
                                                                 uint32_t total, int contiguous, QuantOut o) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
@@ -316,6 +366,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows32_kernel(const void* __re
     }
     clamp_block<CLAMP, B>(v, tau, o.col_counts, counts_s, k0);
     if (two) clamp_block<CLAMP, B>(w, tau, o.col_counts, counts_s, k2);
+    zero_block<ZERO, B>(v, o, k0);
+    if (two) zero_block<ZERO, B>(w, o, k2);
     if (rht) {
 #pragma unroll
       for (int h = 0; h < B / 16; ++h) rht16(v + 16 * h, o.rht_signs);
@@ -1365,6 +1417,34 @@ cudaError_t launch_quant_rows_clamped(const void* x, int dt, int64_t rows, int64
   FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT,
     if (plain) quant_rows32_kernel<FMT, DT, true, true><<<grid, kThreads, smem, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o);
     else quant_rows32_kernel<FMT, DT, false, true><<<grid, kThreads, smem, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows_zeroed(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                                     const QuantOut& o, int num_sms, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  int B = fmt == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nblk = cols / B, total = rows * nblk;
+  if (total >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  int grid = grid_for(cdiv(total, 2), kThreads, num_sms);
+  const FastDiv fd = make_fastdiv((uint32_t)nblk);
+  const int contiguous = ldx == cols;
+  const bool plain = o.rounding == FP4_ROUND_RTN && !o.rht;
+  FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT,
+    if (plain) quant_rows32_kernel<FMT, DT, true, false, true><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o);
+    else quant_rows32_kernel<FMT, DT, false, false, true><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_zeroed(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, const int32_t* hot,
+                               int n, float* amax_out, uint32_t gen, int num_sms, cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const int64_t nch = cols / 16, total = rows * nch;
+  if (total >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  const int grid = grid_for(total, kThreads, num_sms);
+  const FastDiv fd = make_fastdiv((uint32_t)nch);
+  FP4_DISPATCH_DT(dt, DT, amax_zeroed_kernel<DT><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, hot, n,
+                                                                           amax_out, gen));
   return cudaGetLastError();
 }
 

@@ -304,10 +304,21 @@ int fp4_hcp_select(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const fp4_oper
                    int32_t k_hot, int32_t* hot_idx, void* workspace, size_t ws_bytes,
                    void* stream);
 
+/* fp4_hcp_quantize_zeroed: quantize X with the k_hot columns hot_idx (device
+ * int32, ascending, as fp4_hcp_select writes them) set to zero, like
+ * fp4_quantize with transpose 0, rht 0, 1D scaling and the format's own block
+ * (else FP4_ERR_UNSUPPORTED); NVFP4: g from the amax of the zeroed tensor.
+ * The operand of fp4_hcp_gemm's order 0.                                   */
+int fp4_hcp_quantize_zeroed(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols, int64_t ldx,
+                            const fp4_quant_params* p, const int32_t* hot_idx, int32_t k_hot, uint8_t* codes,
+                            uint8_t* scales, float* tensor_scale, void* stream);
+
 /* fp4_hcp_gemm: Y = alpha * (X_hat W_hat^T + A_ext B_ext^T) with bf16 extra K
  * columns on the hot channels H (order 2, "S-O2-B"):
  *   A_ext = [X - X_hat | X]_H,  B_ext = [W_hat | W - W_hat]_H / alpha
- * (order 1 = the page's literal concat: A_ext = X_H, B_ext = (W - W_hat)_H / alpha).
+ * (order 1 = the page's literal concat: A_ext = X_H, B_ext = (W - W_hat)_H / alpha;
+ *  order 0 = hot channels zeroed: xq from fp4_hcp_quantize_zeroed, A_ext = X_H,
+ *  B_ext = W_H / alpha, so Y = alpha Q(X_0) W_hat^T + X_H W_H^T).
  * mode FP4_HCP_SINGLE: one kernel, FP4 K-steps then bf16 K-steps into one
  * TMEM accumulator; FP4_HCP_TWO: the FP4 GEMM, then a bf16 GEMM with C +=.
  * X (M x K) and W (N x K) bf16 with pitches ldx, ldw; xq, wq their

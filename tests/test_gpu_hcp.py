@@ -90,3 +90,57 @@ def test_hcp_zero_hot_is_plain_gemm():
     y1 = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, torch.zeros(1, dtype=torch.int32, device="cuda"), 0,
                           out_dtype=torch.float32)
     assert torch.equal(y0, y1)
+
+
+def _quant_np(q):
+    from _util import untile_scales
+    codes = q.codes.cpu().numpy()
+    nsf = q.k // fp4.BLOCK[q.fmt]
+    sc = q.scales.cpu().numpy()
+    scales = untile_scales(sc, q.rows, nsf) if q.sf_layout == fp4.FP4_SF_MMA else sc[: q.rows * nsf].reshape(q.rows, nsf)
+    g = q.tensor_scale.cpu().numpy()[0] if q.tensor_scale is not None else None
+    return codes, scales, g
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+@pytest.mark.parametrize("sf_layout", [fp4.FP4_SF_ROWMAJOR, fp4.FP4_SF_MMA])
+@pytest.mark.parametrize("rounding", [fp4.FP4_ROUND_RTN, fp4.FP4_ROUND_SR])
+def test_hcp_quantize_zeroed_bit_exact(fmt, sf_layout, rounding):
+    xt, _, xn, _, planted = _data(fmt, M=333, K=512, seed=4)
+    hot = np.sort(np.concatenate([planted, [0, 1, 2, 511]]))   # edges of the row too
+    p = fp4.quant_params(fmt, rounding, sf_layout=sf_layout, sr_seed=3, sr_stream=1)
+    q = fp4.fp4_hcp_quantize_zeroed(xt.cuda(), p, torch.from_numpy(hot.astype(np.int32)).cuda(), len(hot))
+    wc, ws, wg = o.quantize(o.hcp_zero_columns(xn, hot), FMT[fmt], "sr" if rounding else "rtn", sr_seed=3,
+                            sr_stream=1)
+    codes, scales, g = _quant_np(q)
+    assert np.array_equal(scales, ws)
+    assert np.array_equal(codes, wc)
+    if wg is not None:
+        assert np.float32(g).view(np.uint32) == np.float32(wg).view(np.uint32)
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+@pytest.mark.parametrize("mode", [fp4.FP4_HCP_SINGLE, fp4.FP4_HCP_TWO])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_hcp_zeroed_gemm_matches_oracle(fmt, mode, out_dtype):
+    xt, wt, xn, wn, _ = _data(fmt, seed=5)
+    K = xn.shape[1]
+    h = fp4.hcp_num_hot(K)
+    cx, sx, gx = o.quantize(xn, FMT[fmt])
+    hot = o.hcp_select(xn, cx, sx, FMT[fmt], gx, h)
+    hot_d = torch.from_numpy(hot.astype(np.int32)).cuda()
+    x0q = fp4.fp4_hcp_quantize_zeroed(xt.cuda(), fp4.quant_params(fmt), hot_d, h)
+    wq = fp4.fp4_quantize(wt.cuda(), fp4.quant_params(fmt))
+    y = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), x0q, wq, hot_d, h, mode, 0, out_dtype)
+    got = y.float().cpu().numpy().astype(np.float64)
+    yref, bound, _, _ = o.hcp_zeroed_gemm(xn, wn, FMT[fmt], hot)
+    tol = o.gemm_tolerance(bound, yref, out_dtype == torch.bfloat16)
+    if mode == fp4.FP4_HCP_TWO and out_dtype == torch.bfloat16:
+        tol = tol + 2.0 ** -8 * np.abs(yref)
+    err = np.abs(got - yref)
+    assert np.all(err <= tol), f"{(err > tol).sum()} outside; worst {np.max(err - tol)}"
+    # closer to the unquantized product than the order-2 compensation on these activations
+    exact = xn.astype(np.float64) @ wn.astype(np.float64).T
+    xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
+    y2 = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, hot_d, h, mode, 2, torch.float32).cpu().numpy()
+    assert np.abs(got - exact).sum() < np.abs(y2 - exact).sum() * 1.5
