@@ -731,3 +731,60 @@ def hcp_zeroed_gemm(x, w, fmt, hot):
     alpha32 = 1.0 if fmt == MXFP4 else float(np.float32(np.float32(x0q[2]) * np.float32(wq[2])))
     ae, be = a_ext.astype(np.float64), b_ext.astype(np.float64)
     return y + alpha32 * (ae @ be.T), bound + alpha32 * (np.abs(ae) @ np.abs(be).T), x0q, wq
+
+
+# ----------------------------------------------------------------------------
+# FP8 (E4M3) residual columns for the compensated GEMM ([outlier §3.1]'s extra
+# K columns; the MSR write-up §六 runs its high-precision sparse compensation
+# in FP8).  READING: every row of A_ext and of B_ext gets its own fp32 scale
+# s = amax(row) / 448 and each value becomes the nearest E4M3 value of v / s
+# (ties to even, saturating at 448, sign kept); the residual product
+# sum_j A_ext[m, j] B_ext[n, j] is then s_A[m] s_B[n] sum_j a8[m, j] b8[n, j],
+# added by a second GEMM (C += ...).  The columns are those of the bf16 tail
+# without the division by alpha (the row scales carry the magnitudes):
+#   order 2: A = [dX_H | X_H], B = [W_hat_H | dW_H];  order 1: A = X_H, B = dW_H;
+#   order 0 (hot channels zeroed in X): A = X_H, B = W_H.
+# ----------------------------------------------------------------------------
+
+def e4m3_rows(v):
+    """(values, scales): per-row E4M3 rounding of v [R, C] with s = fp32(amax / 448);
+    values are the decoded E4M3 numbers (fp64, without s).  All-zero rows: s = 0."""
+    v = np.asarray(v, dtype=np.float32)
+    amax = np.abs(v).max(axis=1) if v.shape[1] else np.zeros(v.shape[0], np.float32)
+    s = (amax / np.float32(448.0)).astype(np.float32)
+    safe = np.where(s == 0, np.float32(1.0), s).astype(np.float32)
+    t = (np.abs(v) / safe[:, None]).astype(np.float32)
+    mag = e4m3_decode(e4m3_encode_rn_satfinite(t))
+    vals = np.where(np.signbit(v), -mag, mag)
+    vals = np.where(s[:, None] == 0, 0.0, vals)
+    return vals.astype(np.float64), s
+
+
+def hcp_fp8_columns(x, x_codes, x_scales, w, w_codes, w_scales, fmt, g_x, g_w, hot, order=2):
+    """fp32 values of the extra columns (before the E4M3 rounding), per order."""
+    hot = np.asarray(hot, dtype=np.int64)
+    xf = np.asarray(x, dtype=np.float32)[:, hot]
+    wf = np.asarray(w, dtype=np.float32)[:, hot]
+    xh = dequantize(x_codes, x_scales, fmt, g_x)[:, hot]
+    wh = dequantize(w_codes, w_scales, fmt, g_w)[:, hot]
+    dx = (xf - xh).astype(np.float32)
+    dw = (wf - wh).astype(np.float32)
+    if order == 2:
+        return np.concatenate([dx, xf], axis=1), np.concatenate([wh, dw], axis=1)
+    if order == 1:
+        return xf, dw
+    if order == 0:
+        return xf, wf
+    raise ValueError("order must be 0, 1 or 2")
+
+
+def hcp_gemm_fp8(x, x_codes, x_scales, w, w_codes, w_scales, fmt, g_x, g_w, hot, order=2):
+    """Y = alpha Q(X) Q(W)^T + s_A s_B (a8 b8^T) in fp64; returns (Y, bound).
+    For order 0, x_codes / x_scales / g_x are the quantization of X with H zeroed."""
+    y, bound = gemm(x_codes, x_scales, w_codes, w_scales, fmt, g_x, g_w)
+    a, b = hcp_fp8_columns(x, x_codes, x_scales, w, w_codes, w_scales, fmt, g_x, g_w, hot, order)
+    a8, sa = e4m3_rows(a)
+    b8, sb = e4m3_rows(b)
+    A = a8 * sa.astype(np.float64)[:, None]
+    B = b8 * sb.astype(np.float64)[:, None]
+    return y + A @ B.T, bound + np.abs(A) @ np.abs(B).T

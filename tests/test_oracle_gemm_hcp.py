@@ -187,3 +187,51 @@ def test_hcp_zeroed_shrinks_the_hot_blocks_and_the_error(fmt):
     exact = X.astype(np.float64) @ W.astype(np.float64).T
     y0, _ = o.gemm(xc, xs, wc, ws, fmt, gx, gw)
     assert np.abs(y - exact).sum() < 0.5 * np.abs(y0 - exact).sum()
+
+
+def test_e4m3_rows_exact_on_representable_rows():
+    # rows of E4M3 values times 2^k whose largest magnitude is 448 * 2^k: the
+    # scale is exactly 2^k and every value comes back unchanged
+    rng = np.random.default_rng(28)
+    table = o.E4M3_VALUES[:127]
+    rows = []
+    for k in (-20, -3, 0, 5):
+        r = rng.choice(table, 40) * rng.choice([-1, 1], 40)
+        r[7] = -448.0
+        rows.append(r * 2.0 ** k)
+    v = np.array(rows, np.float32)
+    vals, s = o.e4m3_rows(v)
+    assert np.array_equal(s, np.float32([2.0 ** k for k in (-20, -3, 0, 5)]))
+    assert np.array_equal(vals * s.astype(np.float64)[:, None], v.astype(np.float64))
+
+
+def test_e4m3_rows_relative_precision_and_zero_rows():
+    rng = np.random.default_rng(29)
+    v = (rng.standard_normal((8, 64)) * np.exp(rng.uniform(-5, 5, (8, 1)))).astype(np.float32)
+    v[3] = 0.0
+    vals, s = o.e4m3_rows(v)
+    back = vals * s.astype(np.float64)[:, None]
+    assert np.all(back[3] == 0) and s[3] == 0
+    # normal range of the row (>= 2^-6 s): within half an E4M3 ulp (2^-4 relative)
+    normal = (np.abs(v) >= (2.0 ** -6) * s[:, None]) & (v != 0)
+    rel = np.abs(back - v)[normal] / np.abs(v)[normal]
+    assert rel.max() <= 2.0 ** -4 + 1e-12
+
+
+@pytest.mark.parametrize("order", [0, 1, 2])
+def test_hcp_fp8_tail_is_the_bf16_tail_within_e4m3_precision(order):
+    X, W, (xc, xs, gx), (wc, ws, gw), _ = _hcp_fixture(o.NVFP4, seed=30)
+    hot = o.hcp_select(X, xc, xs, o.NVFP4, gx, 10)
+    if order == 0:
+        xc, xs, gx = o.quantize(o.hcp_zero_columns(X, hot), o.NVFP4)
+        y16, _, _, _ = o.hcp_zeroed_gemm(X, W, o.NVFP4, hot)
+    else:
+        y16, _ = o.hcp_gemm(X, xc, xs, W, wc, ws, o.NVFP4, gx, gw, hot, order)
+    y8, _ = o.hcp_gemm_fp8(X, xc, xs, W, wc, ws, o.NVFP4, gx, gw, hot, order)
+    a, b = o.hcp_fp8_columns(X, xc, xs, W, wc, ws, o.NVFP4, gx, gw, hot, order)
+    mag = np.abs(a.astype(np.float64)) @ np.abs(b.astype(np.float64)).T
+    # each product term: E4M3 (2^-4 each, subnormal tail small) and bf16 (2^-8 each) roundings
+    assert np.all(np.abs(y8 - y16) <= 0.15 * mag + 1e-6 * np.abs(y16))
+    # and the tail matters: dropping it moves Y by much more
+    y0, _ = o.gemm(xc, xs, wc, ws, o.NVFP4, gx, gw)
+    assert np.abs(y0 - y16).sum() > 5 * np.abs(y8 - y16).sum()
