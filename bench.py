@@ -195,9 +195,10 @@ def time_extensions(fp4, step, dev, flush, launches, pk):
 
 def time_hcp(fp4, dev, flush, launches, pk):
     """Hot-channel compensation ("大模型4位训练中的异常值动态分析与优化实践" §3-4) on the hot-channel
-    activations: plain NVFP4 GEMM, order-2 compensation (bf16 residual columns) and the variant
-    with the hot channels zeroed before quantizing (their product in bf16); single-kernel mode,
-    h = 9% of K.  Relative L2 error of Y against the fp64 product on 64 sampled rows."""
+    activations: plain NVFP4 GEMM, order-2 compensation (bf16 residual columns), the variant with
+    the hot channels zeroed before quantizing (their product in bf16), single-kernel and with the
+    residual as a second GEMM in bf16 or E4M3; h = 9% of K.  Relative L2 error of Y against the
+    fp64 product on 64 sampled rows."""
     from fp4_block_scaled_e8m0_gb300 import inputs
     d = inputs.hcp_square(OCC_M, OCC_K, OCC_N)
     X, W = d["X"].to(dev), d["W"].to(dev)
@@ -216,7 +217,13 @@ def time_hcp(fp4, dev, flush, launches, pk):
     res = {"workload": f"X[{OCC_M},{OCC_K}] Student-t(3), 1% channels x100; W[{OCC_N},{OCC_K}]; NVFP4; h={h}; bf16 Y"}
     cases = {"plain": lambda: fp4.fp4_gemm(xq, wq, out=Y),
              "order2": lambda: fp4.fp4_hcp_gemm(X, W, xq, wq, hot, h, fp4.FP4_HCP_SINGLE, 2, out=Y, workspace=ws),
-             "zeroed": lambda: fp4.fp4_hcp_gemm(X, W, x0q, wq, hot, h, fp4.FP4_HCP_SINGLE, 0, out=Y, workspace=ws)}
+             "zeroed": lambda: fp4.fp4_hcp_gemm(X, W, x0q, wq, hot, h, fp4.FP4_HCP_SINGLE, 0, out=Y, workspace=ws),
+             "order2_bf16_two_kernel": lambda: fp4.fp4_hcp_gemm(X, W, xq, wq, hot, h, fp4.FP4_HCP_TWO, 2, out=Y,
+                                                                workspace=ws),
+             "order2_fp8_two_kernel": lambda: fp4.fp4_hcp_gemm(X, W, xq, wq, hot, h, fp4.FP4_HCP_TWO_FP8, 2, out=Y,
+                                                               workspace=ws),
+             "zeroed_fp8_two_kernel": lambda: fp4.fp4_hcp_gemm(X, W, x0q, wq, hot, h, fp4.FP4_HCP_TWO_FP8, 0, out=Y,
+                                                               workspace=ws)}
     for name, fn in cases.items():
         r = _rate("tensor", flops, _time_op(fn, flush, launches), pk)
         fn()

@@ -1,5 +1,6 @@
 // C ABI entry points: argument validation, context handling and dispatch to
 // the kernels.  See include/fp4.h for the contract of each call.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -570,11 +571,16 @@ int fp4_hcp_select(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const fp4_oper
 
 static int64_t hcp_kx(int32_t k_hot, int32_t order) { return cdiv((int64_t)(order == 2 ? 2 : 1) * k_hot, 64) * 64; }
 
+// E4M3 extra columns: K padded to 128 (one 128-byte stage row)
+static int64_t hcp_kx8(int32_t k_hot, int32_t order) { return cdiv((int64_t)(order == 2 ? 2 : 1) * k_hot, 128) * 128; }
+
+// the larger of the bf16 layout [A_ext | B_ext] and the E4M3 one [a8 | b8 | sa | sb]
 size_t fp4_hcp_workspace_bytes(int64_t m, int64_t n, int32_t k_hot, int32_t order) {
   if (m <= 0 || n <= 0 || k_hot <= 0) return 0;
-  int64_t kx = hcp_kx(k_hot, order);
-  int64_t a = cdiv(m * kx * 2, 256) * 256;
-  return (size_t)(a + n * kx * 2);
+  const int64_t kx = hcp_kx(k_hot, order), kx8 = hcp_kx8(k_hot, order);
+  const int64_t bf16 = cdiv(m * kx * 2, 256) * 256 + n * kx * 2;
+  const int64_t fp8 = cdiv(m * kx8, 256) * 256 + cdiv(n * kx8, 256) * 256 + cdiv(m * 4, 256) * 256 + n * 4;
+  return (size_t)std::max(bf16, fp8);
 }
 
 int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf16, int64_t ldw,
@@ -582,7 +588,7 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
                  int32_t order, void* workspace, size_t ws_bytes, int32_t out_dtype, void* y, int64_t ldy,
                  void* stream) {
   if (!ctx || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
-  if (mode != FP4_HCP_SINGLE && mode != FP4_HCP_TWO) return FP4_ERR_INVALID_ARG;
+  if (mode != FP4_HCP_SINGLE && mode != FP4_HCP_TWO && mode != FP4_HCP_TWO_FP8) return FP4_ERR_INVALID_ARG;
   if (order < 0 || order > 2) return FP4_ERR_INVALID_ARG;
   int s = check_operand(xq, true);
   if (s) return s;
@@ -614,6 +620,29 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
   if (k_hot == 0 || M == 0 || N == 0) return launch_gemm(g, st);
   if (ws_bytes < fp4_hcp_workspace_bytes(M, N, k_hot, order) || !workspace || !al16(workspace))
     return FP4_ERR_INVALID_ARG;
+  if (mode == FP4_HCP_TWO_FP8) {
+    const int64_t kx8 = hcp_kx8(k_hot, order);
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    uint8_t* a8 = base;
+    uint8_t* b8 = a8 + cdiv(M * kx8, 256) * 256;
+    float* sa = reinterpret_cast<float*>(b8 + cdiv(N * kx8, 256) * 256);
+    float* sb = sa + cdiv(M * 4, 256) * 64;
+    cudaError_t e = launch_hcp_gather_fp8(static_cast<const uint16_t*>(x_bf16), ldx,
+                                          static_cast<const uint16_t*>(w_bf16), ldw, *xq, *wq, hot_idx, k_hot, order,
+                                          kx8, a8, b8, sa, sb, ctx->num_sms, st);
+    if (e != cudaSuccess) return FP4_ERR_CUDA;
+    s = launch_gemm(g, st);   // base FP4 GEMM
+    if (s) return s;
+    g.fp4_part = false;       // E4M3 residual GEMM: C += sa[m] sb[n] acc
+    g.a_ext = a8;
+    g.b_ext = b8;
+    g.kx = kx8;
+    g.ext_fp8 = true;
+    g.row_scale = sa;
+    g.col_scale = sb;
+    g.accumulate = 1;
+    return launch_gemm(g, st);
+  }
   const int64_t kx = hcp_kx(k_hot, order);
   uint16_t* a_ext = static_cast<uint16_t*>(workspace);
   uint16_t* b_ext = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + cdiv(M * kx * 2, 256) * 256);

@@ -107,9 +107,12 @@ cudaError_t launch_encode_e4m3(const float* t, uint8_t* out, int64_t n, cudaStre
 struct GemmArgs {
   const fp4_operand* A;
   const fp4_operand* B;
-  const uint16_t* a_ext;   // [M][kx] bf16 or null
-  const uint16_t* b_ext;   // [N][kx] bf16 or null
-  int64_t kx;              // extra K (multiple of 64), 0 if none
+  const void* a_ext;       // [M][kx] bf16 (or E4M3 bytes with ext_fp8), or null
+  const void* b_ext;       // [N][kx]
+  int64_t kx;              // extra K (multiple of 64; of 128 with ext_fp8), 0 if none
+  bool ext_fp8;            // extra columns are E4M3 (kind::f8f6f4)
+  const float* row_scale;  // [M] and [N]: C (+)= row_scale[m] col_scale[n] acc (no alpha); null: alpha
+  const float* col_scale;
   bool fp4_part;           // false: only the bf16 columns (two-kernel residual GEMM)
   int out_dtype;
   void* C;
@@ -131,6 +134,11 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st);  // returns fp4 status
 cudaError_t launch_hcp_channel_errors(const uint16_t* x, int64_t ldx, const fp4_operand& q, float* err,
                                       int num_sms, cudaStream_t st);
 cudaError_t launch_hcp_topk(const float* err, int64_t k, int k_hot, int32_t* hot_idx, cudaStream_t st);
+// E4M3 extra columns [M][kx] / [N][kx] (kx a multiple of 128) with row scales sa / sb
+cudaError_t launch_hcp_gather_fp8(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
+                                  const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot, int k_hot,
+                                  int order, int64_t kx, uint8_t* a8, uint8_t* b8, float* sa, float* sb, int num_sms,
+                                  cudaStream_t st);
 cudaError_t launch_hcp_gather(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
                               const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot,
                               int k_hot, int order, int64_t kx, uint16_t* a_ext, uint16_t* b_ext,

@@ -56,7 +56,8 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 struct Params {
   int M, N;
   int k_tiles;        // FP4 K stages (256 elements each)
-  int ext_tiles;      // bf16 K stages (64 elements each)
+  int ext_tiles;      // extra K stages: 64 bf16 or 128 E4M3 elements each
+  int ext_fp8;        // extra columns are E4M3 (kind::f8f6f4) instead of bf16
   int nvfp4;
   int sf_atoms;       // atoms (128 rows x 4 scales) per stage and 128-row group: 4 NVFP4, 2 MXFP4
   const float* ts_a;
@@ -72,6 +73,8 @@ struct Params {
   const int2* occ_entries;     // (k, float bits of v)
   const uint16_t* occ_wt;
   int64_t occ_ldt;
+  const float* row_scale;      // if set: C (+)= row_scale[m] col_scale[n] acc instead of alpha acc
+  const float* col_scale;
 };
 
 // ---------------------------------------------------------------------------
@@ -164,6 +167,14 @@ __device__ __forceinline__ uint32_t idesc_fp4(bool ue8m0, uint32_t sf_id) {
   d |= sf_id << 29;             // A scale-factor byte
   return d;
 }
+// kind::f8f6f4 with E4M3 A and B (type code 0), F32 accumulation
+__device__ __forceinline__ uint32_t idesc_e4m3() {
+  uint32_t d = 0;
+  d |= 1u << 4;                 // accumulate in F32
+  d |= (uint32_t)(BN >> 3) << 17;
+  d |= (uint32_t)(BM >> 4) << 24;
+  return d;
+}
 __device__ __forceinline__ uint32_t idesc_bf16() {
   uint32_t d = 0;
   d |= 1u << 4;                 // accumulate in F32
@@ -189,6 +200,12 @@ __device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t adesc, uint64_
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa_tmem), "r"(sfb_tmem));
   }
+}
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -276,8 +293,15 @@ __device__ __forceinline__ void store_exchanged(const Params& p, const uint32_t*
     const int row = row0 + 4 * v + a;
     if (row >= p.M) break;
     float x[4];
+    if (p.row_scale) {   // per-row and per-column scales (E4M3 extra columns)
+      const float rs = p.row_scale[row];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) x[k] = __fmul_rn(__uint_as_float(w[4 * v + k]), alpha);
+      for (int k = 0; k < 4; ++k)
+        x[k] = __fmul_rn(__uint_as_float(w[4 * v + k]), __fmul_rn(rs, c + k < p.N ? p.col_scale[c + k] : 0.0f));
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) x[k] = __fmul_rn(__uint_as_float(w[4 * v + k]), alpha);
+    }
     if (p.out_bf16) {
       __nv_bfloat16* q = static_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + c;
       if (full4 && !p.accumulate) {
@@ -509,8 +533,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int kx = kt - p.k_tiles;
             mbar_arrive(&sf_full[s]);   // no scales in the bf16 stages
             mbar_expect_tx(&full[s], A_TILE + B_TILE);
-            tma_load_2d(stage_a(s), &tm_ax, &full[s], kx * 64, tm * BM);
-            tma_load_2d(stage_b(s), &tm_bx, &full[s], kx * 64, tn * BN);
+            const int ext_elems = p.ext_fp8 ? 128 : 64;   // 128 bytes of K either way
+            tma_load_2d(stage_a(s), &tm_ax, &full[s], kx * ext_elems, tm * BM);
+            tma_load_2d(stage_b(s), &tm_bx, &full[s], kx * ext_elems, tn * BN);
           }
           if (++s == STAGES) { s = 0; phase ^= 1; }
         }
@@ -539,7 +564,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // the 14-bit field; the instruction descriptors are constants.
       const uint64_t da0 = desc_sw128(smem_u32(stage_a(0))), db0 = desc_sw128(smem_u32(stage_b(0)));
       const uint32_t id_even = idesc_fp4(!nvfp4, 0u), id_odd = idesc_fp4(!nvfp4, nvfp4 ? 0u : 2u);
-      const uint32_t id_bf16 = idesc_bf16();
+      const uint32_t id_ext = p.ext_fp8 ? idesc_e4m3() : idesc_bf16();
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.status)) { ok = false; break; }
         acc_phase ^= 1;
@@ -565,8 +590,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         slot + 8 + 8 * (j >> 1), j > 0 ? 1u : acc0, false);
             }
           } else {
+            // 4 MMAs of 32 bytes of K: 16 bf16 or 32 E4M3 elements each
+            if (p.ext_fp8) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) mma_bf16(tmem, da + 2 * j, db + 2 * j, id_bf16, j > 0 ? 1u : acc0);
+              for (int j = 0; j < 4; ++j) mma_e4m3(tmem, da + 2 * j, db + 2 * j, id_ext, j > 0 ? 1u : acc0);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) mma_bf16(tmem, da + 2 * j, db + 2 * j, id_ext, j > 0 ? 1u : acc0);
+            }
           }
           tc_commit(&empty[s]);
           if (++s == STAGES) { s = 0; phase ^= 1; }
@@ -832,7 +863,10 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   p.N = (int)N;
   p.nvfp4 = A.format == FP4_FMT_NVFP4;
   p.k_tiles = g.fp4_part ? (int)cdiv(A.k, 256) : 0;
-  p.ext_tiles = (int)(g.kx / 64);
+  p.ext_fp8 = g.ext_fp8 ? 1 : 0;
+  p.ext_tiles = (int)(g.kx / (g.ext_fp8 ? 128 : 64));
+  p.row_scale = g.row_scale;
+  p.col_scale = g.col_scale;
   p.sf_atoms = p.nvfp4 ? 4 : 2;
   p.ts_a = p.nvfp4 ? A.tensor_scale : nullptr;
   p.ts_b = p.nvfp4 ? B.tensor_scale : nullptr;
@@ -860,8 +894,10 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
     ok &= make_sf_map(&tsb, B.scales, group_bytes, cdiv(N, 128), p.sf_atoms * 4, BN / 128);
   }
   if (g.kx > 0) {
-    ok &= make_map(&tax, g.a_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, M, BM);
-    ok &= make_map(&tbx, g.b_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, N, BN);
+    const CUtensorMapDataType edt = g.ext_fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int eb = g.ext_fp8 ? 1 : 2;
+    ok &= make_map(&tax, g.a_ext, edt, eb, g.kx, M, BM);
+    ok &= make_map(&tbx, g.b_ext, edt, eb, g.kx, N, BN);
   }
   if (!g.fp4_part) {  // residual-only GEMM: no FP4 stages, the maps are never read
     ta = tax;

@@ -189,7 +189,79 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
   }
 }
 
+// E4M3 extra columns: one warp per row of A_ext (rows < M) or B_ext.  The
+// row's values are those of the bf16 tail without 1/alpha (order 2: [dX | X]
+// and [W_hat | dW]; order 1: X and dW; order 0: X and W); the row gets
+// s = amax / 448 and the E4M3 bytes of v / s (nearest, ties to even,
+// saturating, sign kept), zero-padded to kx; all-zero rows get s = 0.
+template <int FMT>
+__global__ void __launch_bounds__(256) gather_fp8_kernel(const uint16_t* __restrict__ x, int64_t ldx,
+                                                         const uint16_t* __restrict__ w, int64_t ldw, fp4_operand xq,
+                                                         fp4_operand wq, const int32_t* __restrict__ hot, int k_hot,
+                                                         int order, int64_t kx, uint8_t* a8, uint8_t* b8, float* sa,
+                                                         float* sb) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nsf_row = xq.k / B, nsf_pad = nsf_padded(xq.k, FMT);
+  const float gx = FMT == FP4_FMT_NVFP4 ? *xq.tensor_scale : 0.0f;
+  const float gw = FMT == FP4_FMT_NVFP4 ? *wq.tensor_scale : 0.0f;
+  const int lane = threadIdx.x & 31;
+  const int ncols = (order == 2 ? 2 : 1) * k_hot;
+  const int64_t rows = xq.rows + wq.rows;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; row < rows; row += nwarps) {
+    const bool is_a = row < xq.rows;
+    const int64_t r = is_a ? row : row - xq.rows;
+    auto value = [&](int j) -> float {
+      const int part = j >= k_hot ? 1 : 0;
+      const int64_t c = hot[j - part * k_hot];
+      if (is_a) {
+        const float xv = bf16_bits_to_float(x[r * ldx + c]);
+        if (order == 2 && part == 0) return __fsub_rn(xv, dequant_elem<FMT>(xq, r, c, gx, nsf_row, nsf_pad));
+        return xv;
+      }
+      const float wv = bf16_bits_to_float(w[r * ldw + c]);
+      if (order == 0) return wv;
+      const float wh = dequant_elem<FMT>(wq, r, c, gw, nsf_row, nsf_pad);
+      if (order == 2 && part == 0) return wh;
+      return __fsub_rn(wv, wh);
+    };
+    float amax = 0.0f;
+    for (int j = lane; j < ncols; j += 32) amax = fmaxf(amax, fabsf(value(j)));
+    amax = warp_max(amax);
+    const float sc = __fdiv_rn(amax, 448.0f);
+    uint8_t* dst = (is_a ? a8 : b8) + r * kx;
+    for (int64_t j0 = 0; j0 < kx; j0 += 128) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = (int)(j0 + 4 * lane + e);
+        uint32_t byte = 0;
+        if (j < ncols && sc > 0.0f) {
+          const float v = value(j);
+          byte = e4m3_rn_satfinite(__fdiv_rn(fabsf(v), sc)) | (signbit(v) ? 0x80u : 0u);
+        }
+        word |= byte << (8 * e);
+      }
+      *reinterpret_cast<uint32_t*>(dst + j0 + 4 * lane) = word;
+    }
+    if (lane == 0) (is_a ? sa : sb)[r] = sc;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_hcp_gather_fp8(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
+                                  const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot, int k_hot,
+                                  int order, int64_t kx, uint8_t* a8, uint8_t* b8, float* sa, float* sb, int num_sms,
+                                  cudaStream_t st) {
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv((xq.rows + wq.rows) * 32, 256),
+                                                               (int64_t)num_sms * 8));
+  if (xq.format == FP4_FMT_MXFP4)
+    gather_fp8_kernel<FP4_FMT_MXFP4><<<grid, 256, 0, st>>>(x, ldx, w, ldw, xq, wq, hot, k_hot, order, kx, a8, b8, sa, sb);
+  else
+    gather_fp8_kernel<FP4_FMT_NVFP4><<<grid, 256, 0, st>>>(x, ldx, w, ldw, xq, wq, hot, k_hot, order, kx, a8, b8, sa, sb);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_hcp_channel_errors(const uint16_t* x, int64_t ldx, const fp4_operand& q, float* err, int num_sms,
                                       cudaStream_t st) {

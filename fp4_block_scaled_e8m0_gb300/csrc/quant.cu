@@ -207,18 +207,42 @@ __global__ void __launch_bounds__(kThreads) amax_rows32_kernel(const void* __res
   block_amax_atomic(m, amax_out, gen);
 }
 
+// Column bitmask of the list hot[0..n) in shared memory (rows up to
+// kZeroSmemCols columns), built by the CTA before use; longer rows search the
+// list per 16 columns instead.
+constexpr int kZeroSmemCols = 65536;
+__device__ __forceinline__ void build_hot_bits(uint32_t* bits, int64_t cols, const int32_t* hot, int n) {
+  const int words = (int)((cols + 31) >> 5);
+  for (int i = threadIdx.x; i < words; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const uint32_t c = (uint32_t)hot[i];
+    if (c < (uint32_t)cols) atomicOr(&bits[c >> 5], 1u << (c & 31));
+  }
+  __syncthreads();
+}
+__device__ __forceinline__ uint32_t hot_bits16(const uint32_t* bits, const int32_t* hot, int n, uint32_t k0) {
+  return bits ? (bits[k0 >> 5] >> (k0 & 31)) & 0xFFFFu : hot_mask16(hot, n, k0);
+}
+
 // amax of x with the ascending columns hot[0..n) left out (16 elements per step)
 template <int DT>
 __global__ void __launch_bounds__(kThreads) amax_zeroed_kernel(const void* __restrict__ x, int64_t ldx, FastDiv nch,
                                                                uint32_t total, const int32_t* __restrict__ hot, int n,
                                                                float* amax_out, uint32_t gen) {
+  extern __shared__ uint32_t zbits_smem[];
+  const uint32_t* bits = nullptr;
+  if ((int64_t)nch.d * 16 <= kZeroSmemCols) {   // uniform over the grid
+    build_hot_bits(zbits_smem, (int64_t)nch.d * 16, hot, n);
+    bits = zbits_smem;
+  }
   float m = 0.0f;
   for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < total; c += gridDim.x * blockDim.x) {
     const uint32_t r = fast_div(c, nch), k0 = (c - r * nch.d) << 4;
     float v[16];
     load8<DT, true>(x, (int64_t)r * ldx + k0, v);
     load8<DT, true>(x, (int64_t)r * ldx + k0 + 8, v + 8);
-    const uint32_t hm = hot_mask16(hot, n, k0);
+    const uint32_t hm = hot_bits16(bits, hot, n, k0);
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       if (!((hm >> j) & 1u)) m = fmaxf(m, fabsf(v[j]));
@@ -314,11 +338,11 @@ __device__ __forceinline__ void clamp_block(float* v, float tau, float* col_coun
 // ZERO: the columns o.zero_idx[0..o.zero_n) are set to 0 before quantizing
 // (hot channels routed around the FP4 operand)
 template <bool ZERO, int B>
-__device__ __forceinline__ void zero_block(float* v, const QuantOut& o, uint32_t k0) {
+__device__ __forceinline__ void zero_block(float* v, const QuantOut& o, const uint32_t* bits, uint32_t k0) {
   if constexpr (ZERO) {
 #pragma unroll
     for (int h = 0; h < B / 16; ++h) {
-      const uint32_t m = hot_mask16(o.zero_idx, o.zero_n, k0 + 16 * h);
+      const uint32_t m = hot_bits16(bits, o.zero_idx, o.zero_n, k0 + 16 * h);
       if (m) {
 #pragma unroll
         for (int j = 0; j < 16; ++j)
@@ -336,6 +360,13 @@ __global__ void __launch_bounds__(kThreads) quant_rows32_kernel(const void* __re
   const float tau = CLAMP ? *o.clamp : 0.0f;
   extern __shared__ uint32_t counts_smem[];
   uint32_t* counts_s = nullptr;
+  uint32_t* zero_bits = nullptr;
+  if constexpr (ZERO) {
+    if (o.out_cols <= kZeroSmemCols) {   // uniform over the grid
+      zero_bits = counts_smem;
+      build_hot_bits(zero_bits, o.out_cols, o.zero_idx, o.zero_n);
+    }
+  }
   if constexpr (CLAMP) {
     if (o.col_counts && o.out_cols <= kClampSmemCols) {   // uniform over the grid
       counts_s = counts_smem;
@@ -366,8 +397,8 @@ __global__ void __launch_bounds__(kThreads) quant_rows32_kernel(const void* __re
     }
     clamp_block<CLAMP, B>(v, tau, o.col_counts, counts_s, k0);
     if (two) clamp_block<CLAMP, B>(w, tau, o.col_counts, counts_s, k2);
-    zero_block<ZERO, B>(v, o, k0);
-    if (two) zero_block<ZERO, B>(w, o, k2);
+    zero_block<ZERO, B>(v, o, zero_bits, k0);
+    if (two) zero_block<ZERO, B>(w, o, zero_bits, k2);
     if (rht) {
 #pragma unroll
       for (int h = 0; h < B / 16; ++h) rht16(v + 16 * h, o.rht_signs);
@@ -1430,9 +1461,10 @@ cudaError_t launch_quant_rows_zeroed(const void* x, int dt, int64_t rows, int64_
   const FastDiv fd = make_fastdiv((uint32_t)nblk);
   const int contiguous = ldx == cols;
   const bool plain = o.rounding == FP4_ROUND_RTN && !o.rht;
+  const size_t smem = cols <= kZeroSmemCols ? sizeof(uint32_t) * (size_t)cdiv(cols, 32) : 0;
   FP4_DISPATCH_FMT(fmt, FMT, FP4_DISPATCH_DT(dt, DT,
-    if (plain) quant_rows32_kernel<FMT, DT, true, false, true><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o);
-    else quant_rows32_kernel<FMT, DT, false, false, true><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o)));
+    if (plain) quant_rows32_kernel<FMT, DT, true, false, true><<<grid, kThreads, smem, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o);
+    else quant_rows32_kernel<FMT, DT, false, false, true><<<grid, kThreads, smem, st>>>(x, ldx, fd, (uint32_t)total, contiguous, o)));
   return cudaGetLastError();
 }
 
@@ -1443,8 +1475,9 @@ cudaError_t launch_amax_zeroed(const void* x, int dt, int64_t rows, int64_t cols
   if (total >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   const int grid = grid_for(total, kThreads, num_sms);
   const FastDiv fd = make_fastdiv((uint32_t)nch);
-  FP4_DISPATCH_DT(dt, DT, amax_zeroed_kernel<DT><<<grid, kThreads, 0, st>>>(x, ldx, fd, (uint32_t)total, hot, n,
-                                                                           amax_out, gen));
+  const size_t smem = cols <= kZeroSmemCols ? sizeof(uint32_t) * (size_t)cdiv(cols, 32) : 0;
+  FP4_DISPATCH_DT(dt, DT, amax_zeroed_kernel<DT><<<grid, kThreads, smem, st>>>(x, ldx, fd, (uint32_t)total, hot, n,
+                                                                              amax_out, gen));
   return cudaGetLastError();
 }
 

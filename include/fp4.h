@@ -72,7 +72,7 @@ enum { FP4_ROUND_RTN = 0, FP4_ROUND_SR = 1 };            /* [outlier] §4.1 */
 enum { FP4_SCALING_1D = 0, FP4_SCALING_2D = 1 };         /* [outlier] §4.1 */
 enum { FP4_SF_ROWMAJOR = 0, FP4_SF_MMA = 1 };
 enum { FP4_DTYPE_BF16 = 0, FP4_DTYPE_F32 = 1 };
-enum { FP4_HCP_SINGLE = 0, FP4_HCP_TWO = 1 };            /* [outlier] §3.1 */
+enum { FP4_HCP_SINGLE = 0, FP4_HCP_TWO = 1, FP4_HCP_TWO_FP8 = 2 };  /* [outlier] §3.1 */
 
 typedef struct fp4_ctx fp4_ctx;
 
@@ -320,7 +320,11 @@ int fp4_hcp_quantize_zeroed(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_
  *  order 0 = hot channels zeroed: xq from fp4_hcp_quantize_zeroed, A_ext = X_H,
  *  B_ext = W_H / alpha, so Y = alpha Q(X_0) W_hat^T + X_H W_H^T).
  * mode FP4_HCP_SINGLE: one kernel, FP4 K-steps then bf16 K-steps into one
- * TMEM accumulator; FP4_HCP_TWO: the FP4 GEMM, then a bf16 GEMM with C +=.
+ * TMEM accumulator; FP4_HCP_TWO: the FP4 GEMM, then a bf16 GEMM with C +=;
+ * FP4_HCP_TWO_FP8: the FP4 GEMM, then an E4M3 GEMM (tcgen05 kind::f8f6f4)
+ * over the same columns without the 1/alpha, each row of A_ext and B_ext
+ * scaled by its own fp32 amax/448 ([msr] §六 runs its compensation in FP8):
+ * C += s_A[m] s_B[n] sum_j a8[m,j] b8[n,j].
  * X (M x K) and W (N x K) bf16 with pitches ldx, ldw; xq, wq their
  * quantizations (FP4_SF_MMA).  Workspace: fp4_hcp_workspace_bytes().       */
 size_t fp4_hcp_workspace_bytes(int64_t m, int64_t n, int32_t k_hot, int32_t order);

@@ -144,3 +144,36 @@ def test_hcp_zeroed_gemm_matches_oracle(fmt, mode, out_dtype):
     xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
     y2 = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, hot_d, h, mode, 2, torch.float32).cpu().numpy()
     assert np.abs(got - exact).sum() < np.abs(y2 - exact).sum() * 1.5
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+@pytest.mark.parametrize("order", [0, 1, 2])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_hcp_fp8_tail_matches_oracle(fmt, order, out_dtype):
+    # E4M3 extra columns (tcgen05 kind::f8f6f4) with per-row scales, added by a
+    # second GEMM; the oracle uses the same E4M3 values, so the GEMM bound holds
+    xt, wt, xn, wn, _ = _data(fmt, seed=6)
+    K = xn.shape[1]
+    h = fp4.hcp_num_hot(K)
+    cx, sx, gx = o.quantize(xn, FMT[fmt])
+    hot = o.hcp_select(xn, cx, sx, FMT[fmt], gx, h)
+    hot_d = torch.from_numpy(hot.astype(np.int32)).cuda()
+    if order == 0:
+        xq = fp4.fp4_hcp_quantize_zeroed(xt.cuda(), fp4.quant_params(fmt), hot_d, h)
+        cx, sx, gx = o.quantize(o.hcp_zero_columns(xn, hot), FMT[fmt])
+    else:
+        xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
+    wq = fp4.fp4_quantize(wt.cuda(), fp4.quant_params(fmt))
+    cw, sw, gw = o.quantize(wn, FMT[fmt])
+    y = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, hot_d, h, fp4.FP4_HCP_TWO_FP8, order, out_dtype)
+    got = y.float().cpu().numpy().astype(np.float64)
+    yref, bound = o.hcp_gemm_fp8(xn, cx, sx, wn, cw, sw, FMT[fmt], gx, gw, hot, order)
+    tol = o.gemm_tolerance(bound, yref, out_dtype == torch.bfloat16)
+    if out_dtype == torch.bfloat16:
+        tol = tol + 2.0 ** -8 * np.abs(yref)          # the base result is rounded to bf16 once more
+    err = np.abs(got - yref)
+    assert np.all(err <= tol), f"{(err > tol).sum()} outside; worst {np.max(err - tol)}"
+    # the FP8 tail does compensate: closer to the unquantized product than plain FP4
+    exact = xn.astype(np.float64) @ wn.astype(np.float64).T
+    y0 = fp4.fp4_gemm(xq, wq, torch.float32).cpu().numpy()
+    assert np.abs(got - exact).sum() < np.abs(y0 - exact).sum()
