@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--cpu-sample", default="512x704", help="MxN rows of the CPU-baseline sample (K stays 2048)")
     ap.add_argument("--ext-launches", type=int, default=20,
                     help="timed launches of each op outside the step (0: skip them)")
+    ap.add_argument("--ext-only", action="store_true",
+                    help="run only the ops outside the step (one warm-up step first) and print their JSON")
     return ap.parse_args()
 
 
@@ -502,6 +504,13 @@ def main():
     for i in range(args.warmup):
         step.run(i)
     torch.cuda.synchronize()
+    if args.ext_only:
+        if args.warmup < 1:
+            step.run(0)
+        ext = time_extensions(fp4, step, dev, flush, max(args.ext_launches, 1), peaks())
+        if rank == 0:
+            print(json.dumps({"extensions": ext}), flush=True)
+        return
 
     names = list(OPS)
     ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
