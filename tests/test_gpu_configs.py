@@ -230,3 +230,110 @@ def test_hcp_square_full():
     for y, label in ((y1, "single"), (y2, "two")):
         got = y.cpu().numpy()[rows].astype(np.float64)
         assert np.all(np.abs(got - yr) <= 1e-3 * bound), label
+
+
+def test_hcp_square_variants_full():
+    """Hot channels zeroed (single kernel) and the E4M3 residual GEMM, at the bench's size."""
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    d = inputs.hcp_square()
+    X, W = d["X"].cuda(), d["W"].cuda()
+    M, K = X.shape
+    h = fp4.hcp_num_hot(K)
+    qx = fp4.fp4_quantize(X, fp4.quant_params(NV))
+    qw = fp4.fp4_quantize(W, fp4.quant_params(NV))
+    hot = fp4.fp4_hcp_select(X, qx, h)
+    hot_np = hot.cpu().numpy()
+    x0q = fp4.fp4_hcp_quantize_zeroed(X, fp4.quant_params(NV), hot, h)
+    y0 = fp4.fp4_hcp_gemm(X, W, x0q, qw, hot, h, fp4.FP4_HCP_SINGLE, 0, torch.bfloat16)
+    y8 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot, h, fp4.FP4_HCP_TWO_FP8, 2, torch.bfloat16)
+    xfull = d["X"].float().numpy()
+    # the zeroed tensor's scale from the whole tensor
+    x0 = o.hcp_zero_columns(xfull, hot_np)
+    g0 = o.nvfp4_tensor_scale(o.tensor_amax(x0))
+    assert np.float32(x0q.tensor_scale.cpu().numpy()[0]).view(np.uint32) == np.float32(g0).view(np.uint32)
+    rows = _sample_rows(M, 3, 8)
+    wn = d["W"].float().numpy()
+    cw = qw.codes.cpu().numpy()
+    sw = untile_scales(qw.scales.cpu().numpy(), W.shape[0], K // 16)
+    gw = qw.tensor_scale.cpu().numpy()[0]
+    # zeroed: codes of the sampled rows bit-exact, then the GEMM bound
+    wc, ws, _ = o.quantize(x0[rows], o.NVFP4, given_amax=o.tensor_amax(x0))
+    c0 = x0q.codes.cpu().numpy()[rows]
+    s0 = untile_scales(x0q.scales.cpu().numpy(), M, K // 16)[rows]
+    assert np.array_equal(c0, wc) and np.array_equal(s0, ws)
+    y, bound = o.gemm(c0, s0, cw, sw, o.NVFP4, g0, gw)
+    a_ext, b_ext = o.hcp_zeroed_operands(xfull[rows], wn, o.NVFP4, g0, gw, hot_np)
+    alpha32 = float(np.float32(np.float32(g0) * np.float32(gw)))
+    y = y + alpha32 * (a_ext.astype(np.float64) @ b_ext.astype(np.float64).T)
+    bound = bound + alpha32 * (np.abs(a_ext.astype(np.float64)) @ np.abs(b_ext.astype(np.float64)).T)
+    got = y0.float().cpu().numpy()[rows].astype(np.float64)
+    assert np.all(np.abs(got - y) <= o.gemm_tolerance(bound, y, True)), "zeroed"
+    # E4M3 residual (two kernels, order 2)
+    cx = qx.codes.cpu().numpy()[rows]
+    sx = untile_scales(qx.scales.cpu().numpy(), M, K // 16)[rows]
+    gx = qx.tensor_scale.cpu().numpy()[0]
+    yr, bound = o.hcp_gemm_fp8(xfull[rows], cx, sx, wn, cw, sw, o.NVFP4, gx, gw, hot_np, 2)
+    got = y8.float().cpu().numpy()[rows].astype(np.float64)
+    tol = o.gemm_tolerance(bound, yr, True) + 2.0 ** -8 * np.abs(yr)
+    assert np.all(np.abs(got - yr) <= tol), "fp8"
+
+
+def test_occ_full():
+    """Outlier clamping and compensation at the bench's size (X 16384x4096, W 4096^2, NVFP4)."""
+    import bench
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    d = inputs.hcp_square(bench.OCC_M, bench.OCC_K, bench.OCC_N)
+    X, W = d["X"].cuda(), d["W"].cuda()
+    M, K = X.shape
+    tau, n_out = fp4.fp4_occ_threshold(X)
+    counts = torch.empty((K,), dtype=torch.float32, device="cuda")
+    xq = fp4.fp4_occ_quantize(X, fp4.quant_params(NV), tau, col_counts=counts)
+    wq = fp4.fp4_quantize(W, fp4.quant_params(NV))
+    y = fp4.fp4_occ_gemm(X, W, xq, wq, tau, counts, bench.OCC_DENSE, fp4.fp4_occ_max_outliers(M, K))
+    assert fp4.fp4_sync_status() == 0
+    xfull = d["X"].float().numpy()
+    a = np.abs(xfull).reshape(-1)
+    rank = int(np.ceil(0.99 * a.size))
+    t = np.float32(np.partition(a, rank - 1)[rank - 1])       # the nearest-rank order statistic
+    assert tau.item() == float(t)
+    out = np.abs(xfull) > t
+    assert n_out.item() == int(out.sum())
+    assert np.array_equal(counts.cpu().numpy(), out.sum(axis=0).astype(np.float32))
+    rows = _sample_rows(M, 3, 9)
+    xc, dx = o.occ_split(xfull[rows], t)
+    wc, ws, _ = o.quantize(xc, o.NVFP4, given_amax=t)
+    c = xq.codes.cpu().numpy()[rows]
+    s = untile_scales(xq.scales.cpu().numpy(), M, K // 16)[rows]
+    assert np.array_equal(c, wc) and np.array_equal(s, ws)
+    g = xq.tensor_scale.cpu().numpy()[0]
+    wn = d["W"].float().numpy()
+    cw = wq.codes.cpu().numpy()
+    sw = untile_scales(wq.scales.cpu().numpy(), W.shape[0], K // 16)
+    gw = wq.tensor_scale.cpu().numpy()[0]
+    yr, bound = o.gemm(c, s, cw, sw, o.NVFP4, g, gw)
+    dxf = dx.astype(np.float64)
+    comp = np.abs(dxf) @ np.abs(wn.astype(np.float64)).T
+    yr = yr + dxf @ wn.astype(np.float64).T
+    tol = 1e-3 * (bound + comp) + 2.0 ** -8 * comp + 2.0 ** -8 * (np.abs(yr) + comp)
+    got = y.float().cpu().numpy()[rows].astype(np.float64)
+    assert np.all(np.abs(got - yr) <= tol)
+
+
+@pytest.mark.parametrize("fmt", [NV, MX])
+def test_block_sizes_full(fmt):
+    """Blocks of 16-128 on the step's X (8192 x 2048), sampled rows bit-exact."""
+    from fp4_block_scaled_e8m0_gb300 import inputs
+    x = inputs.llama1b_mlp_up()["X"]
+    xn = x.float().numpy()
+    rows = _sample_rows(x.shape[0], 4, 10)
+    g = o.nvfp4_tensor_scale(o.tensor_amax(xn)) if fmt == NV else None
+    for block in (16, 32, 64, 128):
+        p = fp4.quant_params(fmt, sf_layout=fp4.FP4_SF_ROWMAJOR, block=block)
+        q = fp4.fp4_quantize(x.cuda(), p)
+        wc, ws, _ = o.quantize(xn[rows], OF[fmt], block=block, given_amax=o.tensor_amax(xn))
+        nsf = x.shape[1] // block
+        sc = q.scales.cpu().numpy()[: x.shape[0] * nsf].reshape(x.shape[0], nsf)[rows]
+        assert np.array_equal(sc, ws), block
+        assert np.array_equal(q.codes.cpu().numpy()[rows], wc), block
+        if g is not None:
+            assert np.float32(q.tensor_scale.cpu().numpy()[0]).view(np.uint32) == np.float32(g).view(np.uint32)
