@@ -248,33 +248,39 @@ __global__ void __launch_bounds__(256) occ_tail_kernel(const void* __restrict__ 
   }
 }
 
-// W [N][K] (pitch ldw) -> WT [K][ldt], 64 x 64 tiles through shared memory,
-// reads and writes as bf16 pairs (32-bit accesses; rows of both are 16-byte
-// aligned and k, ldt even)
+// W [N][K] (pitch ldw) -> WT [K][ldt], 64 x 64 tiles through shared memory:
+// 16-byte reads along k (8 bf16 of one W row) and 16-byte writes along n (8 bf16
+// of one W^T row, gathered from a tile column); W rows are 16-byte aligned,
+// k % 32 == 0, ldt % 8 == 0.
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ w, int64_t ldw, int64_t n,
                                                              int64_t k, uint16_t* __restrict__ wt, int64_t ldt) {
-  __shared__ uint16_t tile[64][66];
+  __shared__ uint16_t tile[64][72];   // 144-byte rows: 16-byte aligned, staggered banks
   const int64_t tiles_k = cdiv(k, 64), tiles = cdiv(n, 64) * tiles_k;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    const int64_t n0 = (t / tiles_k) * 64, k0 = (t % tiles_k) * 64;
-    for (int r = ty; r < 64; r += 8) {
-      const int64_t nn = n0 + r, kk = k0 + 2 * tx;
-      uint32_t v = 0;
-      if (nn < n) {
-        if (kk + 1 < k) v = *reinterpret_cast<const uint32_t*>(w + nn * ldw + kk);
-        else if (kk < k) v = w[nn * ldw + kk];
-      }
-      tile[r][2 * tx] = (uint16_t)v;
-      tile[r][2 * tx + 1] = (uint16_t)(v >> 16);
+  const int t = threadIdx.x;
+  for (int64_t tt = blockIdx.x; tt < tiles; tt += gridDim.x) {
+    const int64_t n0 = (tt / tiles_k) * 64, k0 = (tt % tiles_k) * 64;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {                 // 512 chunks of 8: row r, k chunk kc
+      const int idx = t + 256 * i, r = idx >> 3, kc = (idx & 7) * 8;
+      const int64_t nn = n0 + r, kk = k0 + kc;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (nn < n && kk < k) v = __ldg(reinterpret_cast<const uint4*>(w + nn * ldw + kk));   // k % 8 == 0
+      *reinterpret_cast<uint4*>(&tile[r][kc]) = v;
     }
     __syncthreads();
-    for (int r = ty; r < 64; r += 8) {
-      const int64_t kk = k0 + r, nn = n0 + 2 * tx;
-      if (kk < k) {
-        const uint32_t v = tile[2 * tx][r] | ((uint32_t)tile[2 * tx + 1][r] << 16);
-        if (nn + 1 < n) *reinterpret_cast<uint32_t*>(wt + kk * ldt + nn) = v;
-        else if (nn < n) wt[kk * ldt + nn] = (uint16_t)v;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {                 // 512 chunks of 8: W^T row c (= k), n chunk nc
+      const int idx = t + 256 * i, c = idx >> 3, nc = (idx & 7) * 8;
+      const int64_t kk = k0 + c, nn = n0 + nc;
+      if (kk < k && nn < n) {
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) q[j] = tile[nc + 2 * j][c] | ((uint32_t)tile[nc + 2 * j + 1][c] << 16);
+        if (nn + 8 <= n) {
+          *reinterpret_cast<uint4*>(wt + kk * ldt + nn) = make_uint4(q[0], q[1], q[2], q[3]);
+        } else {
+          for (int j = 0; j < 8 && nn + j < n; ++j) wt[kk * ldt + nn + j] = (uint16_t)(q[j >> 1] >> (16 * (j & 1)));
+        }
       }
     }
     __syncthreads();
@@ -292,10 +298,24 @@ struct OccEntry {
 // outliers, as in the clamp).
 __device__ __forceinline__ uint32_t halves_to_bits(uint32_t m) { return (m & 1u) | ((m >> 15) & 2u); }
 
+__device__ __forceinline__ uint32_t outlier_mask8_bits(const uint4& u, uint32_t tau2) {
+  const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+  uint32_t mask = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t a = q[j] & 0x7FFF7FFFu;
+    const uint32_t m = __vcmpgtu2(a, tau2) & ~__vcmpgtu2(a, 0x7F807F80u);
+    mask |= halves_to_bits(m) << (2 * j);
+  }
+  return mask;
+}
+
 template <int XDT>
 __device__ __forceinline__ uint32_t outlier_mask8(const void* x, int64_t off, float tau, uint32_t tau2) {
   if constexpr (XDT == FP4_DTYPE_BF16) {
-    const uint4 u = ld_nc_v4_l1(static_cast<const uint16_t*>(x) + off);
+    // a plain read-only load (not volatile asm), so that the compiler can put
+    // the loads of all the row's chunks in flight before the masks
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off));
     const uint32_t q[4] = {u.x, u.y, u.z, u.w};
     uint32_t mask = 0;
 #pragma unroll
@@ -348,7 +368,25 @@ __global__ void __launch_bounds__(256) occ_extract_kernel(const void* __restrict
     uint32_t mine = 0;
     uint32_t mk[4] = {0u, 0u, 0u, 0u};
     if (active) {
-      if (short_row) {
+      if (short_row && XDT == FP4_DTYPE_BF16) {
+        // all 16 chunk loads of the row in flight, then the masks
+        uint4 raw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int64_t c0 = 256 * i + 8 * lane;
+          raw[i] = c0 < cols ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + r * ldx + c0))
+                             : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int64_t c0 = 256 * i + 8 * lane;
+          uint32_t m = outlier_mask8_bits(raw[i], tau2);
+          if (m && tail && c0 < cols) m &= ~((dense[c0 >> 5] >> (c0 & 31)) & 0xFFu);
+          mk[i >> 2] |= m << (8 * (i & 3));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mine += __popc(mk[i]);
+      } else if (short_row) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int64_t c0 = 256 * i + 8 * lane;

@@ -1073,17 +1073,29 @@ __device__ __forceinline__ int soft_window_start(float a) {
   return 7 + above - W;
 }
 
+// Terms of the 7 negative thresholds -c_p (all below a = |xs| >= 0): the
+// exponent of each is beta (a + c_p), so t = e^(-beta a) e^(-beta c_p) -- one ex2
+// per element and a launch constant kneg[p] = e^(-beta c_p) per threshold
+// instead of one ex2 per term.  The exponent's rounding is of the same order as
+// in the direct form (both carry beta (a + c_p)).  Used when all 14 thresholds
+// are evaluated (W = 0).
+struct SoftNegConst {
+  float kneg[7];   // e^(-beta c_p), c_p = 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5
+};
+
 // Q_soft'(xs); nbl = -beta log2(e)
 template <int W>
-__device__ __forceinline__ float soft_grad(float xs, float beta, float nbl, const SoftTable* tab) {
+__device__ __forceinline__ float soft_grad(float xs, float beta, float nbl, const SoftTable* tab,
+                                           const SoftNegConst& kc) {
   const float a = fabsf(xs);
   constexpr int n = W == 0 ? 14 : 2 * W;
   const int i0 = W == 0 ? 0 : soft_window_start<W>(a);
+  const float ea = W == 0 ? ex2_approx(a * nbl) : 0.0f;
   float num = 0.0f, den = 1.0f;
 #pragma unroll
   for (int m = 0; m < n; ++m) {
     const float2 e = soft_term<W>(tab, i0, m);
-    const float t = ex2_approx(fabsf(a - e.x) * nbl);
+    const float t = (W == 0 && m < 7) ? ea * kc.kneg[6 - m] : ex2_approx(fabsf(a - e.x) * nbl);
     const float w = fmaf(t, t + 2.0f, 1.0f);              // (1 + t)^2
     num = fmaf(num, w, e.y * t * den);
     den *= w;
@@ -1093,16 +1105,17 @@ __device__ __forceinline__ float soft_grad(float xs, float beta, float nbl, cons
 
 // Q_soft(xs)
 template <int W>
-__device__ __forceinline__ float soft_value(float xs, float nbl, const SoftTable* tab) {
+__device__ __forceinline__ float soft_value(float xs, float nbl, const SoftTable* tab, const SoftNegConst& kc) {
   const float a = fabsf(xs);
   constexpr int n = W == 0 ? 14 : 2 * W;
   const int i0 = W == 0 ? 0 : soft_window_start<W>(a);
+  const float ea = W == 0 ? ex2_approx(a * nbl) : 0.0f;
   float acc = W == 0 ? -6.0f : tab->q[i0];                // the level below the window
 #pragma unroll
   for (int m = 0; m < n; ++m) {
     const float2 e = soft_term<W>(tab, i0, m);
     const float d = a - e.x;
-    const float t = ex2_approx(fabsf(d) * nbl);
+    const float t = (W == 0 && m < 7) ? ea * kc.kneg[6 - m] : ex2_approx(fabsf(d) * nbl);
     acc = fmaf(e.y, __fdividef(d >= 0.0f ? 1.0f : t, 1.0f + t), acc);
   }
   return xs < 0.0f ? -acc : acc;
@@ -1125,17 +1138,19 @@ struct DgeOp {
 template <int W>
 struct SoftGradOp {
   float beta, nbl;
+  SoftNegConst kc;
   static constexpr bool kTable = W != 0, kScale = false, kDy = true;
   __device__ float operator()(float xs, float, float d, const SoftTable* tab) const {
-    return d * soft_grad<W>(xs, beta, nbl, tab);
+    return d * soft_grad<W>(xs, beta, nbl, tab, kc);
   }
 };
 template <int W>
 struct SoftValueOp {
   float nbl;
+  SoftNegConst kc;
   static constexpr bool kTable = W != 0, kScale = true, kDy = false;
   __device__ float operator()(float xs, float s, float, const SoftTable* tab) const {
-    return s * soft_value<W>(xs, nbl, tab);
+    return s * soft_value<W>(xs, nbl, tab, kc);
   }
 };
 
@@ -1241,6 +1256,12 @@ __global__ void __launch_bounds__(256) error_stats_kernel(const void* __restrict
   const bool occ = tau_p != nullptr;
   const float tau = occ ? *tau_p : 0.0f;
   const int64_t units_row = q.k / 16, total = q.rows * units_row;
+  SoftNegConst kc;
+  if constexpr (SOFT) {
+    const float cp[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+#pragma unroll
+    for (int i = 0; i < 7; ++i) kc.kneg[i] = ex2_approx(nbl * cp[i]);
+  }
   double sxx = 0.0, shh = 0.0, sxh = 0.0, see = 0.0;
   for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < total; u += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = u / units_row, c0 = (u - r * units_row) * 16;
@@ -1259,7 +1280,7 @@ __global__ void __launch_bounds__(256) error_stats_kernel(const void* __restrict
         mult = s == 0.0f ? 0.0f : __frcp_rn(s);
       }
 #pragma unroll
-      for (int e = 0; e < 16; ++e) h32[e] = s * soft_value<0>(__fmul_rn(v[e], mult), nbl, nullptr);
+      for (int e = 0; e < 16; ++e) h32[e] = s * soft_value<0>(__fmul_rn(v[e], mult), nbl, nullptr, kc);
     } else {
       const float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
       const uint2 cw = *reinterpret_cast<const uint2*>(q.codes + r * (q.k >> 1) + (c0 >> 1));
@@ -1649,12 +1670,20 @@ int soft_window(float beta) {
   return beta >= 38.82f ? 1 : beta >= 19.41f ? 2 : beta >= 9.71f ? 4 : 0;
 }
 
+static SoftNegConst soft_neg_const(float nbl) {
+  static const float c[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+  SoftNegConst k;
+  for (int p = 0; p < 7; ++p) k.kneg[p] = exp2f(nbl * c[p]);
+  return k;
+}
+
 cudaError_t launch_soft(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
                         int64_t lddy, float* out, int64_t ldo, float beta, int num_sms, cudaStream_t st) {
   const float nbl = -beta * 1.4426950408889634f;  // -beta log2(e)
-#define FP4_SOFT_LAUNCH(W)                                                                                   \
-  return dy ? launch_scaled_map(x, xdt, ldx, q, dy, dydt, lddy, out, ldo, SoftGradOp<W>{beta, nbl}, num_sms, st) \
-            : launch_scaled_map(x, xdt, ldx, q, nullptr, 0, 0, out, ldo, SoftValueOp<W>{nbl}, num_sms, st)
+  const SoftNegConst kc = soft_neg_const(nbl);
+#define FP4_SOFT_LAUNCH(W)                                                                                         \
+  return dy ? launch_scaled_map(x, xdt, ldx, q, dy, dydt, lddy, out, ldo, SoftGradOp<W>{beta, nbl, kc}, num_sms, st) \
+            : launch_scaled_map(x, xdt, ldx, q, nullptr, 0, 0, out, ldo, SoftValueOp<W>{nbl, kc}, num_sms, st)
   switch (soft_window(beta)) {
     case 1: FP4_SOFT_LAUNCH(1);
     case 2: FP4_SOFT_LAUNCH(2);
