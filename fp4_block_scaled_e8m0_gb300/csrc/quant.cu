@@ -1154,11 +1154,17 @@ struct SoftValueOp {
   }
 };
 
+// Work unit: 8 consecutive elements of a row (16 bytes of bf16 x), so that the
+// lanes of a warp read and write contiguous memory; the unit's block scale is
+// looked up per unit (the lanes of one block read the same byte).  U units per
+// thread per iteration keep their loads in flight together.
+constexpr int kMapUnits = 2;
 template <int FMT, int XDT, int DYDT, class Op>
 __global__ void __launch_bounds__(kThreads) scaled_map_kernel(const void* __restrict__ x, int64_t ldx, fp4_operand q,
                                                               const void* __restrict__ dy, int64_t lddy, float* out,
-                                                              int64_t ldo, Op op, FastDiv nsf_div) {
+                                                              int64_t ldo, Op op, FastDiv upr_div) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  constexpr int U = kMapUnits;
   __shared__ SoftTable tab_s;
   const SoftTable* tab = &tab_s;
   if constexpr (Op::kTable) {
@@ -1170,67 +1176,59 @@ __global__ void __launch_bounds__(kThreads) scaled_map_kernel(const void* __rest
   }
   const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
   const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
-  const int64_t total = q.rows * nsf_row;
-  const bool small = total < (int64_t(1) << 31);  // 32-bit block ids, multiply-shift division
-  auto split = [&](int64_t blk, int64_t& r, int64_t& j) {
+  const int64_t upr = q.k / 8, total = q.rows * upr;
+  const bool small = total < (int64_t(1) << 31);  // 32-bit unit ids, multiply-shift division
+  auto split = [&](int64_t u, int64_t& r, int64_t& c0) {
     if (small) {
-      const uint32_t r32 = fast_div((uint32_t)blk, nsf_div);
+      const uint32_t r32 = fast_div((uint32_t)u, upr_div);
       r = r32;
-      j = (uint32_t)blk - r32 * nsf_div.d;
+      c0 = (int64_t)((uint32_t)u - r32 * upr_div.d) * 8;
     } else {
-      r = blk / nsf_row;
-      j = blk - r * nsf_row;
-    }
-  };
-  // xs = x * mult; s the block scale (computed only for ops that use it)
-  auto scale = [&](int64_t r, int64_t j, float& mult, float& s) {
-    const uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
-    if (FMT == FP4_FMT_MXFP4) {
-      mult = e8m0_inv_scale(sb);
-      s = Op::kScale ? e8m0_scale(sb) : 0.0f;
-    } else {
-      s = __fmul_rn(e4m3_decode(sb), g);
-      mult = s == 0.0f ? 0.0f : __frcp_rn(s);
-    }
-  };
-  auto finish = [&](const float* v, const float* d, int64_t r, int64_t j) {
-    float mult, s;
-    scale(r, j, mult, s);
-#pragma unroll
-    for (int q8 = 0; q8 < B / 8; ++q8) {
-      float o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = op(__fmul_rn(v[8 * q8 + e], mult), s, d[8 * q8 + e], tab);
-      float4* dst = reinterpret_cast<float4*>(out + r * ldo + j * B + 8 * q8);
-      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-    }
-  };
-  auto load = [&](int64_t r, int64_t j, float* v, float* d) {
-#pragma unroll
-    for (int q8 = 0; q8 < B / 8; ++q8) {
-      load8<XDT>(x, r * ldx + j * B + 8 * q8, v + 8 * q8);
-      if constexpr (DYDT >= 0) {
-        load8<DYDT>(dy, r * lddy + j * B + 8 * q8, d + 8 * q8);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) d[8 * q8 + e] = 0.0f;
-      }
+      r = u / upr;
+      c0 = (u - r * upr) * 8;
     }
   };
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  // two blocks per iteration: both blocks' x and dy loads are in flight together
-  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total; blk += 2 * stride) {
-    const int64_t blk2 = blk + stride;
-    const bool two = blk2 < total;
-    int64_t r, j, r2 = 0, j2 = 0;
-    split(blk, r, j);
-    if (two) split(blk2, r2, j2);
-    float v[B], d[B], v2[B], d2[B];
-    load(r, j, v, d);
-    if (two) load(r2, j2, v2, d2);
-    finish(v, d, r, j);
-    if (two) finish(v2, d2, r2, j2);
+  for (int64_t u0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u0 < total; u0 += U * stride) {
+    int64_t r[U], c0[U];
+    bool act[U];
+    float v[U][8], d[U][8];
+    uint32_t sb[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int64_t u = u0 + i * stride;
+      act[i] = u < total;
+      r[i] = 0;
+      c0[i] = 0;
+      if (act[i]) split(u, r[i], c0[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      if (act[i]) {
+        load8<XDT>(x, r[i] * ldx + c0[i], v[i]);
+        if constexpr (DYDT >= 0) load8<DYDT>(dy, r[i] * lddy + c0[i], d[i]);
+        sb[i] = q.scales[sf_offset(q.sf_layout, r[i], c0[i] / B, nsf_row, nsf_pad)];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      if (!act[i]) continue;
+      // xs = x * mult exactly as the quantizer formed it; s the block scale
+      float mult, sv;
+      if (FMT == FP4_FMT_MXFP4) {
+        mult = e8m0_inv_scale(sb[i]);
+        sv = Op::kScale ? e8m0_scale(sb[i]) : 0.0f;
+      } else {
+        sv = __fmul_rn(e4m3_decode(sb[i]), g);
+        mult = sv == 0.0f ? 0.0f : __frcp_rn(sv);
+      }
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = op(__fmul_rn(v[i][e], mult), sv, DYDT >= 0 ? d[i][e] : 0.0f, tab);
+      float4* dst = reinterpret_cast<float4*>(out + r[i] * ldo + c0[i]);
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
   }
 }
 
@@ -1639,11 +1637,10 @@ cudaError_t launch_rht16(const void* x, int dt, int64_t rows, int64_t cols, int6
 template <class Op>
 cudaError_t launch_scaled_map(const void* x, int xdt, int64_t ldx, const fp4_operand& q, const void* dy, int dydt,
                               int64_t lddy, float* out, int64_t ldo, const Op& op, int num_sms, cudaStream_t st) {
-  int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
-  int64_t total = q.rows * (q.k / B);
+  const int64_t total = q.rows * (q.k / 8);   // 8-element units
   if (total == 0) return cudaSuccess;
-  const int grid = grid_for(cdiv(total, 2), kThreads, num_sms);
-  const FastDiv fd = make_fastdiv((uint32_t)std::min<int64_t>(q.k / B, 0x7FFFFFFF));
+  const int grid = grid_for(cdiv(total, kMapUnits), kThreads, num_sms);
+  const FastDiv fd = make_fastdiv((uint32_t)std::min<int64_t>(q.k / 8, 0x7FFFFFFF));
   FP4_DISPATCH_FMT(q.format, FMT, FP4_DISPATCH_DT(xdt, XDT,
     if constexpr (!Op::kDy)
       scaled_map_kernel<FMT, XDT, -1, Op><<<grid, kThreads, 0, st>>>(x, ldx, q, dy, lddy, out, ldo, op, fd);
