@@ -770,8 +770,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           warp_exchange_hi3(pk, lane);
           store_exchanged_bf16x2(p, pk, row0, colw, lane);
         }
+      } else if (!p.accumulate) {
+        // fp32 out: both halves in registers, release, then exchange and store
+        // each (the accumulator is free for the next tile's MMAs meanwhile)
+        uint32_t r2[2][32];
+        tmem_ld32_nowait(taddr, r2[0]);
+        tmem_ld32_nowait(taddr + 32, r2[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+        if (any) {
+          warp_exchange_hi3(r2[0], lane);
+          store_exchanged(p, r2[0], row0, colw, alpha, lane);
+          warp_exchange_hi3(r2[1], lane);
+          store_exchanged(p, r2[1], row0, colw + 32, alpha, lane);
+        }
       } else {
-        // fp32 out or C += : 32 columns at a time, so the exchange and the
+        // C += : 32 columns at a time, so the exchange and the
         // read-modify-write fit the register budget (the release waits for
         // the second load)
 #pragma unroll 1
