@@ -269,32 +269,97 @@ __device__ __forceinline__ void rht16_raw(float* v, uint32_t sign_bits) {
     }
   }
 }
-// rht16_raw with the signs as multipliers sig[j] = +-1.0f (exact products):
-// the first butterfly stage becomes fma(x_i, s_i, +-(x_{i+1} s_{i+1})), the
-// same single rounding of the same sum as sign flip + add, on the FP32 pipe
-__device__ __forceinline__ void rht16_raw_mul(float* v, const float* sig) {
-#pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    const float t = __fmul_rn(v[i + 1], sig[i + 1]);
-    const float a = __fmaf_rn(v[i], sig[i], t);
-    v[i + 1] = __fmaf_rn(v[i], sig[i], -t);
-    v[i] = a;
-  }
-#pragma unroll
-  for (int h = 2; h < 16; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i & h) continue;
-      float a = v[i], b = v[i + h];
-      v[i] = __fadd_rn(a, b);
-      v[i + h] = __fsub_rn(a, b);
-    }
-  }
-}
 __device__ __forceinline__ void rht16(float* v, uint32_t sign_bits) {
   rht16_raw(v, sign_bits);
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+}
+
+// ----------------------------------------------------------------------------
+// Packed fp32 pairs (add/sub/mul.rn.f32x2): each lane is rounded exactly as the
+// scalar .rn instruction rounds it (no flush to zero), one issue slot per pair.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// rht16_raw with the signs as multipliers sigma = +-1.0f, on the lane pairs
+// p[k] = (v_k, v_{k+8}), k = 0..7, with sig2[k] = (sigma_k, sigma_{k+8}) as the
+// bit patterns of a packed pair.  Stages 1, 2 and 4 combine elements whose
+// indices differ by 1, 2 or 4, the same offset in both lanes, so each packed
+// operation is two of the scalar ones; the first stage forms the exact
+// products x sigma and then their sum and difference, the same single
+// rounding of the same sums as sign flip + add.  Stage 8 combines the two
+// lanes of one pair and is left to the caller (rht16_x2 / rht16_amax_x2).
+__device__ __forceinline__ void rht16_stages124_x2(uint64_t* p, const uint64_t* sig2) {
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) {
+    const uint64_t a = f2_mul(p[k], sig2[k]), t = f2_mul(p[k + 1], sig2[k + 1]);
+    p[k] = f2_add(a, t);
+    p[k + 1] = f2_sub(a, t);
+  }
+#pragma unroll
+  for (int h = 2; h < 8; h <<= 1) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k & h) continue;
+      const uint64_t a = p[k], b = p[k + h];
+      p[k] = f2_add(a, b);
+      p[k + h] = f2_sub(a, b);
+    }
+  }
+}
+// v becomes H16 diag(sigma) v, bit-identical to rht16_raw
+__device__ __forceinline__ void rht16_x2(float* v, const uint64_t* sig2) {
+  uint64_t p[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) p[k] = f2_pack(v[k], v[k + 8]);
+  rht16_stages124_x2(p, sig2);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float a, b;
+    f2_unpack(p[k], a, b);
+    v[k] = __fadd_rn(a, b);
+    v[k + 8] = __fsub_rn(a, b);
+  }
+}
+// max_j |(H16 diag(sigma) v)_j| without forming the last stage: for the
+// stage-8 pair (a, b), max(|fl(a + b)|, |fl(a - b)|) = fl(|a| + |b|), since
+// rounding is monotone and symmetric and max(|a + b|, |a - b|) = |a| + |b|
+// (a NaN is skipped by fmaxf either way; infinities give the same result).
+__device__ __forceinline__ float rht16_amax_x2(const float* v, const uint64_t* sig2) {
+  uint64_t p[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) p[k] = f2_pack(v[k], v[k + 8]);
+  rht16_stages124_x2(p, sig2);
+  float m = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float a, b;
+    f2_unpack(p[k], a, b);
+    m = fmaxf(m, __fadd_rn(fabsf(a), fabsf(b)));
+  }
+  return m;
 }
 
 __device__ __forceinline__ uint32_t rht_sign_bits(uint64_t seed) {

@@ -633,13 +633,16 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(const void* __restrict__
 // ----------------------------------------------------------------------------
 constexpr int NV_TR = 64, NV_TC = 128, NV_SW = 68;
 
-// the 16 RHT signs as +-1.0f multipliers (kernel parameters)
+// the 16 RHT signs as +-1.0f multipliers (kernel parameters), in the packed
+// pairs rht16_x2 takes: s2[k] = (sigma_k, sigma_{k+8}), sigma_k in the low word
 struct RhtSigns {
-  float s[16];
+  uint64_t s2[8];
 };
 inline RhtSigns rht_sign_floats(uint32_t bits) {
   RhtSigns r;
-  for (int j = 0; j < 16; ++j) r.s[j] = (bits >> j) & 1u ? -1.0f : 1.0f;
+  const uint64_t one = 0x3F800000u, neg_one = 0xBF800000u;
+  for (int k = 0; k < 8; ++k)
+    r.s2[k] = ((bits >> k) & 1u ? neg_one : one) | (((bits >> (k + 8)) & 1u ? neg_one : one) << 32);
   return r;
 }
 
@@ -659,8 +662,9 @@ __device__ __forceinline__ void encode_nv_block(const float* w, bool quarter, fl
     for (int j = 0; j < 16; ++j) xs[j] = __fmul_rn(__fmul_rn(w[j], 0.25f), r);
   } else {
     const float m = quarter ? __fmul_rn(r, 0.25f) : r;
+    const uint64_t m2 = f2_pack(m, m);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) xs[j] = __fmul_rn(w[j], m);
+    for (int k = 0; k < 8; ++k) f2_unpack(f2_mul(f2_pack(w[k], w[k + 8]), m2), xs[k], xs[k + 8]);
   }
   uint32_t packed[2];
   if (!sr) {
@@ -766,14 +770,20 @@ __global__ void __launch_bounds__(kThreads, 4) tile_nv_kernel(const uint16_t* __
           v[2 * i] = __uint_as_float(wv[i] << 16);
           v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
         }
-        if (rht_r) rht16_raw_mul(v, sig_r.s);
         float a = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
         const int64_t col0 = c0 + 32 * q + 16 * h;
         if constexpr (!QUANT) {
+          if (rht_r) {
+            a = rht16_amax_x2(v, sig_r.s2);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
+          }
           m_r = fmaxf(m_r, a);   // zeros past the edges do not raise it
         } else {
+          if (rht_r) rht16_x2(v, sig_r.s2);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
           if (row_ok && col0 < cols)
             encode_nv_block(v, rht_r != 0, g_r, orr, r0 + rr, col0, rht_r ? __fmul_rn(a, 0.25f) : a, sr_r);
         }
@@ -791,13 +801,19 @@ __global__ void __launch_bounds__(kThreads, 4) tile_nv_kernel(const uint16_t* __
           const uint32_t wd = cur[(16 * rb + j) * NV_SW + nv_swz(pw)];
           v[j] = __uint_as_float(e ? (wd & 0xFFFF0000u) : (wd << 16));
         }
-        if (rht_c) rht16_raw_mul(v, sig_c.s);
         float a = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
         if constexpr (!QUANT) {
+          if (rht_c) {
+            a = rht16_amax_x2(v, sig_c.s2);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
+          }
           m_c = fmaxf(m_c, a);
         } else {
+          if (rht_c) rht16_x2(v, sig_c.s2);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
           if (ocol0 < rows && orow + e < cols)
             encode_nv_block(v, rht_c != 0, g_c, oc, orow + e, ocol0, rht_c ? __fmul_rn(a, 0.25f) : a, sr_c);
         }
@@ -813,8 +829,8 @@ __global__ void __launch_bounds__(kThreads, 4) tile_nv_kernel(const uint16_t* __
         vb[j] = __uint_as_float(wd & 0xFFFF0000u);
       }
       if (rht_c) {
-        rht16_raw_mul(va, sig_c.s);
-        rht16_raw_mul(vb, sig_c.s);
+        rht16_x2(va, sig_c.s2);
+        rht16_x2(vb, sig_c.s2);
       }
       float a2 = 0.0f;
 #pragma unroll
