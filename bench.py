@@ -13,6 +13,10 @@ Y[M,N] = X[M,K] W[N,K]^T with M = 8192 tokens, K = 2048, N = 5632 in NVFP4:
             wgrad GEMM dW = dYq_m Xq_t^T (fp32); DGE backward
             dW' = dW * f'(W / s_W) (k = 5, clamp 3.0)
 
+Independent ops run on two streams: the W quantization beside the X one, and
+wgrad + DGE beside dgrad (each op waits for what it reads).  The per-op
+breakdown times every op alone.
+
 Every step runs in the library's CUDA kernels through the C ABI.  Inputs are
 seeded synthetic tensors (X ~ N(0,1), W ~ N(0,0.02), dY ~ N(0,1e-3)) resident
 in HBM before the timed region; L2 is flushed (512 MiB write) before each
@@ -83,10 +87,21 @@ KERNELS_PER_OP = {"quant_x_dual": 2, "quant_w_dual": 2, "fprop": 1, "quant_dy_du
 
 
 class Step:
-    """Buffers and calls of one fwd+bwd step (all device-resident)."""
+    """Buffers and calls of one fwd+bwd step (all device-resident).
+
+    The step's ops form a small dependency graph.  The forward quantizes X and
+    W independently; the backward's dgrad and wgrad are independent, and the
+    DGE scales wgrad's output.  With a side stream, `run` puts the ops in SIDE
+    there (with a context of their own: a context serves one stream at a time)
+    and makes each op wait for the ones it reads on the other stream (WAITS),
+    so that one op's last partial wave overlaps the other's work."""
+
+    SIDE = ("quant_w_dual", "wgrad", "dge")
+    WAITS = {"fprop": "quant_w_dual", "wgrad": "quant_dy_dual"}
 
     def __init__(self, fp4, X, W, dY, dev):
         self.fp4 = fp4
+        self.side_ctx = fp4.Context()
         self.X, self.W, self.dY = X, W, dY
         NV, SR, T2D = fp4.FP4_FMT_NVFP4, fp4.FP4_ROUND_SR, fp4.FP4_SCALING_2D
         self.p_fwd = fp4.quant_params(NV)
@@ -106,38 +121,55 @@ class Step:
         self.dW = torch.empty((N, K), dtype=torch.float32, device=dev)
         self.dWd = torch.empty((N, K), dtype=torch.float32, device=dev)
 
-    def ops(self, step_idx: int):
+    def ops(self, step_idx: int, side_ctx=None):
         f = self.fp4
         off = step_idx << 40      # a fresh SR draw every step
         for p in (self.p_dy_n, self.p_w_t, self.p_dy_m, self.p_x_t):
             p.sr_offset = off
+        sc = side_ctx
         return [
             ("quant_x_dual", lambda: f.fp4_quantize_dual(self.X, self.p_fwd, self.p_x_t, out_rows=self.xq,
                                                          out_cols=self.xq_t)),
             ("quant_w_dual", lambda: f.fp4_quantize_dual(self.W, self.p_fwd, self.p_w_t, out_rows=self.wq,
-                                                         out_cols=self.wq_t)),
+                                                         out_cols=self.wq_t, ctx=sc)),
             ("fprop", lambda: f.fp4_gemm(self.xq, self.wq, out=self.Y)),
             ("quant_dy_dual", lambda: f.fp4_quantize_dual(self.dY, self.p_dy_n, self.p_dy_m, out_rows=self.dyq_n,
                                                           out_cols=self.dyq_m)),
             ("dgrad", lambda: f.fp4_gemm(self.dyq_n, self.wq_t, out=self.dX)),
-            ("wgrad", lambda: f.fp4_gemm(self.dyq_m, self.xq_t, out=self.dW)),
-            ("dge", lambda: f.fp4_dge_backward(self.W, self.wq, self.dW, 5.0, 3.0, 1.0, out=self.dWd)),
+            ("wgrad", lambda: f.fp4_gemm(self.dyq_m, self.xq_t, out=self.dW, ctx=sc)),
+            ("dge", lambda: f.fp4_dge_backward(self.W, self.wq, self.dW, 5.0, 3.0, 1.0, out=self.dWd, ctx=sc)),
         ]
 
-    def run(self, step_idx: int, events=None, before=None, after=None):
-        """Run the step's ops in order on the current stream.  `before`/`after`
-        map an op name to a callable run just before / after it is enqueued
-        (the end-to-end loop uses them to wait for inputs and to start copies)."""
-        for name, fn in self.ops(step_idx):
-            if before and name in before:
-                before[name]()
-            if events is not None:
-                events[name][0].record()
-            fn()
-            if events is not None:
-                events[name][1].record()
-            if after and name in after:
-                after[name]()
+    def run(self, step_idx: int, events=None, before=None, after=None, side=None):
+        """Enqueue the step's ops: all on the current stream in order, or, with a
+        `side` stream, the SIDE ops there (the step still starts after, and
+        ends before, what the current stream holds around it).  `before`/`after`
+        map an op name to a callable taking the op's stream, run just before /
+        after the op is enqueued (the end-to-end loop uses them to wait for
+        inputs and to start copies); `events` brackets each op."""
+        main = torch.cuda.current_stream()
+        if side is not None:
+            side.wait_stream(main)
+        done = {}
+        for name, fn in self.ops(step_idx, self.side_ctx if side is not None else None):
+            s = side if side is not None and name in self.SIDE else main
+            if side is not None and name in self.WAITS:
+                s.wait_event(done[self.WAITS[name]])
+            with torch.cuda.stream(s):
+                if before and name in before:
+                    before[name](s)
+                if events is not None:
+                    events[name][0].record(s)
+                fn()
+                if events is not None:
+                    events[name][1].record(s)
+                if after and name in after:
+                    after[name](s)
+            if side is not None:
+                done[name] = torch.cuda.Event()
+                done[name].record(s)
+        if side is not None:
+            main.wait_stream(side)
 
 
 # ---------------------------------------------------------------------------
@@ -501,8 +533,9 @@ def main():
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    side = torch.cuda.Stream(device=dev)
     for i in range(args.warmup):
-        step.run(i)
+        step.run(i, side=side)
     torch.cuda.synchronize()
     if args.ext_only:
         if args.warmup < 1:
@@ -526,15 +559,16 @@ def main():
     for i in range(args.steps):
         flush.fill_(i & 0xFF)                    # L2 flush, outside the step's events
         ev_step[i][0].record(stream)
-        step.run(args.warmup + i)
+        step.run(args.warmup + i, side=side)
         ev_step[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    # per-op breakdown: further steps with events around every op (outside the
-    # timed region, so the extra event records do not enter the step time)
+    # per-op breakdown: further steps, each op alone on the stream with events
+    # around it (outside the timed region, so the event records do not enter the
+    # step time)
     for i in range(n_breakdown):
         flush.fill_(i & 0xFF)
         step.run(args.warmup + args.steps + i, ev_ops[i])
@@ -542,7 +576,7 @@ def main():
     step_s = np.array([a.elapsed_time(b) * 1e-3 for a, b in ev_step])
     op_s = {n: float(np.mean([e[n][0].elapsed_time(e[n][1]) * 1e-3 for e in ev_ops])) for n in names}
     t_step = reduce_step_time(float(step_s.mean()), dist, dev)
-    status = fp4.fp4_sync_status()
+    status = fp4.fp4_sync_status() | fp4.fp4_sync_status(step.side_ctx)
 
     # ---- end to end through the C ABI with host buffers --------------------------
     h_out = {"Y": torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
@@ -566,20 +600,21 @@ def main():
                 t.copy_(host[k], non_blocking=True)
                 arrived[k].record(s_h2d)
 
-        def copy_back(name, src):
+        def copy_back(name, src, s):
             done = torch.cuda.Event()
-            done.record(stream)
+            done.record(s)
             s_d2h.wait_event(done)
             with torch.cuda.stream(s_d2h):
                 h_out[name].copy_(src, non_blocking=True)
 
         step.run(10_000 + i,
-                 before={"quant_x_dual": lambda: stream.wait_event(arrived["X"]),
-                         "quant_w_dual": lambda: stream.wait_event(arrived["W"]),
-                         "quant_dy_dual": lambda: stream.wait_event(arrived["dY"])},
-                 after={"fprop": lambda: copy_back("Y", step.Y),
-                        "dgrad": lambda: copy_back("dX", step.dX),
-                        "dge": lambda: copy_back("dW", step.dWd)})
+                 before={"quant_x_dual": lambda s: s.wait_event(arrived["X"]),
+                         "quant_w_dual": lambda s: s.wait_event(arrived["W"]),
+                         "quant_dy_dual": lambda s: s.wait_event(arrived["dY"])},
+                 after={"fprop": lambda s: copy_back("Y", step.Y, s),
+                        "dgrad": lambda s: copy_back("dX", step.dX, s),
+                        "dge": lambda s: copy_back("dW", step.dWd, s)},
+                 side=side)
         stream.wait_stream(s_d2h)
         b.record(stream)
         b.synchronize()

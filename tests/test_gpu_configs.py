@@ -143,8 +143,9 @@ def test_llama1b_mlp_up_step():
     d = inputs.llama1b_mlp_up()
     X, W, dY = (d[k].cuda() for k in ("X", "W", "dY"))
     step = bench.Step(fp4, X, W, dY, torch.device("cuda"))
-    step.run(0)
+    step.run(0, side=torch.cuda.Stream())        # the two-stream schedule the bench times
     torch.cuda.synchronize()
+    assert fp4.fp4_sync_status() == 0 and fp4.fp4_sync_status(step.side_ctx) == 0
     xn, wn, dyn = (d[k].float().numpy() for k in ("X", "W", "dY"))
     off = 0                                      # step 0: sr_offset = 0
     r_m = _sample_rows(bench.M, 6, 2)
