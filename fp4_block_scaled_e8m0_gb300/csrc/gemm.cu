@@ -12,8 +12,11 @@
 //
 // Kernel structure (one CTA per SM, persistent over 128 x 256 output tiles):
 //   warp 0       TMA producer: A/B code slabs (128-byte K slabs, 128B swizzle)
-//                and the stage's scale-factor atoms (3-D tensor maps) into a
-//                4-stage shared-memory ring
+//                into a 4-stage shared-memory ring, and the scale-factor atoms
+//                (3-D tensor maps) into a 5-slot ring, one K step ahead of the
+//                slabs: the atoms of step g + 1 are loaded with the slabs of
+//                step g, so they are in tensor memory before step g + 1's
+//                slabs arrive
 //   warp 1       TMEM allocator + MMA issuer (one elected lane): 4 MMAs per
 //                stage; tcgen05.commit frees the stage
 //   warps 2-5    scale-factor stagers, one per TMEM lane quadrant: copy the
@@ -44,14 +47,18 @@ constexpr int A_TILE = BM * KSLAB;         // 16 KB
 constexpr int B_TILE = BN * KSLAB;         // 32 KB
 constexpr int SF_A_MAX = 4 * 512;          // NVFP4: 4 atoms of 128 rows x 4 scales
 constexpr int SF_B_MAX = (BN / 128) * 4 * 512;
-constexpr int STAGE_BYTES = A_TILE + B_TILE + SF_A_MAX + SF_B_MAX;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int SLAB_BYTES = A_TILE + B_TILE;              // one slab stage
+constexpr int SF_BYTES = SF_A_MAX + SF_B_MAX;              // one scale slot
+constexpr int SF_SLOTS = STAGES + 1;   // the scales run one K step ahead of the slabs
+constexpr int SMEM_BYTES = STAGES * SLAB_BYTES + SF_SLOTS * SF_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr int NUM_EPI_WARPS = 16;
 constexpr int NUM_THREADS = 32 * (6 + NUM_EPI_WARPS);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = BN;      // scale-factor slots after the accumulator
-constexpr uint32_t SF_SLOT_COLS = 48;      // 16 (A) + 32 (B) columns per stage
+constexpr uint32_t SF_SLOT_COLS = 48;      // 16 (A) + 32 (B) columns per scale slot
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+static_assert(TMEM_SF_BASE + SF_SLOTS * SF_SLOT_COLS <= TMEM_COLS, "tensor memory");
 
 struct Params {
   int M, N;
@@ -140,8 +147,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
-// arrive on the barrier at the same shared-memory offset in every CTA of `mask`
-
 
 // shared-memory matrix descriptor (K-major, 128-byte swizzle; SBO = 1024 B
 // between 8-row groups)
@@ -227,11 +232,6 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t* r) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 
-// ---------------------------------------------------------------------------
-// the kernel.  CM CTAs along M form a cluster: they share the B tile, which
-// each loads one CM-th of and multicasts to all; a stage is refilled only after
-// every CTA of the cluster has released it.
-// ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
@@ -464,28 +464,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * SLAB_BYTES + SF_SLOTS * SF_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* sf_ready = empty + STAGES;
-  uint64_t* sf_full = sf_ready + STAGES;   // the stage's scale atoms landed (before its A/B slabs)
-  uint64_t* acc_full = sf_full + STAGES;
+  uint64_t* sf_ready = empty + STAGES;     // a scale slot is in tensor memory
+  uint64_t* sf_full = sf_ready + SF_SLOTS; // a scale slot's atoms landed in shared memory
+  uint64_t* acc_full = sf_full + SF_SLOTS;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  auto stage_a = [&](int s) { return smem + s * STAGE_BYTES; };
-  auto stage_b = [&](int s) { return smem + s * STAGE_BYTES + A_TILE; };
-  auto stage_sfa = [&](int s) { return smem + s * STAGE_BYTES + A_TILE + B_TILE; };
-  auto stage_sfb = [&](int s) { return smem + s * STAGE_BYTES + A_TILE + B_TILE + SF_A_MAX; };
+  auto stage_a = [&](int s) { return smem + s * SLAB_BYTES; };
+  auto stage_b = [&](int s) { return smem + s * SLAB_BYTES + A_TILE; };
+  auto slot_sfa = [&](int j) { return smem + STAGES * SLAB_BYTES + j * SF_BYTES; };
+  auto slot_sfb = [&](int j) { return smem + STAGES * SLAB_BYTES + j * SF_BYTES + SF_A_MAX; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&sf_ready[s], 4);
-      mbar_init(&sf_full[s], 1);
+    }
+    for (int j = 0; j < SF_SLOTS; ++j) {
+      mbar_init(&sf_ready[j], 4);
+      mbar_init(&sf_full[j], 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, NUM_EPI_WARPS);
@@ -512,36 +514,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      int s = 0;
-      uint32_t phase = 0;
+      int s = 0, j = 0;
+      uint32_t phase = 0, sphase = 0;
       bool ok = true;
+      int last_j = -1;                 // the slot of the last scale load issued, and its phase
+      uint32_t last_sphase = 0;
       const uint32_t sf_bytes = (uint32_t)atoms * 512;             // one 128-row group, one stage
+      // The scale atoms of step (tile, kt) into slot j (rows of 128 bytes
+      // inside a 128-row group); the extra-column steps have none and only
+      // arrive.  Step g + 1's atoms are issued right after step g's slabs: its
+      // slot was last used by step g - 4, the previous user of slab stage
+      // g mod 4, whose MMAs have completed once empty[g mod 4] is acquired.
+      auto load_sf = [&](int tile, int kt) {
+        if (kt < p.k_tiles) {
+          const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+          mbar_expect_tx(&sf_full[j], sf_bytes * (1 + BN / 128));
+          tma_load_3d(slot_sfa(j), &tm_sfa, &sf_full[j], 0, kt * atoms * 4, tm);
+          tma_load_3d(slot_sfb(j), &tm_sfb, &sf_full[j], 0, kt * atoms * 4, tn * (BN / 128));
+        } else {
+          mbar_arrive(&sf_full[j]);
+        }
+        last_j = j;
+        last_sphase = sphase;
+        if (++j == SF_SLOTS) { j = 0; sphase ^= 1; }
+      };
+      if ((int)blockIdx.x < num_tiles) load_sf(blockIdx.x, 0);
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
         for (int kt = 0; kt < total_k; ++kt) {
           if (!mbar_wait(&empty[s], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_expect_tx(&full[s], A_TILE + B_TILE);
           if (kt < p.k_tiles) {
-            // scale atoms first (rows of 128 bytes inside a 128-row group): they
-            // land, and are staged into tensor memory, while the slabs stream in
-            mbar_expect_tx(&sf_full[s], sf_bytes * (1 + BN / 128));
-            tma_load_3d(stage_sfa(s), &tm_sfa, &sf_full[s], 0, kt * atoms * 4, tm);
-            tma_load_3d(stage_sfb(s), &tm_sfb, &sf_full[s], 0, kt * atoms * 4, tn * (BN / 128));
-            mbar_expect_tx(&full[s], A_TILE + B_TILE);
             tma_load_2d(stage_a(s), &tm_a, &full[s], kt * KSLAB, tm * BM);
             tma_load_2d(stage_b(s), &tm_b, &full[s], kt * KSLAB, tn * BN);
           } else {
             const int kx = kt - p.k_tiles;
-            mbar_arrive(&sf_full[s]);   // no scales in the bf16 stages
-            mbar_expect_tx(&full[s], A_TILE + B_TILE);
             const int ext_elems = p.ext_fp8 ? 128 : 64;   // 128 bytes of K either way
             tma_load_2d(stage_a(s), &tm_ax, &full[s], kx * ext_elems, tm * BM);
             tma_load_2d(stage_b(s), &tm_bx, &full[s], kx * ext_elems, tn * BN);
           }
+          if (kt + 1 < total_k) load_sf(tile, kt + 1);
+          else if (tile + (int)gridDim.x < num_tiles) load_sf(tile + gridDim.x, 0);
           if (++s == STAGES) { s = 0; phase ^= 1; }
         }
       }
       // Drain: acquire every stage once more, i.e. wait (bounded) until the last
-      // data loaded into each stage has been consumed; then no load is in flight.
+      // data loaded into each stage has been consumed, and wait for the last
+      // scale load to land (after an abort it may not have been consumed); then
+      // no load is in flight.
       for (int i = 0; i < STAGES; ++i) {
         const uint64_t t0 = fp4dev::globaltimer_ns();
         for (uint32_t n = 1; !mbar_try_wait(&empty[s], phase ^ 1); ++n) {
@@ -552,15 +572,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (++s == STAGES) { s = 0; phase ^= 1; }
       }
+      if (last_j >= 0) {
+        const uint64_t t0 = fp4dev::globaltimer_ns();
+        for (uint32_t n = 1; !mbar_try_wait(&sf_full[last_j], last_sphase); ++n) {
+          if ((n & 1023u) == 0 && fp4dev::globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+            atomicOr(p.status, FP4_DEVICE_TIMEOUT);
+            break;
+          }
+        }
+      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      int s = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int s = 0, j = 0;
+      uint32_t phase = 0, sphase = 0, acc_phase = 0;
       bool ok = true;
-      // Descriptors are built once: stage s and K step j only move the start
-      // address (16-byte units) by s * STAGE_BYTES / 16 + 2 j, which stays inside
+      // Descriptors are built once: stage s and MMA k only move the start
+      // address (16-byte units) by s * SLAB_BYTES / 16 + 2 k, which stays inside
       // the 14-bit field; the instruction descriptors are constants.
       const uint64_t da0 = desc_sw128(smem_u32(stage_a(0))), db0 = desc_sw128(smem_u32(stage_b(0)));
       const uint32_t id_even = idesc_fp4(!nvfp4, 0u), id_odd = idesc_fp4(!nvfp4, nvfp4 ? 0u : 2u);
@@ -570,15 +599,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc_phase ^= 1;
         tc_fence_after();
         for (int kt = 0; kt < total_k; ++kt) {
-          if (!mbar_wait(&full[s], phase, abort_flag, p.status) || !mbar_wait(&sf_ready[s], phase, abort_flag, p.status)) {
+          if (!mbar_wait(&full[s], phase, abort_flag, p.status) || !mbar_wait(&sf_ready[j], sphase, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t da = da0 + (uint64_t)(s * (STAGE_BYTES >> 4)), db = db0 + (uint64_t)(s * (STAGE_BYTES >> 4));
+          const uint64_t da = da0 + (uint64_t)(s * (SLAB_BYTES >> 4)), db = db0 + (uint64_t)(s * (SLAB_BYTES >> 4));
           const uint32_t acc0 = kt > 0 ? 1u : 0u;
           if (kt < p.k_tiles) {
-            const uint32_t slot = tmem + TMEM_SF_BASE + (uint32_t)s * SF_SLOT_COLS;
+            const uint32_t slot = tmem + TMEM_SF_BASE + (uint32_t)j * SF_SLOT_COLS;
             if (nvfp4) {
 #pragma unroll
               for (int j = 0; j < 4; ++j)
@@ -601,6 +630,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_commit(&empty[s]);
           if (++s == STAGES) { s = 0; phase ^= 1; }
+          if (++j == SF_SLOTS) { j = 0; sphase ^= 1; }
         }
         if (!ok) break;
         tc_commit(acc_full);
@@ -619,21 +649,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the atom's shared-memory row i, for every lane quadrant q.
     const int quad = warp & 3;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    int s = 0;
-    uint32_t phase = 0;
+    int j = 0;                 // scale slot, one per K step in turn
+    uint32_t sphase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       for (int kt = 0; kt < total_k; ++kt) {
         bool got = true;
-        if (lane == 0) got = mbar_wait(&sf_full[s], phase, abort_flag, p.status);
+        if (lane == 0) got = mbar_wait(&sf_full[j], sphase, abort_flag, p.status);
         if (__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) == 0) { ok = false; break; }
         if (kt < p.k_tiles) {
-          const uint32_t slot = tmem + lane_base + TMEM_SF_BASE + (uint32_t)s * SF_SLOT_COLS;
+          const uint32_t slot = tmem + lane_base + TMEM_SF_BASE + (uint32_t)j * SF_SLOT_COLS;
           uint32_t v[16];
           if (nvfp4) {
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
-              const uint4 w = *reinterpret_cast<const uint4*>(stage_sfa(s) + a * 512 + lane * 16);
+              const uint4 w = *reinterpret_cast<const uint4*>(slot_sfa(j) + a * 512 + lane * 16);
               v[4 * a] = w.x; v[4 * a + 1] = w.y; v[4 * a + 2] = w.z; v[4 * a + 3] = w.w;
             }
             tmem_st16(slot, v);
@@ -645,7 +675,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                   const int a = hb * 2 + a2;
-                  const uint4 w = *reinterpret_cast<const uint4*>(stage_sfb(s) + g * 4 * 512 + a * 512 + lane * 16);
+                  const uint4 w = *reinterpret_cast<const uint4*>(slot_sfb(j) + g * 4 * 512 + a * 512 + lane * 16);
                   const int c = (a2 * 2 + g) * 4;
                   v[c] = w.x; v[c + 1] = w.y; v[c + 2] = w.z; v[c + 3] = w.w;
                 }
@@ -655,7 +685,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
 #pragma unroll
             for (int a = 0; a < 2; ++a) {
-              const uint4 w = *reinterpret_cast<const uint4*>(stage_sfa(s) + a * 512 + lane * 16);
+              const uint4 w = *reinterpret_cast<const uint4*>(slot_sfa(j) + a * 512 + lane * 16);
               v[4 * a] = w.x; v[4 * a + 1] = w.y; v[4 * a + 2] = w.z; v[4 * a + 3] = w.w;
             }
             tmem_st8(slot, v);
@@ -663,7 +693,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int a = 0; a < 2; ++a) {
 #pragma unroll
               for (int g = 0; g < 2; ++g) {
-                const uint4 w = *reinterpret_cast<const uint4*>(stage_sfb(s) + g * 2 * 512 + a * 512 + lane * 16);
+                const uint4 w = *reinterpret_cast<const uint4*>(slot_sfb(j) + g * 2 * 512 + a * 512 + lane * 16);
                 const int c = (a * 2 + g) * 4;
                 v[c] = w.x; v[c + 1] = w.y; v[c + 2] = w.z; v[c + 3] = w.w;
               }
@@ -674,8 +704,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_ready[s]);
-        if (++s == STAGES) { s = 0; phase ^= 1; }
+        if (lane == 0) mbar_arrive(&sf_ready[j]);
+        if (++j == SF_SLOTS) { j = 0; sphase ^= 1; }
       }
     }
   } else {
