@@ -791,9 +791,10 @@ __global__ void __launch_bounds__(kThreads, 4) tile_nv_kernel(const uint16_t* __
     }
     const int64_t orow = c0 + 2 * pw, ocol0 = r0 + 16 * rb;   // transposed output row / first column
     if constexpr (!QUANT || !TWO_D) {
-      // the two columns one after the other (the second re-reads the staged
-      // words), so that only one column's values are live at a time
-#pragma unroll 1
+      // the two columns, each from its own re-read of the staged words; the
+      // loop is unrolled so that the compiler can overlap the second column's
+      // reads and Philox rounds with the first's (dY dual: 150 -> 147 us)
+#pragma unroll
       for (int e = 0; e < 2; ++e) {
         float v[16];
 #pragma unroll
