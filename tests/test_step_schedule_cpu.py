@@ -5,8 +5,9 @@ cross-stream waits of `bench.Step.WAITS`, the fork at the step's start and the
 join at its end -- and the ops sharing a context run on one stream.
 
 The buffers each op reads and writes are listed here from the step's data flow
-(quantize X and W, fprop, quantize dY, dgrad, wgrad, DGE on W); a context is
-modelled as a buffer that every call using it writes (its NVFP4 amax scratch).
+(quantize X and W, fprop, quantize dY, dgrad, wgrad, DGE on W).  A context's
+NVFP4 amax scratch is checked separately: the side ops pass the step's side
+context, so each context's calls stay on one stream.
 """
 import itertools
 from types import SimpleNamespace
