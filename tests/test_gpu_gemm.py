@@ -111,6 +111,29 @@ def test_gemm_matches_oracle(fmt, shape, out_dtype):
 
 
 @pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+@pytest.mark.parametrize("M,N,K", [(4000, 7400, 64), (4000, 7400, 256), (3130, 4296, 768)])
+def test_gemm_many_tiles_per_cta(fmt, M, N, K):
+    """The persistent tile loop: 928 (or 425) tiles, ragged in M and N, on at
+    most one CTA per SM, with 1-3 K steps per tile, so each CTA's slab and
+    scale rings wrap across tile boundaries; every element against the oracle,
+    bf16 and fp32 out."""
+    rng = np.random.default_rng(K + fmt)
+    a = (rng.standard_normal((M, K)) * np.exp(rng.uniform(-2, 2, (M, 1)))).astype(np.float32)
+    b = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    at, bt = torch.from_numpy(a).to(torch.bfloat16), torch.from_numpy(b).to(torch.bfloat16)
+    qa = fp4.fp4_quantize(at.cuda(), fp4.quant_params(fmt))
+    qb = fp4.fp4_quantize(bt.cuda(), fp4.quant_params(fmt))
+    ca, sa, ga = o.quantize(at.float().numpy(), FMT[fmt])
+    cb, sb, gb = o.quantize(bt.float().numpy(), FMT[fmt])
+    y, bound = o.gemm(ca, sa, cb, sb, FMT[fmt], ga, gb)
+    for out_dtype in (torch.bfloat16, torch.float32):
+        out = fp4.fp4_gemm(qa, qb, out=torch.empty((M, N), dtype=out_dtype, device="cuda"))
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy().astype(np.float64)
+        _assert_close(got, y, bound, out_dtype, f"fmt={fmt} {M}x{N}x{K} {out_dtype}")
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
 def test_gemm_accumulate(fmt):
     rng = np.random.default_rng(9)
     M, N, K = 256, 256, 512
