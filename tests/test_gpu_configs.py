@@ -184,6 +184,40 @@ def test_llama1b_mlp_up_step():
     assert np.all(np.abs(got - want) <= value_tolerance(sv, want))
 
 
+@pytest.mark.parametrize("two_d", [False, True])
+def test_dual_quantize_many_tiles_ragged(two_d):
+    """The dual NVFP4 quantizer's persistent tile loop: 4144 x 4208 (65 x 33 =
+    2145 tiles of 64 x 128 for 1216 CTAs, so most CTAs prefetch a second tile
+    while quantizing the first; the last tile row holds 48 rows and the last
+    tile column 112 columns).  Row layout RTN (or SR + RHT), transposed layout
+    SR + RHT (with 16 x 16 blocks when two_d), as the step quantizes X and W;
+    sampled rows of both layouts, including the ragged edges, bit for bit."""
+    R, C = 4144, 4208
+    rng = np.random.default_rng(71 + two_d)
+    x = (rng.standard_normal((R, C)) * np.exp(rng.uniform(-2, 2, (R, 1)))).astype(np.float32)
+    x[:, rng.permutation(C)[:5]] *= 50
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    xn = xt.float().numpy()
+    kr = dict(sr_seed=3, sr_stream=0, rht_seed=4, sr_offset=17 << 40)
+    kc = dict(sr_seed=3, sr_stream=2, rht_seed=4, sr_offset=17 << 40)
+    rows_sr = not two_d          # the W-like case keeps the row layout RTN
+    pr = fp4.quant_params(NV, fp4.FP4_ROUND_SR if rows_sr else fp4.FP4_ROUND_RTN, rht=rows_sr, **kr)
+    pc = fp4.quant_params(NV, fp4.FP4_ROUND_SR, fp4.FP4_SCALING_2D if two_d else fp4.FP4_SCALING_1D,
+                          transpose=True, rht=True, **kc)
+    qr, qc = fp4.fp4_quantize_dual(xt.cuda(), pr, pc)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([_sample_rows(R, 6, 5), [R - 48, R - 17, R - 2]]))
+    cols = np.unique(np.concatenate([_sample_rows(C, 6, 6), [C - 112, C - 33, C - 2]]))
+    if rows_sr:
+        _check_quant_rows(xn, qr, {"rounding": "sr", "rht": True, **kr}, rows, "dual rows (SR + RHT)")
+    else:
+        _check_quant_rows(xn, qr, {}, rows, "dual rows (RTN)")
+    pcol = {"rounding": "sr", "rht": True, "transpose": True, **kc}
+    if two_d:
+        pcol["scaling"] = "2d"
+    _check_quant_rows(xn, qc, pcol, cols, "dual cols")
+
+
 def test_ffn7b_gemms_mxfp4():
     from fp4_block_scaled_e8m0_gb300 import inputs
     d = inputs.ffn7b()
