@@ -273,13 +273,20 @@ def tensor_amax(x: np.ndarray) -> np.float32:
 
 
 def _block_amax(w: np.ndarray, bsz: int, two_d: bool) -> np.ndarray:
-    """Per-element block amax (fp32) for 1D blocks along the last axis or 16x16 tiles."""
+    """Block amax (fp32), one value per block: [R, C/bsz] for 1D blocks along
+    the last axis, [R/16, C/16] for 16x16 tiles."""
     r, c = w.shape
     a = np.abs(w)
     if not two_d:
-        m = a.reshape(r, c // bsz, bsz).max(axis=2)
+        return a.reshape(r, c // bsz, bsz).max(axis=2)
+    return a.reshape(r // 16, 16, c // 16, 16).max(axis=(1, 3))
+
+
+def _per_element(m: np.ndarray, bsz: int, two_d: bool) -> np.ndarray:
+    """A per-block array spread over the block's elements (1D: bsz along the
+    last axis; 2D: 16 x 16)."""
+    if not two_d:
         return np.repeat(m, bsz, axis=1)
-    m = a.reshape(r // 16, 16, c // 16, 16).max(axis=(1, 3))
     return np.repeat(np.repeat(m, 16, axis=0), 16, axis=1)
 
 
@@ -344,8 +351,10 @@ def quantize(x, fmt, rounding="rtn", scaling="1d", transpose=False, rht=False,
     if fmt == NVFP4:
         amax_t = tensor_amax(w) if given_amax is None else np.float32(given_amax)
         g = nvfp4_tensor_scale(amax_t)
-    amax_b = _block_amax(w, bsz, two_d)                     # per element
-    sb_el, mult, zero = element_scale_inputs(fmt, amax_b, g)
+    amax_b = _block_amax(w, bsz, two_d)                     # per block
+    sb_blk, mult_blk, zero_blk = element_scale_inputs(fmt, amax_b, g)
+    mult = _per_element(mult_blk, bsz, two_d)
+    zero = _per_element(zero_blk, bsz, two_d)
     xs = (w * mult).astype(np.float32)
     if rounding == "rtn":
         codes = e2m1_encode_rtn(xs)
@@ -354,7 +363,8 @@ def quantize(x, fmt, rounding="rtn", scaling="1d", transpose=False, rht=False,
         codes = e2m1_encode_sr(xs, sr_uniform16(sr_seed, sr_offset, sr_stream, idx))
     codes = np.where(zero, np.uint8(0), codes).astype(np.uint8)
     packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
-    scales = sb_el[:, ::bsz].astype(np.uint8)
+    # one byte per block; 2D tiles repeat theirs over the tile's 16 rows
+    scales = (np.repeat(sb_blk, 16, axis=0) if two_d else sb_blk).astype(np.uint8)
     return packed, scales, g
 
 

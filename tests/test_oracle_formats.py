@@ -70,11 +70,43 @@ def test_e4m3_against_torch():
     assert np.allclose(o.e4m3_decode(np.arange(127)), table)
 
 
+def _num(v: str) -> float:
+    return float.fromhex(v) if "p" in v else float(v)
+
+
 def test_e8m0_golden_points():
     rows = golden("e8m0_scale_points.txt")
-    amax = np.array([float(r[0]) for r in rows], dtype=np.float32)
+    amax = np.array([_num(r[0]) for r in rows], dtype=np.float32)
+    hexpts = np.array([_num(r[0]) for r in rows if "p" in r[0]])
+    assert np.array_equal(hexpts.astype(np.float32).astype(np.float64), hexpts)   # the hex points are fp32 values
     want = np.array([int(r[1]) for r in rows])
     assert np.array_equal(o.e8m0_exponent(amax) + 127, want)
+
+
+def test_mxfp4_tiny_blocks_golden():
+    """Blocks of bf16-subnormal and tiny values (hand-derived codes and bytes):
+    the exponent clamp at -127, the true exponent of subnormal amax, and no
+    flush of subnormal elements to zero before the scaling."""
+    rows = golden("mxfp4_tiny_blocks.txt")
+    blocks = sorted({r[0] for r in rows})
+    x = np.zeros((len(blocks), 32), np.float32)
+    want_codes = np.zeros((len(blocks), 32), np.uint8)
+    want_bytes = np.zeros((len(blocks), 1), np.uint8)
+    for r in rows:
+        b = blocks.index(r[0])
+        if r[1] == "scale":
+            want_bytes[b, 0] = int(r[2])
+        else:
+            x[b, int(r[1])] = _num(r[2])
+            want_codes[b, int(r[1])] = int(r[3])
+    assert np.array_equal(o.bf16_round(x).view(np.uint32), x.view(np.uint32))   # bf16 values, as the fixture says
+    codes, scales, _ = o.quantize(x, o.MXFP4)
+    assert np.array_equal(scales, want_bytes)
+    assert np.array_equal(o.unpack_codes(codes), want_codes)
+    # dequantized values: code value * 2^(byte - 127), exact even when subnormal in fp32
+    deq = o.dequantize(codes, scales, o.MXFP4)
+    want_deq = o.e2m1_decode(want_codes) * np.ldexp(1.0, want_bytes.astype(np.int64) - 127)
+    assert np.array_equal(deq.astype(np.float64), want_deq)
 
 
 def test_e8m0_amax_over_scale_in_4_8():
