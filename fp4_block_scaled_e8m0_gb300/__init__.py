@@ -11,7 +11,6 @@ is present, the calls raise.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import re
 from dataclasses import dataclass
@@ -81,9 +80,10 @@ _SIGNATURES = {
     "fp4_occ_gemm_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I32, _I64]),
     "fp4_occ_gemm": (ctypes.c_int, [_P, _P, _I32, _I64, _P, _I64, ctypes.POINTER(fp4_operand),
                                     ctypes.POINTER(fp4_operand), _P, _P, _I32, _I64, _I32, _P, _I64, _P, _SZ, _P]),
-    "fp4_quant_error_stats": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _F32, _P, _P]),
+    "fp4_quant_error_stats": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _F32, _P, _P, _P]),
     "fp4_gemm": (ctypes.c_int, [_P, ctypes.POINTER(fp4_operand), ctypes.POINTER(fp4_operand), _I32, _P, _I64, _I32,
                                 _P]),
+    "fp4_hcp_num_hot": (_I32, [_I64, ctypes.c_double]),
     "fp4_hcp_select_workspace_bytes": (_SZ, [_I64]),
     "fp4_hcp_select": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(fp4_operand), _I32, _P, _P, _SZ, _P]),
     "fp4_hcp_select_noalloc": (ctypes.c_int, [_P, _I64, ctypes.POINTER(fp4_operand), _I32, _P, _P]),
@@ -339,9 +339,12 @@ def fp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: Optional[tor
     return out
 
 
-def hcp_num_hot(k: int, ratio: float = 0.09) -> int:
-    """h = ceil(ratio * K): the "top 9% of channels" count."""
-    return int(math.ceil(ratio * k))
+def fp4_hcp_num_hot(k: int, ratio: float = 0.09) -> int:
+    """h = ceil(ratio * K), computed by the library: the "top 9%" channel count."""
+    h = int(load_library().fp4_hcp_num_hot(k, ratio))
+    if h < 0:
+        raise ValueError(f"fp4_hcp_num_hot: k = {k}, ratio = {ratio} outside k >= 0, 0 <= ratio <= 1")
+    return h
 
 
 def fp4_hcp_select(x: torch.Tensor, xq: QTensor, k_hot: int, out: Optional[torch.Tensor] = None,
@@ -452,24 +455,27 @@ def fp4_occ_gemm(x: torch.Tensor, w: torch.Tensor, xq: QTensor, wq: QTensor, tau
     return out
 
 
-def fp4_quant_error_sums(x: torch.Tensor, q: QTensor, tau: Optional[torch.Tensor] = None, beta: float = 0.0,
-                         out: Optional[torch.Tensor] = None, ctx=None, stream=None) -> torch.Tensor:
-    """Device float64[4]: sum x^2, sum x_hat^2, sum x x_hat, sum (x - x_hat)^2 (x_hat: the dequantized
-    value, + the clamped-away part with tau, or s Q_soft(x/s) with beta > 0)."""
-    out = out if out is not None else torch.empty((4,), dtype=torch.float64, device=x.device)
+STAT_NAMES = ("cos", "mse", "snr_db", "rel_err")
+
+
+def fp4_quant_error_stats(x: torch.Tensor, q: QTensor, tau: Optional[torch.Tensor] = None, beta: float = 0.0,
+                          ctx=None, stream=None):
+    """(sums, stats), device float64[4] each.  sums: sum x^2, sum x_hat^2, sum x x_hat,
+    sum (x - x_hat)^2 (x_hat: the dequantized value, + the clamped-away part with tau, or
+    s Q_soft(x/s) with beta > 0).  stats: cosine, MSE, SNR (dB), relative L2 error, formed by
+    the library from the sums (names in STAT_NAMES)."""
+    sums = torch.empty((4,), dtype=torch.float64, device=x.device)
+    stats = torch.empty((4,), dtype=torch.float64, device=x.device)
     op = q.operand()
     _check(load_library().fp4_quant_error_stats(_ctx(ctx), _ptr(x), _dtype_code(x), _ld(x), ctypes.byref(op),
-                                                _ptr(tau), beta, _ptr(out), _stream(stream)), "fp4_quant_error_stats")
-    return out
+                                                _ptr(tau), beta, _ptr(sums), _ptr(stats), _stream(stream)),
+           "fp4_quant_error_stats")
+    return sums, stats
 
 
-def error_stats_from_sums(sums, n: int) -> dict:
-    """cosine, MSE and SNR (dB) from the four sums (host arithmetic)."""
-    sxx, shh, sxh, see = (float(v) for v in sums)
-    return {"cos": sxh / math.sqrt(sxx * shh) if sxx > 0 and shh > 0 else float("nan"),
-            "mse": see / n if n else float("nan"),
-            "snr_db": 10.0 * math.log10(sxx / see) if see > 0 and sxx > 0 else float("inf"),
-            "rel_err": math.sqrt(see / sxx) if sxx > 0 else float("nan")}
+def stats_dict(stats) -> dict:
+    """The four quality numbers by name (no arithmetic)."""
+    return {name: float(v) for name, v in zip(STAT_NAMES, stats)}
 
 
 def fp4_encode_e2m1(xs: torch.Tensor, method: int = 0, ctx=None, stream=None) -> torch.Tensor:

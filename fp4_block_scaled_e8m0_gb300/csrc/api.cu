@@ -124,7 +124,27 @@ cudaError_t clear_sf_padding(const fp4_quant_params* p, uint8_t* scales, int64_t
   return cudaMemsetAsync(scales, 0, fp4_scales_bytes(out_rows, blocked, p->format, FP4_SF_MMA, 0), st);
 }
 
+// argument checks of the hot-channel selection, shared by both of its entry
+// points so that they accept and reject the same calls
+int check_hcp_select(const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot, const int32_t* hot_idx) {
+  if (k_hot > 0 && !hot_idx) return FP4_ERR_INVALID_ARG;
+  int s = check_operand(xq, true);
+  if (s) return s;
+  if (!native_block(xq)) return FP4_ERR_UNSUPPORTED;
+  s = check_input(x_bf16, FP4_DTYPE_BF16, xq->rows, xq->k, ldx);
+  if (s) return s;
+  if (k_hot < 0 || k_hot > xq->k) return FP4_ERR_INVALID_ARG;
+  return FP4_OK;
+}
+
 }  // namespace
+
+namespace fp4 {
+int validate_hcp_select(const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
+                        const int32_t* hot_idx) {
+  return check_hcp_select(x_bf16, ldx, xq, k_hot, hot_idx);
+}
+}  // namespace fp4
 
 extern "C" {
 
@@ -479,14 +499,14 @@ int fp4_occ_gemm(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, cons
 }
 
 int fp4_quant_error_stats(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,
-                          const float* tau, float beta, double* sums, void* stream) {
+                          const float* tau, float beta, double* sums, double* stats, void* stream) {
   if (!ctx || !sums || !(beta >= 0.0f && beta <= 1e6f) || (tau && beta > 0.0f)) return FP4_ERR_INVALID_ARG;
   int s = check_operand(q, beta == 0.0f);
   if (s) return s;
   if (q->k % 16) return FP4_ERR_INVALID_ARG;
   s = check_input(x, x_dtype, q->rows, q->k, ldx);
   if (s) return s;
-  return cuda_status(launch_error_stats(x, x_dtype, ldx, *q, op_block(q), tau, beta, sums, ctx->num_sms,
+  return cuda_status(launch_error_stats(x, x_dtype, ldx, *q, op_block(q), tau, beta, sums, stats, ctx->num_sms,
                                         static_cast<cudaStream_t>(stream)));
 }
 
@@ -551,15 +571,17 @@ int fp4_hcp_quantize_zeroed(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_
 
 size_t fp4_hcp_select_workspace_bytes(int64_t k) { return k > 0 ? (size_t)k * 8 : 0; }
 
+int32_t fp4_hcp_num_hot(int64_t k, double ratio) {
+  if (k < 0 || !(ratio >= 0.0 && ratio <= 1.0)) return -1;
+  const double h = std::ceil(ratio * (double)k);
+  return (int32_t)std::min<double>(h, (double)std::min<int64_t>(k, INT32_MAX));
+}
+
 int fp4_hcp_select(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
                    int32_t* hot_idx, void* workspace, size_t ws_bytes, void* stream) {
-  if (!ctx || (k_hot > 0 && !hot_idx)) return FP4_ERR_INVALID_ARG;
-  int s = check_operand(xq, true);
+  if (!ctx) return FP4_ERR_INVALID_ARG;
+  int s = check_hcp_select(x_bf16, ldx, xq, k_hot, hot_idx);
   if (s) return s;
-  if (!native_block(xq)) return FP4_ERR_UNSUPPORTED;
-  s = check_input(x_bf16, FP4_DTYPE_BF16, xq->rows, xq->k, ldx);
-  if (s) return s;
-  if (k_hot < 0 || k_hot > xq->k) return FP4_ERR_INVALID_ARG;
   if (ws_bytes < fp4_hcp_select_workspace_bytes(xq->k) || (xq->k > 0 && !workspace)) return FP4_ERR_INVALID_ARG;
   if (k_hot == 0 || xq->k == 0) return FP4_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

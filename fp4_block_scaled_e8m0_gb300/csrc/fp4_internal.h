@@ -134,6 +134,9 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st);  // returns fp4 status
 cudaError_t launch_hcp_channel_errors(const uint16_t* x, int64_t ldx, const fp4_operand& q, float* err,
                                       int num_sms, cudaStream_t st);
 cudaError_t launch_hcp_topk(const float* err, int64_t k, int k_hot, int32_t* hot_idx, cudaStream_t st);
+// argument checks of fp4_hcp_select (api.cu), also used by fp4_hcp_select_noalloc
+int validate_hcp_select(const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
+                        const int32_t* hot_idx);
 // E4M3 extra columns [M][kx] / [N][kx] (kx a multiple of 128) with row scales sa / sb
 cudaError_t launch_hcp_gather_fp8(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
                                   const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot, int k_hot,
@@ -162,8 +165,10 @@ cudaError_t launch_occ_prepare(const void* x, int xdt, int64_t ldx, const uint16
                                int num_sms, cudaStream_t st);
 // quality sums over q with any block (16-128); tau: OCC reconstruction; beta > 0:
 // the sigmoid-smoothed reconstruction instead of the codes
+// stats (may be null): cosine, MSE, SNR (dB) and relative L2 error from the sums
 cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, int block,
-                               const float* tau, float beta, double* sums, int num_sms, cudaStream_t st);
+                               const float* tau, float beta, double* sums, double* stats, int num_sms,
+                               cudaStream_t st);
 // the row quantizer with the columns o.zero_idx[0..o.zero_n) set to 0 (32-bit block ids)
 cudaError_t launch_quant_rows_zeroed(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt,
                                      const QuantOut& o, int num_sms, cudaStream_t st);

@@ -16,8 +16,6 @@
 // selection (ties to the lower index), and the gather of the extra columns.
 #include <cuda_bf16.h>
 
-#include <mutex>
-
 #include "fp4_device.cuh"
 
 using namespace fp4dev;
@@ -320,25 +318,18 @@ namespace {
 // per-channel fp32 error sums, then one int flag per channel
 static __device__ __align__(256) unsigned char g_hcp_select_scratch[FP4_NOALLOC_MAX_CHANNELS * 8];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
-int g_noalloc_sms[kMaxDevices] = {};
-
 // Device address of the scratch array on the current device (host code may not
-// use the array's name as a device pointer).  Looked up once per device.
-int noalloc_setup(int dev, void** ptr, int* sms) {
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_hcp_select_scratch) != cudaSuccess || !p) return FP4_ERR_CUDA;
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 148;
-    g_noalloc_sms[dev] = n;
-    g_noalloc_ptr[dev] = p;
-  }
-  *ptr = g_noalloc_ptr[dev];
-  *sms = g_noalloc_sms[dev];
+// use the array's name as a device pointer), looked up on every call: after a
+// device reset the module may be loaded again at another address.
+int noalloc_scratch(void** ptr, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP4_ERR_CUDA;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_hcp_select_scratch) != cudaSuccess || !p) return FP4_ERR_CUDA;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  *ptr = p;
+  *sms = n;
   return FP4_OK;
 }
 
@@ -348,24 +339,13 @@ int noalloc_setup(int dev, void** ptr, int* sms) {
 extern "C" int fp4_hcp_select_noalloc(const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
                                       int32_t* hot_idx, void* stream) {
   using namespace fp4;
-  if (!xq || xq->rows < 0 || xq->k < 0) return FP4_ERR_INVALID_ARG;
-  const bool empty = xq->rows == 0 || xq->k == 0;   // pointers of empty buffers may be NULL
-  if (!empty && (!xq->codes || !xq->scales || !x_bf16)) return FP4_ERR_INVALID_ARG;
+  int s = validate_hcp_select(x_bf16, ldx, xq, k_hot, hot_idx);
+  if (s) return s;
   if (xq->k > FP4_NOALLOC_MAX_CHANNELS) return FP4_ERR_TOO_LARGE;
-  if (xq->format != FP4_FMT_MXFP4 && xq->format != FP4_FMT_NVFP4) return FP4_ERR_UNSUPPORTED;
-  if (xq->sf_layout != FP4_SF_ROWMAJOR && xq->sf_layout != FP4_SF_MMA) return FP4_ERR_INVALID_ARG;
-  if (xq->block != 0 && xq->block != (xq->format == FP4_FMT_MXFP4 ? 32 : 16)) return FP4_ERR_UNSUPPORTED;
-  if (xq->k % (xq->format == FP4_FMT_MXFP4 ? 32 : 16)) return FP4_ERR_INVALID_ARG;
-  if (xq->format == FP4_FMT_NVFP4 && !empty && !xq->tensor_scale) return FP4_ERR_INVALID_ARG;
-  if (k_hot < 0 || k_hot > xq->k || (k_hot > 0 && !hot_idx) || ldx < xq->k) return FP4_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(x_bf16) & 15u) || (ldx * 2) % 16 || (reinterpret_cast<uintptr_t>(xq->codes) & 15u))
-    return FP4_ERR_MISALIGNED;
-  if (k_hot == 0 || xq->k == 0 || xq->rows == 0) return FP4_OK;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP4_ERR_CUDA;
+  if (k_hot == 0 || xq->k == 0) return FP4_OK;   // as fp4_hcp_select: rows == 0 still selects (all errors 0)
   void* scratch = nullptr;
   int sms = 0;
-  int s = noalloc_setup(dev, &scratch, &sms);
+  s = noalloc_scratch(&scratch, &sms);
   if (s) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* err = static_cast<float*>(scratch);   // cleared by the launcher before accumulating

@@ -1341,6 +1341,18 @@ __global__ void __launch_bounds__(256) error_stats_kernel(const void* __restrict
   }
 }
 
+// cosine = s2 / sqrt(s0 s1), MSE = s3 / n, SNR = 10 log10(s0 / s3) dB and the
+// relative L2 error sqrt(s3 / s0) from the four sums (one thread); an
+// undefined ratio (a zero denominator) gives NaN, a zero error an infinite SNR
+__global__ void error_stats_finalize_kernel(const double* sums, double n, double* stats) {
+  const double sxx = sums[0], shh = sums[1], sxh = sums[2], see = sums[3];
+  const double nan = __longlong_as_double(0x7FF8000000000000ll), inf = __longlong_as_double(0x7FF0000000000000ll);
+  stats[0] = (sxx > 0.0 && shh > 0.0) ? sxh / sqrt(sxx * shh) : nan;
+  stats[1] = n > 0.0 ? see / n : nan;
+  stats[2] = (sxx > 0.0 && see > 0.0) ? 10.0 * log10(sxx / see) : (sxx > 0.0 ? inf : nan);
+  stats[3] = sxx > 0.0 ? sqrt(see / sxx) : nan;
+}
+
 // ----------------------------------------------------------------------------
 // element encoders
 // ----------------------------------------------------------------------------
@@ -1601,18 +1613,30 @@ cudaError_t launch_quant_rows_blk(const void* x, int dt, int64_t rows, int64_t c
   return cudaGetLastError();
 }
 
-cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, int block,
-                               const float* tau, float beta, double* sums, int num_sms, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(sums, 0, 4 * sizeof(double), st);
-  if (e != cudaSuccess) return e;
+static cudaError_t launch_error_sums(const void* x, int xdt, int64_t ldx, const fp4_operand& q, int block,
+                                     const float* tau, float beta, double* sums, int num_sms, cudaStream_t st) {
   const int64_t total = q.rows * (q.k / 16);
-  if (total == 0) return cudaSuccess;
   const int grid = grid_for(total, 256, num_sms);
   const int sbl = log2_block(block);
   const float nbl = -beta * 1.4426950408889634f;
   FP4_DISPATCH_FMT(q.format, FMT, FP4_DISPATCH_DT(xdt, XDT,
     if (beta > 0.0f) error_stats_kernel<FMT, XDT, true><<<grid, 256, 0, st>>>(x, ldx, q, sbl, nullptr, nbl, sums);
     else error_stats_kernel<FMT, XDT, false><<<grid, 256, 0, st>>>(x, ldx, q, sbl, tau, 0.0f, sums)));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_error_stats(const void* x, int xdt, int64_t ldx, const fp4_operand& q, int block,
+                               const float* tau, float beta, double* sums, double* stats, int num_sms,
+                               cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(sums, 0, 4 * sizeof(double), st);
+  if (e != cudaSuccess) return e;
+  const int64_t total = q.rows * (q.k / 16);
+  if (total > 0) {
+    e = launch_error_sums(x, xdt, ldx, q, block, tau, beta, sums, num_sms, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (!stats) return cudaSuccess;
+  error_stats_finalize_kernel<<<1, 1, 0, st>>>(sums, (double)q.rows * (double)q.k, stats);
   return cudaGetLastError();
 }
 

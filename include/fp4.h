@@ -279,10 +279,16 @@ int fp4_occ_gemm(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, cons
  *              non-NULL: the OCC reconstruction);
  *   beta > 0:  x_hat = s Q_soft(x / s), the sigmoid-smoothed value with q's
  *              scales (q->codes unused; tau must be NULL).
- * fp64 accumulation.  cosine = s2 / sqrt(s0 s1), MSE = s3 / n,
- * SNR = 10 log10(s0 / s3), relative L2 error = sqrt(s3 / s0).              */
+ * fp64 accumulation.
+ * stats (device double[4], may be NULL) = the quality numbers of those pages,
+ * formed on the device from the sums with n = rows * k:
+ *   stats[0] cosine similarity  s2 / sqrt(s0 s1)
+ *   stats[1] mean squared error s3 / n
+ *   stats[2] SNR in dB          10 log10(s0 / s3)   (+inf when s3 = 0)
+ *   stats[3] relative L2 error  sqrt(s3 / s0)
+ * A ratio with a zero denominator otherwise gives NaN.                     */
 int fp4_quant_error_stats(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,
-                          const float* tau, float beta, double* sums, void* stream);
+                          const float* tau, float beta, double* sums, double* stats, void* stream);
 
 /* ---- block-scaled FP4 GEMM ([msr] §四: the GEMMs are >95% of the compute)
  * C[M,N] = alpha * sum_k A[m,k] * B[n,k]  (TN: both operands K-major), FP32
@@ -294,7 +300,13 @@ int fp4_gemm(fp4_ctx* ctx, const fp4_operand* A, const fp4_operand* B, int32_t o
              void* C, int64_t ldc, int32_t accumulate, void* stream);
 
 /* ---- hot-channel compensation ([outlier] §3.1-3.2, §4.1)
- * fp4_hcp_select: e_c = sum_m (X[m,c] - X_hat[m,c])^2 over the M rows of the
+ * fp4_hcp_num_hot: h = ceil(ratio * k), the number of hot channels out of k
+ * when the "top 9%" ([outlier] §4.1: ratio 0.09) are compensated; the product
+ * is taken in double precision.  Returns h (0 <= h <= k), or -1 when k < 0 or
+ * ratio lies outside [0, 1].  Host arithmetic only.                        */
+int32_t fp4_hcp_num_hot(int64_t k, double ratio);
+
+/* fp4_hcp_select: e_c = sum_m (X[m,c] - X_hat[m,c])^2 over the M rows of the
  * bf16 activation X (pitch ldx) and its quantization xq (blocks along K);
  * writes the k_hot channels with the largest e_c, ascending, to hot_idx
  * (device int32[k_hot]); ties go to the lower index.  Caller workspace of
@@ -343,13 +355,16 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
  * channels (512 KiB), which every GPU that loads the library keeps until the
  * process exits.  The pages have no counterpart; it exists for such callers.
  *  - K > FP4_NOALLOC_MAX_CHANNELS returns FP4_ERR_TOO_LARGE (nothing launched).
- *  - The first call on a device looks up the array's device address (once per
- *    device); make that first call before any stream capture.
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress).  The first call on a device may thereby load the
+ *    library's device code, which puts the module and its array in device
+ *    memory outside any caller pool; make that first call before any stream
+ *    capture.  Later calls allocate nothing.
  *  - All calls share the one array: calls that overlap on the GPU (different
  *    streams, or different host threads, on the same device) race and give
  *    wrong results.  Each call clears the error sums it accumulates.
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.
- * Arguments, layout and result as fp4_hcp_select.                          */
+ * Arguments, validation, layout and result as fp4_hcp_select.              */
 #define FP4_NOALLOC_MAX_CHANNELS 65536
 int fp4_hcp_select_noalloc(const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
                            int32_t* hot_idx, void* stream);

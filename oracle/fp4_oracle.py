@@ -552,12 +552,17 @@ def hcp_channel_errors(x, x_codes, x_scales, fmt, g=None) -> np.ndarray:
     return ((np.asarray(x, dtype=np.float64) - xh) ** 2).sum(axis=0)
 
 
-def hcp_select(x, x_codes, x_scales, fmt, g, k_hot: int) -> np.ndarray:
-    """Indices of the k_hot channels with the largest error, ties to the lower
-    index, returned in ascending order ([outlier §4.1]: top 9% of channels)."""
-    e = hcp_channel_errors(x, x_codes, x_scales, fmt, g)
+def hcp_top_channels(e, k_hot: int) -> np.ndarray:
+    """The k_hot channels with the largest error e_c, ties to the lower index,
+    in ascending order ([outlier §4.1]: top 9% of channels)."""
+    e = np.asarray(e, dtype=np.float64)
     order = sorted(range(len(e)), key=lambda c: (-e[c], c))
     return np.array(sorted(order[:k_hot]), dtype=np.int32)
+
+
+def hcp_select(x, x_codes, x_scales, fmt, g, k_hot: int) -> np.ndarray:
+    """Indices of the k_hot channels with the largest quantization error."""
+    return hcp_top_channels(hcp_channel_errors(x, x_codes, x_scales, fmt, g), k_hot)
 
 
 def hcp_num_hot(k: int, ratio: float = 0.09) -> int:

@@ -112,3 +112,48 @@ def test_create_without_gpu_reports_cuda_error(lib):
         pytest.skip("a GPU is present")
     h = ctypes.c_void_p()
     assert lib.fp4_create(ctypes.byref(h)) == fp4.FP4_ERR_CUDA
+
+
+def test_hcp_num_hot_in_the_library(lib):
+    """h = ceil(0.09 K) ("top 9%" of the channels) is the library's arithmetic:
+    369 for K = 4096, equal to the exact rational ceiling over a range of K."""
+    from fractions import Fraction
+    assert lib.fp4_hcp_num_hot(4096, 0.09) == 369
+    for k in list(range(0, 5000)) + [11008, 16384, 65536, 1 << 20]:
+        assert lib.fp4_hcp_num_hot(k, 0.09) == -(-9 * k // 100), k
+        assert lib.fp4_hcp_num_hot(k, 0.09) == int(-(-Fraction(9, 100) * k // 1))
+    assert lib.fp4_hcp_num_hot(10, 1.0) == 10 and lib.fp4_hcp_num_hot(10, 0.0) == 0
+    assert lib.fp4_hcp_num_hot(-1, 0.09) == -1 and lib.fp4_hcp_num_hot(10, 1.5) == -1
+    assert lib.fp4_hcp_num_hot(10, float("nan")) == -1
+    assert fp4.fp4_hcp_num_hot(4096) == 369
+
+
+def test_hcp_select_entry_points_validate_alike(lib):
+    """fp4_hcp_select and fp4_hcp_select_noalloc reject the same bad calls with
+    the same status (validation runs before any CUDA call)."""
+    ctx = ctypes.cast(_fake_ctx(), ctypes.c_void_p)
+    p = 0x100000
+    ws = ctypes.c_void_p(p)
+    out = ctypes.c_void_p(p)
+
+    def both(x, ldx, op, k_hot, hot=out):
+        a = lib.fp4_hcp_select(ctx, x, ldx, ctypes.byref(op), k_hot, hot, ws, 1 << 30, None)
+        b = lib.fp4_hcp_select_noalloc(x, ldx, ctypes.byref(op), k_hot, hot, None)
+        return a, b
+
+    x = ctypes.c_void_p(p)
+    good = fp4.fp4_operand(p, p, p, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA, 64, 512)
+    assert both(x, 500, good, 8) == (fp4.FP4_ERR_INVALID_ARG,) * 2                # ldx < k
+    assert both(ctypes.c_void_p(p + 8), 512, good, 8) == (fp4.FP4_ERR_MISALIGNED,) * 2
+    assert both(x, 512, good, 513) == (fp4.FP4_ERR_INVALID_ARG,) * 2               # k_hot > k
+    assert both(x, 512, good, 8, None) == (fp4.FP4_ERR_INVALID_ARG,) * 2           # no output
+    b64 = fp4.fp4_operand(p, p, p, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_ROWMAJOR, 64, 512, 64)
+    assert both(x, 512, b64, 8) == (fp4.FP4_ERR_UNSUPPORTED,) * 2
+    nots = fp4.fp4_operand(p, p, None, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA, 64, 512)
+    assert both(x, 512, nots, 8) == (fp4.FP4_ERR_INVALID_ARG,) * 2                 # NVFP4 tensor scale
+    # an empty input with an unaligned pointer is accepted by both (nothing is read)
+    empty = fp4.fp4_operand(p, p, p, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA, 0, 512)
+    assert both(ctypes.c_void_p(p + 8), 512, empty, 0) == (fp4.FP4_OK,) * 2
+    wide = fp4.fp4_operand(p, p, p, fp4.FP4_FMT_MXFP4, fp4.FP4_SF_MMA, 16, fp4.FP4_NOALLOC_MAX_CHANNELS + 32)
+    assert lib.fp4_hcp_select_noalloc(x, fp4.FP4_NOALLOC_MAX_CHANNELS + 32, ctypes.byref(wide), 8, out,
+                                      None) == fp4.FP4_ERR_TOO_LARGE

@@ -79,13 +79,15 @@ def test_quality_sums_any_block(fmt, block):
     c, s, g = o.quantize(xn, FMT[fmt], block=block)
     a = xn.astype(np.float64).reshape(-1)
     # dequantized reconstruction
-    got = fp4.fp4_quant_error_sums(xd, q).cpu().numpy()
+    got, st = (t.cpu().numpy() for t in fp4.fp4_quant_error_stats(xd, q))
     h = o.dequantize(c, s, FMT[fmt], g, block=block).astype(np.float64).reshape(-1)
     want = np.array([a @ a, h @ h, a @ h, ((a - h) ** 2).sum()])
     assert np.allclose(got, want, rtol=1e-9, atol=0)
+    rel = o.relative_error(xn, h)
+    assert abs(fp4.stats_dict(st)["rel_err"] - rel) <= 1e-9 * rel
     # sigmoid-smoothed reconstruction
     for beta in (10.0, 40.0):
-        got = fp4.fp4_quant_error_sums(xd, q, beta=beta).cpu().numpy()
+        got = fp4.fp4_quant_error_stats(xd, q, beta=beta)[0].cpu().numpy()
         hs = o.soft_forward(xn, s, FMT[fmt], g, beta, block=block).reshape(-1)
         sv = o.block_scales_expanded(s, FMT[fmt], g, block=block).astype(np.float64).reshape(-1)
         d = 1.5e-5 * sv + 2.0 ** -22 * np.abs(hs)

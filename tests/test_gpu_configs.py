@@ -38,63 +38,64 @@ def _sample_rows(n, count, seed):
     return np.unique(idx)
 
 
-def _check_quant_rows(x_np, q: fp4.QTensor, params_oracle, rows_out, label):
-    """Compare output rows `rows_out` of q with the oracle run on the matching
-    slice (the output layout's rows; for a transposed output these are input
-    columns).  NVFP4 uses the full tensor's amax (after any RHT)."""
-    fmt = OF[q.fmt]
+def _oracle_rows(x_np, fmt_gpu, params_oracle, rows_out):
+    """The oracle's quantization of output rows `rows_out` (the output layout's
+    rows; for a transposed output these are input columns), from the input
+    values alone.  NVFP4 takes the full tensor's amax (after any RHT).  For 2D
+    scaling the rows are widened to whole 16-row groups.  Returns (codes,
+    scales, g, rows)."""
+    fmt = OF[fmt_gpu]
     transpose = params_oracle.get("transpose", False)
     rht = params_oracle.get("rht", False)
     w = x_np.T if transpose else x_np
     given = None
-    if q.fmt == NV:
+    if fmt_gpu == NV:
         ww = o.rht16(np.ascontiguousarray(w), 1, params_oracle.get("rht_seed", 0)) if rht else w
         given = o.tensor_amax(ww)
-    codes = q.codes.cpu().numpy()
-    nsf = q.k // fp4.BLOCK[q.fmt]
-    scales = untile_scales(q.scales.cpu().numpy(), q.rows, nsf)
     two_d = params_oracle.get("scaling") == "2d"
-    # whole 16-row groups for 2D scaling (one scale per 16x16 tile)
+    rows_out = np.unique(np.asarray(rows_out))
     if two_d:
         rows_out = np.unique(np.concatenate([np.arange(r - r % 16, r - r % 16 + 16) for r in rows_out]))
     kw = {k: v for k, v in params_oracle.items() if k not in ("transpose",)}
-    # the SR counter of output element (r, c) is r * cols + c: a one-row slice
-    # starts its indices at 0, so its offset is shifted by r * cols / 8
+    # the SR counter of output element (r, c) is r * cols + c: a slice starting
+    # at row r0 starts its indices at 0, so its offset is shifted by r0 * cols / 8
+    step = 16 if two_d else 1
     want_c, want_s, want_g = [], [], None
-    for r in rows_out:
-        if two_d:
-            continue
-        c, s, g = o.quantize(w[r:r + 1], fmt, **{**kw, "given_amax": given,
-                                                 "sr_offset": kw.get("sr_offset", 0) + (r * w.shape[1]) // 8})
-        want_c.append(c[0])
-        want_s.append(s[0])
+    for i in range(0, len(rows_out), step):
+        r0 = rows_out[i]
+        c, sc, g = o.quantize(w[r0:r0 + step], fmt, **{**kw, "given_amax": given,
+                                                       "sr_offset": kw.get("sr_offset", 0) + (r0 * w.shape[1]) // 8})
+        want_c.extend(c)
+        want_s.extend(sc)
         want_g = g
-    if two_d:
-        for g0 in range(0, len(rows_out), 16):
-            rr = rows_out[g0:g0 + 16]
-            c, s, g = o.quantize(w[rr[0]:rr[0] + 16], fmt, **{**kw, "given_amax": given,
-                                                             "sr_offset": kw.get("sr_offset", 0) + (rr[0] * w.shape[1]) // 8})
-            want_c.extend(c)
-            want_s.extend(s)
-            want_g = g
-    want_c = np.array(want_c)
-    want_s = np.array(want_s)
+    return np.array(want_c), np.array(want_s), want_g, rows_out
+
+
+def _check_quant_rows(x_np, q: fp4.QTensor, params_oracle, rows_out, label):
+    """Sampled output rows of q bit for bit against the oracle; returns the
+    oracle's (codes, scales, g, rows)."""
+    want_c, want_s, want_g, rows_out = _oracle_rows(x_np, q.fmt, params_oracle, rows_out)
+    codes = q.codes.cpu().numpy()
+    nsf = q.k // fp4.BLOCK[q.fmt]
+    scales = untile_scales(q.scales.cpu().numpy(), q.rows, nsf)
     assert np.array_equal(scales[rows_out], want_s), mismatch_report(scales[rows_out], want_s, label + " scales")
     assert np.array_equal(codes[rows_out], want_c), mismatch_report(codes[rows_out], want_c, label + " codes")
     if want_g is not None:
         got_g = q.tensor_scale.cpu().numpy()[0]
         assert np.float32(got_g).view(np.uint32) == np.float32(want_g).view(np.uint32)
+    return want_c, want_s, want_g, rows_out
 
 
-def _check_gemm_rows(qa, qb, y, rows, fmt, out_bf16, label):
-    ca = qa.codes.cpu().numpy()
-    cb = qb.codes.cpu().numpy()
-    sa = untile_scales(qa.scales.cpu().numpy(), qa.rows, qa.k // fp4.BLOCK[fmt])
-    sb = untile_scales(qb.scales.cpu().numpy(), qb.rows, qb.k // fp4.BLOCK[fmt])
-    ga = qa.tensor_scale.cpu().numpy()[0] if qa.tensor_scale is not None else None
-    gb = qb.tensor_scale.cpu().numpy()[0] if qb.tensor_scale is not None else None
-    yr, bound = o.gemm(ca[rows], sa[rows], cb, sb, OF[fmt], ga, gb)
-    got = y[rows].float().cpu().numpy().astype(np.float64)
+def _check_gemm_sampled(a, b, y, fmt, out_bf16, label):
+    """y[rows_a][:, rows_b] against the oracle's GEMM of the oracle's own
+    quantizations of those rows of A and B (each a tuple from _check_quant_rows,
+    which has already compared them with the GPU's codes).  Nothing of the GPU's
+    output enters the expected values."""
+    ca, sa, ga, ra = a
+    cb, sb, gb, rb = b
+    yr, bound = o.gemm(ca, sa, cb, sb, OF[fmt], ga, gb)
+    got = y[torch.from_numpy(ra).to(y.device)][:, torch.from_numpy(rb).to(y.device)].float().cpu().numpy()
+    got = got.astype(np.float64)
     tol = o.gemm_tolerance(bound, yr, out_bf16)
     bad = np.abs(got - yr) > tol
     assert not bad.any(), f"{label}: {bad.sum()} of {bad.size} sampled outputs outside the bound"
@@ -151,19 +152,20 @@ def test_llama1b_mlp_up_step():
     r_m = _sample_rows(bench.M, 6, 2)
     r_n = _sample_rows(bench.N, 6, 3)
     r_k = _sample_rows(bench.K, 6, 4)
-    _check_quant_rows(xn, step.xq, {}, r_m, "fwd X")
-    _check_quant_rows(wn, step.wq, {}, r_n, "fwd W")
-    _check_quant_rows(dyn, step.dyq_n, {"rounding": "sr", "rht": True, "sr_seed": 2, "sr_stream": 0, "rht_seed": 2,
-                                        "sr_offset": off}, r_m, "dY rows")
-    _check_quant_rows(dyn, step.dyq_m, {"rounding": "sr", "rht": True, "sr_seed": 2, "sr_stream": 2, "rht_seed": 2,
-                                        "sr_offset": off, "transpose": True}, r_n, "dY cols")
-    _check_quant_rows(wn, step.wq_t, {"rounding": "sr", "rht": True, "sr_seed": 2, "sr_stream": 1, "rht_seed": 2,
-                                      "sr_offset": off, "transpose": True, "scaling": "2d"}, r_k, "W 2d t")
-    _check_quant_rows(xn, step.xq_t, {"rounding": "sr", "rht": True, "sr_seed": 2, "sr_stream": 3, "rht_seed": 2,
-                                      "sr_offset": off, "transpose": True}, r_k, "X t")
-    _check_gemm_rows(step.xq, step.wq, step.Y, r_m, NV, True, "fprop")
-    _check_gemm_rows(step.dyq_n, step.wq_t, step.dX, r_m, NV, True, "dgrad")
-    _check_gemm_rows(step.dyq_m, step.xq_t, step.dW, r_n, NV, False, "wgrad")
+    # rows of each B operand, i.e. the sampled output columns of its GEMM
+    r_nb = _sample_rows(bench.N, 24, 13)
+    r_kb = _sample_rows(bench.K, 24, 14)
+    sr = {"rounding": "sr", "rht": True, "sr_seed": 2, "rht_seed": 2, "sr_offset": off}
+    xa = _check_quant_rows(xn, step.xq, {}, r_m, "fwd X")
+    wb = _check_quant_rows(wn, step.wq, {}, r_nb, "fwd W")
+    _check_quant_rows(wn, step.wq, {}, r_n, "fwd W rows")
+    dya = _check_quant_rows(dyn, step.dyq_n, {**sr, "sr_stream": 0}, r_m, "dY rows")
+    dyma = _check_quant_rows(dyn, step.dyq_m, {**sr, "sr_stream": 2, "transpose": True}, r_n, "dY cols")
+    wtb = _check_quant_rows(wn, step.wq_t, {**sr, "sr_stream": 1, "transpose": True, "scaling": "2d"}, r_kb, "W 2d t")
+    xtb = _check_quant_rows(xn, step.xq_t, {**sr, "sr_stream": 3, "transpose": True}, r_kb, "X t")
+    _check_gemm_sampled(xa, wb, step.Y, NV, True, "fprop")
+    _check_gemm_sampled(dya, wtb, step.dX, NV, True, "dgrad")
+    _check_gemm_sampled(dyma, xtb, step.dW, NV, False, "wgrad")
     # DGE on the sampled rows of W
     sc = untile_scales(step.wq.scales.cpu().numpy(), bench.N, bench.K // 16)
     g = step.wq.tensor_scale.cpu().numpy()[0]
@@ -218,53 +220,85 @@ def test_dual_quantize_many_tiles_ragged(two_d):
     _check_quant_rows(xn, qc, pcol, cols, "dual cols")
 
 
-def test_ffn7b_gemms_mxfp4():
+def test_ffn7b_step():
+    """The 7B-shaped FFN step the benchmark times (MXFP4, RTN, bf16 out): X, W
+    and dY each quantized in both layouts from one read, then fprop, dgrad and
+    wgrad, in the benchmark's launch configuration.  Sampled rows of every
+    quantized operand bit for bit; sampled rows x sampled columns of every GEMM
+    against the oracle's GEMM of the oracle's quantization of the inputs."""
+    import bench
     from fp4_block_scaled_e8m0_gb300 import inputs
     d = inputs.ffn7b()
     X, W, dY = (d[k].cuda() for k in ("X", "W", "dY"))
     M, K = X.shape
     N = W.shape[0]
-    qx = fp4.fp4_quantize(X, fp4.quant_params(MX))
-    qw = fp4.fp4_quantize(W, fp4.quant_params(MX))
-    y = fp4.fp4_gemm(qx, qw, torch.bfloat16)
-    r_m = _sample_rows(M, 4, 5)
-    _check_quant_rows(d["X"].float().numpy(), qx, {}, r_m, "7b X")
-    _check_gemm_rows(qx, qw, y, r_m, MX, True, "7b fprop")
-    qdy_n, qdy_m = fp4.fp4_quantize_dual(dY, fp4.quant_params(MX), fp4.quant_params(MX, transpose=True))
-    qw_t = fp4.fp4_quantize(W, fp4.quant_params(MX, transpose=True))
-    qx_t = fp4.fp4_quantize(X, fp4.quant_params(MX, transpose=True))
-    dx = fp4.fp4_gemm(qdy_n, qw_t, torch.bfloat16)
-    dw = fp4.fp4_gemm(qdy_m, qx_t, torch.bfloat16)
-    _check_gemm_rows(qdy_n, qw_t, dx, r_m, MX, True, "7b dgrad")
-    _check_gemm_rows(qdy_m, qx_t, dw, _sample_rows(N, 4, 6), MX, True, "7b wgrad")
+    step = bench.FfnStep(fp4, X, W, dY, torch.device("cuda"))
+    step.run(0, side=torch.cuda.Stream())
+    torch.cuda.synchronize()
+    assert fp4.fp4_sync_status() == 0 and fp4.fp4_sync_status(step.side_ctx) == 0
+    xn, wn, dyn = (d[k].float().numpy() for k in ("X", "W", "dY"))
+    r_m, r_n = _sample_rows(M, 4, 5), _sample_rows(N, 4, 6)
+    r_nb, r_kb = _sample_rows(N, 24, 16), _sample_rows(K, 24, 17)
+    t = {"transpose": True}
+    xa = _check_quant_rows(xn, step.xq, {}, r_m, "7b X")
+    wb = _check_quant_rows(wn, step.wq, {}, r_nb, "7b W")
+    dya = _check_quant_rows(dyn, step.dyq_n, {}, r_m, "7b dY rows")
+    wtb = _check_quant_rows(wn, step.wq_t, t, r_kb, "7b W t")
+    dyma = _check_quant_rows(dyn, step.dyq_m, t, r_n, "7b dY cols")
+    xtb = _check_quant_rows(xn, step.xq_t, t, r_kb, "7b X t")
+    _check_gemm_sampled(xa, wb, step.Y, MX, True, "7b fprop")
+    _check_gemm_sampled(dya, wtb, step.dX, MX, True, "7b dgrad")
+    _check_gemm_sampled(dyma, xtb, step.dW, MX, True, "7b wgrad")
+
+
+def _oracle_channel_errors(xn, chunk=1024):
+    """e_c over all rows of xn (NVFP4, the full tensor's amax), by the oracle,
+    one row chunk at a time (fp64 sums)."""
+    amax = o.tensor_amax(xn)
+    g = o.nvfp4_tensor_scale(amax)
+    e = np.zeros(xn.shape[1], np.float64)
+    for r0 in range(0, xn.shape[0], chunk):
+        part = xn[r0:r0 + chunk]
+        c, sc, _ = o.quantize(part, o.NVFP4, given_amax=amax)
+        e += o.hcp_channel_errors(part, c, sc, o.NVFP4, g)
+    return e
 
 
 def test_hcp_square_full():
+    """Hot-channel selection and the compensated GEMM at the benchmark's size.
+    The GPU's hot set equals the oracle's outside a 1e-5 relative band around
+    the h-th largest error (inside it the fp32 sums may order channels
+    differently); the GEMM then runs on the oracle's set and is compared on
+    sampled rows x columns with the oracle's product of the oracle's
+    quantizations."""
     from fp4_block_scaled_e8m0_gb300 import inputs
     d = inputs.hcp_square()
     X, W = d["X"].cuda(), d["W"].cuda()
     M, K = X.shape
-    h = fp4.hcp_num_hot(K)
+    h = fp4.fp4_hcp_num_hot(K)
     assert h == 369
     qx = fp4.fp4_quantize(X, fp4.quant_params(NV))
     qw = fp4.fp4_quantize(W, fp4.quant_params(NV))
-    hot = fp4.fp4_hcp_select(X, qx, h)
-    assert set(d["hot_cols"].tolist()) <= set(hot.cpu().numpy().tolist())
-    y1 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot, h, fp4.FP4_HCP_SINGLE, 2, torch.float32)
-    y2 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot, h, fp4.FP4_HCP_TWO, 2, torch.float32)
-    rows = _sample_rows(M, 3, 7)
-    xn = d["X"].float().numpy()[rows]
+    hot = fp4.fp4_hcp_select(X, qx, h).cpu().numpy()
+    xfull = d["X"].float().numpy()
+    e = _oracle_channel_errors(xfull)
+    hot_o = o.hcp_top_channels(e, h)
+    assert set(d["hot_cols"].tolist()) <= set(hot_o.tolist())
+    t = np.sort(e)[::-1][h - 1]
+    sure_in = set(np.nonzero(e > t * (1 + 1e-5))[0].tolist())
+    sure_out = set(np.nonzero(e < t * (1 - 1e-5))[0].tolist())
+    got = set(hot.tolist())
+    assert sure_in <= got and not (got & sure_out)
+    hot_t = torch.from_numpy(hot_o).cuda()
+    y1 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot_t, h, fp4.FP4_HCP_SINGLE, 2, torch.float32)
+    y2 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot_t, h, fp4.FP4_HCP_TWO, 2, torch.float32)
     wn = d["W"].float().numpy()
-    cx = qx.codes.cpu().numpy()[rows]
-    sx = untile_scales(qx.scales.cpu().numpy(), M, K // 16)[rows]
-    cw = qw.codes.cpu().numpy()
-    sw = untile_scales(qw.scales.cpu().numpy(), W.shape[0], K // 16)
-    gx = qx.tensor_scale.cpu().numpy()[0]
-    gw = qw.tensor_scale.cpu().numpy()[0]
-    yr, bound = o.hcp_gemm(xn, cx, sx, wn, cw, sw, o.NVFP4, gx, gw, hot.cpu().numpy(), 2)
+    cx, sx, gx, rows = _check_quant_rows(xfull, qx, {}, _sample_rows(M, 3, 7), "hcp X")
+    cw, sw, gw, cols = _check_quant_rows(wn, qw, {}, _sample_rows(W.shape[0], 24, 8), "hcp W")
+    yr, bound = o.hcp_gemm(xfull[rows], cx, sx, wn[cols], cw, sw, o.NVFP4, gx, gw, hot_o, 2)
     for y, label in ((y1, "single"), (y2, "two")):
-        got = y.cpu().numpy()[rows].astype(np.float64)
-        assert np.all(np.abs(got - yr) <= 1e-3 * bound), label
+        got_y = y.cpu().numpy()[rows][:, cols].astype(np.float64)
+        assert np.all(np.abs(got_y - yr) <= 1e-3 * bound), label
 
 
 def test_hcp_square_variants_full():
@@ -273,7 +307,7 @@ def test_hcp_square_variants_full():
     d = inputs.hcp_square()
     X, W = d["X"].cuda(), d["W"].cuda()
     M, K = X.shape
-    h = fp4.hcp_num_hot(K)
+    h = fp4.fp4_hcp_num_hot(K)
     qx = fp4.fp4_quantize(X, fp4.quant_params(NV))
     qw = fp4.fp4_quantize(W, fp4.quant_params(NV))
     hot = fp4.fp4_hcp_select(X, qx, h)

@@ -45,7 +45,7 @@ def _data(fmt, M=320, K=512, N=264, seed=1):
 def test_hcp_select_matches_oracle(fmt):
     xt, _, xn, _, planted = _data(fmt)
     K = xn.shape[1]
-    h = fp4.hcp_num_hot(K)
+    h = fp4.fp4_hcp_num_hot(K)
     xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
     got = fp4.fp4_hcp_select(xt.cuda(), xq, h).cpu().numpy()
     assert np.all(np.diff(got) > 0), "indices must be ascending and distinct"
@@ -66,7 +66,7 @@ def test_hcp_select_matches_oracle(fmt):
 def test_hcp_gemm_matches_oracle(fmt, mode, order, out_dtype):
     xt, wt, xn, wn, _ = _data(fmt, seed=2)
     K = xn.shape[1]
-    h = fp4.hcp_num_hot(K)
+    h = fp4.fp4_hcp_num_hot(K)
     xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
     wq = fp4.fp4_quantize(wt.cuda(), fp4.quant_params(fmt))
     cx, sx, gx = o.quantize(xn, FMT[fmt])
@@ -125,7 +125,7 @@ def test_hcp_quantize_zeroed_bit_exact(fmt, sf_layout, rounding):
 def test_hcp_zeroed_gemm_matches_oracle(fmt, mode, out_dtype):
     xt, wt, xn, wn, _ = _data(fmt, seed=5)
     K = xn.shape[1]
-    h = fp4.hcp_num_hot(K)
+    h = fp4.fp4_hcp_num_hot(K)
     cx, sx, gx = o.quantize(xn, FMT[fmt])
     hot = o.hcp_select(xn, cx, sx, FMT[fmt], gx, h)
     hot_d = torch.from_numpy(hot.astype(np.int32)).cuda()
@@ -154,7 +154,7 @@ def test_hcp_fp8_tail_matches_oracle(fmt, order, out_dtype):
     # second GEMM; the oracle uses the same E4M3 values, so the GEMM bound holds
     xt, wt, xn, wn, _ = _data(fmt, seed=6)
     K = xn.shape[1]
-    h = fp4.hcp_num_hot(K)
+    h = fp4.fp4_hcp_num_hot(K)
     cx, sx, gx = o.quantize(xn, FMT[fmt])
     hot = o.hcp_select(xn, cx, sx, FMT[fmt], gx, h)
     hot_d = torch.from_numpy(hot.astype(np.int32)).cuda()

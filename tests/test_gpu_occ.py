@@ -190,8 +190,8 @@ def test_quant_error_stats(fmt, sf_layout):
     q_direct = fp4.fp4_quantize(xd, fp4.quant_params(fmt, sf_layout=sf_layout))
     tau, _ = fp4.fp4_occ_threshold(xd)
     q_occ = fp4.fp4_occ_quantize(xd, fp4.quant_params(fmt, sf_layout=sf_layout), tau)
-    s_direct = fp4.fp4_quant_error_sums(xd, q_direct).cpu().numpy()
-    s_occ = fp4.fp4_quant_error_sums(xd, q_occ, tau).cpu().numpy()
+    s_direct, st_direct = (t.cpu().numpy() for t in fp4.fp4_quant_error_stats(xd, q_direct))
+    s_occ, st_occ = (t.cpu().numpy() for t in fp4.fp4_quant_error_stats(xd, q_occ, tau))
     c, s, g = o.quantize(xn, FMT[fmt])
     h_direct = o.dequantize(c, s, FMT[fmt], g).astype(np.float64)
     h_occ = o.occ_reconstruction(xn, FMT[fmt], o.occ_threshold(xn))
@@ -200,8 +200,12 @@ def test_quant_error_stats(fmt, sf_layout):
         b = hat.reshape(-1)
         want = np.array([a @ a, b @ b, a @ b, ((a - b) ** 2).sum()])
         assert np.allclose(got, want, rtol=1e-9, atol=0), (got, want)
-    st_d = fp4.error_stats_from_sums(s_direct, xn.size)
-    st_o = fp4.error_stats_from_sums(s_occ, xn.size)
-    ref_d = o.quant_error_stats(xn, h_direct)
-    assert abs(st_d["cos"] - ref_d["cos"]) < 1e-9 and abs(st_d["snr_db"] - ref_d["snr_db"]) < 1e-6
+    # the library's cosine / MSE / SNR / relative error against the oracle's
+    for st, hat in ((st_direct, h_direct), (st_occ, h_occ)):
+        got = fp4.stats_dict(st)
+        ref = o.quant_error_stats(xn, hat)
+        assert abs(got["cos"] - ref["cos"]) < 1e-9 and abs(got["snr_db"] - ref["snr_db"]) < 1e-6
+        assert abs(got["mse"] - ref["mse"]) <= 1e-9 * ref["mse"]
+        assert abs(got["rel_err"] - o.relative_error(xn, hat)) <= 1e-9 * o.relative_error(xn, hat)
+    st_d, st_o = fp4.stats_dict(st_direct), fp4.stats_dict(st_occ)
     assert st_o["snr_db"] > st_d["snr_db"] and st_o["cos"] > st_d["cos"]

@@ -182,6 +182,74 @@ def test_quantize_dual_mixed(case, sf_layout):
     _check_quant(qc, o.quantize(xn, o.NVFP4, mode[col_cfg[0]], sc[col_cfg[1]], True, col_cfg[2], **kc), case + " cols")
 
 
+# ---------------------------------------------------------------------------
+# tiny and subnormal blocks
+# ---------------------------------------------------------------------------
+def _tiny_input(shape, seed, fmt):
+    """bf16 values far below 1.  MXFP4: rows scaled by 2^u, u in [-150, -100],
+    so that whole rows and blocks are bf16 subnormals (below 2^-126) or flush
+    to zero in bf16, and others straddle the smallest normal; row 0 holds the
+    hand-derived blocks of tests/golden/mxfp4_tiny_blocks.txt.  NVFP4: rows
+    scaled by 2^u, u in [-140, -100], with one element 2^-100, the tensor amax:
+    the tensor scale stays normal, blocks near 2^-110 keep small E4M3 scales and
+    the subnormal blocks get scale 0 (all codes 0)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape).astype(np.float64)
+    lo = -150 if fmt == fp4.FP4_FMT_MXFP4 else -140
+    x *= np.exp2(rng.uniform(lo, -100, (shape[0], 1)))
+    if fmt == fp4.FP4_FMT_MXFP4:
+        from conftest import golden
+        rows = golden("mxfp4_tiny_blocks.txt")
+        blocks = sorted({r[0] for r in rows})
+        x[0, : 32 * len(blocks)] = 0.0
+        for r in rows:
+            if r[1] != "scale":
+                x[0, 32 * blocks.index(r[0]) + int(r[1])] = float.fromhex(r[2])
+    else:
+        x = np.clip(x, -2.0 ** -101, 2.0 ** -101)
+        x[3, 17] = 2.0 ** -100
+    t = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    return t, t.float().numpy()
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+@pytest.mark.parametrize("rounding", [fp4.FP4_ROUND_RTN, fp4.FP4_ROUND_SR])
+@pytest.mark.parametrize("layout", ["rows", "cols", "dual"])
+def test_quantize_tiny_blocks(fmt, rounding, layout):
+    """Codes and scales of tiny / bf16-subnormal blocks, bit for bit: the E8M0
+    clamp, the subnormal amax's true exponent, no flush to zero of subnormal
+    inputs or of the 2^-127 scale; then the dequantized values (fp32 and bf16)."""
+    x, xn = _tiny_input((160, 288), 90 + fmt, fmt)
+    assert np.count_nonzero(np.abs(xn) < 2.0 ** -126) > 1000            # subnormals are present
+    x = x.cuda()
+    mode = "sr" if rounding else "rtn"
+    kw = dict(sr_seed=11, sr_offset=5, sr_stream=3)
+    pr = fp4.quant_params(fmt, rounding, **kw)
+    pc = fp4.quant_params(fmt, rounding, transpose=True, **kw)
+    outs = []
+    if layout == "rows":
+        outs.append((fp4.fp4_quantize(x, pr), False))
+    elif layout == "cols":
+        outs.append((fp4.fp4_quantize(x, pc), True))
+    else:
+        qr, qc = fp4.fp4_quantize_dual(x, pr, pc)
+        outs += [(qr, False), (qc, True)]
+    for q, tr in outs:
+        want = o.quantize(xn, FMT[fmt], mode, transpose=tr, **kw)
+        _check_quant(q, want, f"tiny {layout} t={tr} fmt={fmt} {mode}")
+        for out_dtype in (torch.float32, torch.bfloat16):
+            got = fp4.fp4_dequantize(q, out_dtype).float().cpu().numpy()
+            wd = o.dequantize(want[0], want[1], FMT[fmt], want[2])
+            if out_dtype == torch.bfloat16:
+                wd = o.bf16_round(wd)
+            assert np.array_equal(got.view(np.uint32), wd.view(np.uint32)), \
+                mismatch_report(got.view(np.uint32), wd.view(np.uint32), f"tiny dequant {out_dtype}")
+        if fmt == fp4.FP4_FMT_MXFP4 and not tr:
+            # the hand-derived blocks: row 0, blocks 0..2 (bytes 0, 0, 1)
+            _, sc, _ = _gpu_quant_np(q)
+            assert sc[0, :3].tolist() == [0, 0, 1]
+
+
 @pytest.mark.parametrize("axis", [-1, 0, 1])
 @pytest.mark.parametrize("shape", [(320, 208), (48, 40)])
 def test_amax(axis, shape):

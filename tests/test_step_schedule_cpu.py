@@ -1,16 +1,20 @@
-"""The benchmark step's two-stream schedule, checked on the host: every pair of
+"""The benchmark steps' two-stream schedules, checked on the host: every pair of
 ops that touch the same buffer (one of them writing it) is ordered by the
 schedule's happens-before relation -- program order on each stream, the
-cross-stream waits of `bench.Step.WAITS`, the fork at the step's start and the
+cross-stream waits of the step's WAITS, the fork at the step's start and the
 join at its end -- and the ops sharing a context run on one stream.
 
-The buffers each op reads and writes are listed here from the step's data flow
-(quantize X and W, fprop, quantize dY, dgrad, wgrad, DGE on W).  A context's
-NVFP4 amax scratch is checked separately: the side ops pass the step's side
-context, so each context's calls stay on one stream.
+The buffers each op reads and writes are listed here from the steps' data flow
+(quantize X and W, fprop, quantize dY, dgrad, wgrad, and for the NVFP4 step the
+DGE on W).  A context's NVFP4 amax scratch is checked separately: the side ops
+pass the step's side context, so each context's calls stay on one stream.  Both
+steps are checked: the 7B FFN step the benchmark's headline times (bench.FfnStep)
+and the LLaMA-1B NVFP4 step (bench.Step).
 """
 import itertools
 from types import SimpleNamespace
+
+import pytest
 
 import bench
 
@@ -34,21 +38,26 @@ WRITES = {
 }
 
 
-def _op_names():
-    step = object.__new__(bench.Step)      # the op list only; no buffers are touched
+STEPS = {"llama": bench.Step, "ffn": bench.FfnStep}
+FFN_OPS = ("quant_x_dual", "quant_w_dual", "fprop", "quant_dy_dual", "dgrad", "wgrad")
+
+
+def _op_names(cls=bench.Step):
+    step = object.__new__(cls)             # the op list only; no buffers are touched
     step.fp4 = None
     step.p_dy_n = step.p_w_t = step.p_dy_m = step.p_x_t = SimpleNamespace()
+    step.p_rows = step.p_cols = SimpleNamespace()
     return [name for name, _ in step.ops(0)]
 
 
-def _schedule(names):
+def _schedule(names, cls=bench.Step):
     """(stream of each op, happens-before as a set of (earlier, later) pairs)."""
-    stream = {n: ("side" if n in bench.Step.SIDE else "main") for n in names}
+    stream = {n: ("side" if n in cls.SIDE else "main") for n in names}
     hb = set()
     for a, b in itertools.combinations(names, 2):          # enqueue order on one stream
         if stream[a] == stream[b]:
             hb.add((a, b))
-    for later, earlier in bench.Step.WAITS.items():        # a side wait: `later` after `earlier`
+    for later, earlier in cls.WAITS.items():               # a side wait: `later` after `earlier`
         hb.add((earlier, later))
     # transitive closure
     changed = True
@@ -70,16 +79,20 @@ def _unordered_conflicts(names, hb):
     return out
 
 
-def test_every_conflicting_pair_is_ordered():
-    names = _op_names()
-    assert set(names) == set(READS) == set(WRITES)
-    _, hb = _schedule(names)
+@pytest.mark.parametrize("which", sorted(STEPS))
+def test_every_conflicting_pair_is_ordered(which):
+    cls = STEPS[which]
+    names = _op_names(cls)
+    assert set(names) == (set(READS) if which == "llama" else set(FFN_OPS))
+    _, hb = _schedule(names, cls)
     assert _unordered_conflicts(names, hb) == []
 
 
-def test_readers_come_after_their_producers():
-    names = _op_names()
-    _, hb = _schedule(names)
+@pytest.mark.parametrize("which", sorted(STEPS))
+def test_readers_come_after_their_producers(which):
+    cls = STEPS[which]
+    names = _op_names(cls)
+    _, hb = _schedule(names, cls)
     producer = {buf: op for op, bufs in WRITES.items() for buf in bufs}
     for op in names:
         for buf in READS[op]:
@@ -87,20 +100,25 @@ def test_readers_come_after_their_producers():
                 assert (producer[buf], op) in hb, f"{op} may read {buf} before {producer[buf]} writes it"
 
 
-def test_each_context_serves_one_stream():
-    names = _op_names()
-    stream, _ = _schedule(names)
+@pytest.mark.parametrize("which", sorted(STEPS))
+def test_each_context_serves_one_stream(which):
+    cls = STEPS[which]
+    names = _op_names(cls)
+    stream, _ = _schedule(names, cls)
     # side ops pass the side context, the others the default one
-    assert {stream[n] for n in names if n in bench.Step.SIDE} == {"side"}
-    assert {stream[n] for n in names if n not in bench.Step.SIDE} == {"main"}
+    assert {stream[n] for n in names if n in cls.SIDE} == {"side"}
+    assert {stream[n] for n in names if n not in cls.SIDE} == {"main"}
 
 
-def test_the_schedule_overlaps_independent_work():
+@pytest.mark.parametrize("which", sorted(STEPS))
+def test_the_schedule_overlaps_independent_work(which):
     """The point of the second stream: the two forward quantizations, and dgrad
     with wgrad, are not ordered against each other."""
-    names = _op_names()
-    _, hb = _schedule(names)
-    for a, b in (("quant_x_dual", "quant_w_dual"), ("dgrad", "wgrad"), ("dgrad", "dge")):
+    cls = STEPS[which]
+    names = _op_names(cls)
+    _, hb = _schedule(names, cls)
+    pairs = [("quant_x_dual", "quant_w_dual"), ("dgrad", "wgrad")] + ([("dgrad", "dge")] if which == "llama" else [])
+    for a, b in pairs:
         assert (a, b) not in hb and (b, a) not in hb
 
 
