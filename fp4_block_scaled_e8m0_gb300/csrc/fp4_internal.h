@@ -129,6 +129,8 @@ struct GemmArgs {
   int64_t occ_ldt;
 };
 int launch_gemm(const GemmArgs& g, cudaStream_t st);  // returns fp4 status
+// the CTA-pair kernel (gemm2.cu): plain FP4 GEMM, no extra columns, no C +=
+int launch_gemm_pair(const GemmArgs& g, cudaStream_t st);
 
 // Hot-channel compensation (hcp.cu)
 cudaError_t launch_hcp_channel_errors(const uint16_t* x, int64_t ldx, const fp4_operand& q, float* err,

@@ -35,6 +35,7 @@
 #include <mutex>
 
 #include "fp4_device.cuh"
+#include "tcgen05.cuh"
 
 namespace fp4 {
 namespace {
@@ -57,7 +58,6 @@ constexpr int NUM_THREADS = 32 * (6 + NUM_EPI_WARPS);
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = BN;      // scale-factor slots after the accumulator
 constexpr uint32_t SF_SLOT_COLS = 48;      // 16 (A) + 32 (B) columns per scale slot
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 static_assert(TMEM_SF_BASE + SF_SLOTS * SF_SLOT_COLS <= TMEM_COLS, "tensor memory");
 
 struct Params {
@@ -84,201 +84,7 @@ struct Params {
   const float* col_scale;
 };
 
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-  return ok != 0;
-}
-
-// Bounded wait: returns false (and raises the abort flag + status word) when the
-// barrier phase does not complete within WAIT_LIMIT_NS or another thread of
-// the CTA has already aborted.
-// The time limit and the abort flag are checked only every 1024 polls: reading
-// %globaltimer is slow, and a check after every failed poll delays the wake-up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = 0;
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 1023u) == 0) {
-      if (*abort_flag) return false;
-      const uint64_t now = fp4dev::globaltimer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > WAIT_LIMIT_NS) {
-        *abort_flag = 1;
-        atomicOr(status, FP4_DEVICE_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-
-
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-// shared-memory matrix descriptor (K-major, 128-byte swizzle; SBO = 1024 B
-// between 8-row groups)
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-  d |= (uint64_t)(1) << 16;                  // leading byte offset (unused with swizzle)
-  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
-  d |= (uint64_t)1 << 46;                    // descriptor version (sm_100 family)
-  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-  return d;
-}
-
-// instruction descriptors
-__device__ __forceinline__ uint32_t idesc_fp4(bool ue8m0, uint32_t sf_id) {
-  uint32_t d = 0;
-  d |= sf_id << 4;              // B scale-factor byte
-  d |= 1u << 7;                 // A: E2M1
-  d |= 1u << 10;                // B: E2M1
-  d |= (uint32_t)(BN >> 3) << 17;
-  d |= (ue8m0 ? 1u : 0u) << 23; // scale type: 1 = UE8M0, 0 = UE4M3
-  d |= (uint32_t)(BM >> 4) << 24;
-  d |= sf_id << 29;             // A scale-factor byte
-  return d;
-}
-// kind::f8f6f4 with E4M3 A and B (type code 0), F32 accumulation
-__device__ __forceinline__ uint32_t idesc_e4m3() {
-  uint32_t d = 0;
-  d |= 1u << 4;                 // accumulate in F32
-  d |= (uint32_t)(BN >> 3) << 17;
-  d |= (uint32_t)(BM >> 4) << 24;
-  return d;
-}
-__device__ __forceinline__ uint32_t idesc_bf16() {
-  uint32_t d = 0;
-  d |= 1u << 4;                 // accumulate in F32
-  d |= 1u << 7;                 // A: BF16
-  d |= 1u << 10;                // B: BF16
-  d |= (uint32_t)(BN >> 3) << 17;
-  d |= (uint32_t)(BM >> 4) << 24;
-  return d;
-}
-
-__device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t acc, bool nvfp4) {
-  if (nvfp4) {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa_tmem), "r"(sfb_tmem));
-  } else {
-    asm volatile(
-        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa_tmem), "r"(sfb_tmem));
-  }
-}
-__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
-}
-
-__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-// 32 lanes x 16 / 32 consecutive 32-bit columns of tensor memory, one register each
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
-               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Accumulator rows -> coalesced stores.  tcgen05.ld (32x32b) gives lane t the
-// 32 words of row t; stored as is, every store instruction would touch 32
-// rows.  Exchanging lane bits 4..2 with word bits 4..2 (three butterfly
-// stages of shfl.xor; at stage m the lanes with bit m set trade their words j,
-// j without bit m, for their partner's words j + m) leaves lane 4b + a holding
-// w[4v + k] = (row 4v + a, word column 4b + k): each lane has 4 consecutive
-// words of one row for every v, and one 16-byte store per lane covers four
-// whole 128-byte row segments per warp instruction.
-__device__ __forceinline__ void warp_exchange_hi3(uint32_t* w, int lane) {
-#pragma unroll
-  for (int m = 16; m >= 4; m >>= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j & m) continue;
-      const uint32_t send = upper ? w[j] : w[j + m];
-      const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
-      if (upper)
-        w[j] = recv;
-      else
-        w[j + m] = recv;
-    }
-  }
-}
+using namespace tc;
 
 // After warp_exchange_hi3 on 32 columns of fp32 accumulators: lane 4b + a
 // writes columns col0 + 4b .. +3 of rows row0 + 4v + a (times alpha; C += when
@@ -592,8 +398,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // address (16-byte units) by s * SLAB_BYTES / 16 + 2 k, which stays inside
       // the 14-bit field; the instruction descriptors are constants.
       const uint64_t da0 = desc_sw128(smem_u32(stage_a(0))), db0 = desc_sw128(smem_u32(stage_b(0)));
-      const uint32_t id_even = idesc_fp4(!nvfp4, 0u), id_odd = idesc_fp4(!nvfp4, nvfp4 ? 0u : 2u);
-      const uint32_t id_ext = p.ext_fp8 ? idesc_e4m3() : idesc_bf16();
+      const uint32_t id_even = idesc_fp4(!nvfp4, 0u, BM, BN), id_odd = idesc_fp4(!nvfp4, nvfp4 ? 0u : 2u, BM, BN);
+      const uint32_t id_ext = p.ext_fp8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN);
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
         if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.status)) { ok = false; break; }
         acc_phase ^= 1;
@@ -847,6 +653,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+}  // namespace
+
+namespace tc {
 // ---------------------------------------------------------------------------
 // host side: tensor maps
 // ---------------------------------------------------------------------------
@@ -854,7 +663,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn get_encode_fn() {
+static EncodeTiledFn get_encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -897,13 +706,16 @@ bool make_sf_map(CUtensorMap* m, const void* base, int64_t group_bytes, int64_t 
   return r == CUDA_SUCCESS;
 }
 
-}  // namespace
+}  // namespace tc
 
 int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   const fp4_operand& A = *g.A;
   const fp4_operand& B = *g.B;
   const int64_t M = A.rows, N = B.rows;
   if (M == 0 || N == 0) return FP4_OK;
+  // the plain GEMM runs on CTA pairs; extra K columns, the outlier epilogue,
+  // row/column scales and C += stay on the one-SM kernel
+  if (g.fp4_part && g.kx == 0 && !g.occ_len && !g.row_scale && !g.accumulate) return launch_gemm_pair(g, st);
   Params p{};
   p.M = (int)M;
   p.N = (int)N;
@@ -934,16 +746,16 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   bool ok = true;
   if (g.fp4_part) {
     const int64_t group_bytes = (int64_t)128 * nsf_padded(A.k, A.format);
-    ok &= make_map(&ta, A.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.k / 2, M, BM);
-    ok &= make_map(&tb, B.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B.k / 2, N, BN);
-    ok &= make_sf_map(&tsa, A.scales, group_bytes, cdiv(M, 128), p.sf_atoms * 4, 1);
-    ok &= make_sf_map(&tsb, B.scales, group_bytes, cdiv(N, 128), p.sf_atoms * 4, BN / 128);
+    ok &= tc::make_map(&ta, A.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.k / 2, M, BM);
+    ok &= tc::make_map(&tb, B.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B.k / 2, N, BN);
+    ok &= tc::make_sf_map(&tsa, A.scales, group_bytes, cdiv(M, 128), p.sf_atoms * 4, 1);
+    ok &= tc::make_sf_map(&tsb, B.scales, group_bytes, cdiv(N, 128), p.sf_atoms * 4, BN / 128);
   }
   if (g.kx > 0) {
     const CUtensorMapDataType edt = g.ext_fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int eb = g.ext_fp8 ? 1 : 2;
-    ok &= make_map(&tax, g.a_ext, edt, eb, g.kx, M, BM);
-    ok &= make_map(&tbx, g.b_ext, edt, eb, g.kx, N, BN);
+    ok &= tc::make_map(&tax, g.a_ext, edt, eb, g.kx, M, BM);
+    ok &= tc::make_map(&tbx, g.b_ext, edt, eb, g.kx, N, BN);
   }
   if (!g.fp4_part) {  // residual-only GEMM: no FP4 stages, the maps are never read
     ta = tax;

@@ -1,0 +1,405 @@
+// Block-scaled FP4 GEMM on CTA pairs (tcgen05 cta_group::2), sm_103a.
+//
+//   C[M,N] = alpha * sum_k A[m,k] B[n,k]      (TN, both operands K-major)
+//
+// The quantized matmul that carries ">95% of the compute" ([msr] §四), E2M1
+// operands with per-block scales (E8M0 / block 32 = MXFP4, E4M3 / block 16 =
+// NVFP4, [lowprec] §1.1), FP32 accumulation in tensor memory.
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 output tile: CTA r
+// holds rows [128 r, 128 r + 128) of the tile's A rows and of its B rows in
+// shared memory, and the pair leader (r = 0) issues one M = 256, N = 256 MMA
+// per 64 K elements that reads both CTAs' operands; each CTA's tensor memory
+// receives its 128 rows x 256 columns of the accumulator.  Per K step of 256
+// elements an SM takes in 32 KB of codes for 2 * 128 * 256 * 256 flop, a
+// third less than a one-SM 128 x 256 tile, so the stage ring holds more K
+// steps and the tensor pipe waits less for operands.
+//
+// Warp roles in each CTA of the pair (one CTA per SM, persistent over tiles):
+//   warp 0       TMA producer: this CTA's A and B slabs (128-byte K slabs,
+//                128-byte swizzle), counted on the pair leader's "full"
+//                barrier of the stage, and the stage's scale atoms (this
+//                CTA's 128 A rows, all 256 B rows of the tile), counted on its
+//                own "sf_full" barrier
+//   warp 1       tensor-memory allocation (both CTAs); in the leader one lane
+//                issues the pair MMAs and commits each stage to both CTAs'
+//                "empty" barriers
+//   warps 2-5    scale stagers, one per tensor-memory lane quadrant: copy the
+//                stage's scale factors shared -> registers -> this CTA's
+//                tensor memory (tcgen05.st) and arrive on the leader's "full"
+//                barrier, so the MMA thread waits on one barrier per stage
+//   warps 6-21   epilogue: 64 accumulator columns each, both 32-column loads
+//                in flight, one wait, the accumulator released to the leader,
+//                then * alpha and stores
+// The scales reach tensor memory through tcgen05.st rather than tcgen05.cp:
+// a pair copy of a 512-byte atom held the tensor pipe ~90 cycles (NVFP4 has 12
+// atoms per stage next to 4 MMAs of ~136 cycles), the stores run beside the MMAs.
+// Every wait is bounded (globaltimer); a wait that gives up sets the context's
+// status word and the CTA drains and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "fp4_device.cuh"
+#include "tcgen05.cuh"
+
+namespace fp4 {
+namespace {
+
+using namespace tc;
+
+constexpr int P_BM = 128;                 // A rows per CTA (256 per pair)
+constexpr int P_BN = 256;                 // output columns per tile (128 B rows per CTA)
+constexpr int P_KSLAB = 128;              // bytes of K per stage per row (256 elements)
+constexpr int P_A_TILE = 128 * P_KSLAB;   // 16 KB
+constexpr int P_B_TILE = 128 * P_KSLAB;   // 16 KB
+constexpr int P_EPI_WARPS = 16;
+constexpr int P_THREADS = 32 * (6 + P_EPI_WARPS);
+constexpr uint32_t P_TMEM_COLS = 512;
+
+template <bool NV>
+struct PairCfg {
+  static constexpr int ATOMS = NV ? 4 : 2;                  // scale atoms per 128 rows per stage
+  static constexpr int SFA_BYTES = ATOMS * 512;             // this CTA's 128 A rows
+  static constexpr int SFB_BYTES = 2 * ATOMS * 512;         // all 256 B rows of the tile
+  static constexpr int STAGE = P_A_TILE + P_B_TILE + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGES = NV ? 5 : 6;
+  static constexpr uint32_t SLOT_COLS = 12 * ATOMS;         // tensor-memory columns of a stage's scales
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM = STAGES * STAGE + BAR_BYTES + 1024;
+  static_assert(STAGE % 1024 == 0, "stage alignment (128-byte swizzle)");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(P_BN + STAGES * SLOT_COLS <= P_TMEM_COLS, "tensor memory");
+};
+
+struct PairParams {
+  int M, N;
+  int k_tiles;        // K stages (256 elements each)
+  const float* ts_a;  // NVFP4 tensor scales (alpha = ts_a * ts_b), null for MXFP4
+  const float* ts_b;
+  void* C;
+  int64_t ldc;
+  unsigned int* status;
+  int tiles_m, tiles_n;   // 256 x 256 tiles
+};
+
+template <bool NV, bool BF16_OUT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
+    fp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                         const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
+                         const PairParams p) {
+  using Cfg = PairCfg<NV>;
+  constexpr int STAGES = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE);   // leader: slabs landed, scales staged
+  uint64_t* empty = full + STAGES;                                             // stage consumed by the MMAs
+  uint64_t* sf_full = empty + STAGES;                                          // this CTA's scale atoms landed
+  uint64_t* acc_full = sf_full + STAGES;
+  uint64_t* acc_empty = acc_full + 1;                                          // leader: both epilogues done
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  auto stage_a = [&](int s) { return smem + s * Cfg::STAGE; };
+  auto stage_b = [&](int s) { return smem + s * Cfg::STAGE + P_A_TILE; };
+  auto stage_sfa = [&](int s) { return smem + s * Cfg::STAGE + P_A_TILE + P_B_TILE; };
+  auto stage_sfb = [&](int s) { return smem + s * Cfg::STAGE + P_A_TILE + P_B_TILE + Cfg::SFA_BYTES; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1 + 8);              // the leader's producer + 4 stager warps in each CTA
+      mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * P_EPI_WARPS);    // every epilogue warp of both CTAs
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(P_TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  tc_fence_before();
+  cluster_sync();            // barriers initialised and tensor memory allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  // the leader's barriers as seen from this CTA
+  const uint32_t full_l = mapa_cluster(&full[0], 0);
+  const uint32_t acc_empty_l = mapa_cluster(acc_empty, 0);
+
+  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int s = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+        const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+        const int row_a = tm * 256 + (int)rank * 128, row_b = tn * 256 + (int)rank * 128;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(&empty[s], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (leader) mbar_expect_tx(&full[s], 2 * (P_A_TILE + P_B_TILE));
+          const uint32_t fb = full_l + (uint32_t)s * 8u;
+          tma_load_2d_pair(stage_a(s), &tm_a, fb, kt * P_KSLAB, row_a);
+          tma_load_2d_pair(stage_b(s), &tm_b, fb, kt * P_KSLAB, row_b);
+          mbar_expect_tx(&sf_full[s], Cfg::SFA_BYTES + Cfg::SFB_BYTES);
+          tma_load_3d(stage_sfa(s), &tm_sfa, &sf_full[s], 0, kt * Cfg::ATOMS * 4, 2 * tm + (int)rank);
+          tma_load_3d(stage_sfb(s), &tm_sfb, &sf_full[s], 0, kt * Cfg::ATOMS * 4, 2 * tn);
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+      }
+      // drain: wait until every stage loaded has been consumed, so that no copy
+      // is in flight when the CTA exits
+      for (int i = 0; i < STAGES; ++i) {
+        mbar_drain_wait(&empty[s], phase ^ 1, p.status);
+        if (++s == STAGES) { s = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (pair leader) ----------------
+    if (leader && lane == 0) {
+      int s = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      const uint64_t da0 = desc_sw128(smem_u32(stage_a(0))), db0 = desc_sw128(smem_u32(stage_b(0)));
+      const uint32_t id_even = idesc_fp4(!NV, 0u, 256, P_BN), id_odd = idesc_fp4(!NV, NV ? 0u : 2u, 256, P_BN);
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+        if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+        acc_phase ^= 1;
+        tc_fence_after();
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          if (!mbar_wait(&full[s], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t da = da0 + (uint64_t)(s * (Cfg::STAGE >> 4)), db = db0 + (uint64_t)(s * (Cfg::STAGE >> 4));
+          const uint32_t slot = tmem + P_BN + (uint32_t)s * Cfg::SLOT_COLS;
+          const uint32_t acc0 = kt > 0 ? 1u : 0u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // scale columns of 64-element K chunk j: NVFP4 one atom per chunk,
+            // MXFP4 one atom per two chunks (bytes 0-1 / 2-3 chosen by the
+            // instruction descriptor); B's two 128-row groups side by side
+            const uint32_t a_col = NV ? 4u * j : 4u * (j >> 1);
+            const uint32_t b_col = 4u * Cfg::ATOMS + (NV ? 8u * j : 8u * (j >> 1));
+            mma_fp4_pair<NV>(tmem, da + 2 * j, db + 2 * j, (!NV && (j & 1)) ? id_odd : id_even, slot + a_col,
+                             slot + b_col, j > 0 ? 1u : acc0);
+          }
+          tc_commit_pair(&empty[s], 0x3);
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit_pair(acc_full, 0x3);
+      }
+      // no MMA may be in flight when the allocation is released
+      tc_commit_pair(drain, 0x1);
+      mbar_drain_wait(drain, 0, nullptr);
+    }
+  } else if (warp < 6) {
+    // ---------------- scale stagers (warps 2..5) ----------------
+    // The tensor-memory image of each 512-byte atom equals a 32x128b.warpx4
+    // copy: lane 32q + i, columns c..c+3 of the atom's place hold the 16 bytes
+    // of the atom's shared-memory row i, for every lane quadrant q.  A stage's
+    // slot: A's atoms (4 columns each), then for each atom of B its two
+    // 128-row groups side by side (columns 8a + 4g after A's).
+    const int quad = warp & 3;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    int s = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+      for (int kt = 0; kt < p.k_tiles; ++kt) {
+        bool got = true;
+        if (lane == 0) got = mbar_wait(&sf_full[s], phase, abort_flag, p.status);
+        if (__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) == 0) { ok = false; break; }
+        const uint32_t slot = tmem + lane_base + P_BN + (uint32_t)s * Cfg::SLOT_COLS;
+        uint32_t v[16];
+#pragma unroll
+        for (int a = 0; a < Cfg::ATOMS; ++a) {
+          const uint4 w = *reinterpret_cast<const uint4*>(stage_sfa(s) + a * 512 + lane * 16);
+          v[4 * a] = w.x; v[4 * a + 1] = w.y; v[4 * a + 2] = w.z; v[4 * a + 3] = w.w;
+        }
+        if constexpr (NV) tmem_st16(slot, v);
+        else tmem_st8(slot, v);
+#pragma unroll
+        for (int piece = 0; piece < Cfg::ATOMS / 2; ++piece) {
+#pragma unroll
+          for (int a2 = 0; a2 < 2; ++a2) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              const int a = piece * 2 + a2;
+              const uint4 w =
+                  *reinterpret_cast<const uint4*>(stage_sfb(s) + g * Cfg::ATOMS * 512 + a * 512 + lane * 16);
+              const int c = (a2 * 2 + g) * 4;
+              v[c] = w.x; v[c + 1] = w.y; v[c + 2] = w.z; v[c + 3] = w.w;
+            }
+          }
+          tmem_st16(slot + 4u * Cfg::ATOMS + 16u * piece, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(full_l + (uint32_t)s * 8u);
+        if (++s == STAGES) { s = 0; phase ^= 1; }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 6..21) ----------------
+    const int quad = warp & 3;               // tensor-memory lanes 32*quad .. +31
+    const int slice = (warp - 6) >> 2;       // accumulator columns 64*slice .. +63
+    uint32_t acc_phase = 0;
+    float alpha = 1.0f;
+    if (NV) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+    for (int tile = pair; tile < num_tiles; tile += npairs) {
+      const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(acc_full, acc_phase, abort_flag, p.status);
+      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      acc_phase ^= 1;
+      tc_fence_after();
+      const int row0 = tm * 256 + (int)rank * 128 + quad * 32;   // this warp's 32 rows
+      const int colw = tn * P_BN + slice * 64;                    // first output column of the slice
+      const bool any = row0 < p.M && colw < p.N;                  // warp-uniform
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(slice * 64);
+      uint32_t r2[2][32];
+      tmem_ld32_nowait(taddr, r2[0]);
+      tmem_ld32_nowait(taddr + 32, r2[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty_l);
+      if (!any) continue;
+      if constexpr (BF16_OUT) {
+        // word i packs columns 2i, 2i + 1 of the slice; after the exchange lane
+        // 4b + a holds columns colw + 8b .. +7 of rows row0 + 4v + a
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t* r = r2[i >> 4];
+          const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * (i & 15)]), alpha),
+                                                         __fmul_rn(__uint_as_float(r[2 * (i & 15) + 1]), alpha));
+          pk[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        warp_exchange_hi3(pk, lane);
+        const int a = lane & 3, c = colw + 8 * (lane >> 2);
+        if (c < p.N) {
+          const bool full8 = c + 8 <= p.N;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const int row = row0 + 4 * v + a;
+            if (row >= p.M) break;
+            uint16_t* q = static_cast<uint16_t*>(p.C) + (int64_t)row * p.ldc + c;
+            if (full8) {
+              *reinterpret_cast<uint4*>(q) = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (c + k >= p.N) break;
+                q[k] = (uint16_t)(pk[4 * v + (k >> 1)] >> (16 * (k & 1)));
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t* w = r2[h];
+          warp_exchange_hi3(w, lane);
+          const int a = lane & 3, c = colw + 32 * h + 4 * (lane >> 2);
+          if (c >= p.N) continue;
+          const bool full4 = c + 4 <= p.N;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const int row = row0 + 4 * v + a;
+            if (row >= p.M) break;
+            float* q = static_cast<float*>(p.C) + (int64_t)row * p.ldc + c;
+            float x[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[k] = __fmul_rn(__uint_as_float(w[4 * v + k]), alpha);
+            if (full4) {
+              *reinterpret_cast<float4*>(q) = make_float4(x[0], x[1], x[2], x[3]);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                if (c + k >= p.N) break;
+                q[k] = x[k];
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();            // no peer access (remote arrives, commits, MMAs) after this point
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(P_TMEM_COLS));
+  }
+}
+
+template <bool NV, bool BF16_OUT>
+int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
+                const PairParams& p, int num_sms, cudaStream_t st) {
+  using Cfg = PairCfg<NV>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fp4_gemm_pair_kernel<NV, BF16_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM) != cudaSuccess)
+      return FP4_ERR_CUDA;
+    attr_set = true;
+  }
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int pairs = std::max(1, std::min(tiles, num_sms / 2));
+  fp4_gemm_pair_kernel<NV, BF16_OUT><<<2 * pairs, P_THREADS, Cfg::SMEM, st>>>(ta, tb, tsa, tsb, p);
+  return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_gemm_pair(const GemmArgs& g, cudaStream_t st) {
+  const fp4_operand& A = *g.A;
+  const fp4_operand& B = *g.B;
+  const int64_t M = A.rows, N = B.rows;
+  if (M == 0 || N == 0) return FP4_OK;
+  const bool nv = A.format == FP4_FMT_NVFP4;
+  PairParams p{};
+  p.M = (int)M;
+  p.N = (int)N;
+  p.k_tiles = (int)cdiv(A.k, 256);
+  p.ts_a = nv ? A.tensor_scale : nullptr;
+  p.ts_b = nv ? B.tensor_scale : nullptr;
+  p.C = g.C;
+  p.ldc = g.ldc;
+  p.status = g.status;
+  p.tiles_m = (int)cdiv(M, 256);
+  p.tiles_n = (int)cdiv(N, P_BN);
+  if (p.k_tiles == 0) return FP4_ERR_INVALID_ARG;
+  const int atoms = nv ? 4 : 2;
+  const int64_t group_bytes = (int64_t)128 * nsf_padded(A.k, A.format);
+  CUtensorMap ta{}, tb{}, tsa{}, tsb{};
+  bool ok = tc::make_map(&ta, A.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.k / 2, M, P_BM);
+  ok &= tc::make_map(&tb, B.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B.k / 2, N, 128);
+  ok &= tc::make_sf_map(&tsa, A.scales, group_bytes, cdiv(M, 128), atoms * 4, 1);
+  ok &= tc::make_sf_map(&tsb, B.scales, group_bytes, cdiv(N, 128), atoms * 4, 2);
+  if (!ok) return FP4_ERR_CUDA;
+  const bool bf16 = g.out_dtype == FP4_DTYPE_BF16;
+  if (nv) return bf16 ? launch_pair<true, true>(ta, tb, tsa, tsb, p, g.num_sms, st)
+                      : launch_pair<true, false>(ta, tb, tsa, tsb, p, g.num_sms, st);
+  return bf16 ? launch_pair<false, true>(ta, tb, tsa, tsb, p, g.num_sms, st)
+              : launch_pair<false, false>(ta, tb, tsa, tsb, p, g.num_sms, st);
+}
+
+}  // namespace fp4
