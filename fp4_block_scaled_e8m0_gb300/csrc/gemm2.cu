@@ -219,9 +219,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     bool ok = true;
     for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
       for (int kt = 0; kt < p.k_tiles; ++kt) {
-        bool got = true;
-        if (lane == 0) got = mbar_wait(&sf_full[s], phase, abort_flag, p.status);
-        if (__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) == 0) { ok = false; break; }
+        // one lane polls, the four stager warps meet at a named barrier
+        if (warp == 2 && lane == 0) (void)mbar_wait(&sf_full[s], phase, abort_flag, p.status);
+        named_sync(1, 4 * 32);
+        if (*abort_flag) { ok = false; break; }
         const uint32_t slot = tmem + lane_base + P_BN + (uint32_t)s * Cfg::SLOT_COLS;
         uint32_t v[16];
 #pragma unroll
@@ -262,10 +263,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     if (NV) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     for (int tile = pair; tile < num_tiles; tile += npairs) {
       const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(acc_full, acc_phase, abort_flag, p.status);
-      ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
+      // one lane polls, the sixteen epilogue warps meet at a named barrier
+      if (warp == 6 && lane == 0) (void)mbar_wait(acc_full, acc_phase, abort_flag, p.status);
+      named_sync(2, P_EPI_WARPS * 32);
+      if (*abort_flag) break;
       acc_phase ^= 1;
       tc_fence_after();
       const int row0 = tm * 256 + (int)rank * 128 + quad * 32;   // this warp's 32 rows
