@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIBNAME = "libfp4gb300.so"
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm2.cu", "hcp.cu", "occ.cu"]
+SOURCES = ["api.cu", "quant.cu", "quant_mx.cu", "gemm.cu", "gemm2.cu", "hcp.cu", "occ.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

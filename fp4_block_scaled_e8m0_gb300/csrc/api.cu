@@ -251,6 +251,9 @@ int fp4_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int
   if (clear_sf_padding(p, scales, out_rows, blocked, st) != cudaSuccess) return FP4_ERR_CUDA;
   QuantOut o = make_out(p, codes, scales, tensor_scale, amax, out_rows, blocked);
   cudaError_t e;
+  if (p->transpose && p->scaling == FP4_SCALING_1D && p->block == block_of(p->format) &&
+      mx_tiled_supported(x_dtype, p->format, nullptr, &o, rows, cols, ldx))
+    return cuda_status(launch_quant_mx_tiled(x, rows, cols, ldx, nullptr, &o, &ctx->scratch->status, ctx->num_sms, st));
   if (p->block != block_of(p->format))
     e = launch_quant_rows_blk(x, x_dtype, rows, cols, ldx, p->format, p->block, o, ctx->num_sms, st);
   else if (!p->transpose && p->scaling == FP4_SCALING_1D)
@@ -301,6 +304,9 @@ int fp4_quantize_dual(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows
   if (clear_sf_padding(pc, scales_cols, cols, rows, st) != cudaSuccess) return FP4_ERR_CUDA;
   QuantOut orow = make_out(pr, codes_rows, scales_rows, ts_rows, amax_r, rows, cols);
   QuantOut ocol = make_out(pc, codes_cols, scales_cols, ts_cols, amax_c, cols, rows);
+  if (pr->scaling == FP4_SCALING_1D && pc->scaling == FP4_SCALING_1D &&
+      mx_tiled_supported(x_dtype, pr->format, &orow, &ocol, rows, cols, ldx))
+    return cuda_status(launch_quant_mx_tiled(x, rows, cols, ldx, &orow, &ocol, &ctx->scratch->status, ctx->num_sms, st));
   return cuda_status(launch_quant_dual(x, x_dtype, rows, cols, ldx, pr->format, orow, ocol,
                                       pr->scaling == FP4_SCALING_2D, pc->scaling == FP4_SCALING_2D, ctx->num_sms, st));
 }

@@ -177,6 +177,12 @@ cudaError_t launch_quant_rows_zeroed(const void* x, int dt, int64_t rows, int64_
 // amax of x with the ascending columns hot[0..n) left out, into a tagged slot
 cudaError_t launch_amax_zeroed(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, const int32_t* hot,
                                int n, float* amax_out, uint32_t gen, int num_sms, cudaStream_t st);
+// MXFP4 RTN quantization of bf16 in the row layout (orow), the transposed
+// layout (ocol) or both (either may be null), 64 x 256 TMA tiles (quant_mx.cu)
+bool mx_tiled_supported(int dt, int fmt, const QuantOut* orow, const QuantOut* ocol, int64_t rows, int64_t cols,
+                        int64_t ldx);
+cudaError_t launch_quant_mx_tiled(const void* x, int64_t rows, int64_t cols, int64_t ldx, const QuantOut* orow,
+                                  const QuantOut* ocol, unsigned int* status, int num_sms, cudaStream_t st);
 // row quantizer for any block of 16-128 elements (row-major scales, no transpose)
 cudaError_t launch_quant_rows_blk(const void* x, int dt, int64_t rows, int64_t cols, int64_t ldx, int fmt, int block,
                                   const QuantOut& o, int num_sms, cudaStream_t st);

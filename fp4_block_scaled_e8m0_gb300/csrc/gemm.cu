@@ -706,6 +706,19 @@ bool make_sf_map(CUtensorMap* m, const void* base, int64_t group_bytes, int64_t 
   return r == CUDA_SUCCESS;
 }
 
+bool make_map_box(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t inner, int64_t rows,
+                  int64_t pitch, int box_inner, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(pitch * elem_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 
 int launch_gemm(const GemmArgs& g, cudaStream_t st) {

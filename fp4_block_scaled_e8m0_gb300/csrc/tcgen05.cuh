@@ -295,6 +295,10 @@ __device__ __forceinline__ void warp_exchange_hi3(uint32_t* w, int lane) {
 bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t inner, int64_t rows,
               int box_rows);
 bool make_sf_map(CUtensorMap* m, const void* base, int64_t group_bytes, int64_t groups, int rows_box, int groups_box);
+// 2-D map over a [rows][inner] matrix with a row pitch of `pitch` elements and
+// a box of box_inner x box_rows elements, no swizzle
+bool make_map_box(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int64_t inner, int64_t rows,
+                  int64_t pitch, int box_inner, int box_rows);
 
 }  // namespace tc
 }  // namespace fp4
