@@ -69,12 +69,12 @@ WORKLOAD = ("llama1b_mlp_up fwd+bwd: X[8192,2048] W[5632,2048] dY[8192,5632] bf1
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample", default="1024x1024", help="MxN rows of the CPU-baseline sample (K stays 4096)")
+    ap.add_argument("--cpu-sample", default="2048x2048", help="MxN rows of the CPU-baseline sample (K stays 4096)")
     ap.add_argument("--ext-launches", type=int, default=20,
                     help="timed launches of each op outside the headline step (0: skip them)")
     ap.add_argument("--ext-only", action="store_true",
@@ -437,7 +437,7 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None

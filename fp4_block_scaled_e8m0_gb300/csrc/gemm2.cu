@@ -73,6 +73,22 @@ struct PairCfg {
   static_assert(P_BN + STAGES * SLOT_COLS <= P_TMEM_COLS, "tensor memory");
 };
 
+// Tile order: groups of up to P_GROUP_M row tiles; inside a group the row tile
+// runs fastest and the column tile next, so that the pairs working at one time
+// share a few A row blocks and B column blocks and re-read them from L2 (with
+// the row tile fastest over the whole of M, the output stream evicted A
+// between waves: 7x the operand bytes came from DRAM)
+constexpr int P_GROUP_M = 16;
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int per_group = P_GROUP_M * tiles_n;
+  const int g = tile / per_group;
+  const int first_m = g * P_GROUP_M;
+  const int gm = min(P_GROUP_M, tiles_m - first_m);
+  const int local = tile - g * per_group;
+  tm = first_m + local % gm;
+  tn = local / gm;
+}
+
 struct PairParams {
   int M, N;
   int k_tiles;        // K stages (256 elements each)
@@ -146,7 +162,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-        const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+        int tm, tn;
+        tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
         const int row_a = tm * 256 + (int)rank * 128, row_b = tn * 256 + (int)rank * 128;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&empty[s], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
@@ -262,7 +279,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     float alpha = 1.0f;
     if (NV) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     for (int tile = pair; tile < num_tiles; tile += npairs) {
-      const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+      int tm, tn;
+      tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
       // one lane polls, the sixteen epilogue warps meet at a named barrier
       if (warp == 6 && lane == 0) (void)mbar_wait(acc_full, acc_phase, abort_flag, p.status);
       named_sync(2, P_EPI_WARPS * 32);
