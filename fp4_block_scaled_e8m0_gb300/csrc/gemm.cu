@@ -726,9 +726,10 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   const fp4_operand& B = *g.B;
   const int64_t M = A.rows, N = B.rows;
   if (M == 0 || N == 0) return FP4_OK;
-  // the plain GEMM runs on CTA pairs; extra K columns, the outlier epilogue,
-  // row/column scales and C += stay on the one-SM kernel
-  if (g.fp4_part && g.kx == 0 && !g.occ_len && !g.row_scale && !g.accumulate) return launch_gemm_pair(g, st);
+  // the FP4 GEMM, alone or with bf16 extra columns, runs on CTA pairs; E4M3
+  // extra columns, the outlier epilogue, row/column scales and C += stay on
+  // the one-SM kernel
+  if (g.fp4_part && !g.ext_fp8 && !g.occ_len && !g.row_scale && !g.accumulate) return launch_gemm_pair(g, st);
   Params p{};
   p.M = (int)M;
   p.N = (int)N;

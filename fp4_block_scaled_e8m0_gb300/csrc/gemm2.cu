@@ -1,6 +1,10 @@
 // Block-scaled FP4 GEMM on CTA pairs (tcgen05 cta_group::2), sm_103a.
 //
-//   C[M,N] = alpha * sum_k A[m,k] B[n,k]      (TN, both operands K-major)
+//   C[M,N] = alpha * ( sum_k A[m,k] B[n,k]  +  sum_j Aext[m,j] Bext[n,j] )
+//
+// (TN, both operands K-major; the optional bf16 part is the hot-channel
+// compensation tail of [outlier] §3.1, "S" mode: extra K columns multiplied
+// by tcgen05.mma.kind::f16 into the same accumulator)
 //
 // The quantized matmul that carries ">95% of the compute" ([msr] §四), E2M1
 // operands with per-block scales (E8M0 / block 32 = MXFP4, E4M3 / block 16 =
@@ -91,7 +95,8 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
 
 struct PairParams {
   int M, N;
-  int k_tiles;        // K stages (256 elements each)
+  int k_tiles;        // FP4 K stages (256 elements each)
+  int ext_tiles;      // extra bf16 K stages (64 elements each) after the FP4 ones
   const float* ts_a;  // NVFP4 tensor scales (alpha = ts_a * ts_b), null for MXFP4
   const float* ts_b;
   void* C;
@@ -104,6 +109,7 @@ template <bool NV, bool BF16_OUT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     fp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
+                         const __grid_constant__ CUtensorMap tm_ax, const __grid_constant__ CUtensorMap tm_bx,
                          const PairParams p) {
   using Cfg = PairCfg<NV>;
   constexpr int STAGES = Cfg::STAGES;
@@ -153,6 +159,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   const uint32_t acc_empty_l = mapa_cluster(acc_empty, 0);
 
   const int num_tiles = p.tiles_m * p.tiles_n;
+  const int total_k = p.k_tiles + p.ext_tiles;
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (warp == 0) {
@@ -165,15 +172,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
         int tm, tn;
         tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
         const int row_a = tm * 256 + (int)rank * 128, row_b = tn * 256 + (int)rank * 128;
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = 0; kt < total_k; ++kt) {
           if (!mbar_wait(&empty[s], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           if (leader) mbar_expect_tx(&full[s], 2 * (P_A_TILE + P_B_TILE));
           const uint32_t fb = full_l + (uint32_t)s * 8u;
-          tma_load_2d_pair(stage_a(s), &tm_a, fb, kt * P_KSLAB, row_a);
-          tma_load_2d_pair(stage_b(s), &tm_b, fb, kt * P_KSLAB, row_b);
-          mbar_expect_tx(&sf_full[s], Cfg::SFA_BYTES + Cfg::SFB_BYTES);
-          tma_load_3d(stage_sfa(s), &tm_sfa, &sf_full[s], 0, kt * Cfg::ATOMS * 4, 2 * tm + (int)rank);
-          tma_load_3d(stage_sfb(s), &tm_sfb, &sf_full[s], 0, kt * Cfg::ATOMS * 4, 2 * tn);
+          if (kt < p.k_tiles) {
+            tma_load_2d_pair(stage_a(s), &tm_a, fb, kt * P_KSLAB, row_a);
+            tma_load_2d_pair(stage_b(s), &tm_b, fb, kt * P_KSLAB, row_b);
+            mbar_expect_tx(&sf_full[s], Cfg::SFA_BYTES + Cfg::SFB_BYTES);
+            tma_load_3d(stage_sfa(s), &tm_sfa, &sf_full[s], 0, kt * Cfg::ATOMS * 4, 2 * tm + (int)rank);
+            tma_load_3d(stage_sfb(s), &tm_sfb, &sf_full[s], 0, kt * Cfg::ATOMS * 4, 2 * tn);
+          } else {
+            // extra bf16 columns: 64 per stage (128 bytes of K), no scales
+            const int kx = (kt - p.k_tiles) * 64;
+            tma_load_2d_pair(stage_a(s), &tm_ax, fb, kx, row_a);
+            tma_load_2d_pair(stage_b(s), &tm_bx, fb, kx, row_b);
+            mbar_arrive(&sf_full[s]);
+          }
           if (++s == STAGES) { s = 0; phase ^= 1; }
         }
       }
@@ -192,25 +207,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       bool ok = true;
       const uint64_t da0 = desc_sw128(smem_u32(stage_a(0))), db0 = desc_sw128(smem_u32(stage_b(0)));
       const uint32_t id_even = idesc_fp4(!NV, 0u, 256, P_BN), id_odd = idesc_fp4(!NV, NV ? 0u : 2u, 256, P_BN);
+      const uint32_t id_ext = idesc_bf16(256, P_BN);
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
         if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.status)) { ok = false; break; }
         acc_phase ^= 1;
         tc_fence_after();
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
+        for (int kt = 0; kt < total_k; ++kt) {
           if (!mbar_wait(&full[s], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint64_t da = da0 + (uint64_t)(s * (Cfg::STAGE >> 4)), db = db0 + (uint64_t)(s * (Cfg::STAGE >> 4));
           const uint32_t slot = tmem + P_BN + (uint32_t)s * Cfg::SLOT_COLS;
           const uint32_t acc0 = kt > 0 ? 1u : 0u;
+          if (kt < p.k_tiles) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // scale columns of 64-element K chunk j: NVFP4 one atom per chunk,
-            // MXFP4 one atom per two chunks (bytes 0-1 / 2-3 chosen by the
-            // instruction descriptor); B's two 128-row groups side by side
-            const uint32_t a_col = NV ? 4u * j : 4u * (j >> 1);
-            const uint32_t b_col = 4u * Cfg::ATOMS + (NV ? 8u * j : 8u * (j >> 1));
-            mma_fp4_pair<NV>(tmem, da + 2 * j, db + 2 * j, (!NV && (j & 1)) ? id_odd : id_even, slot + a_col,
-                             slot + b_col, j > 0 ? 1u : acc0);
+            for (int j = 0; j < 4; ++j) {
+              // scale columns of 64-element K chunk j: NVFP4 one atom per chunk,
+              // MXFP4 one atom per two chunks (bytes 0-1 / 2-3 chosen by the
+              // instruction descriptor); B's two 128-row groups side by side
+              const uint32_t a_col = NV ? 4u * j : 4u * (j >> 1);
+              const uint32_t b_col = 4u * Cfg::ATOMS + (NV ? 8u * j : 8u * (j >> 1));
+              mma_fp4_pair<NV>(tmem, da + 2 * j, db + 2 * j, (!NV && (j & 1)) ? id_odd : id_even, slot + a_col,
+                               slot + b_col, j > 0 ? 1u : acc0);
+            }
+          } else {
+            // 4 bf16 MMAs of 16 K elements (32 bytes) into the same accumulator
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mma_bf16_pair(tmem, da + 2 * j, db + 2 * j, id_ext, j > 0 ? 1u : acc0);
           }
           tc_commit_pair(&empty[s], 0x3);
           if (++s == STAGES) { s = 0; phase ^= 1; }
@@ -235,11 +257,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
-      for (int kt = 0; kt < p.k_tiles; ++kt) {
+      for (int kt = 0; kt < total_k; ++kt) {
         // one lane polls, the four stager warps meet at a named barrier
         if (warp == 2 && lane == 0) (void)mbar_wait(&sf_full[s], phase, abort_flag, p.status);
         named_sync(1, 4 * 32);
         if (*abort_flag) { ok = false; break; }
+        if (kt >= p.k_tiles) {   // extra bf16 columns: no scales to stage
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(full_l + (uint32_t)s * 8u);
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+          continue;
+        }
         const uint32_t slot = tmem + lane_base + P_BN + (uint32_t)s * Cfg::SLOT_COLS;
         uint32_t v[16];
 #pragma unroll
@@ -371,7 +399,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 
 template <bool NV, bool BF16_OUT>
 int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
-                const PairParams& p, int num_sms, cudaStream_t st) {
+                const CUtensorMap& tax, const CUtensorMap& tbx, const PairParams& p, int num_sms, cudaStream_t st) {
   using Cfg = PairCfg<NV>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -382,7 +410,7 @@ int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   }
   const int tiles = p.tiles_m * p.tiles_n;
   const int pairs = std::max(1, std::min(tiles, num_sms / 2));
-  fp4_gemm_pair_kernel<NV, BF16_OUT><<<2 * pairs, P_THREADS, Cfg::SMEM, st>>>(ta, tb, tsa, tsb, p);
+  fp4_gemm_pair_kernel<NV, BF16_OUT><<<2 * pairs, P_THREADS, Cfg::SMEM, st>>>(ta, tb, tsa, tsb, tax, tbx, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -405,6 +433,7 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t st) {
   p.status = g.status;
   p.tiles_m = (int)cdiv(M, 256);
   p.tiles_n = (int)cdiv(N, P_BN);
+  p.ext_tiles = (int)(g.kx / 64);
   if (p.k_tiles == 0) return FP4_ERR_INVALID_ARG;
   const int atoms = nv ? 4 : 2;
   const int64_t group_bytes = (int64_t)128 * nsf_padded(A.k, A.format);
@@ -413,12 +442,17 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t st) {
   ok &= tc::make_map(&tb, B.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B.k / 2, N, 128);
   ok &= tc::make_sf_map(&tsa, A.scales, group_bytes, cdiv(M, 128), atoms * 4, 1);
   ok &= tc::make_sf_map(&tsb, B.scales, group_bytes, cdiv(N, 128), atoms * 4, 2);
+  CUtensorMap tax = ta, tbx = tb;   // never read without extra columns
+  if (g.kx > 0) {
+    ok &= tc::make_map(&tax, g.a_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, M, 128);
+    ok &= tc::make_map(&tbx, g.b_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, N, 128);
+  }
   if (!ok) return FP4_ERR_CUDA;
   const bool bf16 = g.out_dtype == FP4_DTYPE_BF16;
-  if (nv) return bf16 ? launch_pair<true, true>(ta, tb, tsa, tsb, p, g.num_sms, st)
-                      : launch_pair<true, false>(ta, tb, tsa, tsb, p, g.num_sms, st);
-  return bf16 ? launch_pair<false, true>(ta, tb, tsa, tsb, p, g.num_sms, st)
-              : launch_pair<false, false>(ta, tb, tsa, tsb, p, g.num_sms, st);
+  if (nv) return bf16 ? launch_pair<true, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st)
+                      : launch_pair<true, false>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st);
+  return bf16 ? launch_pair<false, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st)
+              : launch_pair<false, false>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st);
 }
 
 }  // namespace fp4
