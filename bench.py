@@ -707,6 +707,47 @@ def time_nvfp4_square(fp4, dev, flush, launches, pk):
     return res
 
 
+def time_fused(fp4, step, dev, flush, launches, pk):
+    """The 7B FFN forward GEMM with X's quantization (MXFP4, RTN, 1D) fused into
+    the GEMM's operand producer, against quantize-then-GEMM (the row quantizer,
+    then the GEMM: two launches), each alone with L2 flushed before it.  Rates
+    are the GEMM's flops over the whole time."""
+    MX = fp4.FP4_FMT_MXFP4
+    p = fp4.quant_params(MX)
+    xq = fp4.alloc_qtensor(FM, FK, MX, fp4.FP4_SF_MMA, dev)
+    fp4.fp4_quantize_dual(step.W, step.p_rows, step.p_cols, out_rows=step.wq, out_cols=step.wq_t)
+
+    def unfused():
+        fp4.fp4_quantize(step.X, p, out=xq)
+        fp4.fp4_gemm(xq, step.wq, out=step.Y)
+
+    res = {"workload": "X[16384,4096] bf16 (as the step) quantized MXFP4 RTN 1D, times the step's quantized "
+                       "W[11008,4096]; bf16 Y"}
+    res["quantize_then_gemm"] = _rate("tensor", FFN_GEMM_FLOPS, _time_op(unfused, flush, launches), pk)
+    res["quantize_rows"] = _rate("hbm", FM * FK * (2 + 0.5 + 1 / 32),
+                                 _time_op(lambda: fp4.fp4_quantize(step.X, p, out=xq), flush, launches), pk)
+    res["gemm"] = _rate("tensor", FFN_GEMM_FLOPS, _time_op(lambda: fp4.fp4_gemm(xq, step.wq, out=step.Y), flush,
+                                                           launches), pk)
+    res["fused"] = _rate("tensor", FFN_GEMM_FLOPS, _time_op(lambda: fp4.fp4_gemm_quant_a(step.X, step.wq, out=step.Y),
+                                                            flush, launches), pk)
+    res["fused_writing_codes"] = _rate("tensor", FFN_GEMM_FLOPS, _time_op(
+        lambda: fp4.fp4_gemm_quant_a(step.X, step.wq, out=step.Y, a_out=xq), flush, launches), pk)
+    # one 256-column tile of output (N = 256): each row of X is quantized once either way
+    for n in (256, 512):
+        wq_n = fp4.fp4_quantize(step.W[:n], p)
+        y_n = torch.empty((FM, n), dtype=torch.bfloat16, device=dev)
+        flops = 2 * FM * n * FK
+
+        def unfused_n():
+            fp4.fp4_quantize(step.X, p, out=xq)
+            fp4.fp4_gemm(xq, wq_n, out=y_n)
+
+        res[f"n{n}_quantize_then_gemm"] = _rate("tensor", flops, _time_op(unfused_n, flush, launches), pk)
+        res[f"n{n}_fused"] = _rate("tensor", flops, _time_op(lambda: fp4.fp4_gemm_quant_a(step.X, wq_n, out=y_n), flush,
+                                                            launches), pk)
+    return res
+
+
 def time_linear_small(fp4, dev, pk, batch=50, replays=20):
     """The small MXFP4 linear fprop (X 256x512, W 512x512: quantize both, GEMM,
     fp32 out) is launch-bound: `batch` iterations are captured in one CUDA graph
@@ -813,6 +854,8 @@ def main():
     t_step = reduce_step_time(t_local, dist, dev)
     status = fp4.fp4_sync_status() | fp4.fp4_sync_status(step.side_ctx)
     t_e2e, h2d, d2h = time_e2e(step, host, args.e2e_steps, side, dev) if args.e2e_steps > 0 else (float("nan"), 0, 0)
+    if args.ext_launches > 0:
+        extensions["fused_quant_a"] = time_fused(fp4, step, dev, flush, args.ext_launches, pk)
 
     # ---- roofline of the dominant kernel --------------------------------------------
     names = list(step.OPS)

@@ -83,6 +83,8 @@ _SIGNATURES = {
     "fp4_quant_error_stats": (ctypes.c_int, [_P, _P, _I32, _I64, ctypes.POINTER(fp4_operand), _P, _F32, _P, _P, _P]),
     "fp4_gemm": (ctypes.c_int, [_P, ctypes.POINTER(fp4_operand), ctypes.POINTER(fp4_operand), _I32, _P, _I64, _I32,
                                 _P]),
+    "fp4_gemm_quant_a": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.POINTER(fp4_operand), _I32, _P, _I64, _P, _P,
+                                        _P]),
     "fp4_hcp_num_hot": (_I32, [_I64, ctypes.c_double]),
     "fp4_hcp_select_workspace_bytes": (_SZ, [_I64]),
     "fp4_hcp_select": (ctypes.c_int, [_P, _P, _I64, ctypes.POINTER(fp4_operand), _I32, _P, _P, _SZ, _P]),
@@ -336,6 +338,22 @@ def fp4_gemm(a: QTensor, b: QTensor, out_dtype=torch.bfloat16, out: Optional[tor
     oa, ob = a.operand(), b.operand()
     _check(load_library().fp4_gemm(_ctx(ctx), ctypes.byref(oa), ctypes.byref(ob), _dtype_code(out), _ptr(out),
                                    _ld(out), int(accumulate), _stream(stream)), "fp4_gemm")
+    return out
+
+
+def fp4_gemm_quant_a(x: torch.Tensor, b: QTensor, out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None,
+                     a_out: Optional[QTensor] = None, ctx=None, stream=None) -> torch.Tensor:
+    """C = Q(x) b^T with x (bf16) quantized to MXFP4 (RTN, 1D) inside the GEMM.
+
+    a_out (an MXFP4 QTensor in the MMA scale layout, e.g. from alloc_qtensor)
+    also receives x's quantization."""
+    m = x.shape[0]
+    out = out if out is not None else torch.empty((m, b.rows), dtype=out_dtype, device=x.device)
+    ob = b.operand()
+    _check(load_library().fp4_gemm_quant_a(_ctx(ctx), _ptr(x), m, _ld(x), ctypes.byref(ob), _dtype_code(out),
+                                           _ptr(out), _ld(out), _ptr(a_out.codes if a_out else None),
+                                           _ptr(a_out.scales if a_out else None), _stream(stream)),
+           "fp4_gemm_quant_a")
     return out
 
 

@@ -546,6 +546,37 @@ int fp4_gemm(fp4_ctx* ctx, const fp4_operand* A, const fp4_operand* B, int32_t o
   return launch_gemm(g, static_cast<cudaStream_t>(stream));
 }
 
+int fp4_gemm_quant_a(fp4_ctx* ctx, const void* x_bf16, int64_t m, int64_t ldx, const fp4_operand* B,
+                     int32_t out_dtype, void* C, int64_t ldc, uint8_t* a_codes, uint8_t* a_scales, void* stream) {
+  if (!ctx || !dtype_ok(out_dtype) || m < 0) return FP4_ERR_INVALID_ARG;
+  int s = check_operand(B, true);
+  if (s) return s;
+  if (!native_block(B) || B->format != FP4_FMT_MXFP4 || B->sf_layout != FP4_SF_MMA) return FP4_ERR_UNSUPPORTED;
+  const int64_t k = B->k, n = B->rows;
+  if (k % 32) return FP4_ERR_INVALID_ARG;
+  if (m > 0 && n > 0 && k == 0) return FP4_ERR_INVALID_ARG;
+  s = check_input(x_bf16, FP4_DTYPE_BF16, m, k, ldx);
+  if (s) return s;
+  if (!present(C, m == 0 || n == 0) || ldc < n) return FP4_ERR_INVALID_ARG;
+  if ((a_codes == nullptr) != (a_scales == nullptr)) return FP4_ERR_INVALID_ARG;
+  if (!al16(C) || (ldc * esize(out_dtype)) % 16 || !al16(a_codes) || !al16(a_scales)) return FP4_ERR_MISALIGNED;
+  if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX) return FP4_ERR_INVALID_ARG;
+  GemmArgs g{};
+  g.B = B;
+  g.fp4_part = true;
+  g.out_dtype = out_dtype;
+  g.C = C;
+  g.ldc = ldc;
+  g.status = &ctx->scratch->status;
+  g.num_sms = ctx->num_sms;
+  g.x_bf16 = x_bf16;
+  g.ldx = ldx;
+  g.m = m;
+  g.qa_codes = a_codes;
+  g.qa_scales = a_scales;
+  return launch_gemm_pair(g, static_cast<cudaStream_t>(stream));
+}
+
 int fp4_hcp_quantize_zeroed(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows, int64_t cols, int64_t ldx,
                             const fp4_quant_params* p, const int32_t* hot_idx, int32_t k_hot, uint8_t* codes,
                             uint8_t* scales, float* tensor_scale, void* stream) {

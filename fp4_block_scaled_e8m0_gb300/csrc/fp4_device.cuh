@@ -94,6 +94,55 @@ __device__ __forceinline__ uint32_t e2m1x2_hw(float lo, float hi) {
   return r & 0xFFu;
 }
 
+// eight fp32 values (bit patterns f[0..7]) times r -> eight E2M1 codes, f[0]
+// in bits 0-3 and f[7] in bits 28-31: the products two at a time with
+// mul.rn.f32x2 (each lane rounded as one fmul.rn, no flush to zero), the
+// hardware conversion (round to nearest even, saturating) two at a time, and
+// the four code bytes gathered into one word
+__device__ __forceinline__ uint32_t e2m1x8_scaled(const uint32_t (&f)[8], float r) {
+  uint32_t out;
+  asm("{\n\t"
+      ".reg .b64 rr, p0, p1, p2, p3;\n\t"
+      ".reg .b32 l0, h0, l1, h1, l2, h2, l3, h3, u0, u1, u2, u3, t0, t1;\n\t"
+      ".reg .b8 c0, c1, c2, c3;\n\t"
+      "mov.b64 rr, {%9, %9};\n\t"
+      "mov.b64 p0, {%1, %2};\n\t"
+      "mov.b64 p1, {%3, %4};\n\t"
+      "mov.b64 p2, {%5, %6};\n\t"
+      "mov.b64 p3, {%7, %8};\n\t"
+      "mul.rn.f32x2 p0, p0, rr;\n\t"
+      "mul.rn.f32x2 p1, p1, rr;\n\t"
+      "mul.rn.f32x2 p2, p2, rr;\n\t"
+      "mul.rn.f32x2 p3, p3, rr;\n\t"
+      "mov.b64 {l0, h0}, p0;\n\t"
+      "mov.b64 {l1, h1}, p1;\n\t"
+      "mov.b64 {l2, h2}, p2;\n\t"
+      "mov.b64 {l3, h3}, p3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, h0, l0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, h1, l1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, h2, l2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, h3, l3;\n\t"
+      "cvt.u32.u8 u0, c0;\n\t"
+      "cvt.u32.u8 u1, c1;\n\t"
+      "cvt.u32.u8 u2, c2;\n\t"
+      "cvt.u32.u8 u3, c3;\n\t"
+      "prmt.b32 t0, u0, u1, 0x0040;\n\t"
+      "prmt.b32 t1, u2, u3, 0x0040;\n\t"
+      "prmt.b32 %0, t0, t1, 0x5410;\n\t"
+      "}"
+      : "=r"(out)
+      : "r"(f[0]), "r"(f[1]), "r"(f[2]), "r"(f[3]), "r"(f[4]), "r"(f[5]), "r"(f[6]), "r"(f[7]), "f"(r));
+  return out;
+}
+
+// eight bf16 (element 2i in the low half of word i of w) times r -> eight
+// E2M1 codes, element 0 in bits 0-3
+__device__ __forceinline__ uint32_t mx_codes8(uint4 w, float r) {
+  const uint32_t f[8] = {w.x << 16, w.x & 0xFFFF0000u, w.y << 16, w.y & 0xFFFF0000u,
+                         w.z << 16, w.z & 0xFFFF0000u, w.w << 16, w.w & 0xFFFF0000u};
+  return e2m1x8_scaled(f, r);
+}
+
 // Compare chain against the midpoints of the grid {0,.5,1,1.5,2,3,4,6}; at a
 // midpoint the even code wins (0.25->0, 0.75->2, 1.25->2, 1.75->4, 2.5->4,
 // 3.5->6, 5->6); the sign bit is kept.
@@ -158,6 +207,17 @@ __device__ __forceinline__ float e8m0_inv_scale(uint32_t byte) {
 }
 __device__ __forceinline__ float e8m0_scale(uint32_t byte) {
   return byte == 0 ? 5.877471754111438e-39f /* 2^-127 */ : __uint_as_float(byte << 23);
+}
+
+// MXFP4 block scale from the magnitude bits of a bf16 block amax: the E8M0
+// byte is the amax's exponent field minus 2, i.e. floor(log2 amax) - 2 + 127
+// (bf16 and fp32 share the exponent field), clamped at the format's minimum
+// (fields 0-2, which include the bf16 subnormals and 0, give byte 0); r =
+// 2^(127 - byte) multiplies each element exactly
+__device__ __forceinline__ void mx_scale_from_bits(uint32_t amax_bits, uint32_t& byte, float& r) {
+  const uint32_t e = (amax_bits >> 7) & 0xFFu;
+  byte = e >= 2 ? e - 2 : 0u;
+  r = e8m0_inv_scale(byte);
 }
 
 // Block scale of one block: writes the scale byte and the multiplier r with

@@ -127,9 +127,18 @@ struct GemmArgs {
   const void* occ_entries;     // (int32 k, float v) pairs
   const uint16_t* occ_wt;      // W^T bf16 [K][occ_ldt], occ_ldt a multiple of 8
   int64_t occ_ldt;
+  // quantize fused into the operand producer (CTA-pair kernel, MXFP4 RTN):
+  // A is the bf16 activation x_bf16 [m][B.k] (pitch ldx, a multiple of 8) and
+  // g.A is unused; its codes / MMA-layout scales are written to qa_* if non-null
+  const void* x_bf16;
+  int64_t ldx;
+  int64_t m;
+  uint8_t* qa_codes;
+  uint8_t* qa_scales;
 };
 int launch_gemm(const GemmArgs& g, cudaStream_t st);  // returns fp4 status
-// the CTA-pair kernel (gemm2.cu): plain FP4 GEMM, no extra columns, no C +=
+// the CTA-pair kernel (gemm2.cu): plain FP4 GEMM or bf16 extra columns, no C +=;
+// with g.x_bf16 the quantize-fused variant
 int launch_gemm_pair(const GemmArgs& g, cudaStream_t st);
 
 // Hot-channel compensation (hcp.cu)

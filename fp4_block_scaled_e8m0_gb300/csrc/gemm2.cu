@@ -35,6 +35,15 @@
 //   warps 6-21   epilogue: 64 accumulator columns each, both 32-column loads
 //                in flight, one wait, the accumulator released to the leader,
 //                then * alpha and stores
+// Fused-quantize variant (MXFP4, round to nearest, blocks of 32 along K: the
+// forward operand of [outlier] §4.1, which needs no tensor-wide amax): A is
+// the bf16 activation itself.  The producer also brings 128-row x 128-column
+// bf16 half-stages of A into a ring of NXS buffers (TMA), and the sixteen
+// epilogue warps, idle while a tile's MMAs run, quantize them ([grad] §2.1,
+// E8M0 scale of [lowprec] §1.1) straight into the stage's 128-byte-swizzled A
+// slab and its scale atoms (optionally writing the codes out as well); they
+// run up to STAGES K steps into the next tile before taking the last tile's
+// accumulator.  The stagers then stage the scales as above.
 // The scales reach tensor memory through tcgen05.st rather than tcgen05.cp:
 // a pair copy of a 512-byte atom held the tensor pipe ~90 cycles (NVFP4 has 12
 // atoms per stage next to 4 MMAs of ~136 cycles), the stores run beside the MMAs.
@@ -77,6 +86,20 @@ struct PairCfg {
   static_assert(P_BN + STAGES * SLOT_COLS <= P_TMEM_COLS, "tensor memory");
 };
 
+// fused-quantize variant (MXFP4): fewer stages, and a ring of bf16 A half-stages
+struct FuseCfg {
+  // two K stages of codes and four bf16 half-stages: a half-stage's buffer is
+  // refilled while the next stage is quantized (with three half-stages the
+  // refill of a stage's second half started only when the stage before it
+  // was done, and each stage waited out a whole TMA latency)
+  static constexpr int STAGES = 2;
+  static constexpr int XS_COLS = 128;                     // bf16 elements of K per half-stage
+  static constexpr int XS_BYTES = 128 * XS_COLS * 2;      // 128 rows: 32 KB
+  static constexpr int NXS = 4;
+  static constexpr int SMEM = STAGES * PairCfg<false>::STAGE + NXS * XS_BYTES + PairCfg<false>::BAR_BYTES + 1024;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+};
+
 // Tile order: groups of up to P_GROUP_M row tiles; inside a group the row tile
 // runs fastest and the column tile next, so that the pairs working at one time
 // share a few A row blocks and B column blocks and re-read them from L2 (with
@@ -103,25 +126,36 @@ struct PairParams {
   int64_t ldc;
   unsigned int* status;
   int tiles_m, tiles_n;   // 256 x 256 tiles
+  // fused-quantize variant: the quantized A written out (null: not written)
+  uint8_t* qa_codes;      // [M][K/2]
+  uint8_t* qa_scales;     // MMA layout, atoms of 128 rows x 4 scales
+  int K;
+  int sf_groups;          // scale atoms per 128 rows in qa_scales (K padded to 256, / 128)
 };
 
-template <bool NV, bool BF16_OUT>
+template <bool NV, bool BF16_OUT, bool FUSE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     fp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                          const __grid_constant__ CUtensorMap tm_ax, const __grid_constant__ CUtensorMap tm_bx,
                          const PairParams p) {
+  static_assert(!(NV && FUSE), "the fused quantizer forms MXFP4 operands");
   using Cfg = PairCfg<NV>;
-  constexpr int STAGES = Cfg::STAGES;
+  constexpr int STAGES = FUSE ? FuseCfg::STAGES : Cfg::STAGES;
+  constexpr int NXS = FUSE ? FuseCfg::NXS : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE);   // leader: slabs landed, scales staged
+  uint8_t* xs_base = smem + STAGES * Cfg::STAGE;                               // bf16 A half-stages (fused)
+  uint64_t* full = reinterpret_cast<uint64_t*>(xs_base + NXS * FuseCfg::XS_BYTES);   // leader: slabs landed, scales staged
   uint64_t* empty = full + STAGES;                                             // stage consumed by the MMAs
   uint64_t* sf_full = empty + STAGES;                                          // this CTA's scale atoms landed
   uint64_t* acc_full = sf_full + STAGES;
   uint64_t* acc_empty = acc_full + 1;                                          // leader: both epilogues done
   uint64_t* drain = acc_empty + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* xs_full = drain + 1;                                               // fused: bf16 half-stage landed
+  uint64_t* xs_empty = xs_full + NXS;                                          // fused: half-stage quantized
+  uint64_t* q_done = xs_empty + NXS;                                           // fused: stage's A codes and scales written
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(q_done + (FUSE ? STAGES : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -131,6 +165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   auto stage_b = [&](int s) { return smem + s * Cfg::STAGE + P_A_TILE; };
   auto stage_sfa = [&](int s) { return smem + s * Cfg::STAGE + P_A_TILE + P_B_TILE; };
   auto stage_sfb = [&](int s) { return smem + s * Cfg::STAGE + P_A_TILE + P_B_TILE + Cfg::SFA_BYTES; };
+  auto stage_x = [&](int x) { return xs_base + x * FuseCfg::XS_BYTES; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -141,6 +176,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 2 * P_EPI_WARPS);    // every epilogue warp of both CTAs
     mbar_init(drain, 1);
+    for (int x = 0; x < NXS; ++x) {
+      mbar_init(&xs_full[x], 1);
+      mbar_init(&xs_empty[x], P_EPI_WARPS);    // the quantizing (epilogue) warps
+    }
+    if (FUSE)
+      for (int s = 0; s < STAGES; ++s) mbar_init(&q_done[s], P_EPI_WARPS);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -165,14 +206,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      int s = 0;
-      uint32_t phase = 0;
+      int s = 0, x = 0;
+      uint32_t phase = 0, xphase = 0;
       bool ok = true;
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
         int tm, tn;
         tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
         const int row_a = tm * 256 + (int)rank * 128, row_b = tn * 256 + (int)rank * 128;
         for (int kt = 0; kt < total_k; ++kt) {
+          if constexpr (FUSE) {
+            // the stage's two bf16 half-stages of this CTA's A rows (zero fill
+            // beyond M and K), each into the ring buffer the stagers released
+            for (int h = 0; h < 2 && ok; ++h) {
+              if (!mbar_wait(&xs_empty[x], xphase ^ 1, abort_flag, p.status)) { ok = false; break; }
+              mbar_expect_tx(&xs_full[x], FuseCfg::XS_BYTES);
+              tma_load_2d(stage_x(x), &tm_a, &xs_full[x], kt * 256 + h * FuseCfg::XS_COLS, row_a);
+              if (++x == NXS) { x = 0; xphase ^= 1; }
+            }
+            if (!ok) break;
+            if (!mbar_wait(&empty[s], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+            if (leader) mbar_expect_tx(&full[s], 2 * P_B_TILE);
+            tma_load_2d_pair(stage_b(s), &tm_b, full_l + (uint32_t)s * 8u, kt * P_KSLAB, row_b);
+            mbar_expect_tx(&sf_full[s], Cfg::SFB_BYTES);
+            tma_load_3d(stage_sfb(s), &tm_sfb, &sf_full[s], 0, kt * Cfg::ATOMS * 4, 2 * tn);
+            if (++s == STAGES) { s = 0; phase ^= 1; }
+            continue;
+          }
           if (!mbar_wait(&empty[s], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           if (leader) mbar_expect_tx(&full[s], 2 * (P_A_TILE + P_B_TILE));
           const uint32_t fb = full_l + (uint32_t)s * 8u;
@@ -197,6 +256,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       for (int i = 0; i < STAGES; ++i) {
         mbar_drain_wait(&empty[s], phase ^ 1, p.status);
         if (++s == STAGES) { s = 0; phase ^= 1; }
+      }
+      // and until every bf16 half-stage requested has landed
+      for (int i = 0; i < NXS; ++i) {
+        mbar_drain_wait(&xs_full[x], xphase ^ 1, p.status);
+        if (++x == NXS) { x = 0; xphase ^= 1; }
       }
     }
   } else if (warp == 1) {
@@ -257,11 +321,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+      int tm, tn;
+      tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
       for (int kt = 0; kt < total_k; ++kt) {
         // one lane polls, the four stager warps meet at a named barrier
-        if (warp == 2 && lane == 0) (void)mbar_wait(&sf_full[s], phase, abort_flag, p.status);
+        if (warp == 2 && lane == 0) {
+          (void)mbar_wait(&sf_full[s], phase, abort_flag, p.status);
+          if constexpr (FUSE) (void)mbar_wait(&q_done[s], phase, abort_flag, p.status);   // A's scale atoms
+        }
         named_sync(1, 4 * 32);
         if (*abort_flag) { ok = false; break; }
+        if constexpr (FUSE) {
+          const int rt = 2 * tm + (int)rank;          // 128-row tile of A
+          if (p.qa_scales != nullptr && tn == 0 && rt * 128 < p.M) {
+            // the stage's two atoms are contiguous in the MMA layout: 8 bytes a thread
+            const int t = threadIdx.x - 64;
+            *reinterpret_cast<uint2*>(p.qa_scales + ((int64_t)rt * p.sf_groups + 2 * kt) * 512 + t * 8) =
+                *reinterpret_cast<const uint2*>(stage_sfa(s) + t * 8);
+          }
+        }
         if (kt >= p.k_tiles) {   // extra bf16 columns: no scales to stage
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(full_l + (uint32_t)s * 8u);
@@ -306,13 +384,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     uint32_t acc_phase = 0;
     float alpha = 1.0f;
     if (NV) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
-    for (int tile = pair; tile < num_tiles; tile += npairs) {
+    // one tile's accumulator -> C; false when the kernel gave up a wait
+    auto epilogue = [&](int tile) -> bool {
       int tm, tn;
       tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
       // one lane polls, the sixteen epilogue warps meet at a named barrier
       if (warp == 6 && lane == 0) (void)mbar_wait(acc_full, acc_phase, abort_flag, p.status);
       named_sync(2, P_EPI_WARPS * 32);
-      if (*abort_flag) break;
+      if (*abort_flag) return false;
       acc_phase ^= 1;
       tc_fence_after();
       const int row0 = tm * 256 + (int)rank * 128 + quad * 32;   // this warp's 32 rows
@@ -326,7 +405,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc_empty_l);
-      if (!any) continue;
+      if (!any) return true;
       if constexpr (BF16_OUT) {
         // word i packs columns 2i, 2i + 1 of the slice; after the exchange lane
         // 4b + a holds columns colw + 8b .. +7 of rows row0 + 4v + a
@@ -386,6 +465,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
           }
         }
       }
+      return true;
+    };
+    if constexpr (!FUSE) {
+      for (int tile = pair; tile < num_tiles; tile += npairs)
+        if (!epilogue(tile)) break;
+    } else {
+      // Quantize A for the MMAs: warp e = warp - 6 takes rows 8e .. 8e + 7 of
+      // this CTA's 128, two rows per step (lanes 0-15 and 16-31), each lane 8
+      // elements of a 128-element half-stage; 4 lanes share a 32-element block.
+      // The last tile's accumulator is taken after the first STAGES K steps of
+      // the next tile are quantized: those need only the last tile's MMAs to
+      // have released their slots, and the next tile's first MMA needs the
+      // accumulator.
+      const int e = warp - 6;
+      const int cl = lane & 15;
+      const int ahead = min(STAGES, p.k_tiles);
+      int s = 0, x = 0, prev = -1;
+      uint32_t phase = 0, xphase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+        int tm, tn;
+        tile_coords(tile, p.tiles_m, p.tiles_n, tm, tn);
+        const int grow0 = tm * 256 + (int)rank * 128;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+          const int x1 = x + 1 == NXS ? 0 : x + 1;
+          if (warp == 6 && lane == 0) {
+            // the slot is free once its B scales were requested (the producer
+            // waits for the MMAs to release it first); the stage's two bf16
+            // half-stages have landed
+            (void)mbar_wait(&sf_full[s], phase, abort_flag, p.status);
+            (void)mbar_wait(&xs_full[x], xphase, abort_flag, p.status);
+            (void)mbar_wait(&xs_full[x1], x1 == 0 ? xphase ^ 1 : xphase, abort_flag, p.status);
+          }
+          named_sync(2, P_EPI_WARPS * 32);
+          if (*abort_flag) { ok = false; break; }
+          uint8_t* a_slab = stage_a(s);
+          uint8_t* sfa = stage_sfa(s);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint8_t* xs = stage_x(h == 0 ? x : x1);
+            const int kcol = kt * 256 + h * FuseCfg::XS_COLS + 8 * cl;   // first element of the lane's 8
+            const bool write_codes = p.qa_codes != nullptr && tn == 0 && kcol < p.K;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 8 * e + 2 * i + (lane >> 4);                  // row of this CTA's 128
+              const uint4 w = *reinterpret_cast<const uint4*>(xs + r * (FuseCfg::XS_COLS * 2) + cl * 16);
+              uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                    __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+              m = max(m & 0xFFFFu, m >> 16);
+              m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+              m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+              uint32_t byte;
+              float rs;
+              fp4dev::mx_scale_from_bits(m, byte, rs);
+              const uint32_t codes = fp4dev::mx_codes8(w, rs);
+              // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+              const int chunk = (h * 4 + (cl >> 2)) ^ (r & 7);
+              *reinterpret_cast<uint32_t*>(a_slab + r * P_KSLAB + chunk * 16 + (cl & 3) * 4) = codes;
+              // scale of block 4h + cl/4 of the stage: atom h, (r % 32) * 16 + ((r / 32) % 4) * 4 + cl / 4
+              if ((cl & 3) == 0) sfa[h * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (cl >> 2)] = (uint8_t)byte;
+              if (write_codes && grow0 + r < p.M)
+                *reinterpret_cast<uint32_t*>(p.qa_codes + (int64_t)(grow0 + r) * (p.K >> 1) + (kcol >> 1)) = codes;
+            }
+          }
+          // the codes were written through the generic proxy; the MMA reads
+          // them through the async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&xs_empty[x]);
+            mbar_arrive(&xs_empty[x1]);
+            mbar_arrive(&q_done[s]);
+          }
+          for (int j = 0; j < 2; ++j)
+            if (++x == NXS) { x = 0; xphase ^= 1; }
+          if (++s == STAGES) { s = 0; phase ^= 1; }
+          if (prev >= 0 && kt == ahead - 1) {
+            if (!epilogue(prev)) { ok = false; break; }
+            prev = -1;
+          }
+        }
+        if (ok) prev = tile;
+      }
+      if (ok && prev >= 0) (void)epilogue(prev);
     }
   }
 
@@ -397,36 +560,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
   }
 }
 
-template <bool NV, bool BF16_OUT>
+template <bool NV, bool BF16_OUT, bool FUSE = false>
 int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
                 const CUtensorMap& tax, const CUtensorMap& tbx, const PairParams& p, int num_sms, cudaStream_t st) {
-  using Cfg = PairCfg<NV>;
+  constexpr int SMEM = FUSE ? FuseCfg::SMEM : PairCfg<NV>::SMEM;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fp4_gemm_pair_kernel<NV, BF16_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM) != cudaSuccess)
+    if (cudaFuncSetAttribute(fp4_gemm_pair_kernel<NV, BF16_OUT, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM) != cudaSuccess)
       return FP4_ERR_CUDA;
     attr_set = true;
   }
   const int tiles = p.tiles_m * p.tiles_n;
   const int pairs = std::max(1, std::min(tiles, num_sms / 2));
-  fp4_gemm_pair_kernel<NV, BF16_OUT><<<2 * pairs, P_THREADS, Cfg::SMEM, st>>>(ta, tb, tsa, tsb, tax, tbx, p);
+  fp4_gemm_pair_kernel<NV, BF16_OUT, FUSE><<<2 * pairs, P_THREADS, SMEM, st>>>(ta, tb, tsa, tsb, tax, tbx, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
 }  // namespace
 
 int launch_gemm_pair(const GemmArgs& g, cudaStream_t st) {
-  const fp4_operand& A = *g.A;
   const fp4_operand& B = *g.B;
-  const int64_t M = A.rows, N = B.rows;
+  const bool fuse = g.x_bf16 != nullptr;          // A = the bf16 activation, quantized in the kernel
+  const int64_t M = fuse ? g.m : g.A->rows, N = B.rows, K = B.k;
   if (M == 0 || N == 0) return FP4_OK;
-  const bool nv = A.format == FP4_FMT_NVFP4;
+  const bool nv = B.format == FP4_FMT_NVFP4;
+  if (fuse && (nv || g.kx > 0)) return FP4_ERR_UNSUPPORTED;
   PairParams p{};
   p.M = (int)M;
   p.N = (int)N;
-  p.k_tiles = (int)cdiv(A.k, 256);
-  p.ts_a = nv ? A.tensor_scale : nullptr;
+  p.k_tiles = (int)cdiv(K, 256);
+  p.ts_a = nv ? g.A->tensor_scale : nullptr;
   p.ts_b = nv ? B.tensor_scale : nullptr;
   p.C = g.C;
   p.ldc = g.ldc;
@@ -434,14 +598,24 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t st) {
   p.tiles_m = (int)cdiv(M, 256);
   p.tiles_n = (int)cdiv(N, P_BN);
   p.ext_tiles = (int)(g.kx / 64);
+  p.qa_codes = g.qa_codes;
+  p.qa_scales = g.qa_scales;
+  p.K = (int)K;
+  p.sf_groups = (int)(nsf_padded(K, B.format) / 4);
   if (p.k_tiles == 0) return FP4_ERR_INVALID_ARG;
   const int atoms = nv ? 4 : 2;
-  const int64_t group_bytes = (int64_t)128 * nsf_padded(A.k, A.format);
+  const int64_t group_bytes = (int64_t)128 * nsf_padded(K, B.format);
   CUtensorMap ta{}, tb{}, tsa{}, tsb{};
-  bool ok = tc::make_map(&ta, A.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A.k / 2, M, P_BM);
-  ok &= tc::make_map(&tb, B.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B.k / 2, N, 128);
-  ok &= tc::make_sf_map(&tsa, A.scales, group_bytes, cdiv(M, 128), atoms * 4, 1);
+  bool ok = tc::make_map(&tb, B.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, N, 128);
   ok &= tc::make_sf_map(&tsb, B.scales, group_bytes, cdiv(N, 128), atoms * 4, 2);
+  if (fuse) {
+    // bf16 A in 128-column x 128-row boxes; the A scale map is never read
+    ok &= tc::make_map_box(&ta, g.x_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, g.ldx, FuseCfg::XS_COLS, 128);
+    tsa = tsb;
+  } else {
+    ok &= tc::make_map(&ta, g.A->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, M, P_BM);
+    ok &= tc::make_sf_map(&tsa, g.A->scales, group_bytes, cdiv(M, 128), atoms * 4, 1);
+  }
   CUtensorMap tax = ta, tbx = tb;   // never read without extra columns
   if (g.kx > 0) {
     ok &= tc::make_map(&tax, g.a_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, M, 128);
@@ -449,6 +623,8 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t st) {
   }
   if (!ok) return FP4_ERR_CUDA;
   const bool bf16 = g.out_dtype == FP4_DTYPE_BF16;
+  if (fuse) return bf16 ? launch_pair<false, true, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st)
+                        : launch_pair<false, false, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st);
   if (nv) return bf16 ? launch_pair<true, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st)
                       : launch_pair<true, false>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st);
   return bf16 ? launch_pair<false, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st)

@@ -39,19 +39,6 @@ constexpr int MX_NBUF = 2;                              // tile buffers per CTA
 constexpr int MX_SMEM = MX_NBUF * MX_TILE_BYTES + 128;  // tiles + barriers
 constexpr int MX_CTAS_PER_SM = 3;
 
-// E8M0 byte and multiplier 2^(127 - byte) from the magnitude bits of a bf16
-// block amax
-__device__ __forceinline__ void mx_scale_from_bits(uint32_t amax_bits, uint32_t& byte, float& r) {
-  const uint32_t e = (amax_bits >> 7) & 0xFFu;
-  byte = e >= 2 ? e - 2 : 0u;
-  r = e8m0_inv_scale(byte);
-}
-
-// two bf16 (the halves of w) times r, to a packed byte of two E2M1 codes
-__device__ __forceinline__ uint32_t mx_pair(uint32_t w, float r) {
-  return e2m1x2_hw(__fmul_rn(__uint_as_float(w << 16), r), __fmul_rn(__uint_as_float(w & 0xFFFF0000u), r));
-}
-
 template <bool ROWS, bool COLS>
 __global__ void __launch_bounds__(MX_THREADS, MX_CTAS_PER_SM)
     mx_tile_kernel(const __grid_constant__ CUtensorMap tm_x, int rows, int cols, uint32_t tiles_c, uint32_t ntiles,
@@ -105,7 +92,7 @@ __global__ void __launch_bounds__(MX_THREADS, MX_CTAS_PER_SM)
         uint32_t byte;
         float r;
         mx_scale_from_bits(m, byte, r);
-        const uint32_t codes = mx_pair(w.x, r) | (mx_pair(w.y, r) << 8) | (mx_pair(w.z, r) << 16) | (mx_pair(w.w, r) << 24);
+        const uint32_t codes = mx_codes8(w, r);
         if (row < rows && col_ok) {
           *reinterpret_cast<uint32_t*>(orow.codes + (int64_t)row * (orow.out_cols >> 1) + (col >> 1)) = codes;
           if ((lane & 3) == 0)
@@ -135,15 +122,11 @@ __global__ void __launch_bounds__(MX_THREADS, MX_CTAS_PER_SM)
           uint32_t q[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            uint32_t v = 0;
+            // rows 8k .. 8k + 7 of this column as fp32 bit patterns
+            uint32_t f[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              // rows 8k + 2i and 8k + 2i + 1 of this column, as one bf16 pair
-              const uint32_t lo = e ? (w[8 * k + 2 * i] >> 16) : (w[8 * k + 2 * i] & 0xFFFFu);
-              const uint32_t hi = e ? (w[8 * k + 2 * i + 1] & 0xFFFF0000u) : (w[8 * k + 2 * i + 1] << 16);
-              v |= mx_pair(lo | hi, r) << (8 * i);
-            }
-            q[k] = v;
+            for (int i = 0; i < 8; ++i) f[i] = e ? (w[8 * k + i] & 0xFFFF0000u) : (w[8 * k + i] << 16);
+            q[k] = e2m1x8_scaled(f, r);
           }
           *reinterpret_cast<uint4*>(ocol.codes + (int64_t)(orow0 + e) * (ocol.out_cols >> 1) + (ocol0 >> 1)) =
               make_uint4(q[0], q[1], q[2], q[3]);

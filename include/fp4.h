@@ -299,6 +299,23 @@ int fp4_quant_error_stats(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t 
 int fp4_gemm(fp4_ctx* ctx, const fp4_operand* A, const fp4_operand* B, int32_t out_dtype,
              void* C, int64_t ldc, int32_t accumulate, void* stream);
 
+/* fp4_gemm_quant_a: C = Q(X) B^T with the activation's quantization fused into
+ * the GEMM's operand producer ([outlier] §4.1's forward operand: round to
+ * nearest, 1D blocks along K, which needs no tensor-wide amax).  X is bf16
+ * [m][k] with pitch ldx (a multiple of 8 elements, 16-byte aligned), k = B->k;
+ * inside the GEMM each tile quantizes its rows of X as fp4_quantize does with
+ * MXFP4, block 32, RTN (Q(x) = s round(x / s), [grad] §2.1; E8M0 scale,
+ * [lowprec] §1.1) and multiplies them with B, an MXFP4 operand in the
+ * FP4_SF_MMA layout.  Every 256 output columns quantize X's rows again.
+ * a_codes / a_scales: both NULL, or both given (16-byte aligned) to receive
+ * X's quantization as well: codes [m][k/2] and FP4_SF_MMA scales of
+ * fp4_scales_bytes(m, k, FP4_FMT_MXFP4, FP4_SF_MMA, 0) bytes, padding
+ * included, the same bytes fp4_quantize writes; written only when B has rows.
+ * out_dtype, C and ldc as fp4_gemm (no accumulate).  C equals fp4_quantize
+ * followed by fp4_gemm bit for bit.  FP4_ERR_UNSUPPORTED for an NVFP4 B.   */
+int fp4_gemm_quant_a(fp4_ctx* ctx, const void* x_bf16, int64_t m, int64_t ldx, const fp4_operand* B,
+                     int32_t out_dtype, void* C, int64_t ldc, uint8_t* a_codes, uint8_t* a_scales, void* stream);
+
 /* ---- hot-channel compensation ([outlier] §3.1-3.2, §4.1)
  * fp4_hcp_num_hot: h = ceil(ratio * k), the number of hot channels out of k
  * when the "top 9%" ([outlier] §4.1: ratio 0.09) are compensated; the product
