@@ -94,53 +94,96 @@ __device__ __forceinline__ uint32_t e2m1x2_hw(float lo, float hi) {
   return r & 0xFFu;
 }
 
-// eight fp32 values (bit patterns f[0..7]) times r -> eight E2M1 codes, f[0]
-// in bits 0-3 and f[7] in bits 28-31: the products two at a time with
-// mul.rn.f32x2 (each lane rounded as one fmul.rn, no flush to zero), the
-// hardware conversion (round to nearest even, saturating) two at a time, and
-// the four code bytes gathered into one word
-__device__ __forceinline__ uint32_t e2m1x8_scaled(const uint32_t (&f)[8], float r) {
+// Eight bf16 times the power of two rb (a bf16 bit pattern) -> eight E2M1
+// codes, element 0 in bits 0-3.  Each product is one fma.rn.f32.bf16 with
+// addend -0: the exact product rounded once to fp32 (subnormals kept), the
+// same value and sign of zero as fmul.rn of the two converted to fp32; then
+// the hardware conversion (round to nearest even, saturating) two at a time,
+// and the four code bytes gathered into one word.  The products run on the
+// FMA pipe, which leaves the integer pipe to the rest of the quantizer.
+// The elements are the halves of w0..w3 in order (H = 2), or half H of each
+// of w0..w7 (H = 0: low halves, H = 1: high halves).
+#define FP4_E2M1X8_TAIL                                            \
+  "cvt.rn.satfinite.e2m1x2.f32 c0, f1, f0;\n\t"                     \
+  "cvt.rn.satfinite.e2m1x2.f32 c1, f3, f2;\n\t"                     \
+  "cvt.rn.satfinite.e2m1x2.f32 c2, f5, f4;\n\t"                     \
+  "cvt.rn.satfinite.e2m1x2.f32 c3, f7, f6;\n\t"                     \
+  "cvt.u32.u8 u0, c0;\n\t"                                          \
+  "cvt.u32.u8 u1, c1;\n\t"                                          \
+  "cvt.u32.u8 u2, c2;\n\t"                                          \
+  "cvt.u32.u8 u3, c3;\n\t"                                          \
+  "prmt.b32 t0, u0, u1, 0x0040;\n\t"                                \
+  "prmt.b32 t1, u2, u3, 0x0040;\n\t"                                \
+  "prmt.b32 %0, t0, t1, 0x5410;\n\t"                                \
+  "}"
+#define FP4_E2M1X8_REGS                                            \
+  "{\n\t"                                                           \
+  ".reg .b16 r, z, e0, e1, e2, e3, e4, e5, e6, e7;\n\t"             \
+  ".reg .f32 mz, f0, f1, f2, f3, f4, f5, f6, f7;\n\t"               \
+  ".reg .b8 c0, c1, c2, c3;\n\t"                                    \
+  ".reg .b32 u0, u1, u2, u3, t0, t1;\n\t"                           \
+  "mov.b32 {r, z}, %1;\n\t"                                         \
+  "mov.f32 mz, 0f80000000;\n\t"
+#define FP4_E2M1X8_FMA                                              \
+  "fma.rn.f32.bf16 f0, e0, r, mz;\n\t"                              \
+  "fma.rn.f32.bf16 f1, e1, r, mz;\n\t"                              \
+  "fma.rn.f32.bf16 f2, e2, r, mz;\n\t"                              \
+  "fma.rn.f32.bf16 f3, e3, r, mz;\n\t"                              \
+  "fma.rn.f32.bf16 f4, e4, r, mz;\n\t"                              \
+  "fma.rn.f32.bf16 f5, e5, r, mz;\n\t"                              \
+  "fma.rn.f32.bf16 f6, e6, r, mz;\n\t"                              \
+  "fma.rn.f32.bf16 f7, e7, r, mz;\n\t"
+
+__device__ __forceinline__ uint32_t mx_codes8(uint4 w, uint32_t rb) {
   uint32_t out;
-  asm("{\n\t"
-      ".reg .b64 rr, p0, p1, p2, p3;\n\t"
-      ".reg .b32 l0, h0, l1, h1, l2, h2, l3, h3, u0, u1, u2, u3, t0, t1;\n\t"
-      ".reg .b8 c0, c1, c2, c3;\n\t"
-      "mov.b64 rr, {%9, %9};\n\t"
-      "mov.b64 p0, {%1, %2};\n\t"
-      "mov.b64 p1, {%3, %4};\n\t"
-      "mov.b64 p2, {%5, %6};\n\t"
-      "mov.b64 p3, {%7, %8};\n\t"
-      "mul.rn.f32x2 p0, p0, rr;\n\t"
-      "mul.rn.f32x2 p1, p1, rr;\n\t"
-      "mul.rn.f32x2 p2, p2, rr;\n\t"
-      "mul.rn.f32x2 p3, p3, rr;\n\t"
-      "mov.b64 {l0, h0}, p0;\n\t"
-      "mov.b64 {l1, h1}, p1;\n\t"
-      "mov.b64 {l2, h2}, p2;\n\t"
-      "mov.b64 {l3, h3}, p3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c0, h0, l0;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c1, h1, l1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c2, h2, l2;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 c3, h3, l3;\n\t"
-      "cvt.u32.u8 u0, c0;\n\t"
-      "cvt.u32.u8 u1, c1;\n\t"
-      "cvt.u32.u8 u2, c2;\n\t"
-      "cvt.u32.u8 u3, c3;\n\t"
-      "prmt.b32 t0, u0, u1, 0x0040;\n\t"
-      "prmt.b32 t1, u2, u3, 0x0040;\n\t"
-      "prmt.b32 %0, t0, t1, 0x5410;\n\t"
-      "}"
-      : "=r"(out)
-      : "r"(f[0]), "r"(f[1]), "r"(f[2]), "r"(f[3]), "r"(f[4]), "r"(f[5]), "r"(f[6]), "r"(f[7]), "f"(r));
+  asm(FP4_E2M1X8_REGS
+      "mov.b32 {e0, e1}, %2;\n\t"
+      "mov.b32 {e2, e3}, %3;\n\t"
+      "mov.b32 {e4, e5}, %4;\n\t"
+      "mov.b32 {e6, e7}, %5;\n\t"
+      FP4_E2M1X8_FMA FP4_E2M1X8_TAIL
+      : "=r"(out) : "r"(rb), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));
   return out;
 }
 
-// eight bf16 (element 2i in the low half of word i of w) times r -> eight
-// E2M1 codes, element 0 in bits 0-3
-__device__ __forceinline__ uint32_t mx_codes8(uint4 w, float r) {
-  const uint32_t f[8] = {w.x << 16, w.x & 0xFFFF0000u, w.y << 16, w.y & 0xFFFF0000u,
-                         w.z << 16, w.z & 0xFFFF0000u, w.w << 16, w.w & 0xFFFF0000u};
-  return e2m1x8_scaled(f, r);
+template <int H>
+__device__ __forceinline__ uint32_t mx_codes8_half(const uint32_t* w, uint32_t rb) {
+  static_assert(H == 0 || H == 1, "half");
+  uint32_t out;
+  if constexpr (H == 0)
+    asm(FP4_E2M1X8_REGS
+        "mov.b32 {e0, z}, %2;\n\t" "mov.b32 {e1, z}, %3;\n\t" "mov.b32 {e2, z}, %4;\n\t" "mov.b32 {e3, z}, %5;\n\t"
+        "mov.b32 {e4, z}, %6;\n\t" "mov.b32 {e5, z}, %7;\n\t" "mov.b32 {e6, z}, %8;\n\t" "mov.b32 {e7, z}, %9;\n\t"
+        FP4_E2M1X8_FMA FP4_E2M1X8_TAIL
+        : "=r"(out) : "r"(rb), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+          "r"(w[7]));
+  else
+    asm(FP4_E2M1X8_REGS
+        "mov.b32 {z, e0}, %2;\n\t" "mov.b32 {z, e1}, %3;\n\t" "mov.b32 {z, e2}, %4;\n\t" "mov.b32 {z, e3}, %5;\n\t"
+        "mov.b32 {z, e4}, %6;\n\t" "mov.b32 {z, e5}, %7;\n\t" "mov.b32 {z, e6}, %8;\n\t" "mov.b32 {z, e7}, %9;\n\t"
+        FP4_E2M1X8_FMA FP4_E2M1X8_TAIL
+        : "=r"(out) : "r"(rb), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+          "r"(w[7]));
+  return out;
+}
+#undef FP4_E2M1X8_TAIL
+#undef FP4_E2M1X8_REGS
+#undef FP4_E2M1X8_FMA
+
+// Per-half magnitude maximum of bf16 pairs: max(|a|, |b|) on each half with
+// the sign bit the xor of the two (max.xorsign.abs.bf16x2, FMA pipe); the
+// caller clears the sign bits.  For finite values the larger magnitude is the
+// larger magnitude bit pattern, so this is the block amax of the bit-pattern
+// form, subnormals included.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t m;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+  return m;
+}
+// magnitude bits of the largest of eight bf16 (the halves of w)
+__device__ __forceinline__ uint32_t bf16x8_amax_bits(uint4 w) {
+  const uint32_t m = bf16x2_absmax(bf16x2_absmax(w.x, w.y), bf16x2_absmax(w.z, w.w)) & 0x7FFF7FFFu;
+  return max(m & 0xFFFFu, m >> 16);
 }
 
 // Compare chain against the midpoints of the grid {0,.5,1,1.5,2,3,4,6}; at a
@@ -212,12 +255,12 @@ __device__ __forceinline__ float e8m0_scale(uint32_t byte) {
 // MXFP4 block scale from the magnitude bits of a bf16 block amax: the E8M0
 // byte is the amax's exponent field minus 2, i.e. floor(log2 amax) - 2 + 127
 // (bf16 and fp32 share the exponent field), clamped at the format's minimum
-// (fields 0-2, which include the bf16 subnormals and 0, give byte 0); r =
-// 2^(127 - byte) multiplies each element exactly
-__device__ __forceinline__ void mx_scale_from_bits(uint32_t amax_bits, uint32_t& byte, float& r) {
+// (fields 0-2, which include the bf16 subnormals and 0, give byte 0); rb =
+// 2^(127 - byte), as a bf16, multiplies each element exactly
+__device__ __forceinline__ void mx_scale_from_bits(uint32_t amax_bits, uint32_t& byte, uint32_t& rb) {
   const uint32_t e = (amax_bits >> 7) & 0xFFu;
   byte = e >= 2 ? e - 2 : 0u;
-  r = e8m0_inv_scale(byte);
+  rb = (254u - byte) << 7;   // 2^(127 - byte) as a bf16 bit pattern (the fp32 one's high half)
 }
 
 // Block scale of one block: writes the scale byte and the multiplier r with

@@ -511,15 +511,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             for (int i = 0; i < 4; ++i) {
               const int r = 8 * e + 2 * i + (lane >> 4);                  // row of this CTA's 128
               const uint4 w = *reinterpret_cast<const uint4*>(xs + r * (FuseCfg::XS_COLS * 2) + cl * 16);
-              uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
-                                    __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
-              m = max(m & 0xFFFFu, m >> 16);
+              uint32_t m = fp4dev::bf16x8_amax_bits(w);
               m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
               m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-              uint32_t byte;
-              float rs;
-              fp4dev::mx_scale_from_bits(m, byte, rs);
-              const uint32_t codes = fp4dev::mx_codes8(w, rs);
+              uint32_t byte, rb;
+              fp4dev::mx_scale_from_bits(m, byte, rb);
+              const uint32_t codes = fp4dev::mx_codes8(w, rb);
               // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
               const int chunk = (h * 4 + (cl >> 2)) ^ (r & 7);
               *reinterpret_cast<uint32_t*>(a_slab + r * P_KSLAB + chunk * 16 + (cl & 3) * 4) = codes;

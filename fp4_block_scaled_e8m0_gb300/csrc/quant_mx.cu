@@ -13,12 +13,13 @@
 // bytes (8 elements), the 4 lanes of a 32-element block share its amax by two
 // shuffles, and the warp writes 128 contiguous bytes of codes.  Column blocks:
 // a thread reads one 32-bit word (a column pair) from each of 32 rows and
-// quantizes both columns' blocks.  The block amax is taken on the bf16 bit
-// patterns (magnitudes order like their 15 low bits, two at a time with a
-// packed integer max), and the E8M0 byte is the bf16 exponent field of the
-// amax minus 2 (bf16 and fp32 share the exponent field): the same bytes as
-// the fp32 form of the scale rule.  x / s is formed exactly as x * 2^(127 - byte)
-// in fp32 before the hardware E2M1 conversion.
+// quantizes both columns' blocks.  The block amax is a packed bf16 magnitude
+// maximum (two columns at a time), and the E8M0 byte is the bf16 exponent
+// field of the amax minus 2 (bf16 and fp32 share the exponent field): the
+// same bytes as the fp32 form of the scale rule.  x / s is formed exactly as
+// x * 2^(127 - byte), one fp32 rounding, before the hardware E2M1 conversion.
+// Both run on the FMA pipe; the integer pipe, which bound the earlier form of
+// this kernel (bit masks, packed integer maxima, unpacking), keeps the rest.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -85,14 +86,12 @@ __global__ void __launch_bounds__(MX_THREADS, MX_CTAS_PER_SM)
       for (int i = 0; i < MX_TR / 8; ++i) {
         const int rr = 8 * i + warp, row = r0 + rr;
         const uint4 w = *reinterpret_cast<const uint4*>(tile + rr * (MX_TC * 2) + lane * 16);
-        uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu), __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
-        m = max(m & 0xFFFFu, m >> 16);
+        uint32_t m = bf16x8_amax_bits(w);
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
         m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-        uint32_t byte;
-        float r;
-        mx_scale_from_bits(m, byte, r);
-        const uint32_t codes = mx_codes8(w, r);
+        uint32_t byte, rb;
+        mx_scale_from_bits(m, byte, rb);
+        const uint32_t codes = mx_codes8(w, rb);
         if (row < rows && col_ok) {
           *reinterpret_cast<uint32_t*>(orow.codes + (int64_t)row * (orow.out_cols >> 1) + (col >> 1)) = codes;
           if ((lane & 3) == 0)
@@ -105,29 +104,23 @@ __global__ void __launch_bounds__(MX_THREADS, MX_CTAS_PER_SM)
       const int p = t & 127, h = t >> 7;
       const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile) + (32 * h) * (MX_TC / 2) + p;
       uint32_t w[32];
-      uint32_t m = 0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        w[j] = tw[j * (MX_TC / 2)];
-        m = __vmaxu2(m, w[j] & 0x7FFF7FFFu);
-      }
+      for (int j = 0; j < 32; ++j) w[j] = tw[j * (MX_TC / 2)];
+      uint32_t m = w[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) m = bf16x2_absmax(m, w[j]);
+      m &= 0x7FFF7FFFu;      // both columns' block amax bits
       const int orow0 = c0 + 2 * p, ocol0 = r0 + 32 * h;   // output row (an input column) and first column
       if (ocol0 < rows) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           if (orow0 + e >= cols) break;
-          uint32_t byte;
-          float r;
-          mx_scale_from_bits(e ? (m >> 16) : (m & 0xFFFFu), byte, r);
+          uint32_t byte, rb;
+          mx_scale_from_bits(e ? (m >> 16) : (m & 0xFFFFu), byte, rb);
           uint32_t q[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // rows 8k .. 8k + 7 of this column as fp32 bit patterns
-            uint32_t f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = e ? (w[8 * k + i] & 0xFFFF0000u) : (w[8 * k + i] << 16);
-            q[k] = e2m1x8_scaled(f, r);
-          }
+          for (int k = 0; k < 4; ++k)   // rows 8k .. 8k + 7 of this column: half e of 8 words
+            q[k] = e ? mx_codes8_half<1>(&w[8 * k], rb) : mx_codes8_half<0>(&w[8 * k], rb);
           *reinterpret_cast<uint4*>(ocol.codes + (int64_t)(orow0 + e) * (ocol.out_cols >> 1) + (ocol0 >> 1)) =
               make_uint4(q[0], q[1], q[2], q[3]);
           ocol.scales[sf_offset(ocol.sf_layout, orow0 + e, ocol0 >> 5, ocol.nsf_row, ocol.nsf_pad)] = (uint8_t)byte;
