@@ -9,6 +9,7 @@
 // neither contract nor reorder it: the results are bit-reproducible.
 #pragma once
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "fp4_internal.h"
@@ -92,6 +93,15 @@ __device__ __forceinline__ uint32_t e2m1x2_hw(float lo, float hi) {
   asm("{\n.reg .b8 q;\ncvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\ncvt.u32.u8 %0, q;\n}"
       : "=r"(r) : "f"(hi), "f"(lo));
   return r & 0xFFu;
+}
+
+// one byte of two E2M1 codes (low nibble = first element) -> their exact values
+// (sign included) by the hardware conversion to f16x2, then to fp32
+__device__ __forceinline__ void e2m1x2_decode(uint32_t byte, float& lo, float& hi) {
+  uint32_t h2;
+  asm("{\n.reg .b8 c;\ncvt.u8.u32 c, %1;\ncvt.rn.f16x2.e2m1x2 %0, c;\n}" : "=r"(h2) : "r"(byte));
+  lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
 }
 
 // Eight bf16 times the power of two rb (a bf16 bit pattern) -> eight E2M1

@@ -901,54 +901,84 @@ __global__ void __launch_bounds__(kThreads) dequant_blk_kernel(fp4_operand q, in
   }
 }
 
-template <int FMT, int ODT>
-__global__ void __launch_bounds__(kThreads) dequant_kernel(fp4_operand q, void* out, int64_t ldo) {
-  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
-  const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
-  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 1.0f;
-  const int64_t total = q.rows * nsf_row;
-  for (int64_t blk = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; blk < total;
-       blk += (int64_t)gridDim.x * blockDim.x) {
-    int64_t r = blk / nsf_row, j = blk - r * nsf_row;
-    uint32_t sb = q.scales[sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad)];
-    float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
-    const uint8_t* cp = q.codes + r * (q.k >> 1) + j * (B / 2);
-    uint32_t w[B / 8];
-    if constexpr (B == 16) {
-      uint2 u = *reinterpret_cast<const uint2*>(cp);
-      w[0] = u.x; w[1] = u.y;
-    } else {
-      uint4 u = *reinterpret_cast<const uint4*>(cp);
-      w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+// one block of codes -> B values (code * s exactly, then * g for NVFP4), stored
+template <int FMT, int ODT, int B>
+__device__ __forceinline__ void dequant_store(const uint32_t* w, uint32_t sb, float g, void* out, int64_t base) {
+  const float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
+  // each code (sign included) exactly as f16 by the hardware conversion, then
+  // code * s (exact: short significands; MXFP4 a power of two), then * g (NVFP4)
+  float v[B];
+#pragma unroll
+  for (int e = 0; e < B / 2; ++e) {
+    float lo, hi;
+    e2m1x2_decode((w[e >> 2] >> (8 * (e & 3))) & 0xFFu, lo, hi);
+    v[2 * e] = __fmul_rn(lo, s);
+    v[2 * e + 1] = __fmul_rn(hi, s);
+    if (FMT == FP4_FMT_NVFP4) {
+      v[2 * e] = __fmul_rn(v[2 * e], g);
+      v[2 * e + 1] = __fmul_rn(v[2 * e + 1], g);
     }
-    float v[B];
+  }
+  if constexpr (ODT == FP4_DTYPE_F32) {
+    float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + base);
 #pragma unroll
-    for (int e = 0; e < B; ++e) {
-      uint32_t c = (w[e >> 3] >> (4 * (e & 7))) & 15u;
-      uint32_t m = c & 7u;
-      float mag = m < 4 ? 0.5f * (float)m : (m == 4 ? 2.0f : m == 5 ? 3.0f : m == 6 ? 4.0f : 6.0f);
-      float val = __fmul_rn(mag, s);  // exact (short significands; MXFP4 power of two)
-      if (FMT == FP4_FMT_NVFP4) val = __fmul_rn(val, g);
-      v[e] = (c & 8u) ? -val : val;
-    }
-    int64_t base = r * ldo + j * B;
-    if constexpr (ODT == FP4_DTYPE_F32) {
-      float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(out) + base);
+    for (int e = 0; e < B / 4; ++e) o4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+  } else {
+    uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + base);
 #pragma unroll
-      for (int e = 0; e < B / 4; ++e) o4[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-    } else {
-      uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + base);
+    for (int e = 0; e < B / 8; ++e) {
+      uint32_t pk[4];
 #pragma unroll
-      for (int e = 0; e < B / 8; ++e) {
-        uint32_t p[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * e + 2 * i], v[8 * e + 2 * i + 1]);
-          p[i] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        o4[e] = make_uint4(p[0], p[1], p[2], p[3]);
+      for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * e + 2 * i], v[8 * e + 2 * i + 1]);
+        pk[i] = *reinterpret_cast<uint32_t*>(&h);
       }
+      o4[e] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
+  }
+}
+
+template <int B>
+__device__ __forceinline__ void load_codes(const uint8_t* cp, uint32_t* w) {
+  if constexpr (B == 16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(cp);
+    w[0] = u.x; w[1] = u.y;
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(cp);
+    w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+  }
+}
+
+// Two blocks per thread and step, both blocks' loads in flight before either
+// is decoded; 32-bit block ids (rows row0 ..) with the multiply-shift divider.
+template <int FMT, int ODT>
+__global__ void __launch_bounds__(kThreads) dequant_kernel(fp4_operand q, void* out, int64_t ldo, int64_t row0,
+                                                           FastDiv nblk, uint32_t total) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nsf_row = nblk.d, nsf_pad = nsf_padded(q.k, FMT);
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 1.0f;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t blk = blockIdx.x * blockDim.x + threadIdx.x; blk < total; blk += 2 * stride) {
+    const uint32_t blk2 = blk + stride;
+    const bool two = blk2 < total && blk2 > blk;
+    const uint32_t ra = fast_div(blk, nblk), ja = blk - ra * nblk.d;
+    const int64_t r = row0 + ra;
+    uint32_t rb = 0, jb = 0;
+    if (two) {
+      rb = fast_div(blk2, nblk);
+      jb = blk2 - rb * nblk.d;
+    }
+    const int64_t r2 = row0 + rb;
+    uint32_t w[B / 8], w2[B / 8];
+    const uint32_t sb = q.scales[sf_offset(q.sf_layout, r, ja, nsf_row, nsf_pad)];
+    load_codes<B>(q.codes + r * (q.k >> 1) + (int64_t)ja * (B / 2), w);
+    uint32_t sb2 = 0;
+    if (two) {
+      sb2 = q.scales[sf_offset(q.sf_layout, r2, jb, nsf_row, nsf_pad)];
+      load_codes<B>(q.codes + r2 * (q.k >> 1) + (int64_t)jb * (B / 2), w2);
+    }
+    dequant_store<FMT, ODT, B>(w, sb, g, out, r * ldo + (int64_t)ja * B);
+    if (two) dequant_store<FMT, ODT, B>(w2, sb2, g, out, r2 * ldo + (int64_t)jb * B);
   }
 }
 
@@ -1653,12 +1683,19 @@ cudaError_t launch_dequant(const fp4_operand& q, int out_dt, void* out, int64_t 
       else dequant_blk_kernel<FMT, FP4_DTYPE_BF16><<<grid, kThreads, 0, st>>>(q, sbl, out, ldo));
     return cudaGetLastError();
   }
-  int64_t total = q.rows * (q.k / B);
-  if (total == 0) return cudaSuccess;
-  int grid = grid_for(total, kThreads, num_sms);
-  FP4_DISPATCH_FMT(q.format, FMT,
-    if (out_dt == FP4_DTYPE_F32) dequant_kernel<FMT, FP4_DTYPE_F32><<<grid, kThreads, 0, st>>>(q, out, ldo);
-    else dequant_kernel<FMT, FP4_DTYPE_BF16><<<grid, kThreads, 0, st>>>(q, out, ldo));
+  const int64_t nsf_row = q.k / B;
+  if (q.rows == 0 || nsf_row == 0) return cudaSuccess;
+  // launches of at most 2^31 blocks (32-bit block ids)
+  const int64_t rows_per = std::max<int64_t>(1, ((int64_t(1) << 31) - 1) / nsf_row);
+  const FastDiv fd = make_fastdiv((uint32_t)nsf_row);
+  for (int64_t r0 = 0; r0 < q.rows; r0 += rows_per) {
+    const int64_t total = std::min(rows_per, q.rows - r0) * nsf_row;
+    const int grid = grid_for(cdiv(total, 2), kThreads, num_sms);
+    FP4_DISPATCH_FMT(q.format, FMT,
+      if (out_dt == FP4_DTYPE_F32)
+        dequant_kernel<FMT, FP4_DTYPE_F32><<<grid, kThreads, 0, st>>>(q, out, ldo, r0, fd, (uint32_t)total);
+      else dequant_kernel<FMT, FP4_DTYPE_BF16><<<grid, kThreads, 0, st>>>(q, out, ldo, r0, fd, (uint32_t)total));
+  }
   return cudaGetLastError();
 }
 
