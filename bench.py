@@ -79,6 +79,12 @@ def parse():
                     help="timed launches of each op outside the headline step (0: skip them)")
     ap.add_argument("--ext-only", action="store_true",
                     help="run only the measurements outside the headline step and print their JSON")
+    ap.add_argument("--only", default=None,
+                    help="profiling runs (ncu): after one full 7B FFN step, launch the comma-separated ops of "
+                         "that step, or 'fused_quant_a' (the forward GEMM with X quantized inside), "
+                         "--only-launches times each; 'llama_step' runs the LLaMA-1B step's ops instead. "
+                         "Prints nothing but 'ok'")
+    ap.add_argument("--only-launches", type=int, default=1)
     return ap.parse_args()
 
 
@@ -793,6 +799,38 @@ def time_linear_small(fp4, dev, pk, batch=50, replays=20):
             "note": "launch-bound (3 launches of a few microseconds each): reported, not held to the roofline bar"}
 
 
+def run_only(fp4, inputs, args, dev):
+    """Launch named ops for a profiler (one stream, in order, L2 flushed before each)."""
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    if args.only == "llama_step":
+        d = inputs.llama1b_mlp_up()
+        step = Step(fp4, *(d[k].to(dev) for k in ("X", "W", "dY")), dev)
+        for i in range(args.only_launches):
+            flush.fill_(i & 0xFF)
+            for _, fn in step.ops(i):
+                fn()
+    else:
+        d = inputs.ffn7b()
+        step = FfnStep(fp4, *(d[k].to(dev) for k in ("X", "W", "dY")), dev)
+        ops = dict(step.ops(0))
+        ops["fused_quant_a"] = lambda: fp4.fp4_gemm_quant_a(step.X, step.wq, out=step.Y)
+        names = args.only.split(",")
+        for n in names:
+            if n not in ops:
+                raise SystemExit(f"--only: unknown op {n!r} (ops: {', '.join(ops)})")
+        for _, fn in step.ops(0):
+            fn()
+        for i in range(args.only_launches):
+            for n in names:
+                flush.fill_(i & 0xFF)
+                ops[n]()
+    torch.cuda.synchronize()
+    status = fp4.fp4_sync_status()
+    if status:
+        raise SystemExit(f"device status {status}")
+    print("ok")
+
+
 # ---------------------------------------------------------------------------
 # main
 # ---------------------------------------------------------------------------
@@ -820,6 +858,9 @@ def main():
         if dist:
             dist.barrier()
     fp4.load_library()
+    if args.only:
+        run_only(fp4, inputs, args, dev)
+        return
     pk = peaks()
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     side = torch.cuda.Stream(device=dev)
