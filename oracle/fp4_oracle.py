@@ -803,3 +803,91 @@ def hcp_gemm_fp8(x, x_codes, x_scales, w, w_codes, w_scales, fmt, g_x, g_w, hot,
     A = a8 * sa.astype(np.float64)[:, None]
     B = b8 * sb.astype(np.float64)[:, None]
     return y + A @ B.T, bound + np.abs(A) @ np.abs(B).T
+
+
+# ----------------------------------------------------------------------------
+# HCP extra columns as MXFP8 in the FP4 accumulator (single kernel)
+#
+# READING (the pages fix no FP8 format for the compensation: [msr] §六 runs its
+# compensation in FP8, [lowprec] §1.1 describes the MX family, elements sharing
+# a power-of-two E8M0 scale per 32): the extra columns of the bf16 tail, with
+# B already divided by alpha but not rounded to bf16, are quantized along the
+# hot-channel axis in blocks of 32.  Each part of the columns (order 2: [dX_H |
+# X_H] and [W_hat_H | dW_H]) is padded with zeros to a multiple of 32 so that
+# no block mixes the two parts.  A block's scale is 2^e with e the smallest
+# integer such that amax / 2^e <= 448 (E4M3's largest value, so no element
+# saturates), clamped to E8M0's [-127, 127] (amax 0: -127); each element is
+# the nearest E4M3 value of v / 2^e, ties to even, sign kept.  A block-scaled
+# FP8 MMA multiplies the columns into the FP4 part's accumulator:
+#   Y = alpha (X_hat W_hat^T + sum_j a8[m,j] 2^ea[m,j/32] b8[n,j] 2^eb[n,j/32]).
+# ----------------------------------------------------------------------------
+
+def mxfp8_exponent(amax: np.ndarray) -> np.ndarray:
+    """Smallest e with amax / 2**e <= 448, clamped to [-127, 127]; amax 0 -> -127.
+
+    amax = m * 2**x with m in [0.5, 1) (frexp, exact): amax / 2**(x - 9) = 512 m
+    lies in [256, 512), at most 448 exactly when m <= 7/8.  Pinned by a brute-force
+    search over exponents and hand-derived points."""
+    amax = np.asarray(amax, dtype=np.float32).astype(np.float64)
+    m, x = np.frexp(amax)
+    e = x.astype(np.int64) - 9 + (m > 0.875).astype(np.int64)
+    e = np.where(amax == 0.0, -127, e)
+    return np.clip(e, -127, 127)
+
+
+def mxfp8_quantize_rows(v, block: int = 32):
+    """v [R, C] (C a multiple of `block`) -> (codes uint8 [R, C], exps int [R, C / block]):
+    E4M3 bytes (bit 7 the sign) of v / 2**e and the blocks' exponents e."""
+    v = np.asarray(v, dtype=np.float32)
+    R, C = v.shape
+    blocks = v.reshape(R, C // block, block)
+    amax = np.abs(blocks).max(axis=2) if C else np.zeros((R, 0), np.float32)
+    e = mxfp8_exponent(amax)
+    # v * 2**-e: the exact product rounded once to fp32
+    t = (np.abs(blocks).astype(np.float64) * np.exp2(-e.astype(np.float64))[:, :, None]).astype(np.float32)
+    mag = e4m3_encode_rn_satfinite(t)
+    sign = np.signbit(blocks).astype(np.uint8) << 7
+    return (mag | sign).reshape(R, C).astype(np.uint8), e
+
+
+def mxfp8_values(codes, exps, block: int = 32) -> np.ndarray:
+    """fp64 values dec(code) * 2**e of mxfp8_quantize_rows' output."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    mag = e4m3_decode(codes & 0x7F)
+    val = np.where(codes & 0x80, -mag, mag)
+    return val * np.repeat(np.exp2(np.asarray(exps, dtype=np.float64)), block, axis=1)
+
+
+def hcp_mxfp8_columns(x, x_codes, x_scales, w, w_codes, w_scales, fmt, g_x, g_w, hot, order=2):
+    """fp32 extra columns before the MXFP8 rounding, each part padded to a
+    multiple of 32 with zeros: A [M, parts * kp], B [N, parts * kp] (B / alpha)."""
+    a, b = hcp_fp8_columns(x, x_codes, x_scales, w, w_codes, w_scales, fmt, g_x, g_w, hot, order)
+    if fmt == NVFP4:
+        inv_alpha = np.float32(np.float32(1.0) / np.float32(np.float32(g_x) * np.float32(g_w)))
+        b = (b * inv_alpha).astype(np.float32)
+    k = len(np.asarray(hot))
+    parts = 2 if order == 2 else 1
+    kp = -(-k // 32) * 32
+
+    def pad(v):
+        out = np.zeros((v.shape[0], parts * kp), np.float32)
+        for p in range(parts):
+            out[:, p * kp: p * kp + k] = v[:, p * k: (p + 1) * k]
+        return out
+    return pad(a), pad(b)
+
+
+def hcp_gemm_mxfp8(x, x_codes, x_scales, w, w_codes, w_scales, fmt, g_x, g_w, hot, order=2):
+    """Y = alpha (Q(X) Q(W)^T + A8 B8^T) in fp64 (A8, B8 the MXFP8 columns'
+    values); returns (Y, bound).  For order 0, x_codes / x_scales / g_x are the
+    quantization of X with H zeroed."""
+    A = operand_values(x_codes, x_scales, fmt)
+    B = operand_values(w_codes, w_scales, fmt)
+    a, b = hcp_mxfp8_columns(x, x_codes, x_scales, w, w_codes, w_scales, fmt, g_x, g_w, hot, order)
+    A8 = mxfp8_values(*mxfp8_quantize_rows(a))
+    B8 = mxfp8_values(*mxfp8_quantize_rows(b))
+    alpha = 1.0 if fmt == MXFP4 else float(np.float32(g_x)) * float(np.float32(g_w))
+    alpha32 = 1.0 if fmt == MXFP4 else float(np.float32(np.float32(g_x) * np.float32(g_w)))
+    y = alpha * (A @ B.T) + alpha32 * (A8 @ B8.T)
+    bound = alpha * (np.abs(A) @ np.abs(B).T) + alpha32 * (np.abs(A8) @ np.abs(B8).T)
+    return y, bound
