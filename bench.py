@@ -325,7 +325,8 @@ def time_hcp(fp4, dev, flush, launches, pk):
     """Hot-channel compensation ("大模型4位训练中的异常值动态分析与优化实践" §3-4) on the hot-channel
     activations: plain NVFP4 GEMM, order-2 compensation (bf16 residual columns), the variant with
     the hot channels zeroed before quantizing (their product in bf16), single-kernel and with the
-    residual as a second GEMM in bf16 or E4M3; h = 9% of K.  Relative L2 error of Y against the
+    residual as a second GEMM in bf16 or E4M3, and single-kernel with MXFP8 residual columns;
+    h = 9% of K.  Relative L2 error of Y against the
     fp64 product on 64 sampled rows."""
     from fp4_block_scaled_e8m0_gb300 import inputs
     d = inputs.hcp_square(OCC_M, OCC_K, OCC_N)
@@ -351,7 +352,11 @@ def time_hcp(fp4, dev, flush, launches, pk):
              "order2_fp8_two_kernel": lambda: fp4.fp4_hcp_gemm(X, W, xq, wq, hot, h, fp4.FP4_HCP_TWO_FP8, 2, out=Y,
                                                                workspace=ws),
              "zeroed_fp8_two_kernel": lambda: fp4.fp4_hcp_gemm(X, W, x0q, wq, hot, h, fp4.FP4_HCP_TWO_FP8, 0, out=Y,
-                                                               workspace=ws)}
+                                                               workspace=ws),
+             "order2_mxfp8": lambda: fp4.fp4_hcp_gemm(X, W, xq, wq, hot, h, fp4.FP4_HCP_SINGLE_MXFP8, 2, out=Y,
+                                                      workspace=ws),
+             "zeroed_mxfp8": lambda: fp4.fp4_hcp_gemm(X, W, x0q, wq, hot, h, fp4.FP4_HCP_SINGLE_MXFP8, 0, out=Y,
+                                                      workspace=ws)}
     for name, fn in cases.items():
         r = _rate("tensor", flops, _time_op(fn, flush, launches), pk)
         fn()

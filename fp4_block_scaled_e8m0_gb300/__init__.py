@@ -29,7 +29,7 @@ FP4_ROUND_RTN, FP4_ROUND_SR = 0, 1
 FP4_SCALING_1D, FP4_SCALING_2D = 0, 1
 FP4_SF_ROWMAJOR, FP4_SF_MMA = 0, 1
 FP4_DTYPE_BF16, FP4_DTYPE_F32 = 0, 1
-FP4_HCP_SINGLE, FP4_HCP_TWO, FP4_HCP_TWO_FP8 = 0, 1, 2
+FP4_HCP_SINGLE, FP4_HCP_TWO, FP4_HCP_TWO_FP8, FP4_HCP_SINGLE_MXFP8 = 0, 1, 2, 3
 BLOCK = {FP4_FMT_MXFP4: 32, FP4_FMT_NVFP4: 16}
 
 

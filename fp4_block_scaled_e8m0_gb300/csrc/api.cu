@@ -633,13 +633,30 @@ static int64_t hcp_kx(int32_t k_hot, int32_t order) { return cdiv((int64_t)(orde
 // E4M3 extra columns: K padded to 128 (one 128-byte stage row)
 static int64_t hcp_kx8(int32_t k_hot, int32_t order) { return cdiv((int64_t)(order == 2 ? 2 : 1) * k_hot, 128) * 128; }
 
-// the larger of the bf16 layout [A_ext | B_ext] and the E4M3 one [a8 | b8 | sa | sb]
+// MXFP8 extra columns: each part padded to 32 columns, the whole to 128 (one stage)
+static int64_t hcp_kxm(int32_t k_hot, int32_t order) {
+  return cdiv((int64_t)(order == 2 ? 2 : 1) * cdiv(k_hot, 32) * 32, 128) * 128;
+}
+// MXFP8 layout: [a8 | b8 | sa | sb], scales of rows padded to 128
+static int64_t hcp_mx8_bytes(int64_t m, int64_t n, int64_t kxm, int64_t* off_b8, int64_t* off_sa, int64_t* off_sb) {
+  const int64_t b8 = cdiv(m * kxm, 256) * 256;
+  const int64_t sa = b8 + cdiv(n * kxm, 256) * 256;
+  const int64_t sb = sa + cdiv(m, 128) * 128 * (kxm / 32);
+  if (off_b8) *off_b8 = b8;
+  if (off_sa) *off_sa = sa;
+  if (off_sb) *off_sb = sb;
+  return sb + cdiv(n, 128) * 128 * (kxm / 32);
+}
+
+// the largest of the bf16 layout [A_ext | B_ext], the E4M3 one [a8 | b8 | sa | sb]
+// and the MXFP8 one
 size_t fp4_hcp_workspace_bytes(int64_t m, int64_t n, int32_t k_hot, int32_t order) {
   if (m <= 0 || n <= 0 || k_hot <= 0) return 0;
   const int64_t kx = hcp_kx(k_hot, order), kx8 = hcp_kx8(k_hot, order);
   const int64_t bf16 = cdiv(m * kx * 2, 256) * 256 + n * kx * 2;
   const int64_t fp8 = cdiv(m * kx8, 256) * 256 + cdiv(n * kx8, 256) * 256 + cdiv(m * 4, 256) * 256 + n * 4;
-  return (size_t)std::max(bf16, fp8);
+  const int64_t mx8 = hcp_mx8_bytes(m, n, hcp_kxm(k_hot, order), nullptr, nullptr, nullptr);
+  return (size_t)std::max(std::max(bf16, fp8), mx8);
 }
 
 int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf16, int64_t ldw,
@@ -647,7 +664,8 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
                  int32_t order, void* workspace, size_t ws_bytes, int32_t out_dtype, void* y, int64_t ldy,
                  void* stream) {
   if (!ctx || !dtype_ok(out_dtype)) return FP4_ERR_INVALID_ARG;
-  if (mode != FP4_HCP_SINGLE && mode != FP4_HCP_TWO && mode != FP4_HCP_TWO_FP8) return FP4_ERR_INVALID_ARG;
+  if (mode != FP4_HCP_SINGLE && mode != FP4_HCP_TWO && mode != FP4_HCP_TWO_FP8 && mode != FP4_HCP_SINGLE_MXFP8)
+    return FP4_ERR_INVALID_ARG;
   if (order < 0 || order > 2) return FP4_ERR_INVALID_ARG;
   int s = check_operand(xq, true);
   if (s) return s;
@@ -679,6 +697,23 @@ int fp4_hcp_gemm(fp4_ctx* ctx, const void* x_bf16, int64_t ldx, const void* w_bf
   if (k_hot == 0 || M == 0 || N == 0) return launch_gemm(g, st);
   if (ws_bytes < fp4_hcp_workspace_bytes(M, N, k_hot, order) || !workspace || !al16(workspace))
     return FP4_ERR_INVALID_ARG;
+  if (mode == FP4_HCP_SINGLE_MXFP8) {
+    const int64_t kxm = hcp_kxm(k_hot, order);
+    int64_t ob8, osa, osb;
+    hcp_mx8_bytes(M, N, kxm, &ob8, &osa, &osb);
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    cudaError_t e = launch_hcp_gather_mx8(static_cast<const uint16_t*>(x_bf16), ldx,
+                                          static_cast<const uint16_t*>(w_bf16), ldw, *xq, *wq, hot_idx, k_hot, order,
+                                          kxm, base, base + osa, base + ob8, base + osb, ctx->num_sms, st);
+    if (e != cudaSuccess) return FP4_ERR_CUDA;
+    g.a_ext = base;
+    g.b_ext = base + ob8;
+    g.a_ext_sf = base + osa;
+    g.b_ext_sf = base + osb;
+    g.kx = kxm;
+    g.ext_mx8 = true;
+    return launch_gemm(g, st);
+  }
   if (mode == FP4_HCP_TWO_FP8) {
     const int64_t kx8 = hcp_kx8(k_hot, order);
     uint8_t* base = static_cast<uint8_t*>(workspace);

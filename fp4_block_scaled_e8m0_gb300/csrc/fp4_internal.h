@@ -107,10 +107,13 @@ cudaError_t launch_encode_e4m3(const float* t, uint8_t* out, int64_t n, cudaStre
 struct GemmArgs {
   const fp4_operand* A;
   const fp4_operand* B;
-  const void* a_ext;       // [M][kx] bf16 (or E4M3 bytes with ext_fp8), or null
+  const void* a_ext;       // [M][kx] bf16 (or E4M3 bytes with ext_fp8 / ext_mx8), or null
   const void* b_ext;       // [N][kx]
-  int64_t kx;              // extra K (multiple of 64; of 128 with ext_fp8), 0 if none
-  bool ext_fp8;            // extra columns are E4M3 (kind::f8f6f4)
+  int64_t kx;              // extra K (multiple of 64; of 128 with ext_fp8 / ext_mx8), 0 if none
+  bool ext_fp8;            // extra columns are E4M3 (kind::f8f6f4), per-row scales in the epilogue
+  bool ext_mx8;            // extra columns are MXFP8: E4M3 with E8M0 block scales (CTA-pair kernel,
+  const uint8_t* a_ext_sf; //   kind::mxf8f6f4 into the FP4 accumulator); their scales, MMA layout
+  const uint8_t* b_ext_sf;
   const float* row_scale;  // [M] and [N]: C (+)= row_scale[m] col_scale[n] acc (no alpha); null: alpha
   const float* col_scale;
   bool fp4_part;           // false: only the bf16 columns (two-kernel residual GEMM)
@@ -149,6 +152,11 @@ cudaError_t launch_hcp_topk(const float* err, int64_t k, int k_hot, int32_t* hot
 int validate_hcp_select(const void* x_bf16, int64_t ldx, const fp4_operand* xq, int32_t k_hot,
                         const int32_t* hot_idx);
 // E4M3 extra columns [M][kx] / [N][kx] (kx a multiple of 128) with row scales sa / sb
+// MXFP8 extra columns (E4M3 codes [rows][kxm], E8M0 scales in the MMA layout)
+cudaError_t launch_hcp_gather_mx8(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
+                                  const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot, int k_hot,
+                                  int order, int64_t kxm, uint8_t* a8, uint8_t* sa, uint8_t* b8, uint8_t* sb,
+                                  int num_sms, cudaStream_t st);
 cudaError_t launch_hcp_gather_fp8(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
                                   const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot, int k_hot,
                                   int order, int64_t kx, uint8_t* a8, uint8_t* b8, float* sa, float* sb, int num_sms,

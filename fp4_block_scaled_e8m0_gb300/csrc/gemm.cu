@@ -730,6 +730,7 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   // extra columns, the outlier epilogue, row/column scales and C += stay on
   // the one-SM kernel
   if (g.fp4_part && !g.ext_fp8 && !g.occ_len && !g.row_scale && !g.accumulate) return launch_gemm_pair(g, st);
+  if (g.ext_mx8) return FP4_ERR_UNSUPPORTED;   // MXFP8 extra columns exist on the pair kernel only
   Params p{};
   p.M = (int)M;
   p.N = (int)N;

@@ -131,6 +131,7 @@ struct PairParams {
   uint8_t* qa_scales;     // MMA layout, atoms of 128 rows x 4 scales
   int K;
   int sf_groups;          // scale atoms per 128 rows in qa_scales (K padded to 256, / 128)
+  int ext_mx8;            // extra columns are MXFP8 (128 per stage, one scale atom per 128 rows)
 };
 
 template <bool NV, bool BF16_OUT, bool FUSE>
@@ -138,6 +139,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
     fp4_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                          const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                          const __grid_constant__ CUtensorMap tm_ax, const __grid_constant__ CUtensorMap tm_bx,
+                         const __grid_constant__ CUtensorMap tm_sfax, const __grid_constant__ CUtensorMap tm_sfbx,
                          const PairParams p) {
   static_assert(!(NV && FUSE), "the fused quantizer forms MXFP4 operands");
   using Cfg = PairCfg<NV>;
@@ -241,6 +243,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
             mbar_expect_tx(&sf_full[s], Cfg::SFA_BYTES + Cfg::SFB_BYTES);
             tma_load_3d(stage_sfa(s), &tm_sfa, &sf_full[s], 0, kt * Cfg::ATOMS * 4, 2 * tm + (int)rank);
             tma_load_3d(stage_sfb(s), &tm_sfb, &sf_full[s], 0, kt * Cfg::ATOMS * 4, 2 * tn);
+          } else if (p.ext_mx8) {
+            // MXFP8 extra columns: 128 per stage (128 bytes of K) and their scale
+            // atoms (this CTA's 128 A rows, the tile's 256 B rows)
+            const int xt = kt - p.k_tiles;
+            tma_load_2d_pair(stage_a(s), &tm_ax, fb, xt * 128, row_a);
+            tma_load_2d_pair(stage_b(s), &tm_bx, fb, xt * 128, row_b);
+            mbar_expect_tx(&sf_full[s], 512 + 1024);
+            tma_load_3d(stage_sfa(s), &tm_sfax, &sf_full[s], 0, xt * 4, 2 * tm + (int)rank);
+            tma_load_3d(stage_sfb(s), &tm_sfbx, &sf_full[s], 0, xt * 4, 2 * tn);
           } else {
             // extra bf16 columns: 64 per stage (128 bytes of K), no scales
             const int kx = (kt - p.k_tiles) * 64;
@@ -293,6 +304,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
               mma_fp4_pair<NV>(tmem, da + 2 * j, db + 2 * j, (!NV && (j & 1)) ? id_odd : id_even, slot + a_col,
                                slot + b_col, j > 0 ? 1u : acc0);
             }
+          } else if (p.ext_mx8) {
+            // 4 MXFP8 MMAs of 32 K elements (32 bytes), scale byte j of the
+            // stage's atoms: A's at the slot's first columns, B's two 128-row
+            // groups where the FP4 stages keep B's
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mma_mxf8_pair(tmem, da + 2 * j, db + 2 * j, idesc_mxf8((uint32_t)j, 256, P_BN), slot,
+                            slot + 4u * Cfg::ATOMS, j > 0 ? 1u : acc0);
           } else {
             // 4 bf16 MMAs of 16 K elements (32 bytes) into the same accumulator
 #pragma unroll
@@ -340,14 +359,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
                 *reinterpret_cast<const uint2*>(stage_sfa(s) + t * 8);
           }
         }
-        if (kt >= p.k_tiles) {   // extra bf16 columns: no scales to stage
+        const uint32_t slot = tmem + lane_base + P_BN + (uint32_t)s * Cfg::SLOT_COLS;
+        uint32_t v[16];
+        if (kt >= p.k_tiles) {
+          if (p.ext_mx8) {
+            // MXFP8 extra columns: A's one atom at the slot's columns 0-3, B's
+            // two 128-row groups at 4 * ATOMS + 0-7
+            const uint4 wa = *reinterpret_cast<const uint4*>(stage_sfa(s) + lane * 16);
+            v[0] = wa.x; v[1] = wa.y; v[2] = wa.z; v[3] = wa.w;
+            v[4] = v[5] = v[6] = v[7] = 0u;
+            tmem_st8(slot, v);
+            const uint4 w0 = *reinterpret_cast<const uint4*>(stage_sfb(s) + lane * 16);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(stage_sfb(s) + 512 + lane * 16);
+            v[0] = w0.x; v[1] = w0.y; v[2] = w0.z; v[3] = w0.w;
+            v[4] = w1.x; v[5] = w1.y; v[6] = w1.z; v[7] = w1.w;
+            tmem_st8(slot + 4u * Cfg::ATOMS, v);
+            tmem_st_wait();
+            tc_fence_before();
+          }
+          // extra bf16 columns: no scales to stage
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(full_l + (uint32_t)s * 8u);
           if (++s == STAGES) { s = 0; phase ^= 1; }
           continue;
         }
-        const uint32_t slot = tmem + lane_base + P_BN + (uint32_t)s * Cfg::SLOT_COLS;
-        uint32_t v[16];
 #pragma unroll
         for (int a = 0; a < Cfg::ATOMS; ++a) {
           const uint4 w = *reinterpret_cast<const uint4*>(stage_sfa(s) + a * 512 + lane * 16);
@@ -559,7 +594,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 
 template <bool NV, bool BF16_OUT, bool FUSE = false>
 int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
-                const CUtensorMap& tax, const CUtensorMap& tbx, const PairParams& p, int num_sms, cudaStream_t st) {
+                const CUtensorMap& tax, const CUtensorMap& tbx, const CUtensorMap& tsax, const CUtensorMap& tsbx,
+                const PairParams& p, int num_sms, cudaStream_t st) {
   constexpr int SMEM = FUSE ? FuseCfg::SMEM : PairCfg<NV>::SMEM;
   static bool attr_set = false;
   if (!attr_set) {
@@ -570,7 +606,8 @@ int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   }
   const int tiles = p.tiles_m * p.tiles_n;
   const int pairs = std::max(1, std::min(tiles, num_sms / 2));
-  fp4_gemm_pair_kernel<NV, BF16_OUT, FUSE><<<2 * pairs, P_THREADS, SMEM, st>>>(ta, tb, tsa, tsb, tax, tbx, p);
+  fp4_gemm_pair_kernel<NV, BF16_OUT, FUSE><<<2 * pairs, P_THREADS, SMEM, st>>>(ta, tb, tsa, tsb, tax, tbx, tsax, tsbx,
+                                                                              p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 
@@ -594,7 +631,8 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t st) {
   p.status = g.status;
   p.tiles_m = (int)cdiv(M, 256);
   p.tiles_n = (int)cdiv(N, P_BN);
-  p.ext_tiles = (int)(g.kx / 64);
+  p.ext_mx8 = g.ext_mx8 ? 1 : 0;
+  p.ext_tiles = (int)(g.kx / (g.ext_mx8 ? 128 : 64));
   p.qa_codes = g.qa_codes;
   p.qa_scales = g.qa_scales;
   p.K = (int)K;
@@ -613,19 +651,25 @@ int launch_gemm_pair(const GemmArgs& g, cudaStream_t st) {
     ok &= tc::make_map(&ta, g.A->codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K / 2, M, P_BM);
     ok &= tc::make_sf_map(&tsa, g.A->scales, group_bytes, cdiv(M, 128), atoms * 4, 1);
   }
-  CUtensorMap tax = ta, tbx = tb;   // never read without extra columns
-  if (g.kx > 0) {
+  CUtensorMap tax = ta, tbx = tb, tsax = tsb, tsbx = tsb;   // never read without extra columns
+  if (g.kx > 0 && g.ext_mx8) {
+    // E4M3 codes [rows][kx] and E8M0 scales in the MMA layout (kx / 32 per row)
+    ok &= tc::make_map(&tax, g.a_ext, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.kx, M, 128);
+    ok &= tc::make_map(&tbx, g.b_ext, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.kx, N, 128);
+    ok &= tc::make_sf_map(&tsax, g.a_ext_sf, 4 * g.kx, cdiv(M, 128), 4, 1);
+    ok &= tc::make_sf_map(&tsbx, g.b_ext_sf, 4 * g.kx, cdiv(N, 128), 4, 2);
+  } else if (g.kx > 0) {
     ok &= tc::make_map(&tax, g.a_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, M, 128);
     ok &= tc::make_map(&tbx, g.b_ext, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.kx, N, 128);
   }
   if (!ok) return FP4_ERR_CUDA;
   const bool bf16 = g.out_dtype == FP4_DTYPE_BF16;
-  if (fuse) return bf16 ? launch_pair<false, true, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st)
-                        : launch_pair<false, false, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st);
-  if (nv) return bf16 ? launch_pair<true, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st)
-                      : launch_pair<true, false>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st);
-  return bf16 ? launch_pair<false, true>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st)
-              : launch_pair<false, false>(ta, tb, tsa, tsb, tax, tbx, p, g.num_sms, st);
+  if (fuse) return bf16 ? launch_pair<false, true, true>(ta, tb, tsa, tsb, tax, tbx, tsax, tsbx, p, g.num_sms, st)
+                        : launch_pair<false, false, true>(ta, tb, tsa, tsb, tax, tbx, tsax, tsbx, p, g.num_sms, st);
+  if (nv) return bf16 ? launch_pair<true, true>(ta, tb, tsa, tsb, tax, tbx, tsax, tsbx, p, g.num_sms, st)
+                      : launch_pair<true, false>(ta, tb, tsa, tsb, tax, tbx, tsax, tsbx, p, g.num_sms, st);
+  return bf16 ? launch_pair<false, true>(ta, tb, tsa, tsb, tax, tbx, tsax, tsbx, p, g.num_sms, st)
+              : launch_pair<false, false>(ta, tb, tsa, tsb, tax, tbx, tsax, tsbx, p, g.num_sms, st);
 }
 
 }  // namespace fp4

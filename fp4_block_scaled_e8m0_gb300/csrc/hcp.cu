@@ -246,6 +246,172 @@ __global__ void __launch_bounds__(256) gather_fp8_kernel(const uint16_t* __restr
   }
 }
 
+// MXFP8 extra columns for the single-kernel tail: one warp per (row, 32-column
+// block) of A_ext or B_ext, rows padded to a multiple of 128 (padding rows get
+// scale bytes 0 and no codes).  The values are gather_kernel's (B divided by
+// alpha), each part padded with zeros to kp = 32 * ceil(k_hot / 32) columns and
+// the whole to kxm; a block's E8M0 exponent is the smallest e with
+// amax / 2^e <= 448 (E4M3's largest value), clamped to [-127, 127] (amax 0:
+// -127), and each element the E4M3 byte of |v| * 2^-e (one fp32 rounding, then
+// nearest, ties to even) with v's sign in bit 7.  Scales in the MMA layout.
+template <int FMT>
+__global__ void __launch_bounds__(256) gather_mx8_kernel(const uint16_t* __restrict__ src, int64_t ld, fp4_operand q,
+                                                         const int32_t* __restrict__ hot, int k_hot, int order,
+                                                         int64_t kxm, bool is_a, const float* ts_other,
+                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  const int64_t nsf_row = q.k / B, nsf_pad = nsf_padded(q.k, FMT);
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
+  const float inv_alpha = (FMT == FP4_FMT_NVFP4 && !is_a) ? __frcp_rn(__fmul_rn(*ts_other, g)) : 1.0f;
+  const int lane = threadIdx.x & 31;
+  const int64_t nblk = kxm / 32, kp = cdiv(k_hot, 32) * 32;
+  const int parts = order == 2 ? 2 : 1;
+  const int64_t units = cdiv(q.rows, 128) * 128 * nblk;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t u = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; u < units; u += nwarps) {
+    const int64_t r = u / nblk, jb = u - r * nblk;
+    const int64_t col = jb * 32 + lane;
+    const int part = (int)(col / kp);
+    const int64_t idx = col - (int64_t)part * kp;
+    float v = 0.0f;
+    if (r < q.rows && part < parts && idx < k_hot) {
+      const int64_t c = hot[idx];
+      const float x = bf16_bits_to_float(src[r * ld + c]);
+      // A, order 2: part 0 -> x - x_hat, part 1 -> x ;  A, orders 1 and 0: x
+      // B, order 2: part 0 -> x_hat, part 1 -> x - x_hat ;  B, order 1: x - x_hat ;  B, order 0: x  (all / alpha)
+      const bool want_hat = !is_a && order == 2 && part == 0;
+      const bool want_delta = is_a ? (order == 2 && part == 0) : (!want_hat && order != 0);
+      if (want_delta || want_hat) {
+        const float xh = dequant_elem<FMT>(q, r, c, g, nsf_row, nsf_pad);
+        v = want_hat ? xh : __fsub_rn(x, xh);
+      } else {
+        v = x;
+      }
+      if (!is_a) v = __fmul_rn(v, inv_alpha);
+    }
+    float m = fabsf(v);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    // amax = 1.f * 2^(E - 127) = (1.f / 2) * 2^(E - 126): e = E - 126 - 9, + 1 when 1.f > 1.75
+    const uint32_t bits = __float_as_uint(m);
+    int e = (int)(bits >> 23) - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    e = max(-127, min(127, e));
+    if (lane == 0)
+      scales[((r >> 7) * (nblk >> 2) + (jb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (jb & 3)] =
+          (uint8_t)(e + 127);
+    if (r < q.rows) {
+      const float t = __fmul_rn(fabsf(v), __uint_as_float((uint32_t)(127 - e) << 23));   // |v| * 2^-e
+      codes[r * kxm + col] = (uint8_t)(e4m3_rn_satfinite(t) | (signbit(v) ? 0x80u : 0u));
+    }
+  }
+}
+
+// gather_mx8_kernel with each row staged first: a warp reads its row's bf16
+// values, FP4 codes and block scales with coalesced loads into shared memory
+// (with ~9% of the channels hot, nearly every 32-byte sector of the row is
+// needed, and the per-block warps of the kernel above fetched each hot value,
+// code and scale on its own), then each lane forms one whole 32-column block
+// of the row from shared memory (no shuffles).  The hot list is kept in the
+// CTA's shared memory transposed, ht[i][b] = channel of column 32 b + i, so
+// that the lanes of a warp read consecutive words.  Same bytes.
+template <int FMT>
+__global__ void __launch_bounds__(256) gather_mx8_rows_kernel(const uint16_t* __restrict__ src, int64_t ld,
+                                                              fp4_operand q, const int32_t* __restrict__ hot,
+                                                              int k_hot, int order, int64_t kxm, bool is_a,
+                                                              const float* ts_other, uint8_t* __restrict__ codes,
+                                                              uint8_t* __restrict__ scales) {
+  constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  extern __shared__ __align__(16) uint8_t row_smem[];
+  const int64_t K = q.k, nsf_row = K / B, nsf_pad = nsf_padded(K, FMT);
+  const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
+  const float inv_alpha = (FMT == FP4_FMT_NVFP4 && !is_a) ? __frcp_rn(__fmul_rn(*ts_other, g)) : 1.0f;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  // 32-bit block arithmetic: a part's columns kp = 32 kpb; blocks beyond the parts are padding
+  const int nblk = (int)(kxm / 32), kpb = (int)cdiv(k_hot, 32), parts = order == 2 ? 2 : 1;
+  int32_t* ht = reinterpret_cast<int32_t*>(row_smem);                  // [32][kpb], -1 past k_hot
+  const int64_t per_warp = cdiv(K * 2 + K / 2 + nsf_pad, 16) * 16;     // 16-byte aligned regions
+  uint8_t* wbase = row_smem + cdiv((int64_t)32 * kpb * 4, 16) * 16 + (int64_t)warp * per_warp;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(wbase);                   // the row's bf16
+  uint8_t* cs = wbase + K * 2;                                         // its FP4 codes
+  uint8_t* ss = cs + K / 2;                                            // its block scales
+  for (int t = threadIdx.x; t < 32 * kpb; t += blockDim.x) {
+    const int b = t / 32, i = t - b * 32;                              // column 32 b + i of a part
+    ht[i * kpb + b] = 32 * b + i < k_hot ? hot[32 * b + i] : -1;
+  }
+  __syncthreads();
+  const int64_t rows_pad = cdiv(q.rows, 128) * 128;
+  for (int64_t r = (int64_t)blockIdx.x * nw + warp; r < rows_pad; r += (int64_t)gridDim.x * nw) {
+    const bool real = r < q.rows;
+    if (real) {
+      const uint16_t* xr = src + r * ld;
+      for (int64_t c = 8 * lane; c < K; c += 256) *reinterpret_cast<uint4*>(xs + c) = ld_nc_v4(xr + c);
+      const uint8_t* cr = q.codes + r * (K >> 1);
+      for (int64_t c = 16 * lane; c < (K >> 1); c += 512) *reinterpret_cast<uint4*>(cs + c) = ld_nc_v4(cr + c);
+      // the row's scales: four consecutive ones at a time (one 32-bit word in the MMA layout)
+      for (int64_t j = 4 * lane; j < nsf_pad; j += 128)
+        *reinterpret_cast<uint32_t*>(ss + j) =
+            *reinterpret_cast<const uint32_t*>(q.scales + sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad));
+    }
+    __syncwarp();
+    for (int jb = lane; jb < nblk; jb += 32) {
+      const int part = jb >= kpb ? 1 : 0;
+      const int b = jb - part * kpb;                                   // block within the part
+      // A, order 2: x - x_hat | x;  A, orders 1, 0: x;
+      // B, order 2: x_hat | x - x_hat;  B, order 1: x - x_hat;  B, order 0: x  (B / alpha)
+      const bool want_hat = !is_a && order == 2 && part == 0;
+      const bool want_delta = is_a ? (order == 2 && part == 0) : (!want_hat && order != 0);
+      const bool live = real && jb < parts * kpb;
+      float v[32];
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int c = live ? ht[i * kpb + b] : -1;
+        float x = 0.0f;
+        if (c >= 0) {
+          x = bf16_bits_to_float(xs[c]);
+          if (want_delta || want_hat) {
+            const uint32_t byte = cs[c >> 1];
+            const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
+            const uint32_t sb = ss[c / B];
+            const uint32_t mm = code & 7u;
+            const float mag = mm < 4 ? 0.5f * (float)mm : (mm == 4 ? 2.0f : mm == 5 ? 3.0f : mm == 6 ? 4.0f : 6.0f);
+            float xh = FMT == FP4_FMT_MXFP4 ? __fmul_rn(mag, e8m0_scale(sb))
+                                            : __fmul_rn(__fmul_rn(mag, e4m3_decode(sb)), g);
+            xh = (code & 8u) ? -xh : xh;
+            x = want_hat ? xh : __fsub_rn(x, xh);
+          }
+          if (!is_a) x = __fmul_rn(x, inv_alpha);
+        }
+        v[i] = x;
+        m = fmaxf(m, fabsf(x));
+      }
+      const uint32_t bits = __float_as_uint(m);
+      int e = (int)(bits >> 23) - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+      e = max(-127, min(127, e));
+      scales[((r >> 7) * (nblk >> 2) + (jb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (jb & 3)] =
+          (uint8_t)(e + 127);
+      if (real) {
+        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);     // 2^-e
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float x = v[4 * k + i];
+            word |= (e4m3_rn_satfinite(__fmul_rn(fabsf(x), inv)) | (signbit(x) ? 0x80u : 0u)) << (8 * i);
+          }
+          w[k] = word;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(codes + r * kxm + (int64_t)jb * 32);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+    __syncwarp();   // the row's buffers are refilled for the next row
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_hcp_gather_fp8(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
@@ -286,6 +452,57 @@ cudaError_t launch_hcp_topk(const float* err, int64_t k, int k_hot, int32_t* hot
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   compact_kernel<<<1, 1024, 0, st>>>(rank, k, k_hot, hot_idx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hcp_gather_mx8(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
+                                  const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot, int k_hot,
+                                  int order, int64_t kxm, uint8_t* a8, uint8_t* sa, uint8_t* b8, uint8_t* sb,
+                                  int num_sms, cudaStream_t st) {
+  // rows staged in shared memory (bf16 values, codes, scales: ~2.6 K bytes a
+  // warp) while up to eight warps' rows and the hot list fit in 96 KB; wider
+  // rows read the hot values directly
+  const int64_t row_bytes = cdiv(xq.k * 2 + xq.k / 2 + nsf_padded(xq.k, xq.format), 16) * 16;
+  const int64_t hot_bytes = cdiv((int64_t)32 * cdiv(k_hot, 32) * 4, 16) * 16;
+  const int warps = (int)std::min<int64_t>(8, ((int64_t)(96 * 1024) - hot_bytes) / row_bytes);
+  if (warps >= 1) {
+    const int smem = (int)(hot_bytes + warps * row_bytes);
+    auto grid_rows = [&](int64_t rows) {
+      return (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(cdiv(rows, 128) * 128, warps), (int64_t)num_sms * 2));
+    };
+    cudaError_t e;
+    if (xq.format == FP4_FMT_MXFP4) {
+      e = cudaFuncSetAttribute(gather_mx8_rows_kernel<FP4_FMT_MXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      gather_mx8_rows_kernel<FP4_FMT_MXFP4><<<grid_rows(xq.rows), 32 * warps, smem, st>>>(
+          x, ldx, xq, hot, k_hot, order, kxm, true, nullptr, a8, sa);
+      gather_mx8_rows_kernel<FP4_FMT_MXFP4><<<grid_rows(wq.rows), 32 * warps, smem, st>>>(
+          w, ldw, wq, hot, k_hot, order, kxm, false, nullptr, b8, sb);
+    } else {
+      e = cudaFuncSetAttribute(gather_mx8_rows_kernel<FP4_FMT_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      gather_mx8_rows_kernel<FP4_FMT_NVFP4><<<grid_rows(xq.rows), 32 * warps, smem, st>>>(
+          x, ldx, xq, hot, k_hot, order, kxm, true, nullptr, a8, sa);
+      gather_mx8_rows_kernel<FP4_FMT_NVFP4><<<grid_rows(wq.rows), 32 * warps, smem, st>>>(
+          w, ldw, wq, hot, k_hot, order, kxm, false, xq.tensor_scale, b8, sb);
+    }
+    return cudaGetLastError();
+  }
+  auto grid = [&](int64_t rows) {
+    return (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(cdiv(rows, 128) * 128 * (kxm / 32) * 32, 256),
+                                                        (int64_t)num_sms * 8));
+  };
+  if (xq.format == FP4_FMT_MXFP4) {
+    gather_mx8_kernel<FP4_FMT_MXFP4><<<grid(xq.rows), 256, 0, st>>>(x, ldx, xq, hot, k_hot, order, kxm, true, nullptr,
+                                                                    a8, sa);
+    gather_mx8_kernel<FP4_FMT_MXFP4><<<grid(wq.rows), 256, 0, st>>>(w, ldw, wq, hot, k_hot, order, kxm, false, nullptr,
+                                                                    b8, sb);
+  } else {
+    gather_mx8_kernel<FP4_FMT_NVFP4><<<grid(xq.rows), 256, 0, st>>>(x, ldx, xq, hot, k_hot, order, kxm, true, nullptr,
+                                                                    a8, sa);
+    gather_mx8_kernel<FP4_FMT_NVFP4><<<grid(wq.rows), 256, 0, st>>>(w, ldw, wq, hot, k_hot, order, kxm, false,
+                                                                    xq.tensor_scale, b8, sb);
+  }
   return cudaGetLastError();
 }
 

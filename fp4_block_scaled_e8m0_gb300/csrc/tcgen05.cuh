@@ -174,6 +174,18 @@ __device__ __forceinline__ uint32_t idesc_fp4(bool ue8m0, uint32_t sf_id, int m,
   d |= sf_id << 29;             // A scale-factor byte
   return d;
 }
+// kind::mxf8f6f4 with E4M3 A and B (type code 0) and UE8M0 block scales, one
+// scale per 32 K elements (scale_vec::1X): the K = 32 MMA j of a 128-element
+// stage takes byte j of each 4-scale group (sf_id)
+__device__ __forceinline__ uint32_t idesc_mxf8(uint32_t sf_id, int m, int n) {
+  uint32_t d = 0;
+  d |= sf_id << 4;              // B scale-factor byte
+  d |= (uint32_t)(n >> 3) << 17;
+  d |= 1u << 23;                // scale type UE8M0
+  d |= (uint32_t)(m >> 4) << 24;
+  d |= sf_id << 29;             // A scale-factor byte
+  return d;
+}
 // kind::f8f6f4 with E4M3 A and B (type code 0), F32 accumulation
 __device__ __forceinline__ uint32_t idesc_e4m3(int m, int n) {
   uint32_t d = 0;
@@ -225,6 +237,14 @@ __device__ __forceinline__ void mma_fp4_pair(uint32_t d_tmem, uint64_t adesc, ui
             d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa_tmem), "r"(sfb_tmem));
   }
+}
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa_tmem), "r"(sfb_tmem));
 }
 __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                               uint32_t acc) {

@@ -72,7 +72,7 @@ enum { FP4_ROUND_RTN = 0, FP4_ROUND_SR = 1 };            /* [outlier] §4.1 */
 enum { FP4_SCALING_1D = 0, FP4_SCALING_2D = 1 };         /* [outlier] §4.1 */
 enum { FP4_SF_ROWMAJOR = 0, FP4_SF_MMA = 1 };
 enum { FP4_DTYPE_BF16 = 0, FP4_DTYPE_F32 = 1 };
-enum { FP4_HCP_SINGLE = 0, FP4_HCP_TWO = 1, FP4_HCP_TWO_FP8 = 2 };  /* [outlier] §3.1 */
+enum { FP4_HCP_SINGLE = 0, FP4_HCP_TWO = 1, FP4_HCP_TWO_FP8 = 2, FP4_HCP_SINGLE_MXFP8 = 3 };  /* [outlier] §3.1 */
 
 typedef struct fp4_ctx fp4_ctx;
 
@@ -353,7 +353,11 @@ int fp4_hcp_quantize_zeroed(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_
  * FP4_HCP_TWO_FP8: the FP4 GEMM, then an E4M3 GEMM (tcgen05 kind::f8f6f4)
  * over the same columns without the 1/alpha, each row of A_ext and B_ext
  * scaled by its own fp32 amax/448 ([msr] §六 runs its compensation in FP8):
- * C += s_A[m] s_B[n] sum_j a8[m,j] b8[n,j].
+ * C += s_A[m] s_B[n] sum_j a8[m,j] b8[n,j];  FP4_HCP_SINGLE_MXFP8: one kernel,
+ * the bf16 tail's columns (B / alpha) as MXFP8 in the FP4 accumulator
+ * (tcgen05 kind::mxf8f6f4): each part padded to 32 columns, blocks of 32 with
+ * an E8M0 scale 2^e, e the smallest exponent keeping the block amax <= 448,
+ * and E4M3 elements (nearest, ties to even).
  * X (M x K) and W (N x K) bf16 with pitches ldx, ldw; xq, wq their
  * quantizations (FP4_SF_MMA).  Workspace: fp4_hcp_workspace_bytes().       */
 size_t fp4_hcp_workspace_bytes(int64_t m, int64_t n, int32_t k_hot, int32_t order);

@@ -177,3 +177,38 @@ def test_hcp_fp8_tail_matches_oracle(fmt, order, out_dtype):
     exact = xn.astype(np.float64) @ wn.astype(np.float64).T
     y0 = fp4.fp4_gemm(xq, wq, torch.float32).cpu().numpy()
     assert np.abs(got - exact).sum() < np.abs(y0 - exact).sum()
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+@pytest.mark.parametrize("order", [0, 1, 2])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("shape", [(320, 512, 264, 6), (700, 1024, 520, 7)])
+def test_hcp_mxfp8_single_kernel_matches_oracle(fmt, order, out_dtype, shape):
+    # MXFP8 extra columns (E4M3, E8M0 per 32; tcgen05 kind::mxf8f6f4) in the FP4
+    # accumulator of one CTA-pair kernel; the oracle uses the same MXFP8 values,
+    # so the GEMM bound holds.  The second shape has several 256 x 256 tiles,
+    # ragged edges and more hot channels than one 128-column stage holds.
+    M, K, N, seed = shape
+    xt, wt, xn, wn, _ = _data(fmt, M=M, K=K, N=N, seed=seed)
+    h = fp4.fp4_hcp_num_hot(K)
+    cx, sx, gx = o.quantize(xn, FMT[fmt])
+    hot = o.hcp_select(xn, cx, sx, FMT[fmt], gx, h)
+    hot_d = torch.from_numpy(hot.astype(np.int32)).cuda()
+    if order == 0:
+        xq = fp4.fp4_hcp_quantize_zeroed(xt.cuda(), fp4.quant_params(fmt), hot_d, h)
+        cx, sx, gx = o.quantize(o.hcp_zero_columns(xn, hot), FMT[fmt])
+    else:
+        xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
+    wq = fp4.fp4_quantize(wt.cuda(), fp4.quant_params(fmt))
+    cw, sw, gw = o.quantize(wn, FMT[fmt])
+    y = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, hot_d, h, fp4.FP4_HCP_SINGLE_MXFP8, order, out_dtype)
+    got = y.float().cpu().numpy().astype(np.float64)
+    yref, bound = o.hcp_gemm_mxfp8(xn, cx, sx, wn, cw, sw, FMT[fmt], gx, gw, hot, order)
+    tol = o.gemm_tolerance(bound, yref, out_dtype == torch.bfloat16)
+    err = np.abs(got - yref)
+    assert np.all(err <= tol), f"{(err > tol).sum()} outside; worst {np.max(err - tol)}"
+    assert fp4.fp4_sync_status() == fp4.FP4_OK
+    # and it compensates: closer to the unquantized product than the plain FP4 GEMM
+    exact = xn.astype(np.float64) @ wn.astype(np.float64).T
+    y0 = fp4.fp4_gemm(xq, wq, torch.float32).cpu().numpy()
+    assert np.abs(got - exact).sum() < np.abs(y0 - exact).sum()
