@@ -212,3 +212,21 @@ def test_hcp_mxfp8_single_kernel_matches_oracle(fmt, order, out_dtype, shape):
     exact = xn.astype(np.float64) @ wn.astype(np.float64).T
     y0 = fp4.fp4_gemm(xq, wq, torch.float32).cpu().numpy()
     assert np.abs(got - exact).sum() < np.abs(y0 - exact).sum()
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+def test_hcp_mxfp8_hot_list_in_any_order(fmt):
+    # the extra columns follow the order of hot_idx, ascending or not (the
+    # gather takes a per-tile range for ascending lists and scans otherwise)
+    xt, wt, xn, wn, _ = _data(fmt, M=300, K=1024, N=264, seed=9)
+    h = fp4.fp4_hcp_num_hot(1024)
+    cx, sx, gx = o.quantize(xn, FMT[fmt])
+    hot = np.random.default_rng(3).permutation(o.hcp_select(xn, cx, sx, FMT[fmt], gx, h))
+    hot_d = torch.from_numpy(hot.astype(np.int32)).cuda()
+    xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
+    wq = fp4.fp4_quantize(wt.cuda(), fp4.quant_params(fmt))
+    cw, sw, gw = o.quantize(wn, FMT[fmt])
+    y = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, hot_d, h, fp4.FP4_HCP_SINGLE_MXFP8, 2, torch.float32)
+    yref, bound = o.hcp_gemm_mxfp8(xn, cx, sx, wn, cw, sw, FMT[fmt], gx, gw, hot, 2)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - yref)
+    assert np.all(err <= o.gemm_tolerance(bound, yref, False))
