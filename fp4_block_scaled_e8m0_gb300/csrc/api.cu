@@ -531,7 +531,8 @@ int fp4_gemm(fp4_ctx* ctx, const fp4_operand* A, const fp4_operand* B, int32_t o
   if (A->k % 32) return FP4_ERR_INVALID_ARG;
   if (A->rows > 0 && B->rows > 0 && A->k == 0) return FP4_ERR_INVALID_ARG;
   if (ldc < B->rows) return FP4_ERR_INVALID_ARG;
-  if (!al16(C) || (ldc * esize(out_dtype)) % 16) return FP4_ERR_MISALIGNED;
+  // alignment matters only for an output with elements (as for inputs)
+  if (A->rows > 0 && B->rows > 0 && (!al16(C) || (ldc * esize(out_dtype)) % 16)) return FP4_ERR_MISALIGNED;
   if (A->rows > INT32_MAX || B->rows > INT32_MAX) return FP4_ERR_INVALID_ARG;
   GemmArgs g{};
   g.A = A;
@@ -559,10 +560,13 @@ int fp4_gemm_quant_a(fp4_ctx* ctx, const void* x_bf16, int64_t m, int64_t ldx, c
   if (s) return s;
   if (!present(C, m == 0 || n == 0) || ldc < n) return FP4_ERR_INVALID_ARG;
   if ((a_codes == nullptr) != (a_scales == nullptr)) return FP4_ERR_INVALID_ARG;
-  if (!al16(C) || (ldc * esize(out_dtype)) % 16 || !al16(a_codes) || !al16(a_scales)) return FP4_ERR_MISALIGNED;
   if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX) return FP4_ERR_INVALID_ARG;
+  // nothing to compute (an empty X has a NULL pointer; an empty output any pitch)
+  if (m == 0 || n == 0) return FP4_OK;
+  if (!al16(C) || (ldc * esize(out_dtype)) % 16 || !al16(a_codes) || !al16(a_scales)) return FP4_ERR_MISALIGNED;
   GemmArgs g{};
   g.B = B;
+  g.quant_a = true;
   g.fp4_part = true;
   g.out_dtype = out_dtype;
   g.C = C;

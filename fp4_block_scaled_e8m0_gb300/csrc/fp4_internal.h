@@ -130,9 +130,11 @@ struct GemmArgs {
   const void* occ_entries;     // (int32 k, float v) pairs
   const uint16_t* occ_wt;      // W^T bf16 [K][occ_ldt], occ_ldt a multiple of 8
   int64_t occ_ldt;
-  // quantize fused into the operand producer (CTA-pair kernel, MXFP4 RTN):
-  // A is the bf16 activation x_bf16 [m][B.k] (pitch ldx, a multiple of 8) and
-  // g.A is unused; its codes / MMA-layout scales are written to qa_* if non-null
+  // quantize fused into the operand producer (CTA-pair kernel, MXFP4 RTN), when
+  // quant_a: A is the bf16 activation x_bf16 [m][B.k] (pitch ldx, a multiple of
+  // 8) and g.A is unused; its codes / MMA-layout scales are written to qa_* if
+  // non-null
+  bool quant_a;
   const void* x_bf16;
   int64_t ldx;
   int64_t m;

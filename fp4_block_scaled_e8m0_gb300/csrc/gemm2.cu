@@ -615,7 +615,7 @@ int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
 
 int launch_gemm_pair(const GemmArgs& g, cudaStream_t st) {
   const fp4_operand& B = *g.B;
-  const bool fuse = g.x_bf16 != nullptr;          // A = the bf16 activation, quantized in the kernel
+  const bool fuse = g.quant_a;                    // A = the bf16 activation, quantized in the kernel
   const int64_t M = fuse ? g.m : g.A->rows, N = B.rows, K = B.k;
   if (M == 0 || N == 0) return FP4_OK;
   const bool nv = B.format == FP4_FMT_NVFP4;

@@ -145,3 +145,32 @@ def test_fused_argument_checks():
     assert call(x, wq_mx, ldc=32) == fp4.FP4_ERR_INVALID_ARG               # ldc < N
     assert call(x, wq_mx) == fp4.FP4_OK
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (200, 8, 32), (130, 264, 96)])
+def test_fused_edge_shapes(M, N, K):
+    """One row; eight output columns and K = 32 (one block, a stage mostly
+    zero-filled); K not a multiple of 128: equal to fp4_quantize + fp4_gemm and
+    to the oracle's codes."""
+    rng = np.random.default_rng(M * 7 + N + K)
+    x, xn = _x(rng, M, K)
+    w, _ = _w(rng, N, K)
+    wq = fp4.fp4_quantize(w, fp4.quant_params(MX))
+    y, a_out, y_ref, xq = _fused_and_unfused(x, wq, torch.float32)
+    assert torch.equal(y.view(torch.int32), y_ref.view(torch.int32))
+    ca, sa, _ = o.quantize(xn, o.MXFP4)
+    assert np.array_equal(a_out.codes.cpu().numpy(), ca)
+    assert np.array_equal(untile_scales(a_out.scales.cpu().numpy(), M, K // 32), sa)
+
+
+def test_fused_empty_operands():
+    """No rows of X, or no rows of B: nothing to compute, FP4_OK."""
+    w, _ = _w(np.random.default_rng(1), 64, 256)
+    wq = fp4.fp4_quantize(w, fp4.quant_params(MX))
+    x0 = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    assert fp4.fp4_gemm_quant_a(x0, wq).shape == (0, 64)
+    x, _ = _x(np.random.default_rng(2), 32, 256)
+    w0 = fp4.fp4_quantize(torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"), fp4.quant_params(MX))
+    assert fp4.fp4_gemm_quant_a(x, w0).shape == (32, 0)
+    torch.cuda.synchronize()
+    assert fp4.fp4_sync_status() == fp4.FP4_OK
