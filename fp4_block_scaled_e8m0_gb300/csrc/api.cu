@@ -80,6 +80,8 @@ int check_operand(const fp4_operand* q, bool need_codes) {
   if (q->k % op_block(q) != 0) return FP4_ERR_INVALID_ARG;
   if (q->format == FP4_FMT_NVFP4 && !present(q->tensor_scale, empty)) return FP4_ERR_INVALID_ARG;
   if (need_codes && !al16(q->codes)) return FP4_ERR_MISALIGNED;
+  // MMA-layout scales are read by TMA and by 32-bit loads (one word = 4 scales)
+  if (!empty && q->sf_layout == FP4_SF_MMA && !al16(q->scales)) return FP4_ERR_MISALIGNED;
   return FP4_OK;
 }
 

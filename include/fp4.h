@@ -41,6 +41,8 @@
  *    to 256 elements; 512-byte atoms of 128 rows x 4 scales, atom (rt, kt) at
  *    byte ((rt * (kpad/block/4)) + kt) * 512, element (r, j) inside the atom
  *    at (r % 32) * 16 + ((r / 32) % 4) * 4 + (j % 4).  Padding bytes are 0.
+ *    A call that reads FP4_SF_MMA scales (an fp4_operand) wants them 16-byte
+ *    aligned (FP4_ERR_MISALIGNED otherwise), as it wants the codes.
  */
 #ifndef FP4_GB300_H
 #define FP4_GB300_H

@@ -102,6 +102,8 @@ def test_gemm_validation(lib):
     assert g(a, nots) == fp4.FP4_ERR_INVALID_ARG                        # NVFP4 needs its tensor scale
     assert g(a, b, ldc=500) == fp4.FP4_ERR_INVALID_ARG                  # ldc < N
     assert g(a, b, ldc=516) == fp4.FP4_ERR_MISALIGNED                   # ldc * 2 % 16
+    bs = fp4.fp4_operand(p, p + 4, p, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA, 512, 512)
+    assert g(a, bs) == fp4.FP4_ERR_MISALIGNED                           # MMA-layout scales: 16-byte aligned
     b64 = fp4.fp4_operand(p, p, p, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_ROWMAJOR, 512, 512, 64)
     assert g(a, b64) == fp4.FP4_ERR_UNSUPPORTED                         # the MMA consumes 16 / 32 only
 
