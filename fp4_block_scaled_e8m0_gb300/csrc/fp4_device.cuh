@@ -242,6 +242,13 @@ __device__ __forceinline__ uint32_t e4m3_rn_satfinite(float t) {
   return r & 0xFFu;
 }
 
+// two signed values: the E4M3 byte of `lo` in bits 0-7, of `hi` in bits 8-15
+__device__ __forceinline__ uint32_t e4m3x2_rn_satfinite(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 __device__ __forceinline__ float e4m3_decode(uint32_t b) {
   uint32_t e = (b >> 3) & 15u, m = b & 7u;
   return e == 0 ? __fmul_rn((float)m, 0.001953125f)            // m * 2^-9

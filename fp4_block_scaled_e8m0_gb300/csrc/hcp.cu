@@ -306,19 +306,40 @@ __global__ void __launch_bounds__(256) gather_mx8_kernel(const uint16_t* __restr
   }
 }
 
-// gather_mx8_kernel with each row staged first: a warp reads its row's bf16
-// values, FP4 codes and block scales with coalesced loads into shared memory
-// (with ~9% of the channels hot, nearly every 32-byte sector of the row is
-// needed, and the per-block warps of the kernel above fetched each hot value,
-// code and scale on its own), then each lane forms one whole 32-column block
-// of the row from shared memory (no shuffles).  The hot list is kept in the
-// CTA's shared memory transposed, ht[i][b] = channel of column 32 b + i, so
-// that the lanes of a warp read consecutive words.  Same bytes.
+// 16- and 4-byte global -> shared copies (cp.async) and their completion
+__device__ __forceinline__ void cpa16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cpa4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cpa_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cpa_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// gather_mx8_kernel with each row staged first: a warp copies its row's bf16
+// values (and, for orders 1 and 2, its FP4 codes and block scales) into shared
+// memory with 16-byte cp.async copies (with ~9% of the channels hot, nearly
+// every 32-byte sector of the row is needed, and the per-block warps of the
+// kernel above fetched each hot value, code and scale on its own), then each
+// lane forms one whole 32-column block of the row from shared memory (no
+// shuffles).  Each warp has two row buffers: the copies of its next row are in
+// flight while it forms the current one, so the loads are never waited for
+// one at a time.  The hot list is kept in the CTA's shared memory transposed,
+// ht[i][b] = channel of column 32 b + i, so that the lanes of a warp read
+// consecutive words.  Same bytes as gather_mx8_kernel.  (Lane = element of a
+// block with a warp reduction for the block amax measured slower: the lanes'
+// byte stores and the reductions' latency outweigh the shared reads it saves.)
+//   buf_bytes: one row buffer (16-byte multiple): 2K (+ K/2 + the padded
+//   scale count when order != 0); shared memory = the hot list + 2 buffers a warp
 template <int FMT>
 __global__ void __launch_bounds__(256) gather_mx8_rows_kernel(const uint16_t* __restrict__ src, int64_t ld,
                                                               fp4_operand q, const int32_t* __restrict__ hot,
                                                               int k_hot, int order, int64_t kxm, bool is_a,
-                                                              const float* ts_other, uint8_t* __restrict__ codes,
+                                                              const float* ts_other, int64_t buf_bytes,
+                                                              uint8_t* __restrict__ codes,
                                                               uint8_t* __restrict__ scales) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
   extern __shared__ __align__(16) uint8_t row_smem[];
@@ -328,31 +349,41 @@ __global__ void __launch_bounds__(256) gather_mx8_rows_kernel(const uint16_t* __
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   // 32-bit block arithmetic: a part's columns kp = 32 kpb; blocks beyond the parts are padding
   const int nblk = (int)(kxm / 32), kpb = (int)cdiv(k_hot, 32), parts = order == 2 ? 2 : 1;
+  const bool need_q = is_a ? order == 2 : order != 0;                 // x_hat is used
   int32_t* ht = reinterpret_cast<int32_t*>(row_smem);                  // [32][kpb], -1 past k_hot
-  const int64_t per_warp = cdiv(K * 2 + K / 2 + nsf_pad, 16) * 16;     // 16-byte aligned regions
-  uint8_t* wbase = row_smem + cdiv((int64_t)32 * kpb * 4, 16) * 16 + (int64_t)warp * per_warp;
-  uint16_t* xs = reinterpret_cast<uint16_t*>(wbase);                   // the row's bf16
-  uint8_t* cs = wbase + K * 2;                                         // its FP4 codes
-  uint8_t* ss = cs + K / 2;                                            // its block scales
+  uint8_t* wbase = row_smem + cdiv((int64_t)32 * kpb * 4, 16) * 16 + (int64_t)warp * 2 * buf_bytes;
   for (int t = threadIdx.x; t < 32 * kpb; t += blockDim.x) {
     const int b = t / 32, i = t - b * 32;                              // column 32 b + i of a part
     ht[i * kpb + b] = 32 * b + i < k_hot ? hot[32 * b + i] : -1;
   }
   __syncthreads();
-  const int64_t rows_pad = cdiv(q.rows, 128) * 128;
-  for (int64_t r = (int64_t)blockIdx.x * nw + warp; r < rows_pad; r += (int64_t)gridDim.x * nw) {
-    const bool real = r < q.rows;
-    if (real) {
+  // row r into buffer `buf` (a commit group of its own, empty past the rows)
+  auto stage = [&](int64_t r, uint8_t* buf) {
+    if (r < q.rows) {
       const uint16_t* xr = src + r * ld;
-      for (int64_t c = 8 * lane; c < K; c += 256) *reinterpret_cast<uint4*>(xs + c) = ld_nc_v4(xr + c);
-      const uint8_t* cr = q.codes + r * (K >> 1);
-      for (int64_t c = 16 * lane; c < (K >> 1); c += 512) *reinterpret_cast<uint4*>(cs + c) = ld_nc_v4(cr + c);
-      // the row's scales: four consecutive ones at a time (one 32-bit word in the MMA layout)
-      for (int64_t j = 4 * lane; j < nsf_pad; j += 128)
-        *reinterpret_cast<uint32_t*>(ss + j) =
-            *reinterpret_cast<const uint32_t*>(q.scales + sf_offset(q.sf_layout, r, j, nsf_row, nsf_pad));
+      for (int64_t c = 8 * lane; c < K; c += 256) cpa16(buf + 2 * c, xr + c);
+      if (need_q) {
+        const uint8_t* cr = q.codes + r * (K >> 1);
+        for (int64_t c = 16 * lane; c < (K >> 1); c += 512) cpa16(buf + 2 * K + c, cr + c);
+        // four consecutive scales at a time (one 32-bit word in the MMA layout)
+        for (int64_t j = 4 * lane; j < nsf_pad; j += 128)
+          cpa4(buf + 2 * K + (K >> 1) + j, q.scales + sf_offset(FP4_SF_MMA, r, j, nsf_row, nsf_pad));
+      }
     }
-    __syncwarp();
+    cpa_commit();
+  };
+  const int64_t rows_pad = cdiv(q.rows, 128) * 128, rstep = (int64_t)gridDim.x * nw;
+  int64_t r = (int64_t)blockIdx.x * nw + warp;
+  stage(r, wbase);
+  for (int pb = 0; r < rows_pad; r += rstep, pb ^= 1) {
+    stage(r + rstep, wbase + (pb ^ 1) * buf_bytes);                    // the next row streams in
+    cpa_wait<1>();                                                     // this lane's copies of row r
+    __syncwarp();                                                      // ... and every lane's
+    const uint8_t* buf = wbase + pb * buf_bytes;
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(buf);
+    const uint8_t* cs = buf + 2 * K;
+    const uint8_t* ss = cs + (K >> 1);
+    const bool real = r < q.rows;
     for (int jb = lane; jb < nblk; jb += 32) {
       const int part = jb >= kpb ? 1 : 0;
       const int b = jb - part * kpb;                                   // block within the part
@@ -361,27 +392,27 @@ __global__ void __launch_bounds__(256) gather_mx8_rows_kernel(const uint16_t* __
       const bool want_hat = !is_a && order == 2 && part == 0;
       const bool want_delta = is_a ? (order == 2 && part == 0) : (!want_hat && order != 0);
       const bool live = real && jb < parts * kpb;
+      // branch-free per element (the two parts' lanes take different forms,
+      // and a branch per element would run them one after the other): every
+      // lane reads a valid column (0 for padding), forms x and, where x_hat is
+      // used, x_hat (the signed E2M1 value by the hardware decode, times the
+      // block scale), then selects
       float v[32];
       float m = 0.0f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int c = live ? ht[i * kpb + b] : -1;
-        float x = 0.0f;
-        if (c >= 0) {
-          x = bf16_bits_to_float(xs[c]);
-          if (want_delta || want_hat) {
-            const uint32_t byte = cs[c >> 1];
-            const uint32_t code = (c & 1) ? (byte >> 4) : (byte & 15u);
-            const uint32_t sb = ss[c / B];
-            const uint32_t mm = code & 7u;
-            const float mag = mm < 4 ? 0.5f * (float)mm : (mm == 4 ? 2.0f : mm == 5 ? 3.0f : mm == 6 ? 4.0f : 6.0f);
-            float xh = FMT == FP4_FMT_MXFP4 ? __fmul_rn(mag, e8m0_scale(sb))
-                                            : __fmul_rn(__fmul_rn(mag, e4m3_decode(sb)), g);
-            xh = (code & 8u) ? -xh : xh;
-            x = want_hat ? xh : __fsub_rn(x, xh);
-          }
-          if (!is_a) x = __fmul_rn(x, inv_alpha);
+        const int cc = max(c, 0);
+        float x = bf16_bits_to_float(xs[cc]);
+        if (need_q) {
+          float xh, unused;
+          e2m1x2_decode((uint32_t)cs[cc >> 1] >> ((cc & 1) << 2), xh, unused);
+          const uint32_t sb = ss[cc / B];
+          xh = FMT == FP4_FMT_MXFP4 ? __fmul_rn(xh, e8m0_scale(sb)) : __fmul_rn(__fmul_rn(xh, e4m3_decode(sb)), g);
+          x = want_hat ? xh : want_delta ? __fsub_rn(x, xh) : x;
         }
+        if (!is_a) x = __fmul_rn(x, inv_alpha);
+        x = c >= 0 ? x : 0.0f;
         v[i] = x;
         m = fmaxf(m, fabsf(x));
       }
@@ -395,21 +426,20 @@ __global__ void __launch_bounds__(256) gather_mx8_rows_kernel(const uint16_t* __
         uint32_t w[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          uint32_t word = 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float x = v[4 * k + i];
-            word |= (e4m3_rn_satfinite(__fmul_rn(fabsf(x), inv)) | (signbit(x) ? 0x80u : 0u)) << (8 * i);
-          }
-          w[k] = word;
+          // the signed conversion: RN is symmetric, so each byte is the code
+          // of |x| 2^-e with x's sign bit (-0 included)
+          const uint32_t lo = e4m3x2_rn_satfinite(__fmul_rn(v[4 * k], inv), __fmul_rn(v[4 * k + 1], inv));
+          const uint32_t hi = e4m3x2_rn_satfinite(__fmul_rn(v[4 * k + 2], inv), __fmul_rn(v[4 * k + 3], inv));
+          w[k] = lo | (hi << 16);
         }
         uint4* dst = reinterpret_cast<uint4*>(codes + r * kxm + (int64_t)jb * 32);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
     }
-    __syncwarp();   // the row's buffers are refilled for the next row
+    __syncwarp();   // every lane is done with this buffer before it is refilled
   }
+  cpa_wait<0>();
 }
 
 }  // namespace
@@ -459,14 +489,16 @@ cudaError_t launch_hcp_gather_mx8(const uint16_t* x, int64_t ldx, const uint16_t
                                   const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot, int k_hot,
                                   int order, int64_t kxm, uint8_t* a8, uint8_t* sa, uint8_t* b8, uint8_t* sb,
                                   int num_sms, cudaStream_t st) {
-  // rows staged in shared memory (bf16 values, codes, scales: ~2.6 K bytes a
-  // warp) while up to eight warps' rows and the hot list fit in 96 KB; wider
-  // rows read the hot values directly
-  const int64_t row_bytes = cdiv(xq.k * 2 + xq.k / 2 + nsf_padded(xq.k, xq.format), 16) * 16;
+  // rows staged in shared memory, two buffers a warp (bf16 values; codes and
+  // scales for orders 1 and 2: ~10 K bytes a buffer at K = 4096), while at
+  // least one warp's buffers and the hot list fit in 100 KB (two CTAs an SM);
+  // wider rows read the hot values directly
+  const int64_t buf_bytes =
+      cdiv(xq.k * 2 + (order != 0 ? xq.k / 2 + nsf_padded(xq.k, xq.format) : 0), 16) * 16;
   const int64_t hot_bytes = cdiv((int64_t)32 * cdiv(k_hot, 32) * 4, 16) * 16;
-  const int warps = (int)std::min<int64_t>(8, ((int64_t)(96 * 1024) - hot_bytes) / row_bytes);
+  const int warps = (int)std::min<int64_t>(8, ((int64_t)(100 * 1024) - hot_bytes) / (2 * buf_bytes));
   if (warps >= 1) {
-    const int smem = (int)(hot_bytes + warps * row_bytes);
+    const int smem = (int)(hot_bytes + warps * 2 * buf_bytes);
     auto grid_rows = [&](int64_t rows) {
       return (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(cdiv(rows, 128) * 128, warps), (int64_t)num_sms * 2));
     };
@@ -475,16 +507,16 @@ cudaError_t launch_hcp_gather_mx8(const uint16_t* x, int64_t ldx, const uint16_t
       e = cudaFuncSetAttribute(gather_mx8_rows_kernel<FP4_FMT_MXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       gather_mx8_rows_kernel<FP4_FMT_MXFP4><<<grid_rows(xq.rows), 32 * warps, smem, st>>>(
-          x, ldx, xq, hot, k_hot, order, kxm, true, nullptr, a8, sa);
+          x, ldx, xq, hot, k_hot, order, kxm, true, nullptr, buf_bytes, a8, sa);
       gather_mx8_rows_kernel<FP4_FMT_MXFP4><<<grid_rows(wq.rows), 32 * warps, smem, st>>>(
-          w, ldw, wq, hot, k_hot, order, kxm, false, nullptr, b8, sb);
+          w, ldw, wq, hot, k_hot, order, kxm, false, nullptr, buf_bytes, b8, sb);
     } else {
       e = cudaFuncSetAttribute(gather_mx8_rows_kernel<FP4_FMT_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
       gather_mx8_rows_kernel<FP4_FMT_NVFP4><<<grid_rows(xq.rows), 32 * warps, smem, st>>>(
-          x, ldx, xq, hot, k_hot, order, kxm, true, nullptr, a8, sa);
+          x, ldx, xq, hot, k_hot, order, kxm, true, nullptr, buf_bytes, a8, sa);
       gather_mx8_rows_kernel<FP4_FMT_NVFP4><<<grid_rows(wq.rows), 32 * warps, smem, st>>>(
-          w, ldw, wq, hot, k_hot, order, kxm, false, xq.tensor_scale, b8, sb);
+          w, ldw, wq, hot, k_hot, order, kxm, false, xq.tensor_scale, buf_bytes, b8, sb);
     }
     return cudaGetLastError();
   }
