@@ -332,15 +332,19 @@ __device__ __forceinline__ void cpa_wait() { asm volatile("cp.async.wait_group %
 // consecutive words.  Same bytes as gather_mx8_kernel.  (Lane = element of a
 // block with a warp reduction for the block amax measured slower: the lanes'
 // byte stores and the reductions' latency outweigh the shared reads it saves.)
+// The same staging serves the bf16 extra columns (MX8 = false): there each
+// lane forms 8 consecutive columns of the row (one 16-byte store), the values
+// of gather_kernel.
+//   kx: the row width of the output (MXFP8: kxm, bf16: kx)
 //   buf_bytes: one row buffer (16-byte multiple): 2K (+ K/2 + the padded
-//   scale count when order != 0); shared memory = the hot list + 2 buffers a warp
-template <int FMT>
-__global__ void __launch_bounds__(256) gather_mx8_rows_kernel(const uint16_t* __restrict__ src, int64_t ld,
-                                                              fp4_operand q, const int32_t* __restrict__ hot,
-                                                              int k_hot, int order, int64_t kxm, bool is_a,
-                                                              const float* ts_other, int64_t buf_bytes,
-                                                              uint8_t* __restrict__ codes,
-                                                              uint8_t* __restrict__ scales) {
+//   scale count when order != 0); shared memory = the hot list (32 kpb words)
+//   + 2 buffers a warp
+template <int FMT, bool MX8>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ src, int64_t ld, fp4_operand q,
+                                                          const int32_t* __restrict__ hot, int k_hot, int order,
+                                                          int64_t kx, bool is_a, const float* ts_other,
+                                                          int64_t buf_bytes, void* __restrict__ out,
+                                                          uint8_t* __restrict__ scales) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
   extern __shared__ __align__(16) uint8_t row_smem[];
   const int64_t K = q.k, nsf_row = K / B, nsf_pad = nsf_padded(K, FMT);
@@ -348,13 +352,15 @@ __global__ void __launch_bounds__(256) gather_mx8_rows_kernel(const uint16_t* __
   const float inv_alpha = (FMT == FP4_FMT_NVFP4 && !is_a) ? __frcp_rn(__fmul_rn(*ts_other, g)) : 1.0f;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   // 32-bit block arithmetic: a part's columns kp = 32 kpb; blocks beyond the parts are padding
-  const int nblk = (int)(kxm / 32), kpb = (int)cdiv(k_hot, 32), parts = order == 2 ? 2 : 1;
+  const int nblk = (int)(kx / 32), kpb = (int)cdiv(k_hot, 32), parts = order == 2 ? 2 : 1;
   const bool need_q = is_a ? order == 2 : order != 0;                 // x_hat is used
-  int32_t* ht = reinterpret_cast<int32_t*>(row_smem);                  // [32][kpb], -1 past k_hot
+  // MX8: [32][kpb], -1 past k_hot; bf16: the list as given
+  int32_t* ht = reinterpret_cast<int32_t*>(row_smem);
   uint8_t* wbase = row_smem + cdiv((int64_t)32 * kpb * 4, 16) * 16 + (int64_t)warp * 2 * buf_bytes;
   for (int t = threadIdx.x; t < 32 * kpb; t += blockDim.x) {
     const int b = t / 32, i = t - b * 32;                              // column 32 b + i of a part
-    ht[i * kpb + b] = 32 * b + i < k_hot ? hot[32 * b + i] : -1;
+    if (MX8) ht[i * kpb + b] = t < k_hot ? hot[t] : -1;
+    else ht[t] = t < k_hot ? hot[t] : -1;
   }
   __syncthreads();
   // row r into buffer `buf` (a commit group of its own, empty past the rows)
@@ -372,10 +378,11 @@ __global__ void __launch_bounds__(256) gather_mx8_rows_kernel(const uint16_t* __
     }
     cpa_commit();
   };
-  const int64_t rows_pad = cdiv(q.rows, 128) * 128, rstep = (int64_t)gridDim.x * nw;
+  // MX8: the scales of the rows up to the next multiple of 128 are written too
+  const int64_t rows_end = MX8 ? cdiv(q.rows, 128) * 128 : q.rows, rstep = (int64_t)gridDim.x * nw;
   int64_t r = (int64_t)blockIdx.x * nw + warp;
   stage(r, wbase);
-  for (int pb = 0; r < rows_pad; r += rstep, pb ^= 1) {
+  for (int pb = 0; r < rows_end; r += rstep, pb ^= 1) {
     stage(r + rstep, wbase + (pb ^ 1) * buf_bytes);                    // the next row streams in
     cpa_wait<1>();                                                     // this lane's copies of row r
     __syncwarp();                                                      // ... and every lane's
@@ -384,57 +391,94 @@ __global__ void __launch_bounds__(256) gather_mx8_rows_kernel(const uint16_t* __
     const uint8_t* cs = buf + 2 * K;
     const uint8_t* ss = cs + (K >> 1);
     const bool real = r < q.rows;
-    for (int jb = lane; jb < nblk; jb += 32) {
-      const int part = jb >= kpb ? 1 : 0;
-      const int b = jb - part * kpb;                                   // block within the part
-      // A, order 2: x - x_hat | x;  A, orders 1, 0: x;
-      // B, order 2: x_hat | x - x_hat;  B, order 1: x - x_hat;  B, order 0: x  (B / alpha)
-      const bool want_hat = !is_a && order == 2 && part == 0;
-      const bool want_delta = is_a ? (order == 2 && part == 0) : (!want_hat && order != 0);
-      const bool live = real && jb < parts * kpb;
-      // branch-free per element (the two parts' lanes take different forms,
-      // and a branch per element would run them one after the other): every
-      // lane reads a valid column (0 for padding), forms x and, where x_hat is
-      // used, x_hat (the signed E2M1 value by the hardware decode, times the
-      // block scale), then selects
-      float v[32];
-      float m = 0.0f;
+    if constexpr (MX8) {
+      for (int jb = lane; jb < nblk; jb += 32) {
+        const int part = jb >= kpb ? 1 : 0;
+        const int b = jb - part * kpb;                                   // block within the part
+        // A, order 2: x - x_hat | x;  A, orders 1, 0: x;
+        // B, order 2: x_hat | x - x_hat;  B, order 1: x - x_hat;  B, order 0: x  (B / alpha)
+        const bool want_hat = !is_a && order == 2 && part == 0;
+        const bool want_delta = is_a ? (order == 2 && part == 0) : (!want_hat && order != 0);
+        const bool live = real && jb < parts * kpb;
+        // branch-free per element (the two parts' lanes take different forms,
+        // and a branch per element would run them one after the other): every
+        // lane reads a valid column (0 for padding), forms x and, where x_hat is
+        // used, x_hat (the signed E2M1 value by the hardware decode, times the
+        // block scale), then selects
+        float v[32];
+        float m = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int c = live ? ht[i * kpb + b] : -1;
-        const int cc = max(c, 0);
-        float x = bf16_bits_to_float(xs[cc]);
-        if (need_q) {
-          float xh, unused;
-          e2m1x2_decode((uint32_t)cs[cc >> 1] >> ((cc & 1) << 2), xh, unused);
-          const uint32_t sb = ss[cc / B];
-          xh = FMT == FP4_FMT_MXFP4 ? __fmul_rn(xh, e8m0_scale(sb)) : __fmul_rn(__fmul_rn(xh, e4m3_decode(sb)), g);
-          x = want_hat ? xh : want_delta ? __fsub_rn(x, xh) : x;
+        for (int i = 0; i < 32; ++i) {
+          const int c = live ? ht[i * kpb + b] : -1;
+          const int cc = max(c, 0);
+          float x = bf16_bits_to_float(xs[cc]);
+          if (need_q) {
+            float xh, unused;
+            e2m1x2_decode((uint32_t)cs[cc >> 1] >> ((cc & 1) << 2), xh, unused);
+            const uint32_t sb = ss[cc / B];
+            xh = FMT == FP4_FMT_MXFP4 ? __fmul_rn(xh, e8m0_scale(sb)) : __fmul_rn(__fmul_rn(xh, e4m3_decode(sb)), g);
+            x = want_hat ? xh : want_delta ? __fsub_rn(x, xh) : x;
+          }
+          if (!is_a) x = __fmul_rn(x, inv_alpha);
+          x = c >= 0 ? x : 0.0f;
+          v[i] = x;
+          m = fmaxf(m, fabsf(x));
         }
-        if (!is_a) x = __fmul_rn(x, inv_alpha);
-        x = c >= 0 ? x : 0.0f;
-        v[i] = x;
-        m = fmaxf(m, fabsf(x));
+        const uint32_t bits = __float_as_uint(m);
+        int e = (int)(bits >> 23) - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+        e = max(-127, min(127, e));
+        scales[((r >> 7) * (nblk >> 2) + (jb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (jb & 3)] =
+            (uint8_t)(e + 127);
+        if (real) {
+          const float inv = __uint_as_float((uint32_t)(127 - e) << 23);     // 2^-e
+          uint32_t w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            // the signed conversion: RN is symmetric, so each byte is the code
+            // of |x| 2^-e with x's sign bit (-0 included)
+            const uint32_t lo = e4m3x2_rn_satfinite(__fmul_rn(v[4 * k], inv), __fmul_rn(v[4 * k + 1], inv));
+            const uint32_t hi = e4m3x2_rn_satfinite(__fmul_rn(v[4 * k + 2], inv), __fmul_rn(v[4 * k + 3], inv));
+            w[k] = lo | (hi << 16);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + r * kx + (int64_t)jb * 32);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
       }
-      const uint32_t bits = __float_as_uint(m);
-      int e = (int)(bits >> 23) - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-      e = max(-127, min(127, e));
-      scales[((r >> 7) * (nblk >> 2) + (jb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (jb & 3)] =
-          (uint8_t)(e + 127);
-      if (real) {
-        const float inv = __uint_as_float((uint32_t)(127 - e) << 23);     // 2^-e
-        uint32_t w[8];
+    } else {
+      // bf16 columns j0 .. j0 + 7 of the row (parts of k_hot columns, no padding
+      // between them; zeros past them), branch-free like the blocks above
+      const int live_cols = parts * k_hot;
+      uint16_t* orow = static_cast<uint16_t*>(out) + r * kx;
+      for (int j0 = 8 * lane; j0 < kx; j0 += 256) {
+        float v[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          // the signed conversion: RN is symmetric, so each byte is the code
-          // of |x| 2^-e with x's sign bit (-0 included)
-          const uint32_t lo = e4m3x2_rn_satfinite(__fmul_rn(v[4 * k], inv), __fmul_rn(v[4 * k + 1], inv));
-          const uint32_t hi = e4m3x2_rn_satfinite(__fmul_rn(v[4 * k + 2], inv), __fmul_rn(v[4 * k + 3], inv));
-          w[k] = lo | (hi << 16);
+        for (int e = 0; e < 8; ++e) {
+          const int j = j0 + e;
+          const int part = j >= k_hot ? 1 : 0;
+          const bool live = j < live_cols;
+          const int c = live ? ht[j - part * k_hot] : -1;
+          const int cc = max(c, 0);
+          float x = bf16_bits_to_float(xs[cc]);
+          if (need_q) {
+            float xh, unused;
+            e2m1x2_decode((uint32_t)cs[cc >> 1] >> ((cc & 1) << 2), xh, unused);
+            const uint32_t sb = ss[cc / B];
+            xh = FMT == FP4_FMT_MXFP4 ? __fmul_rn(xh, e8m0_scale(sb)) : __fmul_rn(__fmul_rn(xh, e4m3_decode(sb)), g);
+            const bool want_hat = !is_a && order == 2 && part == 0;
+            const bool want_delta = is_a ? (order == 2 && part == 0) : (!want_hat && order != 0);
+            x = want_hat ? xh : want_delta ? __fsub_rn(x, xh) : x;
+          }
+          if (!is_a) x = __fmul_rn(x, inv_alpha);
+          v[e] = c >= 0 ? x : 0.0f;
         }
-        uint4* dst = reinterpret_cast<uint4*>(codes + r * kxm + (int64_t)jb * 32);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        uint32_t pk[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+          pk[k] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(orow + j0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
     }
     __syncwarp();   // every lane is done with this buffer before it is refilled
@@ -485,41 +529,49 @@ cudaError_t launch_hcp_topk(const float* err, int64_t k, int k_hot, int32_t* hot
   return cudaGetLastError();
 }
 
-cudaError_t launch_hcp_gather_mx8(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
-                                  const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot, int k_hot,
-                                  int order, int64_t kxm, uint8_t* a8, uint8_t* sa, uint8_t* b8, uint8_t* sb,
-                                  int num_sms, cudaStream_t st) {
-  // rows staged in shared memory, two buffers a warp (bf16 values; codes and
-  // scales for orders 1 and 2: ~10 K bytes a buffer at K = 4096), while at
-  // least one warp's buffers and the hot list fit in 100 KB (two CTAs an SM);
-  // wider rows read the hot values directly
+// Launch the staged-row gather (MX8: MXFP8 codes + scales; else bf16 columns)
+// for A (X's rows) and B (W's rows); false when a row's two buffers do not fit
+template <bool MX8>
+bool launch_gather_rows(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw, const fp4_operand& xq,
+                        const fp4_operand& wq, const int32_t* hot, int k_hot, int order, int64_t kx, void* a_out,
+                        uint8_t* sa, void* b_out, uint8_t* sb, int num_sms, cudaStream_t st, cudaError_t* err) {
+  // two buffers a warp (bf16 values; codes and scales for orders 1 and 2:
+  // ~10 K bytes a buffer at K = 4096), while at least one warp's buffers and
+  // the hot list fit in 100 KB (two CTAs an SM)
   const int64_t buf_bytes =
       cdiv(xq.k * 2 + (order != 0 ? xq.k / 2 + nsf_padded(xq.k, xq.format) : 0), 16) * 16;
   const int64_t hot_bytes = cdiv((int64_t)32 * cdiv(k_hot, 32) * 4, 16) * 16;
   const int warps = (int)std::min<int64_t>(8, ((int64_t)(100 * 1024) - hot_bytes) / (2 * buf_bytes));
-  if (warps >= 1) {
-    const int smem = (int)(hot_bytes + warps * 2 * buf_bytes);
-    auto grid_rows = [&](int64_t rows) {
-      return (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(cdiv(rows, 128) * 128, warps), (int64_t)num_sms * 2));
-    };
-    cudaError_t e;
-    if (xq.format == FP4_FMT_MXFP4) {
-      e = cudaFuncSetAttribute(gather_mx8_rows_kernel<FP4_FMT_MXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      gather_mx8_rows_kernel<FP4_FMT_MXFP4><<<grid_rows(xq.rows), 32 * warps, smem, st>>>(
-          x, ldx, xq, hot, k_hot, order, kxm, true, nullptr, buf_bytes, a8, sa);
-      gather_mx8_rows_kernel<FP4_FMT_MXFP4><<<grid_rows(wq.rows), 32 * warps, smem, st>>>(
-          w, ldw, wq, hot, k_hot, order, kxm, false, nullptr, buf_bytes, b8, sb);
-    } else {
-      e = cudaFuncSetAttribute(gather_mx8_rows_kernel<FP4_FMT_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      gather_mx8_rows_kernel<FP4_FMT_NVFP4><<<grid_rows(xq.rows), 32 * warps, smem, st>>>(
-          x, ldx, xq, hot, k_hot, order, kxm, true, nullptr, buf_bytes, a8, sa);
-      gather_mx8_rows_kernel<FP4_FMT_NVFP4><<<grid_rows(wq.rows), 32 * warps, smem, st>>>(
-          w, ldw, wq, hot, k_hot, order, kxm, false, xq.tensor_scale, buf_bytes, b8, sb);
-    }
+  if (warps < 1) return false;
+  const int smem = (int)(hot_bytes + warps * 2 * buf_bytes);
+  auto grid_rows = [&](int64_t rows) {
+    const int64_t rows_end = MX8 ? cdiv(rows, 128) * 128 : rows;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(rows_end, warps), (int64_t)num_sms * 2));
+  };
+  auto run = [&](auto kernel) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (xq.rows > 0)
+      kernel<<<grid_rows(xq.rows), 32 * warps, smem, st>>>(x, ldx, xq, hot, k_hot, order, kx, true, nullptr,
+                                                           buf_bytes, a_out, sa);
+    if (wq.rows > 0)
+      kernel<<<grid_rows(wq.rows), 32 * warps, smem, st>>>(w, ldw, wq, hot, k_hot, order, kx, false,
+                                                           xq.tensor_scale, buf_bytes, b_out, sb);
     return cudaGetLastError();
-  }
+  };
+  *err = xq.format == FP4_FMT_MXFP4 ? run(gather_rows_kernel<FP4_FMT_MXFP4, MX8>)
+                                    : run(gather_rows_kernel<FP4_FMT_NVFP4, MX8>);
+  return true;
+}
+
+cudaError_t launch_hcp_gather_mx8(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw,
+                                  const fp4_operand& xq, const fp4_operand& wq, const int32_t* hot, int k_hot,
+                                  int order, int64_t kxm, uint8_t* a8, uint8_t* sa, uint8_t* b8, uint8_t* sb,
+                                  int num_sms, cudaStream_t st) {
+  // rows staged in shared memory; wider rows read the hot values directly
+  cudaError_t e = cudaSuccess;
+  if (launch_gather_rows<true>(x, ldx, w, ldw, xq, wq, hot, k_hot, order, kxm, a8, sa, b8, sb, num_sms, st, &e))
+    return e;
   auto grid = [&](int64_t rows) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(cdiv(rows, 128) * 128 * (kxm / 32) * 32, 256),
                                                         (int64_t)num_sms * 8));
@@ -541,6 +593,11 @@ cudaError_t launch_hcp_gather_mx8(const uint16_t* x, int64_t ldx, const uint16_t
 cudaError_t launch_hcp_gather(const uint16_t* x, int64_t ldx, const uint16_t* w, int64_t ldw, const fp4_operand& xq,
                               const fp4_operand& wq, const int32_t* hot, int k_hot, int order, int64_t kx,
                               uint16_t* a_ext, uint16_t* b_ext, int num_sms, cudaStream_t st) {
+  // rows staged in shared memory; wider rows: one thread per output element
+  cudaError_t e = cudaSuccess;
+  if (launch_gather_rows<false>(x, ldx, w, ldw, xq, wq, hot, k_hot, order, kx, a_ext, nullptr, b_ext, nullptr,
+                                num_sms, st, &e))
+    return e;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(xq.rows * kx, 256), (int64_t)num_sms * 8));
   const int gridb = (int)std::max<int64_t>(1, std::min<int64_t>(cdiv(wq.rows * kx, 256), (int64_t)num_sms * 8));
   if (xq.format == FP4_FMT_MXFP4) {

@@ -265,7 +265,8 @@ def _oracle_channel_errors(xn, chunk=1024):
 
 
 def test_hcp_square_full():
-    """Hot-channel selection and the compensated GEMM at the benchmark's size.
+    """Hot-channel selection and the compensated GEMM (bf16 and MXFP8 extra columns)
+    at the benchmark's size.
     The GPU's hot set equals the oracle's outside a 1e-5 relative band around
     the h-th largest error (inside it the fp32 sums may order channels
     differently); the GEMM then runs on the oracle's set and is compared on
@@ -292,6 +293,7 @@ def test_hcp_square_full():
     hot_t = torch.from_numpy(hot_o).cuda()
     y1 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot_t, h, fp4.FP4_HCP_SINGLE, 2, torch.float32)
     y2 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot_t, h, fp4.FP4_HCP_TWO, 2, torch.float32)
+    y3 = fp4.fp4_hcp_gemm(X, W, qx, qw, hot_t, h, fp4.FP4_HCP_SINGLE_MXFP8, 2, torch.float32)
     wn = d["W"].float().numpy()
     cx, sx, gx, rows = _check_quant_rows(xfull, qx, {}, _sample_rows(M, 3, 7), "hcp X")
     cw, sw, gw, cols = _check_quant_rows(wn, qw, {}, _sample_rows(W.shape[0], 24, 8), "hcp W")
@@ -299,6 +301,10 @@ def test_hcp_square_full():
     for y, label in ((y1, "single"), (y2, "two")):
         got_y = y.cpu().numpy()[rows][:, cols].astype(np.float64)
         assert np.all(np.abs(got_y - yr) <= 1e-3 * bound), label
+    # the MXFP8 extra columns: the oracle's product with the same MXFP8 values
+    y3r, bound3 = o.hcp_gemm_mxfp8(xfull[rows], cx, sx, wn[cols], cw, sw, o.NVFP4, gx, gw, hot_o, 2)
+    got3 = y3.cpu().numpy()[rows][:, cols].astype(np.float64)
+    assert np.all(np.abs(got3 - y3r) <= o.gemm_tolerance(bound3, y3r, False)), "single mxfp8"
 
 
 def test_hcp_square_variants_full():

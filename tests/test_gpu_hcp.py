@@ -216,8 +216,7 @@ def test_hcp_mxfp8_single_kernel_matches_oracle(fmt, order, out_dtype, shape):
 
 @pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
 def test_hcp_mxfp8_hot_list_in_any_order(fmt):
-    # the extra columns follow the order of hot_idx, ascending or not (the
-    # gather takes a per-tile range for ascending lists and scans otherwise)
+    # the extra columns follow the order of hot_idx, ascending or not
     xt, wt, xn, wn, _ = _data(fmt, M=300, K=1024, N=264, seed=9)
     h = fp4.fp4_hcp_num_hot(1024)
     cx, sx, gx = o.quantize(xn, FMT[fmt])
