@@ -498,12 +498,9 @@ int fp4_occ_gemm(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, cons
     g.b_ext = reinterpret_cast<const uint16_t*>(base + L.b_ext);
     g.kx = L.kx;
   }
-  g.occ_start = reinterpret_cast<const uint32_t*>(base + L.row_start);
-  g.occ_len = reinterpret_cast<const uint32_t*>(base + L.row_len);
-  g.occ_entries = base + L.entries;
-  g.occ_wt = reinterpret_cast<const uint16_t*>(base + L.wt);
-  g.occ_ldt = L.ldt;
-  return launch_gemm(g, st);
+  s = launch_gemm(g, st);   // the clamped FP4 product and the dense columns
+  if (s) return s;
+  return cuda_status(launch_occ_correct(y, ldy, out_dtype, M, N, workspace, L, ctx->num_sms, st));
 }
 
 int fp4_quant_error_stats(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t ldx, const fp4_operand* q,

@@ -123,13 +123,6 @@ struct GemmArgs {
   int accumulate;
   unsigned int* status;
   int num_sms;
-  // optional per-row sparse correction added in the epilogue (outlier
-  // compensation): Y[m, :] += sum over entries (k, v) of row m of v * WT[k, :]
-  const uint32_t* occ_start;   // [M] first entry of each row, or null
-  const uint32_t* occ_len;     // [M] entries of each row
-  const void* occ_entries;     // (int32 k, float v) pairs
-  const uint16_t* occ_wt;      // W^T bf16 [K][occ_ldt], occ_ldt a multiple of 8
-  int64_t occ_ldt;
   // quantize fused into the operand producer (CTA-pair kernel, MXFP4 RTN), when
   // quant_a: A is the bf16 activation x_bf16 [m][B.k] (pitch ldx, a multiple of
   // 8) and g.A is unused; its codes / MMA-layout scales are written to qa_* if
@@ -184,6 +177,9 @@ cudaError_t launch_occ_prepare(const void* x, int xdt, int64_t ldx, const uint16
                                const fp4_operand& xq, const fp4_operand& wq, const float* tau, const float* col_counts,
                                int k_dense, int64_t max_outliers, void* ws, const OccLayout& L, unsigned int* status,
                                int num_sms, cudaStream_t st);
+// after the GEMM stored Y [m][n] (pitch ldy): the scattered outliers' product
+cudaError_t launch_occ_correct(void* y, int64_t ldy, int out_dtype, int64_t m, int64_t n, const void* ws,
+                               const OccLayout& L, int num_sms, cudaStream_t st);
 // quality sums over q with any block (16-128); tau: OCC reconstruction; beta > 0:
 // the sigmoid-smoothed reconstruction instead of the codes
 // stats (may be null): cosine, MSE, SNR (dB) and relative L2 error from the sums

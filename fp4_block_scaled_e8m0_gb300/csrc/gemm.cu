@@ -75,11 +75,6 @@ struct Params {
   int accumulate;
   unsigned int* status;
   int tiles_m, tiles_n;
-  const uint32_t* occ_start;   // sparse per-row correction (see GemmArgs), null if none
-  const uint32_t* occ_len;
-  const int2* occ_entries;     // (k, float bits of v)
-  const uint16_t* occ_wt;
-  int64_t occ_ldt;
   const float* row_scale;      // if set: C (+)= row_scale[m] col_scale[n] acc instead of alpha acc
   const float* col_scale;
 };
@@ -143,95 +138,6 @@ __device__ __forceinline__ void store_exchanged(const Params& p, const uint32_t*
   }
 }
 
-// Sparse correction in the exchanged layout (see warp_exchange_hi3): lane
-// 4b + a holds w[4v + k] = accumulator (row 4v + a, column col0 + 4b + k).
-// Every value becomes alpha * acc plus, for each entry (k, v) of its row,
-// v * WT[k, column], in fp32.  The 8 lanes of one row read 4 consecutive bf16
-// columns each: 64 contiguous bytes of a W^T row per entry.  mylen / mystart:
-// the entry list of row row0 + lane (shuffled to the lanes that hold it).
-__device__ __forceinline__ void occ_correct_exchanged(const Params& p, uint32_t* w, float alpha, int col0, int lane,
-                                                      uint32_t mylen, uint32_t mystart) {
-  const int a = lane & 3, c = col0 + 4 * (lane >> 2);
-  const bool colok = c < p.N;          // W^T rows are zero-padded to a multiple of 8
-#pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    const uint32_t len = __shfl_sync(0xFFFFFFFFu, mylen, 4 * v + a);
-    const uint32_t start = __shfl_sync(0xFFFFFFFFu, mystart, 4 * v + a);
-    float y[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) y[k] = __fmul_rn(__uint_as_float(w[4 * v + k]), alpha);
-    if (colok) {
-      for (uint32_t i = 0; i < len; ++i) {
-        const int2 en = p.occ_entries[start + i];
-        const float val = __int_as_float(en.y);
-        uint2 u;
-        asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];"
-                     : "=r"(u.x), "=r"(u.y) : "l"(p.occ_wt + (int64_t)en.x * p.occ_ldt + c));
-        y[0] = fmaf(val, __uint_as_float(u.x << 16), y[0]);
-        y[1] = fmaf(val, __uint_as_float(u.x & 0xFFFF0000u), y[1]);
-        y[2] = fmaf(val, __uint_as_float(u.y << 16), y[2]);
-        y[3] = fmaf(val, __uint_as_float(u.y & 0xFFFF0000u), y[3]);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) w[4 * v + k] = __float_as_uint(y[k]);
-  }
-}
-
-// The same on packed bf16 pairs after warp_exchange_hi3: lane 4b + a holds
-// w[4v + k] = columns col0 + 8b + 2k, +1 of row 4v + a.  Each value is
-// unpacked, corrected in fp32 and rounded to bf16 again (the output was
-// rounded once before: two roundings of at most 2^-9 each).  The 8 lanes of a
-// row read 16 contiguous bytes each: 128 bytes of a W^T row per entry.
-__device__ __forceinline__ uint4 ld_nc_u4(const void* ptr) {
-  uint4 u;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "l"(ptr));
-  return u;
-}
-
-__device__ __forceinline__ void occ_correct_bf16x2(const Params& p, uint32_t* w, int col0, int lane, uint32_t mylen,
-                                                   uint32_t mystart) {
-  const int a = lane & 3, c = col0 + 8 * (lane >> 2);
-  const bool colok = c < p.N;
-  constexpr int PF = 4;                // entries fetched together (their loads overlap)
-#pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    const uint32_t len = __shfl_sync(0xFFFFFFFFu, mylen, 4 * v + a);
-    const uint32_t start = __shfl_sync(0xFFFFFFFFu, mystart, 4 * v + a);
-    if (!colok || len == 0) continue;
-    float y[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      y[2 * k] = __uint_as_float(w[4 * v + k] << 16);
-      y[2 * k + 1] = __uint_as_float(w[4 * v + k] & 0xFFFF0000u);
-    }
-    for (uint32_t i0 = 0; i0 < len; i0 += PF) {
-      int2 en[PF];
-#pragma unroll
-      for (int j = 0; j < PF; ++j) en[j] = i0 + j < len ? p.occ_entries[start + i0 + j] : make_int2(0, 0);
-      uint4 u[PF];
-#pragma unroll
-      for (int j = 0; j < PF; ++j)
-        u[j] = i0 + j < len ? ld_nc_u4(p.occ_wt + (int64_t)en[j].x * p.occ_ldt + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int j = 0; j < PF; ++j) {
-        const float val = __int_as_float(en[j].y);   // 0 for the padding slots
-        const uint32_t q[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          y[2 * k] = fmaf(val, __uint_as_float(q[k] << 16), y[2 * k]);
-          y[2 * k + 1] = fmaf(val, __uint_as_float(q[k] & 0xFFFF0000u), y[2 * k + 1]);
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(y[2 * k], y[2 * k + 1]);
-      w[4 * v + k] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-  }
-}
-
 // bf16 out without accumulation, 64 columns: word i of w packs columns 2i and
 // 2i + 1 (scaled and rounded).  After warp_exchange_hi3 lane 4b + a holds
 // columns col0 + 8b .. +7 of rows row0 + 4v + a: one 16-byte store each.
@@ -260,9 +166,6 @@ __device__ __forceinline__ void store_exchanged_bf16x2(const Params& p, const ui
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-// OCC: the epilogue adds the per-row sparse correction (a separate
-// instantiation, so that the plain kernel's register budget is untouched)
-template <bool OCC>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fp4_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
@@ -537,55 +440,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int colw = tn * BN + cbase;             // first output column of the slice
       const bool any = row0 < p.M && colw < p.N;   // warp-uniform
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)cbase;
-      if (OCC && p.out_bf16 && !p.accumulate) {
-        // as the plain bf16 path, plus the rows' sparse corrections on the
-        // exchanged packed values (see occ_correct_bf16x2)
-        uint32_t r2[2][32];
-        tmem_ld32_nowait(taddr, r2[0]);
-        tmem_ld32_nowait(taddr + 32, r2[1]);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acc_empty);
-        if (any) {
-          const int myrow = row0 + lane;
-          const uint32_t mylen = myrow < p.M ? p.occ_len[myrow] : 0u;
-          const uint32_t mystart = mylen ? p.occ_start[myrow] : 0u;
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const uint32_t* r = r2[i >> 4];
-            const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * (i & 15)]), alpha),
-                                                           __fmul_rn(__uint_as_float(r[2 * (i & 15) + 1]), alpha));
-            pk[i] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-          warp_exchange_hi3(pk, lane);
-          occ_correct_bf16x2(p, pk, colw, lane, mylen, mystart);
-          store_exchanged_bf16x2(p, pk, row0, colw, lane);
-        }
-      } else if (OCC) {
-        // fp32 out or C += : 32 columns at a time (the release waits for the
-        // second load), corrections in fp32 on the exchanged values
-        const int myrow = row0 + lane;
-        const uint32_t mylen = (any && myrow < p.M) ? p.occ_len[myrow] : 0u;
-        const uint32_t mystart = mylen ? p.occ_start[myrow] : 0u;
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r[32];
-          tmem_ld32_nowait(taddr + 32 * h, r);
-          tmem_ld_wait();
-          if (h == 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
-          }
-          if (any) {
-            warp_exchange_hi3(r, lane);
-            occ_correct_exchanged(p, r, alpha, colw + 32 * h, lane, mylen, mystart);
-            store_exchanged(p, r, row0, colw + 32 * h, 1.0f, lane);
-          }
-        }
-      } else if (p.out_bf16 && !p.accumulate) {
+      if (p.out_bf16 && !p.accumulate) {
         uint32_t r2[2][32];
         tmem_ld32_nowait(taddr, r2[0]);
         tmem_ld32_nowait(taddr + 32, r2[1]);
@@ -726,10 +581,10 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   const fp4_operand& B = *g.B;
   const int64_t M = A.rows, N = B.rows;
   if (M == 0 || N == 0) return FP4_OK;
-  // the FP4 GEMM, alone or with bf16 extra columns, runs on CTA pairs; E4M3
-  // extra columns, the outlier epilogue, row/column scales and C += stay on
-  // the one-SM kernel
-  if (g.fp4_part && !g.ext_fp8 && !g.occ_len && !g.row_scale && !g.accumulate) return launch_gemm_pair(g, st);
+  // the FP4 GEMM, alone or with bf16 or MXFP8 extra columns, runs on CTA
+  // pairs; E4M3 extra columns, row/column scales and C += stay on the one-SM
+  // kernel
+  if (g.fp4_part && !g.ext_fp8 && !g.row_scale && !g.accumulate) return launch_gemm_pair(g, st);
   if (g.ext_mx8) return FP4_ERR_UNSUPPORTED;   // MXFP8 extra columns exist on the pair kernel only
   Params p{};
   p.M = (int)M;
@@ -750,11 +605,6 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
   p.status = g.status;
   p.tiles_m = (int)cdiv(M, BM);
   p.tiles_n = (int)cdiv(N, BN);
-  p.occ_start = g.occ_start;
-  p.occ_len = g.occ_len;
-  p.occ_entries = static_cast<const int2*>(g.occ_entries);
-  p.occ_wt = g.occ_wt;
-  p.occ_ldt = g.occ_ldt;
   if (p.k_tiles + p.ext_tiles == 0) return FP4_ERR_INVALID_ARG;
 
   CUtensorMap ta{}, tb{}, tsa{}, tsb{}, tax{}, tbx{};
@@ -786,19 +636,13 @@ int launch_gemm(const GemmArgs& g, cudaStream_t st) {
 
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(fp4_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(fp4_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess)
+    if (cudaFuncSetAttribute(fp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
       return FP4_ERR_CUDA;
     attr_set = true;
   }
   const int tiles = p.tiles_m * p.tiles_n;
   const int grid = std::min(tiles, g.num_sms);
-  if (p.occ_len)
-    fp4_gemm_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, tsa, tsb, tax, tbx, p);
-  else
-    fp4_gemm_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, tsa, tsb, tax, tbx, p);
+  fp4_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, tsa, tsb, tax, tbx, p);
   return cudaGetLastError() == cudaSuccess ? FP4_OK : FP4_ERR_CUDA;
 }
 

@@ -292,6 +292,131 @@ struct OccEntry {
   float v;
 };
 
+// L2 eviction-priority policies (createpolicy) and the loads / stores that
+// carry them: the correction streams Y once (evict first) and re-reads the
+// rows of W^T that its entries name (evict last), so that W^T stays in L2
+// while Y passes through
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint4 ld_v4_hint(const void* ptr, uint64_t pol) {
+  uint4 u;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "l"(ptr), "l"(pol));
+  return u;
+}
+__device__ __forceinline__ void st_v4_hint(void* ptr, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+// The scattered outliers' product ([msr] §三: computed apart from the
+// quantized GEMM and added back), after the GEMM stored Y:
+//   Y[m, :] += sum over the entries (k, v) of row m of  v * W^T[k, :]
+// in fp32 on the stored values, entry by entry in list order (bf16 Y is
+// rounded again: the stored value was rounded once).  One thread per 8
+// columns of a row (16-byte reads of W^T, whose rows are zero-padded to a
+// multiple of 8 columns), the threads of a row side by side; rows without
+// entries are not touched.  (A warp per row, passing over its columns, kept
+// one 512-byte load of Y in flight per warp: 176 us on a 16384 x 4096 Y.)
+template <bool BF16>
+__global__ void __launch_bounds__(256) occ_correct_kernel(void* __restrict__ y, int64_t ldy, int64_t M, int64_t N,
+                                                          FastDiv upr_div, const uint32_t* __restrict__ row_start,
+                                                          const uint32_t* __restrict__ row_len,
+                                                          const OccEntry* __restrict__ ent,
+                                                          const uint16_t* __restrict__ wt, int64_t ldt) {
+  const uint32_t upr = upr_div.d;                      // 8-column units per row
+  const uint32_t total = (uint32_t)M * upr;
+  const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+  for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += gridDim.x * blockDim.x) {
+    const uint32_t m = fast_div(u, upr_div);
+    const uint32_t len = row_len[m];
+    if (len == 0) continue;
+    const uint32_t s0 = row_start[m];
+    const int64_t c = (int64_t)(u - m * upr) * 8;
+    const bool full = c + 8 <= N;
+    float acc[8];
+    if constexpr (BF16) {
+      const uint16_t* yp = static_cast<const uint16_t*>(y) + (int64_t)m * ldy + c;
+      if (full) {
+        const uint4 q = ld_v4_hint(yp, stream);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[2 * k] = __uint_as_float(w[k] << 16);
+          acc[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = c + j < N ? __uint_as_float((uint32_t)yp[j] << 16) : 0.0f;
+      }
+    } else {
+      const float* yp = static_cast<const float*>(y) + (int64_t)m * ldy + c;
+      if (full) {
+        const uint4 a = ld_v4_hint(yp, stream), b = ld_v4_hint(yp + 4, stream);
+        acc[0] = __uint_as_float(a.x); acc[1] = __uint_as_float(a.y);
+        acc[2] = __uint_as_float(a.z); acc[3] = __uint_as_float(a.w);
+        acc[4] = __uint_as_float(b.x); acc[5] = __uint_as_float(b.y);
+        acc[6] = __uint_as_float(b.z); acc[7] = __uint_as_float(b.w);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = c + j < N ? yp[j] : 0.0f;
+      }
+    }
+    for (uint32_t i0 = 0; i0 < len; i0 += 4) {
+      OccEntry e[4];
+      uint4 q[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) e[j] = i0 + j < len ? ent[s0 + i0 + j] : OccEntry{0, 0.0f};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        q[j] = i0 + j < len ? ld_v4_hint(wt + (int64_t)e[j].k * ldt + c, keep) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (i0 + j >= len) break;   // the row's true entries only
+        const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[2 * k] = fmaf(e[j].v, __uint_as_float(w[k] << 16), acc[2 * k]);
+          acc[2 * k + 1] = fmaf(e[j].v, __uint_as_float(w[k] & 0xFFFF0000u), acc[2 * k + 1]);
+        }
+      }
+    }
+    if constexpr (BF16) {
+      uint16_t* yp = static_cast<uint16_t*>(y) + (int64_t)m * ldy + c;
+      uint32_t pk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * k], acc[2 * k + 1]);
+        pk[k] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      if (full) {
+        st_v4_hint(yp, make_uint4(pk[0], pk[1], pk[2], pk[3]), stream);
+      } else {
+        for (int j = 0; j < 8 && c + j < N; ++j) yp[j] = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
+      }
+    } else {
+      float* yp = static_cast<float*>(y) + (int64_t)m * ldy + c;
+      if (full) {
+        st_v4_hint(yp, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                                  __float_as_uint(acc[3])), stream);
+        st_v4_hint(yp + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]), __float_as_uint(acc[6]),
+                                      __float_as_uint(acc[7])), stream);
+      } else {
+        for (int j = 0; j < 8 && c + j < N; ++j) yp[j] = acc[j];
+      }
+    }
+  }
+}
+
 // 8-bit mask of the outliers |x| > tau among 8 consecutive elements.  bf16:
 // on the bit patterns, two elements per instruction (for bf16 x, |x| > tau iff
 // the magnitude bits exceed those of tau truncated to bf16; NaNs are not
@@ -566,6 +691,31 @@ cudaError_t launch_occ_prepare(const void* x, int xdt, int64_t ldx, const uint16
     if (xdt == FP4_DTYPE_BF16) FP4_OCC_EXTRACT(FP4_FMT_NVFP4, FP4_DTYPE_BF16); else FP4_OCC_EXTRACT(FP4_FMT_NVFP4, FP4_DTYPE_F32);
   }
 #undef FP4_OCC_EXTRACT
+  return cudaGetLastError();
+}
+
+cudaError_t launch_occ_correct(void* y, int64_t ldy, int out_dtype, int64_t m, int64_t n, const void* ws,
+                               const OccLayout& L, int num_sms, cudaStream_t st) {
+  if (m == 0 || n == 0) return cudaSuccess;
+  const uint8_t* base = static_cast<const uint8_t*>(ws);
+  const auto* rs = reinterpret_cast<const uint32_t*>(base + L.row_start);
+  const auto* rl = reinterpret_cast<const uint32_t*>(base + L.row_len);
+  const auto* ent = reinterpret_cast<const OccEntry*>(base + L.entries);
+  const auto* wt = reinterpret_cast<const uint16_t*>(base + L.wt);
+  // 8-column units with 32-bit ids (below 2^31, so that the grid stride
+  // cannot wrap): row bands of at most that many units per launch
+  const int64_t upr = cdiv(n, 8), band = std::max<int64_t>(1, ((int64_t(1) << 31) - 1) / upr);
+  const FastDiv fd = make_fastdiv((uint32_t)upr);
+  const int esz = out_dtype == FP4_DTYPE_BF16 ? 2 : 4;
+  for (int64_t r0 = 0; r0 < m; r0 += band) {
+    const int64_t rows = std::min(band, m - r0);
+    void* yb = static_cast<uint8_t*>(y) + r0 * ldy * esz;
+    const int grid = grid_cap(rows * upr, 256, num_sms);
+    if (out_dtype == FP4_DTYPE_BF16)
+      occ_correct_kernel<true><<<grid, 256, 0, st>>>(yb, ldy, rows, n, fd, rs + r0, rl + r0, ent, wt, L.ldt);
+    else
+      occ_correct_kernel<false><<<grid, 256, 0, st>>>(yb, ldy, rows, n, fd, rs + r0, rl + r0, ent, wt, L.ldt);
+  }
   return cudaGetLastError();
 }
 
