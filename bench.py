@@ -82,8 +82,9 @@ def parse():
     ap.add_argument("--only", default=None,
                     help="profiling runs (ncu): after one full 7B FFN step, launch the comma-separated ops of "
                          "that step, or 'fused_quant_a' (the forward GEMM with X quantized inside), "
-                         "--only-launches times each; 'llama_step' runs the LLaMA-1B step's ops instead. "
-                         "Prints nothing but 'ok'")
+                         "--only-launches times each; 'llama_step' runs the LLaMA-1B step's ops instead; "
+                         "'hcp_order2', 'hcp_order2_mxfp8', 'hcp_zeroed_mxfp8', 'occ_gemm' run one op of the "
+                         "hot-channel / outlier workload. Prints nothing but 'ok'")
     ap.add_argument("--only-launches", type=int, default=1)
     return ap.parse_args()
 
@@ -815,6 +816,41 @@ def time_linear_small(fp4, dev, pk, batch=50, replays=20):
             "note": "launch-bound (launches of a few microseconds each): reported, not held to the roofline bar"}
 
 
+def hcp_occ_op(fp4, inputs, name, dev):
+    """One op of the hot-channel / outlier workload (the inputs of time_hcp and
+    time_occ), prepared and returned as a closure, for profiling runs."""
+    d = inputs.hcp_square(OCC_M, OCC_K, OCC_N)
+    X, W = d["X"].to(dev), d["W"].to(dev)
+    p = fp4.quant_params(fp4.FP4_FMT_NVFP4)
+    lib = fp4.load_library()
+    Y = torch.empty((OCC_M, OCC_N), dtype=torch.bfloat16, device=dev)
+    wq = fp4.fp4_quantize(W, p)
+    if name.startswith("hcp_"):
+        xq = fp4.fp4_quantize(X, p)
+        h = fp4.fp4_hcp_num_hot(OCC_K)
+        hot = fp4.fp4_hcp_select(X, xq, h)
+        ws = torch.empty((lib.fp4_hcp_workspace_bytes(OCC_M, OCC_N, h, 2),), dtype=torch.uint8, device=dev)
+        if name == "hcp_order2":
+            return lambda: fp4.fp4_hcp_gemm(X, W, xq, wq, hot, h, fp4.FP4_HCP_SINGLE, 2, out=Y, workspace=ws)
+        if name == "hcp_order2_mxfp8":
+            return lambda: fp4.fp4_hcp_gemm(X, W, xq, wq, hot, h, fp4.FP4_HCP_SINGLE_MXFP8, 2, out=Y, workspace=ws)
+        if name == "hcp_zeroed_mxfp8":
+            x0q = fp4.fp4_hcp_quantize_zeroed(X, p, hot, h)
+            return lambda: fp4.fp4_hcp_gemm(X, W, x0q, wq, hot, h, fp4.FP4_HCP_SINGLE_MXFP8, 0, out=Y, workspace=ws)
+    elif name == "occ_gemm":
+        ws_t = torch.empty((lib.fp4_occ_threshold_workspace_bytes(fp4.FP4_DTYPE_BF16),), dtype=torch.uint8,
+                           device=dev)
+        tau, _ = fp4.fp4_occ_threshold(X, workspace=ws_t)
+        counts = torch.empty((OCC_K,), dtype=torch.float32, device=dev)
+        xq = fp4.alloc_qtensor(OCC_M, OCC_K, fp4.FP4_FMT_NVFP4, fp4.FP4_SF_MMA, dev)
+        fp4.fp4_occ_quantize(X, p, tau, out=xq, col_counts=counts)
+        cap = fp4.fp4_occ_max_outliers(OCC_M, OCC_K)
+        ws = torch.empty((lib.fp4_occ_gemm_workspace_bytes(OCC_M, OCC_N, OCC_K, OCC_DENSE, cap),), dtype=torch.uint8,
+                         device=dev)
+        return lambda: fp4.fp4_occ_gemm(X, W, xq, wq, tau, counts, OCC_DENSE, cap, out=Y, workspace=ws)
+    raise SystemExit(f"--only: unknown op {name!r}")
+
+
 def run_only(fp4, inputs, args, dev):
     """Launch named ops for a profiler (one stream, in order, L2 flushed before each)."""
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -825,6 +861,11 @@ def run_only(fp4, inputs, args, dev):
             flush.fill_(i & 0xFF)
             for _, fn in step.ops(i):
                 fn()
+    elif args.only.startswith(("hcp_", "occ_")):
+        fn = hcp_occ_op(fp4, inputs, args.only, dev)
+        for i in range(args.only_launches):
+            flush.fill_(i & 0xFF)
+            fn()
     else:
         d = inputs.ffn7b()
         step = FfnStep(fp4, *(d[k].to(dev) for k in ("X", "W", "dY")), dev)
