@@ -83,8 +83,8 @@ def parse():
                     help="profiling runs (ncu): after one full 7B FFN step, launch the comma-separated ops of "
                          "that step, or 'fused_quant_a' (the forward GEMM with X quantized inside), "
                          "--only-launches times each; 'llama_step' runs the LLaMA-1B step's ops instead; "
-                         "'hcp_order2', 'hcp_order2_mxfp8', 'hcp_zeroed_mxfp8', 'occ_gemm' run one op of the "
-                         "hot-channel / outlier workload. Prints nothing but 'ok'")
+                         "'hcp_select', 'hcp_order2', 'hcp_order2_mxfp8', 'hcp_zeroed_mxfp8', 'occ_gemm' run one op "
+                         "of the hot-channel / outlier workload. Prints nothing but 'ok'")
     ap.add_argument("--only-launches", type=int, default=1)
     return ap.parse_args()
 
@@ -830,6 +830,8 @@ def hcp_occ_op(fp4, inputs, name, dev):
         h = fp4.fp4_hcp_num_hot(OCC_K)
         hot = fp4.fp4_hcp_select(X, xq, h)
         ws = torch.empty((lib.fp4_hcp_workspace_bytes(OCC_M, OCC_N, h, 2),), dtype=torch.uint8, device=dev)
+        if name == "hcp_select":
+            return lambda: fp4.fp4_hcp_select(X, xq, h)
         if name == "hcp_order2":
             return lambda: fp4.fp4_hcp_gemm(X, W, xq, wq, hot, h, fp4.FP4_HCP_SINGLE, 2, out=Y, workspace=ws)
         if name == "hcp_order2_mxfp8":

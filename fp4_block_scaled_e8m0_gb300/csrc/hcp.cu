@@ -41,41 +41,77 @@ __device__ __forceinline__ float dequant_elem(const fp4_operand& q, int64_t r, i
   return (code & 8u) ? -v : v;
 }
 
-// err[c] += sum over this thread's rows of (x - x_hat)^2; one thread per block of
-// B consecutive channels, rows strided over gridDim.y
+// err[c] += sum over this CTA's rows of (x - x_hat)^2.  threadIdx.x: a block of
+// B consecutive channels (row-contiguous lanes: a warp reads whole 512-byte
+// runs of a row), threadIdx.y: a row group; rows strided over the grid's y
+// extent, two rows' loads in flight.  The row groups' sums meet in shared
+// memory, and each CTA adds one value per channel to err.
 template <int FMT>
-__global__ void __launch_bounds__(256) channel_err_kernel(const uint16_t* __restrict__ x, int64_t ldx, fp4_operand q,
+__global__ void __launch_bounds__(512) channel_err_kernel(const uint16_t* __restrict__ x, int64_t ldx, fp4_operand q,
                                                           float* err) {
   constexpr int B = FMT == FP4_FMT_MXFP4 ? 32 : 16;
+  __shared__ float part[512];
   const int64_t nblk = q.k / B;
   const int64_t cb = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (cb >= nblk) return;
+  const bool live = cb < nblk;
   const int64_t nsf_row = nblk, nsf_pad = nsf_padded(q.k, FMT);
   const float g = FMT == FP4_FMT_NVFP4 ? *q.tensor_scale : 0.0f;
   float acc[B];
 #pragma unroll
   for (int j = 0; j < B; ++j) acc[j] = 0.0f;
-  for (int64_t r = blockIdx.y; r < q.rows; r += gridDim.y) {
-    uint32_t sb = q.scales[sf_offset(q.sf_layout, r, cb, nsf_row, nsf_pad)];
-    float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
-    float v[B];
+  if (live) {
+#pragma unroll 2
+    for (int64_t r = blockIdx.y * (int64_t)blockDim.y + threadIdx.y; r < q.rows; r += (int64_t)gridDim.y * blockDim.y) {
+      const uint32_t sb = q.scales[sf_offset(q.sf_layout, r, cb, nsf_row, nsf_pad)];
+      const float s = FMT == FP4_FMT_MXFP4 ? e8m0_scale(sb) : e4m3_decode(sb);
+      float v[B];
 #pragma unroll
-    for (int h = 0; h < B / 8; ++h) load8<FP4_DTYPE_BF16>(x, r * ldx + cb * B + 8 * h, v + 8 * h);
-    const uint8_t* cp = q.codes + r * (q.k >> 1) + cb * (B / 2);
+      for (int h = 0; h < B / 8; ++h) load8<FP4_DTYPE_BF16>(x, r * ldx + cb * B + 8 * h, v + 8 * h);
+      // the block's B/2 code bytes in one 8- or 16-byte load
+      uint32_t cw[B / 8];
+      const uint8_t* cp = q.codes + r * (q.k >> 1) + cb * (B / 2);
+      if constexpr (B == 16) {
+        const uint2 u = *reinterpret_cast<const uint2*>(cp);
+        cw[0] = u.x;
+        cw[1] = u.y;
+      } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(cp);
+        cw[0] = u.x;
+        cw[1] = u.y;
+        cw[2] = u.z;
+        cw[3] = u.w;
+      }
+      // x_hat of two elements from each code byte: the signed E2M1 values by
+      // the hardware decode, times the block scale (and g)
 #pragma unroll
-    for (int j = 0; j < B; ++j) {
-      uint32_t code = (cp[j >> 1] >> (4 * (j & 1))) & 15u;
-      uint32_t m = code & 7u;
-      float mag = m < 4 ? 0.5f * (float)m : (m == 4 ? 2.0f : m == 5 ? 3.0f : m == 6 ? 4.0f : 6.0f);
-      float xh = __fmul_rn(mag, s);
-      if (FMT == FP4_FMT_NVFP4) xh = __fmul_rn(xh, g);
-      if (code & 8u) xh = -xh;
-      float d = __fsub_rn(v[j], xh);
-      acc[j] = __fmaf_rn(d, d, acc[j]);
+      for (int j2 = 0; j2 < B / 2; ++j2) {
+        float h0, h1;
+        e2m1x2_decode(cw[j2 >> 2] >> (8 * (j2 & 3)), h0, h1);
+        h0 = __fmul_rn(h0, s);
+        h1 = __fmul_rn(h1, s);
+        if (FMT == FP4_FMT_NVFP4) {
+          h0 = __fmul_rn(h0, g);
+          h1 = __fmul_rn(h1, g);
+        }
+        const float d0 = __fsub_rn(v[2 * j2], h0), d1 = __fsub_rn(v[2 * j2 + 1], h1);
+        acc[2 * j2] = __fmaf_rn(d0, d0, acc[2 * j2]);
+        acc[2 * j2 + 1] = __fmaf_rn(d1, d1, acc[2 * j2 + 1]);
+      }
     }
   }
+  // the row groups' sums, channel by channel, then one atomic add per channel
+  const int t = threadIdx.y * blockDim.x + threadIdx.x;
 #pragma unroll
-  for (int j = 0; j < B; ++j) atomicAdd(&err[cb * B + j], acc[j]);
+  for (int j = 0; j < B; ++j) {
+    part[t] = acc[j];
+    __syncthreads();
+    if (threadIdx.y == 0 && live) {
+      float sum = part[threadIdx.x];
+      for (int y = 1; y < (int)blockDim.y; ++y) sum += part[y * blockDim.x + threadIdx.x];
+      atomicAdd(&err[cb * B + j], sum);
+    }
+    __syncthreads();
+  }
 }
 
 // rank[c] += the number of channels j in this CTA's slice of 256 that beat c
@@ -507,13 +543,16 @@ cudaError_t launch_hcp_channel_errors(const uint16_t* x, int64_t ldx, const fp4_
   if (e != cudaSuccess || q.rows == 0 || q.k == 0) return e;
   const int B = q.format == FP4_FMT_MXFP4 ? 32 : 16;
   const int64_t nblk = q.k / B;
-  dim3 grid((unsigned)cdiv(nblk, 256), 1);
-  int64_t want_y = cdiv((int64_t)num_sms * 8, grid.x);
-  grid.y = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want_y, q.rows));
+  // 512 threads: up to 256 channel blocks x the rest as row groups
+  const int bx = (int)std::min<int64_t>(256, cdiv(nblk, 32) * 32), by = 512 / bx;
+  dim3 block((unsigned)bx, (unsigned)by);
+  dim3 grid((unsigned)cdiv(nblk, bx), 1);
+  const int64_t want_y = cdiv((int64_t)num_sms * 2, grid.x);   // two CTAs an SM
+  grid.y = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want_y, cdiv(q.rows, by)));
   if (q.format == FP4_FMT_MXFP4)
-    channel_err_kernel<FP4_FMT_MXFP4><<<grid, 256, 0, st>>>(x, ldx, q, err);
+    channel_err_kernel<FP4_FMT_MXFP4><<<grid, block, 0, st>>>(x, ldx, q, err);
   else
-    channel_err_kernel<FP4_FMT_NVFP4><<<grid, 256, 0, st>>>(x, ldx, q, err);
+    channel_err_kernel<FP4_FMT_NVFP4><<<grid, block, 0, st>>>(x, ldx, q, err);
   return cudaGetLastError();
 }
 
