@@ -229,3 +229,36 @@ def test_hcp_mxfp8_hot_list_in_any_order(fmt):
     yref, bound = o.hcp_gemm_mxfp8(xn, cx, sx, wn, cw, sw, FMT[fmt], gx, gw, hot, 2)
     err = np.abs(y.cpu().numpy().astype(np.float64) - yref)
     assert np.all(err <= o.gemm_tolerance(bound, yref, False))
+
+
+@pytest.mark.parametrize("fmt", [fp4.FP4_FMT_MXFP4, fp4.FP4_FMT_NVFP4])
+@pytest.mark.parametrize("order", [0, 2])
+def test_hcp_wide_rows_take_the_per_element_gathers(fmt, order):
+    # K = 20480: a row's two staging buffers no longer fit the shared-memory
+    # budget, so both gathers (bf16 and MXFP8 columns) read the hot values
+    # directly; same oracle products as at small K
+    M, K, N = 130, 20480, 136
+    xt, wt, xn, wn, _ = _data(fmt, M=M, K=K, N=N, seed=21)
+    h = fp4.fp4_hcp_num_hot(K)
+    cx, sx, gx = o.quantize(xn, FMT[fmt])
+    hot = o.hcp_select(xn, cx, sx, FMT[fmt], gx, h)
+    hot_d = torch.from_numpy(hot.astype(np.int32)).cuda()
+    if order == 0:
+        xq = fp4.fp4_hcp_quantize_zeroed(xt.cuda(), fp4.quant_params(fmt), hot_d, h)
+        cx, sx, gx = o.quantize(o.hcp_zero_columns(xn, hot), FMT[fmt])
+    else:
+        xq = fp4.fp4_quantize(xt.cuda(), fp4.quant_params(fmt))
+    wq = fp4.fp4_quantize(wt.cuda(), fp4.quant_params(fmt))
+    cw, sw, gw = o.quantize(wn, FMT[fmt])
+    y = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, hot_d, h, fp4.FP4_HCP_SINGLE, order, torch.float32)
+    if order == 0:
+        yref, bound, _, _ = o.hcp_zeroed_gemm(xn, wn, FMT[fmt], hot)
+    else:
+        yref, bound = o.hcp_gemm(xn, cx, sx, wn, cw, sw, FMT[fmt], gx, gw, hot, order)
+    err = np.abs(y.cpu().numpy().astype(np.float64) - yref)
+    assert np.all(err <= o.gemm_tolerance(bound, yref, False)), "bf16 columns"
+    y8 = fp4.fp4_hcp_gemm(xt.cuda(), wt.cuda(), xq, wq, hot_d, h, fp4.FP4_HCP_SINGLE_MXFP8, order, torch.float32)
+    yref8, bound8 = o.hcp_gemm_mxfp8(xn, cx, sx, wn, cw, sw, FMT[fmt], gx, gw, hot, order)
+    err8 = np.abs(y8.cpu().numpy().astype(np.float64) - yref8)
+    assert np.all(err8 <= o.gemm_tolerance(bound8, yref8, False)), "MXFP8 columns"
+    assert fp4.fp4_sync_status() == fp4.FP4_OK
