@@ -503,10 +503,15 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# the sources the kernels in profiles/dram_traffic.json are built from (the
+# CTA-pair GEMM, the MXFP4 dual quantizer and the headers they include)
+TRAFFIC_SOURCES = ("gemm2.cu", "quant_mx.cu", "tcgen05.cuh", "fp4_device.cuh", "fp4_internal.h")
+
+
 def source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp4_block_scaled_e8m0_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in TRAFFIC_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

@@ -356,8 +356,8 @@ template <int N>
 __device__ __forceinline__ void cpa_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // gather_mx8_kernel with each row staged first: a warp copies its row's bf16
-// values (and, for orders 1 and 2, its FP4 codes and block scales) into shared
-// memory with 16-byte cp.async copies (with ~9% of the channels hot, nearly
+// values (and, where x_hat is used - A at order 2, B at orders 1 and 2 - its FP4
+// codes and block scales) into shared memory with 16-byte cp.async copies (with ~9% of the channels hot, nearly
 // every 32-byte sector of the row is needed, and the per-block warps of the
 // kernel above fetched each hot value, code and scale on its own), then each
 // lane forms one whole 32-column block of the row from shared memory (no
