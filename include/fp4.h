@@ -255,9 +255,10 @@ int fp4_occ_quantize(fp4_ctx* ctx, const void* x, int32_t x_dtype, int64_t rows,
  *    fp4_occ_quantize; ties to the lower index) become extra bf16 K columns of
  *    the FP4 GEMM: A_ext = bf16(dX_H / alpha), B_ext = W_H (alpha = gX gW,
  *    1 for MXFP4), accumulated with the FP4 part on the tensor cores;
- *  - every other outlier (|x| > tau) is listed per row and the GEMM epilogue
- *    adds v * W^T[k, :] to its row of Y in fp32 (a bf16 Y is rounded once
- *    before and once after: each rounding within 2^-9).
+ *  - every other outlier (|x| > tau) is listed per row, and after the GEMM
+ *    stored Y a second pass adds v * W^T[k, :] to its row of Y in fp32, in
+ *    list order (a bf16 Y is rounded once before and once after: each
+ *    rounding within 2^-9).
  * k_dense = 0 sends all outliers to the second part (col_counts may be NULL).
  * An outlier so large that dX / alpha leaves the bf16 range makes its extra
  * column infinite (|x| / tau ~ 1e28 for weights of amax 1e-3).
