@@ -251,10 +251,13 @@ __global__ void __launch_bounds__(256) occ_tail_kernel(const void* __restrict__ 
 // W [N][K] (pitch ldw) -> WT [K][ldt], 64 x 64 tiles through shared memory:
 // 16-byte reads along k (8 bf16 of one W row) and 16-byte writes along n (8 bf16
 // of one W^T row, gathered from a tile column); W rows are 16-byte aligned,
-// k % 32 == 0, ldt % 8 == 0.
+// k % 32 == 0, ldt % 8 == 0.  The tile's 16-byte chunk q of row r sits at chunk
+// q ^ (r / 8 % 8): the column reads of the write-out (8 rows 8 apart, a word
+// each) then fall on distinct banks; with padded rows they all hit one bank.
+__device__ __forceinline__ int tr_swz(int r, int c) { return ((((c >> 3) ^ (r >> 3)) & 7) << 3) | (c & 7); }
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __restrict__ w, int64_t ldw, int64_t n,
                                                              int64_t k, uint16_t* __restrict__ wt, int64_t ldt) {
-  __shared__ uint16_t tile[64][72];   // 144-byte rows: 16-byte aligned, staggered banks
+  __shared__ __align__(16) uint16_t tile[64][64];
   const int64_t tiles_k = cdiv(k, 64), tiles = cdiv(n, 64) * tiles_k;
   const int t = threadIdx.x;
   for (int64_t tt = blockIdx.x; tt < tiles; tt += gridDim.x) {
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __r
       const int64_t nn = n0 + r, kk = k0 + kc;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (nn < n && kk < k) v = __ldg(reinterpret_cast<const uint4*>(w + nn * ldw + kk));   // k % 8 == 0
-      *reinterpret_cast<uint4*>(&tile[r][kc]) = v;
+      *reinterpret_cast<uint4*>(&tile[r][tr_swz(r, kc)]) = v;
     }
     __syncthreads();
 #pragma unroll
@@ -275,7 +278,8 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* __r
       if (kk < k && nn < n) {
         uint32_t q[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) q[j] = tile[nc + 2 * j][c] | ((uint32_t)tile[nc + 2 * j + 1][c] << 16);
+        for (int j = 0; j < 4; ++j)
+          q[j] = tile[nc + 2 * j][tr_swz(nc + 2 * j, c)] | ((uint32_t)tile[nc + 2 * j + 1][tr_swz(nc + 2 * j + 1, c)] << 16);
         if (nn + 8 <= n) {
           *reinterpret_cast<uint4*>(wt + kk * ldt + nn) = make_uint4(q[0], q[1], q[2], q[3]);
         } else {
