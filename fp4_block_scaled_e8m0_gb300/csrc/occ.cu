@@ -425,18 +425,20 @@ __global__ void __launch_bounds__(256) occ_correct_kernel(void* __restrict__ y, 
 // on the bit patterns, two elements per instruction (for bf16 x, |x| > tau iff
 // the magnitude bits exceed those of tau truncated to bf16; NaNs are not
 // outliers, as in the clamp).
-__device__ __forceinline__ uint32_t halves_to_bits(uint32_t m) { return (m & 1u) | ((m >> 15) & 2u); }
-
-__device__ __forceinline__ uint32_t outlier_mask8_bits(const uint4& u, uint32_t tau2) {
-  const uint32_t q[4] = {u.x, u.y, u.z, u.w};
-  uint32_t mask = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t a = q[j] & 0x7FFF7FFFu;
-    const uint32_t m = __vcmpgtu2(a, tau2) & ~__vcmpgtu2(a, 0x7F807F80u);
-    mask |= halves_to_bits(m) << (2 * j);
-  }
-  return mask;
+// Per 16-bit half of q (a bf16 pair): bit 15 / 31 set where taub < |x|_h <=
+// 0x7F80 (an outlier, NaN excluded), by subtractions that cannot borrow across
+// the halves (magnitudes and taub + 1 are at most 0x8000): in a half,
+// (a | 0x8000) - (taub + 1) has bit 15 set iff a > taub, and 0xFF80 - a iff
+// a <= 0x7F80.  tau2p1 = (taub + 1) in both halves.
+__device__ __forceinline__ uint32_t outlier_halves(uint32_t q, uint32_t tau2p1) {
+  const uint32_t a = q & 0x7FFF7FFFu;
+  return ((a | 0x80008000u) - tau2p1) & (0xFF80FF80u - a) & 0x80008000u;
+}
+// the 8 elements' bits (element 2j from word j's low half, 2j + 1 from its high half)
+__device__ __forceinline__ uint32_t outlier_mask8_bits(const uint4& u, uint32_t tau2p1) {
+  const uint32_t t = (outlier_halves(u.x, tau2p1) >> 15) | (outlier_halves(u.y, tau2p1) >> 13) |
+                     (outlier_halves(u.z, tau2p1) >> 11) | (outlier_halves(u.w, tau2p1) >> 9);
+  return (t & 0x55u) | ((t >> 15) & 0xAAu);
 }
 
 template <int XDT>
@@ -444,16 +446,7 @@ __device__ __forceinline__ uint32_t outlier_mask8(const void* x, int64_t off, fl
   if constexpr (XDT == FP4_DTYPE_BF16) {
     // a plain read-only load (not volatile asm), so that the compiler can put
     // the loads of all the row's chunks in flight before the masks
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off));
-    const uint32_t q[4] = {u.x, u.y, u.z, u.w};
-    uint32_t mask = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t a = q[j] & 0x7FFF7FFFu;
-      const uint32_t m = __vcmpgtu2(a, tau2) & ~__vcmpgtu2(a, 0x7F807F80u);
-      mask |= halves_to_bits(m) << (2 * j);
-    }
-    return mask;
+    return outlier_mask8_bits(__ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off)), tau2);
   } else {
     float e[8];
     load8<FP4_DTYPE_F32, true>(x, off, e);
@@ -480,7 +473,8 @@ __global__ void __launch_bounds__(256) occ_extract_kernel(const void* __restrict
   __shared__ uint32_t warp_off[8];
   __shared__ uint32_t cta_base;
   const float tau = *tau_p;
-  const uint32_t taub = (__float_as_uint(tau) >> 16) & 0x7FFFu, tau2 = taub | (taub << 16);
+  // bf16 x: |x| > tau iff its magnitude bits exceed those of tau truncated to bf16
+  const uint32_t taub = (__float_as_uint(tau) >> 16) & 0x7FFFu, tau2 = (taub + 1u) | ((taub + 1u) << 16);
   const bool tail = tail_inv_alpha<FMT>(xq, wq) != 0.0f;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   auto scat_mask = [&](int64_t r, int64_t c0) {
