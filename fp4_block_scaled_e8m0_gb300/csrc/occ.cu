@@ -337,7 +337,8 @@ __global__ void __launch_bounds__(256) occ_correct_kernel(void* __restrict__ y, 
                                                           const uint32_t* __restrict__ row_len,
                                                           const OccEntry* __restrict__ ent,
                                                           const uint16_t* __restrict__ wt, int64_t ldt) {
-  const uint32_t upr = upr_div.d;                      // 8-column units per row
+  constexpr int G = 2;                                 // 8-column groups a thread
+  const uint32_t upr = upr_div.d;                      // 8G-column units per row
   const uint32_t total = (uint32_t)M * upr;
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += gridDim.x * blockDim.x) {
@@ -345,77 +346,93 @@ __global__ void __launch_bounds__(256) occ_correct_kernel(void* __restrict__ y, 
     const uint32_t len = row_len[m];
     if (len == 0) continue;
     const uint32_t s0 = row_start[m];
-    const int64_t c = (int64_t)(u - m * upr) * 8;
-    const bool full = c + 8 <= N;
-    float acc[8];
-    if constexpr (BF16) {
-      const uint16_t* yp = static_cast<const uint16_t*>(y) + (int64_t)m * ldy + c;
-      if (full) {
-        const uint4 q = ld_v4_hint(yp, stream);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const int64_t cu = (int64_t)(u - m * upr) * (8 * G);
+    float acc[G][8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc[2 * k] = __uint_as_float(w[k] << 16);
-          acc[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    for (int g = 0; g < G; ++g) {
+      const int64_t c = cu + 8 * g;
+      const bool full = c + 8 <= N;
+      if constexpr (BF16) {
+        const uint16_t* yp = static_cast<const uint16_t*>(y) + (int64_t)m * ldy + c;
+        if (full) {
+          const uint4 q = ld_v4_hint(yp, stream);
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            acc[g][2 * k] = __uint_as_float(w[k] << 16);
+            acc[g][2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[g][j] = c + j < N ? __uint_as_float((uint32_t)yp[j] << 16) : 0.0f;
         }
       } else {
+        const float* yp = static_cast<const float*>(y) + (int64_t)m * ldy + c;
+        if (full) {
+          const uint4 a = ld_v4_hint(yp, stream), b = ld_v4_hint(yp + 4, stream);
+          acc[g][0] = __uint_as_float(a.x); acc[g][1] = __uint_as_float(a.y);
+          acc[g][2] = __uint_as_float(a.z); acc[g][3] = __uint_as_float(a.w);
+          acc[g][4] = __uint_as_float(b.x); acc[g][5] = __uint_as_float(b.y);
+          acc[g][6] = __uint_as_float(b.z); acc[g][7] = __uint_as_float(b.w);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = c + j < N ? __uint_as_float((uint32_t)yp[j] << 16) : 0.0f;
-      }
-    } else {
-      const float* yp = static_cast<const float*>(y) + (int64_t)m * ldy + c;
-      if (full) {
-        const uint4 a = ld_v4_hint(yp, stream), b = ld_v4_hint(yp + 4, stream);
-        acc[0] = __uint_as_float(a.x); acc[1] = __uint_as_float(a.y);
-        acc[2] = __uint_as_float(a.z); acc[3] = __uint_as_float(a.w);
-        acc[4] = __uint_as_float(b.x); acc[5] = __uint_as_float(b.y);
-        acc[6] = __uint_as_float(b.z); acc[7] = __uint_as_float(b.w);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = c + j < N ? yp[j] : 0.0f;
+          for (int j = 0; j < 8; ++j) acc[g][j] = c + j < N ? yp[j] : 0.0f;
+        }
       }
     }
     for (uint32_t i0 = 0; i0 < len; i0 += 4) {
       OccEntry e[4];
-      uint4 q[4];
+      uint4 q[4][G];
 #pragma unroll
       for (int j = 0; j < 4; ++j) e[j] = i0 + j < len ? ent[s0 + i0 + j] : OccEntry{0, 0.0f};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        q[j] = i0 + j < len ? ld_v4_hint(wt + (int64_t)e[j].k * ldt + c, keep) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int g = 0; g < G; ++g)   // W^T rows are padded to 8: a group starting below N is readable
+          q[j][g] = (i0 + j < len && cu + 8 * g < N) ? ld_v4_hint(wt + (int64_t)e[j].k * ldt + cu + 8 * g, keep)
+                                                      : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (i0 + j >= len) break;   // the row's true entries only
-        const uint32_t w[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc[2 * k] = fmaf(e[j].v, __uint_as_float(w[k] << 16), acc[2 * k]);
-          acc[2 * k + 1] = fmaf(e[j].v, __uint_as_float(w[k] & 0xFFFF0000u), acc[2 * k + 1]);
+        for (int g = 0; g < G; ++g) {
+          const uint32_t w[4] = {q[j][g].x, q[j][g].y, q[j][g].z, q[j][g].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            acc[g][2 * k] = fmaf(e[j].v, __uint_as_float(w[k] << 16), acc[g][2 * k]);
+            acc[g][2 * k + 1] = fmaf(e[j].v, __uint_as_float(w[k] & 0xFFFF0000u), acc[g][2 * k + 1]);
+          }
         }
       }
     }
-    if constexpr (BF16) {
-      uint16_t* yp = static_cast<uint16_t*>(y) + (int64_t)m * ldy + c;
-      uint32_t pk[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * k], acc[2 * k + 1]);
-        pk[k] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      if (full) {
-        st_v4_hint(yp, make_uint4(pk[0], pk[1], pk[2], pk[3]), stream);
+    for (int g = 0; g < G; ++g) {
+      const int64_t c = cu + 8 * g;
+      if (c >= N) break;
+      const bool full = c + 8 <= N;
+      if constexpr (BF16) {
+        uint16_t* yp = static_cast<uint16_t*>(y) + (int64_t)m * ldy + c;
+        uint32_t pk[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(acc[g][2 * k], acc[g][2 * k + 1]);
+          pk[k] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        if (full) {
+          st_v4_hint(yp, make_uint4(pk[0], pk[1], pk[2], pk[3]), stream);
+        } else {
+          for (int j = 0; j < 8 && c + j < N; ++j) yp[j] = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
+        }
       } else {
-        for (int j = 0; j < 8 && c + j < N; ++j) yp[j] = (uint16_t)(pk[j >> 1] >> (16 * (j & 1)));
-      }
-    } else {
-      float* yp = static_cast<float*>(y) + (int64_t)m * ldy + c;
-      if (full) {
-        st_v4_hint(yp, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
-                                  __float_as_uint(acc[3])), stream);
-        st_v4_hint(yp + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]), __float_as_uint(acc[6]),
-                                      __float_as_uint(acc[7])), stream);
-      } else {
-        for (int j = 0; j < 8 && c + j < N; ++j) yp[j] = acc[j];
+        float* yp = static_cast<float*>(y) + (int64_t)m * ldy + c;
+        if (full) {
+          st_v4_hint(yp, make_uint4(__float_as_uint(acc[g][0]), __float_as_uint(acc[g][1]),
+                                    __float_as_uint(acc[g][2]), __float_as_uint(acc[g][3])), stream);
+          st_v4_hint(yp + 4, make_uint4(__float_as_uint(acc[g][4]), __float_as_uint(acc[g][5]),
+                                        __float_as_uint(acc[g][6]), __float_as_uint(acc[g][7])), stream);
+        } else {
+          for (int j = 0; j < 8 && c + j < N; ++j) yp[j] = acc[g][j];
+        }
       }
     }
   }
@@ -700,9 +717,9 @@ cudaError_t launch_occ_correct(void* y, int64_t ldy, int out_dtype, int64_t m, i
   const auto* rl = reinterpret_cast<const uint32_t*>(base + L.row_len);
   const auto* ent = reinterpret_cast<const OccEntry*>(base + L.entries);
   const auto* wt = reinterpret_cast<const uint16_t*>(base + L.wt);
-  // 8-column units with 32-bit ids (below 2^31, so that the grid stride
+  // 16-column units with 32-bit ids (below 2^31, so that the grid stride
   // cannot wrap): row bands of at most that many units per launch
-  const int64_t upr = cdiv(n, 8), band = std::max<int64_t>(1, ((int64_t(1) << 31) - 1) / upr);
+  const int64_t upr = cdiv(n, 16), band = std::max<int64_t>(1, ((int64_t(1) << 31) - 1) / upr);
   const FastDiv fd = make_fastdiv((uint32_t)upr);
   const int esz = out_dtype == FP4_DTYPE_BF16 ? 2 : 4;
   for (int64_t r0 = 0; r0 < m; r0 += band) {
